@@ -1,0 +1,394 @@
+/*
+ * bkv_oracle.c -- plain, slow, obviously-correct CPU oracle for the paged
+ * (block) KV cache hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg do.  It shares no code, header, table or
+ * helper with the CUDA library; the two only see the same seeded inputs.
+ *
+ * Every routine is the plain definition written out, one scalar loop at a
+ * time, in the order the pages state it.  Floating point is fp64 throughout;
+ * bf16 and fp32 inputs are widened exactly (a bf16 value is the top 16 bits
+ * of an IEEE binary32 value).
+ *
+ * Sources (web pages; section names as printed on them):
+ *   [P1] "Padding and Batching with Block KV" (vllm-neuron design notes)
+ *        - Block KV Cache Architecture / Block Structure, Block Table
+ *        - Slot Mapping / The Core Formula, Slot Mapping Computation
+ *        - Special Block and Slot Values / Block ID 0 vs. Sentinel -1,
+ *          Slot ID -1: Padding Tokens
+ *        - Padding with Block KV / Slot Mapping for Padded Tokens
+ *        - Cache Masking / mask_cache, mask_active
+ *   [P2] "ブロック表" (vLLM v1 BlockTable walkthrough)
+ *        - 設計動機 (kernel block_size vs manager block_size; CUDA-graph
+ *          padding of the slot-mapping tail)
+ *        - 境界と失敗 (block_size % kernel_block_size != 0 is an error)
+ *   [P4] "Decode Context-Length Bucketing"
+ *        - Design / Per-step bucket selection (needed_seq), Block-table
+ *          head-trim vs. SWA tail-trim
+ *
+ * Readings where the pages leave a step open (each is marked R<n> below):
+ *   R2  any block-table entry <= 0 (upstream null block 0 or the -1
+ *       sentinel) yields slot -1 / is never read.
+ *   R3  a token is padding if its index is >= num_tokens or its request
+ *       index is negative.
+ *   R5  manager block m expands to kernel blocks m*bpk + t, t < bpk;
+ *       m <= 0 expands to bpk entries of -1.
+ *   R6  attention is scaled dot-product attention; GQA query head h reads
+ *       KV head h / (num_q_heads / num_kv_heads).
+ *   R7  mask_mode 0: query t of a request with cache length L sits at
+ *       position L - q_len + t and sees keys j <= that position; mask_mode 1:
+ *       every query sees every key j < L (an all-ones mask_active).
+ *   R9  a row with no visible key (context length 0, e.g. a padded batch
+ *       row) outputs 0.
+ *   R10 a key whose block-table entry is <= 0 is masked out, not read.
+ *   R12 a position past the table width gives slot -1 and counts an error.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_DT_BF16 0
+#define ORC_DT_F32 1
+
+/* ------------------------------------------------------------------ */
+/* element access                                                      */
+/* ------------------------------------------------------------------ */
+
+/* Widen one element of a bf16 or fp32 array to double, exactly. */
+static double orc_load(const void *base, int64_t idx, int dtype)
+{
+    if (dtype == ORC_DT_BF16) {
+        uint32_t bits = ((uint32_t)((const uint16_t *)base)[idx]) << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float *)base)[idx];
+}
+
+static int orc_elem_bytes(int dtype)
+{
+    return dtype == ORC_DT_BF16 ? 2 : (dtype == ORC_DT_F32 ? 4 : 0);
+}
+
+/* ------------------------------------------------------------------ */
+/* O1: slot mapping                                                    */
+/* ------------------------------------------------------------------ */
+
+/*
+ * slot = block_table[r][p / bs] * bs + p % bs             [P1 The Core Formula]
+ * The table row of request r is looked up at logical block p / bs
+ * ([P1 Slot Mapping Computation]); the slot buffer is max_num_tokens long
+ * and every entry past num_tokens is the padding id -1 ([P2 設計動機],
+ * CUDA-graph tail; [P1 Slot Mapping for Padded Tokens]).
+ *
+ * Returns the number of tokens flagged as bad input (request index past the
+ * batch, negative position, position past the table width), or -1 when the
+ * arguments themselves are invalid.
+ */
+int64_t orc_compute_slot_mapping(const int32_t *block_table, int32_t num_reqs,
+                                 int64_t bt_stride, int32_t bt_cols,
+                                 const int32_t *req_indices,
+                                 const int64_t *positions, int64_t num_tokens,
+                                 int64_t max_num_tokens, int32_t block_size,
+                                 int64_t *slot_mapping)
+{
+    if (block_size <= 0 || num_tokens < 0 || max_num_tokens < num_tokens ||
+        num_reqs < 0 || bt_cols < 0 || bt_stride < bt_cols)
+        return -1;
+    int64_t errors = 0;
+    for (int64_t i = 0; i < max_num_tokens; ++i) {
+        slot_mapping[i] = -1; /* PAD_SLOT_ID */
+        if (i >= num_tokens)
+            continue; /* tail padding (R3) */
+        int32_t r = req_indices[i];
+        int64_t p = positions[i];
+        if (r < 0)
+            continue; /* padded request (R3) */
+        if (r >= num_reqs || p < 0) {
+            errors += 1;
+            continue;
+        }
+        int64_t logical_block = p / block_size;
+        int64_t offset = p % block_size;
+        if (logical_block >= bt_cols) { /* R12 */
+            errors += 1;
+            continue;
+        }
+        int64_t block_number = block_table[(int64_t)r * bt_stride + logical_block];
+        if (block_number <= 0)
+            continue; /* null block 0 or sentinel -1 (R2) */
+        slot_mapping[i] = block_number * block_size + offset;
+    }
+    return errors;
+}
+
+/* ------------------------------------------------------------------ */
+/* O2: manager -> kernel block expansion                               */
+/* ------------------------------------------------------------------ */
+
+/*
+ * One manager block of block_size tokens is blocks_per_kv_block =
+ * block_size / kernel_block_size kernel blocks ([P2 設計動機], e.g. 32 -> 16,
+ * two kernel blocks each); an indivisible pair is an error ([P2 境界と失敗]).
+ * The layout (R5) is the one under which a kernel block id addresses the
+ * same bytes as the manager view: kernel block m*bpk + t holds tokens
+ * [t*kbs, (t+1)*kbs) of manager block m.
+ *
+ * Returns 0, or 1 for invalid arguments.  Columns of the output past
+ * mgr_cols * bpk are left as they were.
+ */
+int orc_map_to_kernel_blocks(const int32_t *mgr_table, int32_t rows,
+                             int64_t mgr_stride, int32_t mgr_cols,
+                             int32_t block_size, int32_t kernel_block_size,
+                             int32_t *kernel_table, int64_t kernel_stride)
+{
+    if (block_size <= 0 || kernel_block_size <= 0 ||
+        block_size % kernel_block_size != 0 || rows < 0 || mgr_cols < 0 ||
+        mgr_stride < mgr_cols)
+        return 1;
+    int64_t bpk = block_size / kernel_block_size;
+    if (kernel_stride < (int64_t)mgr_cols * bpk)
+        return 1;
+    for (int32_t r = 0; r < rows; ++r) {
+        for (int32_t j = 0; j < mgr_cols; ++j) {
+            int64_t m = mgr_table[(int64_t)r * mgr_stride + j];
+            for (int64_t t = 0; t < bpk; ++t) {
+                int64_t out = (m > 0) ? m * bpk + t : -1;
+                kernel_table[(int64_t)r * kernel_stride + j * bpk + t] = (int32_t)out;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* O3: KV cache write (scatter)                                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * k_cache[s / bs][s % bs][:][:] = k_new[i], and the same for V, for every
+ * token i whose slot s is non-negative ([P1 Block Structure] gives the
+ * (total_blocks, block_size, num_kv_heads, head_dim) layout; [P1 Slot ID -1:
+ * Padding Tokens] says a -1 slot writes nothing).  A slot past the cache is
+ * skipped and counted.  The copy is bit-for-bit.
+ *
+ * Token i's row starts new_token_stride elements after token i-1's, and
+ * holds num_kv_heads * head_dim contiguous elements.
+ *
+ * Returns the number of out-of-range slots, -1 for invalid arguments, or -2
+ * when two tokens name the same slot (such input has no single correct
+ * result and is rejected).
+ */
+int64_t orc_cache_write(const void *k_new, const void *v_new,
+                        int64_t num_tokens, int64_t new_token_stride,
+                        const int64_t *slot_mapping, void *k_cache,
+                        void *v_cache, int64_t total_blocks, int32_t block_size,
+                        int32_t num_kv_heads, int32_t head_dim, int dtype)
+{
+    int eb = orc_elem_bytes(dtype);
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (eb == 0 || num_tokens < 0 || total_blocks < 0 || block_size <= 0 ||
+        num_kv_heads <= 0 || head_dim <= 0 || new_token_stride < row)
+        return -1;
+    int64_t capacity = total_blocks * block_size;
+    unsigned char *seen = (unsigned char *)calloc((size_t)(capacity > 0 ? capacity : 1), 1);
+    if (!seen)
+        return -1;
+    int64_t errors = 0;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0)
+            continue;
+        if (s >= capacity) {
+            errors += 1;
+            continue;
+        }
+        if (seen[s]) {
+            free(seen);
+            return -2;
+        }
+        seen[s] = 1;
+    }
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0 || s >= capacity)
+            continue;
+        int64_t block = s / block_size;
+        int64_t offset = s % block_size;
+        int64_t dst = (block * block_size + offset) * row; /* element index */
+        int64_t src = i * new_token_stride;
+        memcpy((char *)k_cache + dst * eb, (const char *)k_new + src * eb, (size_t)(row * eb));
+        memcpy((char *)v_cache + dst * eb, (const char *)v_new + src * eb, (size_t)(row * eb));
+    }
+    free(seen);
+    return errors;
+}
+
+/* ------------------------------------------------------------------ */
+/* O4: GQA paged decode attention (one request)                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * For request r with cache length L = context_lens[r] ([P1 mask_cache]: the
+ * valid positions are [0, L), and L counts this step's tokens) and each of
+ * its q_len query tokens t, each query head h:
+ *
+ *   key position j is visible iff  j < L,  j <= L - q_len + t (mask_mode 0,
+ *   R7), and its table entry b = block_table[r][j / bs] is a real block
+ *   (b > 0, R10; b < total_blocks, otherwise counted as an error);
+ *   s_j = scale * sum_d q[r,t,h,d] * K[b, j % bs, h / G, d]        (R6)
+ *   out[r,t,h,:] = sum_j softmax(s)_j * V[b, j % bs, h / G, :]
+ *
+ * and 0 when no key is visible (R9).  The softmax subtracts the maximum
+ * before exponentiating; that changes no value, only avoids overflow.
+ *
+ * q and out are (num_reqs, q_len, num_q_heads, head_dim); out is fp64.
+ * Returns the number of bad table entries met (positions past the table
+ * width or ids past the cache), or -1 for invalid arguments.
+ */
+int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_table,
+                                 int64_t bt_stride, int32_t bt_cols,
+                                 const int32_t *context_lens, int32_t num_reqs,
+                                 int32_t q_len, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int64_t total_blocks,
+                                 double scale, int mask_mode, int dtype,
+                                 double *out)
+{
+    if (orc_elem_bytes(dtype) == 0 || r < 0 || r >= num_reqs || q_len <= 0 ||
+        num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 ||
+        bt_cols < 0 || bt_stride < bt_cols || (mask_mode != 0 && mask_mode != 1))
+        return -1;
+    const int64_t D = head_dim;
+    const int64_t G = num_q_heads / num_kv_heads;
+    const int64_t L = context_lens[r] > 0 ? context_lens[r] : 0;
+    int64_t errors = 0;
+
+    /* Which key positions may be read at all: j < L with a real block. */
+    unsigned char *readable = (unsigned char *)malloc((size_t)(L > 0 ? L : 1));
+    double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    if (!readable || !s) {
+        free(readable);
+        free(s);
+        return -1;
+    }
+    for (int64_t j = 0; j < L; ++j) {
+        readable[j] = 0;
+        int64_t lb = j / block_size;
+        if (lb >= bt_cols) {
+            if (j % block_size == 0)
+                errors += 1;
+            continue;
+        }
+        int64_t b = block_table[(int64_t)r * bt_stride + lb];
+        if (b <= 0)
+            continue;
+        if (b >= total_blocks) {
+            if (j % block_size == 0)
+                errors += 1;
+            continue;
+        }
+        readable[j] = 1;
+    }
+
+    for (int64_t t = 0; t < q_len; ++t) {
+        int64_t last_visible = (mask_mode == 0) ? (L - q_len + t) : (L - 1);
+        for (int64_t h = 0; h < num_q_heads; ++h) {
+            int64_t g = h / G;
+            const int64_t qoff = (((int64_t)r * q_len + t) * num_q_heads + h) * D;
+            double *o = out + qoff;
+            for (int64_t d = 0; d < D; ++d)
+                o[d] = 0.0;
+
+            double m = -INFINITY;
+            int any = 0;
+            for (int64_t j = 0; j < L && j <= last_visible; ++j) {
+                if (!readable[j])
+                    continue;
+                int64_t b = block_table[(int64_t)r * bt_stride + j / block_size];
+                int64_t krow = ((b * block_size + j % block_size) * num_kv_heads + g) * D;
+                double dot = 0.0;
+                for (int64_t d = 0; d < D; ++d)
+                    dot += orc_load(q, qoff + d, dtype) * orc_load(k_cache, krow + d, dtype);
+                s[j] = scale * dot;
+                if (!any || s[j] > m)
+                    m = s[j];
+                any = 1;
+            }
+            if (!any)
+                continue; /* R9: nothing visible -> 0 */
+
+            double denom = 0.0;
+            for (int64_t j = 0; j < L && j <= last_visible; ++j) {
+                if (!readable[j])
+                    continue;
+                int64_t b = block_table[(int64_t)r * bt_stride + j / block_size];
+                int64_t vrow = ((b * block_size + j % block_size) * num_kv_heads + g) * D;
+                double w = exp(s[j] - m);
+                denom += w;
+                for (int64_t d = 0; d < D; ++d)
+                    o[d] += w * orc_load(v_cache, vrow + d, dtype);
+            }
+            for (int64_t d = 0; d < D; ++d)
+                o[d] /= denom;
+        }
+    }
+    free(readable);
+    free(s);
+    return errors;
+}
+
+/* The whole batch: every request in turn. */
+int64_t orc_paged_decode(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_table, int64_t bt_stride,
+                         int32_t bt_cols, const int32_t *context_lens,
+                         int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int64_t total_blocks, double scale,
+                         int mask_mode, int dtype, double *out)
+{
+    int64_t errors = 0;
+    for (int32_t r = 0; r < num_reqs; ++r) {
+        int64_t e = orc_paged_decode_request(r, q, k_cache, v_cache, block_table,
+                                             bt_stride, bt_cols, context_lens,
+                                             num_reqs, q_len, num_q_heads,
+                                             num_kv_heads, head_dim, block_size,
+                                             total_blocks, scale, mask_mode,
+                                             dtype, out);
+        if (e < 0)
+            return e;
+        errors += e;
+    }
+    return errors;
+}
+
+/* ------------------------------------------------------------------ */
+/* needed_seq and bucket choice, used only to report bytes             */
+/* ------------------------------------------------------------------ */
+
+/*
+ * [P4 Design / Per-step bucket selection]: needed_seq = max(num_computed) +
+ * 1 + num_speculative_tokens; the bucket is the smallest of buckets U
+ * {max_model_len} that is >= needed_seq.  buckets must be ascending.
+ * Returns the chosen bucket, or -1 if even max_model_len is too small.
+ */
+int64_t orc_decode_bucket(const int64_t *num_computed, int64_t n,
+                          int64_t num_speculative_tokens, const int64_t *buckets,
+                          int64_t num_buckets, int64_t max_model_len)
+{
+    int64_t mx = 0;
+    for (int64_t i = 0; i < n; ++i)
+        if (num_computed[i] > mx)
+            mx = num_computed[i];
+    int64_t needed = mx + 1 + num_speculative_tokens;
+    for (int64_t k = 0; k < num_buckets; ++k)
+        if (buckets[k] >= needed)
+            return buckets[k];
+    return max_model_len >= needed ? max_model_len : -1;
+}

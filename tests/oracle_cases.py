@@ -1,0 +1,51 @@
+"""Test helpers: build the oracle's view of a workload (host caches filled by the
+oracle's own slot mapping and cache write).  Calls only ``oracle`` and the
+seeded generators."""
+import numpy as np
+
+import oracle
+from paged_kv_cache_slot_gb300 import workloads as wl
+
+BF16_NAN = np.uint16(0x7FC0)
+
+
+def nan_cache(w: wl.Workload, total_blocks=None, block_size=None, sparse=False):
+    """NaN-filled host caches; ``sparse`` leaves them uninitialised instead, so
+    that the pages of a large cache are only committed where rows are written
+    (the oracle never reads anything else)."""
+    tb = w.total_kernel_blocks if total_blocks is None else total_blocks
+    bs = w.kernel_block_size if block_size is None else block_size
+    shape = (tb, bs, w.num_kv_heads, w.head_dim)
+    if sparse:
+        return np.empty(shape, w.np_dtype)
+    if w.dtype == "bf16":
+        return np.full(shape, BF16_NAN, np.uint16)
+    return np.full(shape, np.nan, np.float32)
+
+
+def kernel_table(w: wl.Workload):
+    if w.kernel_block_size == w.block_size:
+        return w.block_table.copy()
+    return oracle.map_to_kernel_blocks(w.block_table, w.block_size, w.kernel_block_size)
+
+
+def fill_oracle_cache(w: wl.Workload, rows=None, kcache=None, vcache=None, table=None):
+    """Write every token (prior and this step's) of ``rows`` into NaN-poisoned
+    caches through the oracle.  Returns (k_cache, v_cache, kernel_table)."""
+    table = kernel_table(w) if table is None else table
+    sparse = w.total_kernel_blocks * w.kernel_block_size * w.num_kv_heads * w.head_dim * w.elem_bytes > (256 << 20)
+    kc = nan_cache(w, sparse=sparse) if kcache is None else kcache
+    vc = nan_cache(w, sparse=sparse) if vcache is None else vcache
+    rows = range(w.num_rows) if rows is None else rows
+    for r in rows:
+        L = int(w.context_lens[r])
+        if L == 0:
+            continue
+        k, v = w.kv_rows(r, 0, L)
+        req = np.full(L, r, np.int32)
+        pos = np.arange(L, dtype=np.int64)
+        slots, err = oracle.compute_slot_mapping(table, req, pos, w.kernel_block_size)
+        assert err == 0
+        kc, vc, err = oracle.cache_write(k, v, slots, kc, vc, inplace=True)
+        assert err == 0
+    return kc, vc, table
