@@ -1,0 +1,370 @@
+"""Benchmark of the paged KV cache hot path on GB300.
+
+One step = one pass of the whole path over one batch of the Llama-3-8B-shaped
+decode workload (32 requests, contexts uniform in [512, 4096], H_q 32,
+H_kv 8, head_dim 128, block_size 64, bf16): manager->kernel block expansion,
+slot mapping of the step's tokens, the K/V cache scatter, and the paged
+decode (partition + merge kernels).  Inputs are seeded, synthetic and
+resident in HBM; the caches were filled beforehand through the same
+library.  L2 is flushed (a write of 2x the L2 size) before every timed step,
+outside the timed interval.
+
+value  = decode KV bytes needed per step (cache_len rows x K,V x H_kv x D x 2B)
+         / device time of the step (CUDA events), aggregated over ranks.
+e2e    = the same bytes / time of a step that also copies the step's inputs
+         from pinned host memory and reads the output back.
+roofline.achieved = the same bytes / device time of the decode call alone.
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bkv|reference]
+Under torchrun every rank runs an independent replica (the path has no
+exchange step); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode KV-read GB/s (% HBM peak); slot-map+cache-write tokens/s"
+WORKLOAD = "llama3_decode"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "paged_decode_llama3_decode.txt")
+DECODE_SOURCES = ["bkv_decode.cu", "bkv_decode_tc.cu", "bkv_decode.cuh"]
+
+
+def _dist():
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("nccl")
+        return dist
+    return None
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _decode_source_sha():
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        p = os.path.join(ROOT, "paged_kv_cache_slot_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic():
+    """dram bytes per decode launch from the committed ncu summary, if it still
+    describes the current kernel source (else None)."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    kv = {}
+    for line in open(PROFILE_TRAFFIC):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("decode_source_sha256") != _decode_source_sha():
+        return None
+    try:
+        return int(kv["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv") if os.path.isdir(
+            os.path.join(ROOT, "gpurun_out")) else f"/tmp/bkv_clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _cpu_baseline(budget_s: float, workload: str = WORKLOAD):
+    """The oracle, as it stands, on a bounded sample of the workload: requests
+    decoded one at a time (single thread, fp64) until ``budget_s`` passes."""
+    import oracle
+    from oracle.cases import fill_oracle_cache
+    from paged_kv_cache_slot_gb300 import workloads as wl
+
+    w = wl.make(workload)
+    q = w.q()
+    order = np.argsort(w.context_lens)[::-1]        # fixed order, longest first
+    done_bytes, done_t, n = 0, 0.0, 0
+    per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+    for r in order:
+        kc, vc, table = fill_oracle_cache(w, rows=[int(r)])
+        t0 = time.perf_counter()
+        oracle.paged_decode_request(int(r), q, kc, vc, table, w.context_lens)
+        done_t += time.perf_counter() - t0
+        done_bytes += int(w.context_lens[r]) * per_tok
+        n += 1
+        del kc, vc
+        if done_t >= budget_s:
+            break
+    return {"value": done_bytes / done_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {w.num_rows} requests of {workload} decoded by the fp64 C oracle "
+                      f"({done_bytes / 1e6:.1f} MB of K/V, {done_t:.1f} s, single thread)"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle timed on the host cores, same metric and config."""
+    dist = _dist()
+    rank = dist.get_rank() if dist else 0
+    if rank != 0:
+        return
+    import oracle
+    from oracle.cases import fill_oracle_cache
+    from paged_kv_cache_slot_gb300 import workloads as wl
+
+    w = wl.make(WORKLOAD)
+    q = w.q()
+    per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+    rows = [int(np.argsort(w.context_lens)[len(w.context_lens) // 2])]  # the median-length request
+    kc, vc, table = fill_oracle_cache(w, rows=rows)
+    step_bytes = sum(int(w.context_lens[r]) for r in rows) * per_tok
+
+    def one_step():
+        t0 = time.perf_counter()
+        for r in rows:
+            oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one_step()
+    times = [one_step() for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    value = step_bytes / (ms / 1e3) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama3_decode: 32 req, ctx U[512,4096]+1, H_q 32, H_kv 8, D 128, bs 64, bf16",
+                       "sample": f"request {rows[0]} ({int(w.context_lens[rows[0]])} positions) per step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"one median-length request ({step_bytes / 1e6:.1f} MB K/V) per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _time_steps(torch, fn, steps, flush, stream):
+    """Per-step device times (ms) with an L2 flush before each step, outside the events."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_bkv(args):
+    import torch
+
+    from paged_kv_cache_slot_gb300 import bkv
+    from paged_kv_cache_slot_gb300 import workloads as wl
+    from paged_kv_cache_slot_gb300.build import build
+    from paged_kv_cache_slot_gb300.staging import DeviceWorkload
+
+    dist = _dist()
+    rank = dist.get_rank() if dist else 0
+    world = dist.get_world_size() if dist else 1
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if rank == 0:
+        build()
+    if dist:
+        dist.barrier()
+    bkv.load()
+
+    w = wl.make(WORKLOAD)
+    dw = DeviceWorkload(w, device=f"cuda:{local}")
+    stream = torch.cuda.Stream()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=f"cuda:{local}")
+    kv_bytes = dw.decode_kv_bytes()
+
+    def step():
+        dw.step(stream=stream)
+
+    def decode_only():
+        dw.decode(stream=stream)
+
+    # pinned host copies of the step's inputs for the end-to-end leg
+    host_in = {name: getattr(dw, name).cpu().pin_memory()
+               for name in ("mgr_table", "req_indices", "positions", "k_new", "v_new", "q", "context_lens")}
+    host_out = torch.empty(dw.out.shape, dtype=dw.out.dtype, pin_memory=True)
+    h2d_bytes = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h_bytes = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for name, t in host_in.items():
+            getattr(dw, name).copy_(t, non_blocking=True)
+        dw.step(stream=stream)
+        host_out.copy_(dw.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+            e2e_step()
+            decode_only()
+    torch.cuda.synchronize()
+
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        step_ms = _time_steps(torch, step, args.steps, flush, stream)
+        dec_ms = _time_steps(torch, decode_only, args.steps, flush, stream)
+        e2e_ms = _time_steps(torch, e2e_step, args.steps, flush, stream)
+        t_wall = time.perf_counter() - t_wall0
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+
+    ms = sum(step_ms) / len(step_ms)
+    dms = sum(dec_ms) / len(dec_ms)
+    ems = sum(e2e_ms) / len(e2e_ms)
+    if dist:
+        t = torch.tensor([ms, dms, ems], dtype=torch.float64, device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, dms, ems = t.tolist()
+
+    # secondary half of the metric: slot mapping + cache write on the ragged mixed step
+    secondary = None
+    if rank == 0 and not args.no_secondary:
+        rw = wl.make("ragged_step")
+        rdw = DeviceWorkload(rw, device=f"cuda:{local}", fill_prior=False)
+
+        def wstep():
+            rdw.write_step(stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                wstep()
+        wms = _time_steps(torch, wstep, max(args.steps, 20), flush, stream)
+        wm = statistics.median(wms)
+        secondary = {"workload": f"ragged_step: {rw.num_tokens} tokens of 64 requests, bs 16, H_kv 8, D 128, bf16",
+                     "tokens_per_s": rw.num_tokens / (wm / 1e3), "GB_per_s": rdw.write_bytes() / (wm / 1e3) / 1e9,
+                     "ms_per_step": wm, "kernels_per_step": 2}
+        del rdw
+
+    if rank != 0:
+        return
+    peak, peak_kind = _peaks()
+    achieved = kv_bytes / (dms / 1e3) / 1e9
+    value = world * kv_bytes / (ms / 1e3) / 1e9
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "llama3_decode: 32 req, ctx U[512,4096] + 1 new token, H_q 32, H_kv 8, D 128, "
+                               "bs 64, bf16, fp32 accumulate",
+                   "kv_bytes_per_step": kv_bytes, "l2": "flushed before every timed step (2x L2 write)",
+                   "parallelism": f"replicas x{world}", "step": "expand + slot map + write + decode + merge"},
+        # library kernels in the timed region: step (5) + decode alone (2) + end-to-end step (5), per step
+        "gpu_launches": args.steps * (5 + 2 + 5),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": _profiled_traffic(),
+                     "kernel": "bkv_paged_decode (partition + merge, CUDA events around the call)",
+                     "peak_kind": f"{peak_kind} copy bandwidth"},
+        "decode_ms": dms,
+        "e2e": {"value": world * kv_bytes / (ems / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ems},
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+    }
+    if secondary:
+        line["secondary"] = secondary
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="bkv", choices=["bkv", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_bkv(args)
+    d = _dist()
+    if d:
+        d.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

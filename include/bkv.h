@@ -1,0 +1,194 @@
+/*
+ * bkv.h -- C ABI of libbkv.so, the GB300 (sm_103a) paged (block) KV cache
+ * hot path: slot mapping, manager-to-kernel block expansion, the KV cache
+ * scatter, and GQA paged decode attention with a split-KV merge.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *   stated otherwise.  Arrays are dense row-major unless a stride is given
+ *   (strides count elements, not bytes).  The library allocates no memory.
+ * - Every call is asynchronous: it validates its scalar arguments on the
+ *   host, enqueues kernels on `stream` (0 = the legacy default stream) and
+ *   returns.  Nothing is read from device memory on the host.
+ * - Return value: BKV_OK, or an error status.  BKV_ERR_INVALID_ARG and
+ *   BKV_ERR_UNSUPPORTED are decided on the host before anything is enqueued;
+ *   BKV_ERR_CUDA means a launch failed (text from bkv_last_cuda_error()).
+ * - Bad DATA in device memory (a block id past the cache, a slot past the
+ *   cache, a position past the table width, a request index past the batch)
+ *   never faults: the token or block is treated as padding (-1) and, when
+ *   `err_count` is non-null, *err_count (a device int32) is incremented.
+ * - The KV cache layout of record is (total_blocks, block_size,
+ *   num_kv_heads, head_dim) for K and for V, separately.
+ *
+ * Sources: "Padding and Batching with Block KV" (vllm-neuron design notes),
+ * "ブロック表" (vLLM v1 BlockTable walkthrough), "KV Caching with vLLM" and
+ * "Decode Context-Length Bucketing" (Neuron docs).  Each declaration names the
+ * section that defines its operation.
+ */
+#ifndef BKV_H_
+#define BKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *bkv_stream_t; /* same object as cudaStream_t */
+
+enum {
+    BKV_OK = 0,
+    BKV_ERR_INVALID_ARG = 1, /* a scalar argument or null pointer is invalid */
+    BKV_ERR_UNSUPPORTED = 2, /* dtype / head_dim / shape this build does not handle */
+    BKV_ERR_CUDA = 3         /* a CUDA launch failed; see bkv_last_cuda_error() */
+};
+
+enum { BKV_BF16 = 0, BKV_F32 = 1 };
+
+enum {
+    BKV_MASK_CAUSAL = 0, /* query t of a request of cache length L is at L - q_len + t */
+    BKV_MASK_ALL = 1     /* every query sees every cached position < L */
+};
+
+/* Static text for a status code. */
+const char *bkv_status_string(int status);
+
+/* Text of the last CUDA error seen by this library in this thread ("" if none). */
+const char *bkv_last_cuda_error(void);
+
+/* Library version, e.g. "bkv 0.1.0 sm_103a". */
+const char *bkv_version(void);
+
+/*
+ * bkv_compute_slot_mapping
+ *   Defined by "Padding and Batching with Block KV", Slot Mapping: From
+ *   Position to Cache Location (The Core Formula; Slot Mapping Computation),
+ *   Special Block and Slot Values, and "ブロック表" 設計動機 (the padded tail of
+ *   the slot buffer written with PAD for CUDA-graph reuse).
+ *
+ *   For i in [0, max_num_tokens):
+ *     slot_mapping[i] = block_table[r * bt_stride + p / block_size] * block_size
+ *                       + p % block_size,   r = req_indices[i], p = positions[i]
+ *   and slot_mapping[i] = -1 when i >= num_tokens, r < 0 (a padded request),
+ *   the table entry is <= 0 (the null block 0 or the sentinel -1), r >=
+ *   num_reqs, p < 0, or p / block_size >= bt_cols.  The last three count as
+ *   errors in *err_count.  Results are exact 64-bit integers.
+ *
+ *   block_table  int32 [num_reqs, bt_stride], first bt_cols columns used.
+ *   req_indices  int32 [num_tokens]; positions int64 [num_tokens].
+ *   slot_mapping int64 [max_num_tokens], written in full.
+ *   err_count    int32*, nullable.
+ *   INVALID_ARG: block_size <= 0, num_tokens < 0, max_num_tokens <
+ *   num_tokens, bt_stride < bt_cols, a needed pointer is null.
+ */
+int bkv_compute_slot_mapping(const int32_t *block_table, int32_t num_reqs, int64_t bt_stride,
+                             int32_t bt_cols, const int32_t *req_indices, const int64_t *positions,
+                             int64_t num_tokens, int64_t max_num_tokens, int32_t block_size,
+                             int64_t *slot_mapping, int32_t *err_count, bkv_stream_t stream);
+
+/*
+ * bkv_map_to_kernel_blocks
+ *   Defined by "ブロック表" 設計動機 (a manager block of block_size tokens is
+ *   blocks_per_kv_block = block_size / kernel_block_size kernel blocks) and
+ *   境界と失敗 (an indivisible pair is an error).
+ *
+ *   With bpk = block_size / kernel_block_size, for every row r and manager
+ *   column j < mgr_cols, t < bpk:
+ *     kernel_table[r * kernel_stride + j * bpk + t] = m > 0 ? m * bpk + t : -1,
+ *     m = mgr_table[r * mgr_stride + j]
+ *   so that the kernel view (total_blocks * bpk, kernel_block_size, H, D) of
+ *   a cache is the same memory as the manager view.  Columns at or past
+ *   mgr_cols * bpk are not written.  m * bpk + t must fit in int32.
+ *
+ *   INVALID_ARG: kernel_block_size <= 0, block_size % kernel_block_size != 0,
+ *   kernel_stride < mgr_cols * bpk, mgr_stride < mgr_cols, null pointers.
+ */
+int bkv_map_to_kernel_blocks(const int32_t *mgr_table, int32_t rows, int64_t mgr_stride,
+                             int32_t mgr_cols, int32_t block_size, int32_t kernel_block_size,
+                             int32_t *kernel_table, int64_t kernel_stride, bkv_stream_t stream);
+
+/*
+ * bkv_cache_write
+ *   Defined by "Padding and Batching with Block KV", Block Structure (cache
+ *   layout) and Slot ID -1: Padding Tokens (a -1 slot writes nothing).
+ *
+ *   For every i < num_tokens with s = slot_mapping[i] >= 0:
+ *     k_cache[s / block_size][s % block_size][:][:] = k_new[i][:][:]  (and V)
+ *   a bit-for-bit copy of num_kv_heads * head_dim elements.  s >=
+ *   total_blocks * block_size is skipped and counted in *err_count.  Two
+ *   tokens naming the same slot is invalid input: one of them lands.
+ *
+ *   k_new, v_new  [num_tokens, new_token_stride] elements of `dtype`; the
+ *                 first num_kv_heads * head_dim of each row are copied
+ *                 (new_token_stride lets them be slices of a fused buffer).
+ *   k_cache, v_cache  [total_blocks, block_size, num_kv_heads, head_dim].
+ *   INVALID_ARG: non-positive sizes, new_token_stride < num_kv_heads *
+ *   head_dim, null pointers.  UNSUPPORTED: dtype not BKV_BF16 / BKV_F32.
+ */
+int bkv_cache_write(const void *k_new, const void *v_new, int64_t num_tokens,
+                    int64_t new_token_stride, const int64_t *slot_mapping, void *k_cache,
+                    void *v_cache, int64_t total_blocks, int32_t block_size, int32_t num_kv_heads,
+                    int32_t head_dim, int dtype, int32_t *err_count, bkv_stream_t stream);
+
+/*
+ * bkv_paged_decode_workspace_size
+ *   Bytes of device workspace bkv_paged_decode needs for these sizes on the
+ *   CURRENT device (the split of long contexts into partitions depends on
+ *   its SM count).  Returns 0 for invalid sizes.  Call it with the same
+ *   arguments, on the same device, as the decode it is for.
+ */
+size_t bkv_paged_decode_workspace_size(int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                       int32_t max_context_len);
+
+/*
+ * bkv_paged_decode
+ *   Defined by "Padding and Batching with Block KV", Cache Masking
+ *   (mask_cache: positions [0, cache_len) are valid; mask_active: the mask
+ *   between this step's query tokens) and Special Block and Slot Values (a
+ *   null / -1 block entry contributes nothing); "Decode Context-Length
+ *   Bucketing", Problem (read only the blocks a request needs, not the full
+ *   max_model_len row).
+ *
+ *   For request r with L = context_lens[r] (cache length INCLUDING this
+ *   step's q_len tokens), query token t < q_len, query head h, G =
+ *   num_q_heads / num_kv_heads:
+ *     key j is visible iff j < L, j <= L - q_len + t (BKV_MASK_CAUSAL only)
+ *     and b = block_table[r * bt_stride + j / block_size] > 0;
+ *     out[r][t][h] = softmax_j(softmax_scale * q[r][t][h] . K[b][j % block_size][h / G])
+ *                    . V[b][j % block_size][h / G]
+ *   and 0 when no key is visible (e.g. L = 0 for a padded NULL row).  Only
+ *   the ceil(L / block_size) table entries a request needs are read; cache
+ *   memory at masked positions is never used (it may hold NaN).
+ *
+ *   q, out    [num_reqs, q_len, num_q_heads, head_dim] of `dtype`; out is
+ *             rounded to nearest-even from fp32.
+ *   k_cache, v_cache  [total_blocks, block_size, num_kv_heads, head_dim].
+ *   block_table int32 [num_reqs, bt_stride], bt_cols columns valid.
+ *   context_lens int32 [num_reqs].
+ *   max_context_len  host-side upper bound on context_lens (sizes the grid);
+ *             a larger context_lens[r] is clamped to it and counted as an error.
+ *   softmax_scale    <= 0 selects 1 / sqrt(head_dim).
+ *   workspace        device scratch of workspace_bytes >=
+ *                    bkv_paged_decode_workspace_size(...); may be null when
+ *                    that size is 0.  Used only while the call's kernels run.
+ *   Ids >= total_blocks and positions past bt_cols are masked and counted.
+ *   INVALID_ARG: num_q_heads % num_kv_heads != 0, non-positive sizes, bad
+ *   mask_mode, workspace too small, null pointers.
+ *   UNSUPPORTED: dtype not BKV_BF16 / BKV_F32, head_dim > 256 or odd.
+ */
+int bkv_paged_decode(const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
+                     const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs,
+                     int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t block_size, int64_t total_blocks, float softmax_scale, int mask_mode,
+                     int dtype, void *out, void *workspace, size_t workspace_bytes,
+                     int32_t *err_count, bkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BKV_H_ */

@@ -1,9 +1,9 @@
-"""Test helpers: build the oracle's view of a workload (host caches filled by the
-oracle's own slot mapping and cache write).  Calls only ``oracle`` and the
-seeded generators."""
+"""The oracle's view of a seeded workload: host caches filled by the oracle's
+own slot mapping and cache write.  TEST INFRASTRUCTURE, like the rest of
+this package; it calls only the oracle and the seeded input generators."""
 import numpy as np
 
-import oracle
+from . import compute_slot_mapping, cache_write, map_to_kernel_blocks
 from paged_kv_cache_slot_gb300 import workloads as wl
 
 BF16_NAN = np.uint16(0x7FC0)
@@ -26,7 +26,7 @@ def nan_cache(w: wl.Workload, total_blocks=None, block_size=None, sparse=False):
 def kernel_table(w: wl.Workload):
     if w.kernel_block_size == w.block_size:
         return w.block_table.copy()
-    return oracle.map_to_kernel_blocks(w.block_table, w.block_size, w.kernel_block_size)
+    return map_to_kernel_blocks(w.block_table, w.block_size, w.kernel_block_size)
 
 
 def fill_oracle_cache(w: wl.Workload, rows=None, kcache=None, vcache=None, table=None):
@@ -44,8 +44,8 @@ def fill_oracle_cache(w: wl.Workload, rows=None, kcache=None, vcache=None, table
         k, v = w.kv_rows(r, 0, L)
         req = np.full(L, r, np.int32)
         pos = np.arange(L, dtype=np.int64)
-        slots, err = oracle.compute_slot_mapping(table, req, pos, w.kernel_block_size)
+        slots, err = compute_slot_mapping(table, req, pos, w.kernel_block_size)
         assert err == 0
-        kc, vc, err = oracle.cache_write(k, v, slots, kc, vc, inplace=True)
+        kc, vc, err = cache_write(k, v, slots, kc, vc, inplace=True)
         assert err == 0
     return kc, vc, table

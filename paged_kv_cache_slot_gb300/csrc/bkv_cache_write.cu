@@ -1,0 +1,118 @@
+// bkv_cache_write.cu -- scatter of new K/V rows into the paged caches.
+//
+// "Padding and Batching with Block KV", Block Structure and Slot ID -1:
+// Padding Tokens.  Row i (num_kv_heads * head_dim elements) lands at flat
+// row s = slot_mapping[i] of the (total_blocks * block_size, H_kv * D) view
+// of each cache; s < 0 writes nothing.
+//
+// One warp per token: a token's row is contiguous in both the source and the
+// cache (2 KiB at H_kv = 8, D = 128, bf16), so each lane moves 16-byte
+// vectors, all loads of a round issued before its stores.  HBM-bound: the
+// algorithmic traffic is 2 * row bytes read + 2 * row bytes written + 8 bytes
+// of slot id per token.
+#include "bkv_internal.cuh"
+
+namespace bkv {
+
+constexpr int kCwWarps = 8;     // warps per block
+constexpr int kCwUnroll = 4;    // 16-byte vectors in flight per lane per tensor
+
+// 16-byte path: row_bytes, the source stride and every base are multiples of 16.
+__global__ void __launch_bounds__(kCwWarps * 32) cache_write_vec16_kernel(
+    const char *__restrict__ k_new, const char *__restrict__ v_new, int64_t num_tokens, int64_t src_stride_bytes,
+    const int64_t *__restrict__ slot_mapping, char *__restrict__ k_cache, char *__restrict__ v_cache,
+    int64_t capacity, int64_t row_bytes, int32_t *err_count) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (int64_t)blockIdx.x * kCwWarps + (threadIdx.x >> 5);
+    const int64_t wstep = (int64_t)gridDim.x * kCwWarps;
+    for (int64_t i = warp0; i < num_tokens; i += wstep) {
+        const int64_t s = __ldg(slot_mapping + i);
+        if (s < 0) continue;
+        if (s >= capacity) {
+            if (lane == 0 && err_count) atomicAdd(err_count, 1);
+            continue;
+        }
+        const char *ks = k_new + i * src_stride_bytes;
+        const char *vs = v_new + i * src_stride_bytes;
+        char *kd = k_cache + s * row_bytes;
+        char *vd = v_cache + s * row_bytes;
+        for (int64_t base = (int64_t)lane * 16; base < row_bytes; base += 32 * 16 * kCwUnroll) {
+            uint4 kr[kCwUnroll], vr[kCwUnroll];
+#pragma unroll
+            for (int u = 0; u < kCwUnroll; ++u) {
+                const int64_t off = base + (int64_t)u * 32 * 16;
+                if (off < row_bytes) {
+                    kr[u] = __ldg(reinterpret_cast<const uint4 *>(ks + off));
+                    vr[u] = __ldg(reinterpret_cast<const uint4 *>(vs + off));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kCwUnroll; ++u) {
+                const int64_t off = base + (int64_t)u * 32 * 16;
+                if (off < row_bytes) {
+                    *reinterpret_cast<uint4 *>(kd + off) = kr[u];
+                    *reinterpret_cast<uint4 *>(vd + off) = vr[u];
+                }
+            }
+        }
+    }
+}
+
+// Element path for rows or strides that are not 16-byte multiples.
+template <typename E>
+__global__ void __launch_bounds__(kCwWarps * 32) cache_write_elem_kernel(
+    const E *__restrict__ k_new, const E *__restrict__ v_new, int64_t num_tokens, int64_t src_stride,
+    const int64_t *__restrict__ slot_mapping, E *__restrict__ k_cache, E *__restrict__ v_cache, int64_t capacity,
+    int64_t row, int32_t *err_count) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (int64_t)blockIdx.x * kCwWarps + (threadIdx.x >> 5);
+    const int64_t wstep = (int64_t)gridDim.x * kCwWarps;
+    for (int64_t i = warp0; i < num_tokens; i += wstep) {
+        const int64_t s = __ldg(slot_mapping + i);
+        if (s < 0) continue;
+        if (s >= capacity) {
+            if (lane == 0 && err_count) atomicAdd(err_count, 1);
+            continue;
+        }
+        for (int64_t e = lane; e < row; e += 32) {
+            k_cache[s * row + e] = k_new[i * src_stride + e];
+            v_cache[s * row + e] = v_new[i * src_stride + e];
+        }
+    }
+}
+
+}  // namespace bkv
+
+extern "C" int bkv_cache_write(const void *k_new, const void *v_new, int64_t num_tokens, int64_t new_token_stride,
+                               const int64_t *slot_mapping, void *k_cache, void *v_cache, int64_t total_blocks,
+                               int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int dtype,
+                               int32_t *err_count, bkv_stream_t stream) {
+    if (dtype != BKV_BF16 && dtype != BKV_F32) return BKV_ERR_UNSUPPORTED;
+    if (num_tokens < 0 || total_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return BKV_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (new_token_stride < row) return BKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return BKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return BKV_ERR_INVALID_ARG;
+    const int64_t eb = dtype == BKV_BF16 ? 2 : 4;
+    const int64_t capacity = total_blocks * block_size;
+    const int threads = bkv::kCwWarps * 32;
+    const unsigned grid = bkv::grid_for(num_tokens, bkv::kCwWarps, 16);
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool vec16 = (row * eb) % 16 == 0 && (new_token_stride * eb) % 16 == 0 && bkv::aligned(k_new, 16) &&
+                       bkv::aligned(v_new, 16) && bkv::aligned(k_cache, 16) && bkv::aligned(v_cache, 16);
+    if (vec16) {
+        bkv::cache_write_vec16_kernel<<<grid, threads, 0, st>>>(
+            (const char *)k_new, (const char *)v_new, num_tokens, new_token_stride * eb, slot_mapping,
+            (char *)k_cache, (char *)v_cache, capacity, row * eb, err_count);
+    } else if (eb == 2) {
+        bkv::cache_write_elem_kernel<uint16_t><<<grid, threads, 0, st>>>(
+            (const uint16_t *)k_new, (const uint16_t *)v_new, num_tokens, new_token_stride, slot_mapping,
+            (uint16_t *)k_cache, (uint16_t *)v_cache, capacity, row, err_count);
+    } else {
+        bkv::cache_write_elem_kernel<uint32_t><<<grid, threads, 0, st>>>(
+            (const uint32_t *)k_new, (const uint32_t *)v_new, num_tokens, new_token_stride, slot_mapping,
+            (uint32_t *)k_cache, (uint32_t *)v_cache, capacity, row, err_count);
+    }
+    return bkv::launch_status();
+}

@@ -1,0 +1,375 @@
+// bkv_decode.cu -- GQA paged decode attention: planner, the generic
+// CUDA-core partition kernel, the split-KV merge kernel and the ABI entry
+// points.
+//
+// "Padding and Batching with Block KV", Cache Masking: a query of request r
+// sees cached positions [0, cache_len) (mask_cache) and, among this step's
+// tokens, those the mask_active reading allows (causal by default, all-ones
+// on request).  Special Block and Slot Values: a null (0) or sentinel (-1)
+// table entry contributes nothing.  "Decode Context-Length Bucketing",
+// Problem: read only the ceil(cache_len / block_size) blocks a request needs.
+//
+// Work decomposition: a unit is (request, KV head, partition of `chunk`
+// logical positions).  Every query row of the KV head's GQA group (q_len *
+// G rows) is handled in the unit, so each K/V byte is read once.  A unit
+// writes an unnormalised partial (o, running max m, weight sum l) to the
+// workspace; the merge kernel combines a request's partitions with
+// log-sum-exp weights.  Partition boundaries depend only on logical
+// positions, so the result is independent of where blocks sit in memory.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "bkv_decode.cuh"
+
+namespace bkv {
+
+static constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+__device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Cache length of request r, clamped to the host bound (an excess is an error).
+__device__ __forceinline__ int32_t clamped_len(const DecodeArgs &a, int r, bool count) {
+    int32_t L = __ldg(a.ctx + r);
+    if (L > a.max_ctx) {
+        if (count && a.err) atomicAdd(a.err, 1);
+        L = a.max_ctx;
+    }
+    return L > 0 ? L : 0;
+}
+
+// ---------------------------------------------------------------------------
+// Generic partition kernel: any dtype, head_dim <= 256, any block size.
+// CTA = (unit = (request * H_kv + KV head) * n_chunks + partition, group of
+// up to QR query rows); four
+// warps stride over the partition's positions, lanes split head_dim, dot
+// products reduce with warp shuffles, each warp keeps its own online softmax
+// and the four are combined through shared memory at the end.
+// ---------------------------------------------------------------------------
+template <typename T, int DPL, int QR>
+__global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a) {
+    constexpr int NW = 4;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int rg = blockIdx.x / a.n_chunks;
+    const int c = blockIdx.x - rg * a.n_chunks;
+    const int r = rg / a.H_kv;
+    const int g = rg - r * a.H_kv;
+    const int i0 = blockIdx.y * QR;
+
+    const int32_t L = clamped_len(a, r, c == 0 && g == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+    const int32_t start = c * a.chunk;
+    if (start >= L) return;
+    const int32_t end = min(start + a.chunk, L);
+    const int nrows = min(QR, a.nq - i0);
+
+    const T *Q = static_cast<const T *>(a.q);
+    const T *K = static_cast<const T *>(a.k);
+    const T *V = static_cast<const T *>(a.v);
+
+    float q[QR][DPL];
+    int32_t lastv[QR];
+    int32_t jmax = -1;
+#pragma unroll
+    for (int i = 0; i < QR; ++i) {
+        if (i < nrows) {
+            const int row = i0 + i;
+            const int t = row / a.G;
+            const int h = g * a.G + (row - t * a.G);
+            const int64_t qb = (((int64_t)r * a.q_len + t) * a.H_q + h) * a.D;
+            lastv[i] = a.mask_mode == 0 ? L - a.q_len + t : L - 1;
+            jmax = max(jmax, lastv[i]);
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) {
+                const int d = e * 32 + lane;
+                q[i][e] = d < a.D ? to_f(Q[qb + d]) * a.scale_log2 : 0.f;
+            }
+        } else {
+            lastv[i] = -1;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) q[i][e] = 0.f;
+        }
+    }
+
+    float m[QR], l[QR], o[QR][DPL];
+#pragma unroll
+    for (int i = 0; i < QR; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
+    }
+
+    for (int32_t j = start + warp; j < end && j <= jmax; j += NW) {
+        const int32_t lb = j / a.bs;
+        const int32_t off = j - lb * a.bs;
+        const bool first = (j == start) || (off == 0);  // count a bad entry once per CTA
+        if (lb >= a.bt_cols) {
+            if (first && lane == 0 && a.err) atomicAdd(a.err, 1);
+            continue;
+        }
+        const int64_t b = __ldg(a.bt + (int64_t)r * a.bt_stride + lb);
+        if (b <= 0) continue;  // null block or sentinel: masked, never read
+        if (b >= a.total_blocks) {
+            if (first && lane == 0 && a.err) atomicAdd(a.err, 1);
+            continue;
+        }
+        const int64_t rowoff = ((b * a.bs + off) * a.H_kv + g) * a.D;
+        float kv[DPL];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) {
+            const int d = e * 32 + lane;
+            kv[e] = d < a.D ? to_f(K[rowoff + d]) : 0.f;
+        }
+        float s[QR];
+#pragma unroll
+        for (int i = 0; i < QR; ++i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc = fmaf(q[i][e], kv[e], acc);
+            s[i] = warp_sum(acc);
+        }
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) {
+            const int d = e * 32 + lane;
+            kv[e] = d < a.D ? to_f(V[rowoff + d]) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < QR; ++i) {
+            if (i < nrows && j <= lastv[i]) {
+                const float mn = fmaxf(m[i], s[i]);
+                const float corr = exp2f(m[i] - mn);
+                const float p = exp2f(s[i] - mn);
+                l[i] = fmaf(l[i], corr, p);
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[i][e] = fmaf(o[i][e], corr, p * kv[e]);
+                m[i] = mn;
+            }
+        }
+    }
+
+    // Combine the four warps' (m, l, o) and write the partition's partial.
+    __shared__ float sm_m[NW][QR], sm_l[NW][QR];
+    __shared__ float sm_o[NW][QR][32 * DPL];
+#pragma unroll
+    for (int i = 0; i < QR; ++i) {
+        if (lane == 0) {
+            sm_m[warp][i] = m[i];
+            sm_l[warp][i] = l[i];
+        }
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) sm_o[warp][i][e * 32 + lane] = o[i][e];
+    }
+    __syncthreads();
+    const int64_t unit = (int64_t)rg * a.n_chunks + c;
+    for (int idx = threadIdx.x; idx < nrows * a.D; idx += blockDim.x) {
+        const int i = idx / a.D;
+        const int d = idx - i * a.D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w][i]);
+        float acc = 0.f, lsum = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float f = exp2f(sm_m[w][i] - M);
+                acc = fmaf(f, sm_o[w][i][d], acc);
+                lsum = fmaf(f, sm_l[w][i], lsum);
+            }
+        }
+        const int64_t prow = unit * a.nq + i0 + i;
+        a.ws_o[prow * a.D + d] = acc;
+        if (d == 0) {
+            a.ws_ml[prow * 2 + 0] = M;
+            a.ws_ml[prow * 2 + 1] = lsum;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Merge: out = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the
+// request's partitions; 0 when no partition saw a visible key.  One warp per
+// output row (r, t, h).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int64_t rows = (int64_t)a.num_reqs * a.q_len * a.H_q;
+    if (row >= rows) return;
+    const int h = (int)(row % a.H_q);
+    const int64_t rt = row / a.H_q;
+    const int t = (int)(rt % a.q_len);
+    const int r = (int)(rt / a.q_len);
+    const int g = h / a.G;
+    const int i = t * a.G + (h - g * a.G);
+    const int32_t L = clamped_len(a, r, false);
+    const int nch = L > 0 ? (int)ceil_div<int32_t>(L, a.chunk) : 0;
+    const int64_t unit0 = ((int64_t)r * a.H_kv + g) * a.n_chunks;
+    T *out = static_cast<T *>(a.out) + row * a.D;
+
+    float M = -INFINITY;
+    for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.ws_ml[((unit0 + c) * a.nq + i) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (M == -INFINITY) {
+        for (int d = lane; d < a.D; d += 32) store_out(out + d, 0.f);
+        return;
+    }
+    float lsum = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+        const float *ml = a.ws_ml + ((unit0 + c) * a.nq + i) * 2;
+        lsum += exp2f(ml[0] - M) * ml[1];
+    }
+    lsum = warp_sum(lsum);
+    const float inv = 1.f / lsum;
+    for (int d = lane; d < a.D; d += 32) {
+        float acc = 0.f;
+        for (int c = 0; c < nch; ++c) {
+            const int64_t prow = (unit0 + c) * a.nq + i;
+            const float w = exp2f(a.ws_ml[prow * 2] - M);
+            acc = fmaf(w, a.ws_o[prow * a.D + d], acc);
+        }
+        store_out(out + d, acc * inv);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Planner
+// ---------------------------------------------------------------------------
+static int64_t gcd64(int64_t x, int64_t y) {
+    while (y) {
+        int64_t t = x % y;
+        x = y;
+        y = t;
+    }
+    return x;
+}
+
+bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t max_context_len, DecodePlan *plan) {
+    if (num_reqs <= 0 || q_len <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        max_context_len < 0 || num_q_heads % num_kv_heads != 0 || block_size > 65536)
+        return false;
+    // Partitions are whole 128-position tiles and whole blocks.
+    const int64_t align = (int64_t)block_size / gcd64(block_size, 128) * 128;
+    const int64_t units = (int64_t)num_reqs * num_kv_heads;
+    const int64_t sms = current_sm_count();
+    int64_t chunk = ceil_div<int64_t>(512, align) * align;
+    if (units * ceil_div<int64_t>(max_context_len, chunk) < 4 * sms) {
+        // Few, short units: split finer so the grid still fills the device.
+        const int64_t want = ceil_div<int64_t>((int64_t)max_context_len * units, 4 * sms);
+        chunk = ceil_div<int64_t>(want > 0 ? want : 1, align) * align;
+    }
+    if (chunk > (int64_t)1 << 30) return false;
+    const int64_t n_chunks = max_context_len > 0 ? ceil_div<int64_t>(max_context_len, chunk) : 1;
+    const int64_t nq = (int64_t)q_len * (num_q_heads / num_kv_heads);
+    if (units * n_chunks >= ((int64_t)1 << 31) || nq > 65535 * 8) return false;
+    plan->chunk = (int32_t)chunk;
+    plan->n_chunks = (int32_t)n_chunks;
+    plan->nq = (int32_t)nq;
+    const int64_t prows = units * n_chunks * nq;
+    const int64_t o_bytes = ceil_div<int64_t>(prows * head_dim * 4, 256) * 256;
+    plan->ws_bytes = (size_t)(o_bytes + prows * 2 * 4);
+    return true;
+}
+
+template <typename T, int DPL>
+static void launch_generic(const DecodeArgs &a, cudaStream_t st) {
+    constexpr int QR = 8;
+    dim3 grid(a.n_chunks * a.num_reqs * a.H_kv, ceil_div(a.nq, QR));
+    decode_generic_kernel<T, DPL, QR><<<grid, 128, 0, st>>>(a);
+}
+
+template <typename T>
+static void launch_generic_dpl(const DecodeArgs &a, cudaStream_t st) {
+    if (a.D <= 32) launch_generic<T, 1>(a, st);
+    else if (a.D <= 64) launch_generic<T, 2>(a, st);
+    else if (a.D <= 128) launch_generic<T, 4>(a, st);
+    else launch_generic<T, 8>(a, st);
+}
+
+}  // namespace bkv
+
+extern "C" size_t bkv_paged_decode_workspace_size(int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
+                                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                                  int32_t max_context_len) {
+    bkv::DecodePlan p;
+    if (!bkv::make_decode_plan(num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                               &p))
+        return 0;
+    return p.ws_bytes;
+}
+
+extern "C" int bkv_paged_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                                int64_t bt_stride, int32_t bt_cols, const int32_t *context_lens,
+                                int32_t max_context_len, int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t total_blocks,
+                                float softmax_scale, int mask_mode, int dtype, void *out, void *workspace,
+                                size_t workspace_bytes, int32_t *err_count, bkv_stream_t stream) {
+    if (dtype != BKV_BF16 && dtype != BKV_F32) return BKV_ERR_UNSUPPORTED;
+    if (head_dim > 256 || head_dim % 2 != 0) return BKV_ERR_UNSUPPORTED;
+    if (mask_mode != BKV_MASK_CAUSAL && mask_mode != BKV_MASK_ALL) return BKV_ERR_INVALID_ARG;
+    if (bt_cols < 0 || bt_stride < bt_cols || total_blocks < 0) return BKV_ERR_INVALID_ARG;
+    bkv::DecodePlan plan;
+    if (!bkv::make_decode_plan(num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                               &plan))
+        return BKV_ERR_INVALID_ARG;
+    if (!q || !out || !context_lens || (bt_cols > 0 && !block_table)) return BKV_ERR_INVALID_ARG;
+    if (max_context_len > 0 && (!k_cache || !v_cache)) return BKV_ERR_INVALID_ARG;
+    if (workspace_bytes < plan.ws_bytes || !workspace || !bkv::aligned(workspace, 16)) return BKV_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / sqrtf((float)head_dim);
+
+    bkv::DecodeArgs a;
+    a.q = q;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.bt = block_table;
+    a.bt_stride = bt_stride;
+    a.bt_cols = bt_cols;
+    a.ctx = context_lens;
+    a.max_ctx = max_context_len;
+    a.num_reqs = num_reqs;
+    a.q_len = q_len;
+    a.H_q = num_q_heads;
+    a.H_kv = num_kv_heads;
+    a.D = head_dim;
+    a.bs = block_size;
+    a.total_blocks = total_blocks;
+    a.scale_log2 = softmax_scale * bkv::kLog2e;
+    a.mask_mode = mask_mode;
+    a.chunk = plan.chunk;
+    a.n_chunks = plan.n_chunks;
+    a.G = num_q_heads / num_kv_heads;
+    a.nq = plan.nq;
+    const int64_t prows = (int64_t)num_reqs * num_kv_heads * plan.n_chunks * plan.nq;
+    a.ws_o = static_cast<float *>(workspace);
+    a.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                        bkv::ceil_div<int64_t>(prows * head_dim * 4, 256) * 256);
+    a.out = out;
+    a.err = err_count;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    int rc = BKV_ERR_UNSUPPORTED;
+    if (bkv::decode_tc_supported(a)) rc = bkv::launch_decode_tc(a, st);
+    if (rc == BKV_ERR_UNSUPPORTED) {
+        if (dtype == BKV_BF16) bkv::launch_generic_dpl<__nv_bfloat16>(a, st);
+        else bkv::launch_generic_dpl<float>(a, st);
+        rc = bkv::launch_status();
+    }
+    if (rc != BKV_OK) return rc;
+
+    const int64_t rows = (int64_t)num_reqs * q_len * num_q_heads;
+    const unsigned mgrid = (unsigned)bkv::ceil_div<int64_t>(rows, 4);
+    if (dtype == BKV_BF16) bkv::decode_merge_kernel<__nv_bfloat16><<<mgrid, 128, 0, st>>>(a);
+    else bkv::decode_merge_kernel<float><<<mgrid, 128, 0, st>>>(a);
+    return bkv::launch_status();
+}

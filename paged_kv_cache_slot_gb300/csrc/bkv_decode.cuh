@@ -1,0 +1,49 @@
+// bkv_decode.cuh -- shared declarations of the paged decode kernels.
+#pragma once
+
+#include "bkv_internal.cuh"
+
+namespace bkv {
+
+// Everything a decode launch needs; passed by value to every kernel.
+struct DecodeArgs {
+    const void *q;
+    const void *k;
+    const void *v;
+    const int32_t *bt;
+    int64_t bt_stride;
+    int32_t bt_cols;
+    const int32_t *ctx;
+    int32_t max_ctx;
+    int32_t num_reqs, q_len, H_q, H_kv, D, bs;
+    int64_t total_blocks;
+    float scale_log2;  // softmax_scale * log2(e): scores are kept in base 2
+    int mask_mode;
+    int32_t chunk;     // tokens per split-KV partition (multiple of the tile and of bs)
+    int32_t n_chunks;  // partitions per request at max_ctx
+    int32_t G;         // query heads per KV head
+    int32_t nq;        // query rows per KV head: q_len * G, row i = t * G + (h % G)
+    float *ws_o;       // [num_reqs * H_kv * n_chunks][nq][D] unnormalised partial outputs
+    float *ws_ml;      // [num_reqs * H_kv * n_chunks][nq][2]  (running max in base 2, sum of weights)
+    void *out;
+    int32_t *err;
+};
+
+// Split of each request's context into partitions; identical for the
+// workspace query and the decode call.
+struct DecodePlan {
+    int32_t chunk;
+    int32_t n_chunks;
+    int32_t nq;
+    size_t ws_bytes;
+};
+
+bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int32_t max_context_len, DecodePlan *plan);
+
+// tcgen05 / TMA partition kernel for bf16, head_dim 128 (bkv_decode_tc.cu).
+// Returns BKV_ERR_UNSUPPORTED when the shape is outside what it handles.
+int launch_decode_tc(const DecodeArgs &a, cudaStream_t stream);
+bool decode_tc_supported(const DecodeArgs &a);
+
+}  // namespace bkv

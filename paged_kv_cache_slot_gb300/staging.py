@@ -1,0 +1,131 @@
+"""Device staging of a seeded workload for the GPU tests and the benchmark.
+
+Uploads a :class:`~paged_kv_cache_slot_gb300.workloads.Workload` and fills
+the paged caches with every request's prior tokens THROUGH THE LIBRARY
+(slot mapping + cache write kernels), exactly as a serving step would have
+written them.  Caches start as NaN so that any read of a position that was
+never written shows up in the output.
+
+``DeviceWorkload.step()`` is one pass of the hot path over one batch:
+block expansion (manager -> kernel ids), slot mapping of this step's tokens,
+the K/V scatter and the paged decode (partition + merge kernels).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import bkv
+from .workloads import Workload
+
+PRIOR_FILL_TOKENS = 1 << 16  # tokens uploaded per prior-fill batch
+
+
+def _t(a: np.ndarray, device, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(device)
+
+
+class DeviceWorkload:
+    def __init__(self, w: Workload, device="cuda", background: str = "nan", fill_prior: bool = True):
+        self.w = w
+        self.device = torch.device(device)
+        dev = self.device
+        self.tdtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        kshape = (w.total_kernel_blocks, w.kernel_block_size, w.num_kv_heads, w.head_dim)
+        fill = float("nan") if background == "nan" else 0.0
+        self.k_cache = torch.full(kshape, fill, dtype=self.tdtype, device=dev)
+        self.v_cache = torch.full(kshape, fill, dtype=self.tdtype, device=dev)
+        self.mgr_table = _t(w.block_table, dev)
+        self.kernel_table = torch.empty((w.num_rows, w.width * w.blocks_per_kv_block), dtype=torch.int32, device=dev)
+        bkv.bkv_map_to_kernel_blocks(self.mgr_table, w.block_size, w.kernel_block_size, self.kernel_table)
+        self.context_lens = _t(w.context_lens, dev)
+        self.max_context_len = int(w.context_lens.max()) if w.num_rows else 0
+        req, pos = w.step_tokens()
+        self.req_indices = _t(req, dev)
+        self.positions = _t(pos, dev)
+        self.slot_mapping = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
+        kn, vn = w.step_kv()
+        self.k_new = _t(kn, dev, self.tdtype if w.dtype == "bf16" else None)
+        self.v_new = _t(vn, dev, self.tdtype if w.dtype == "bf16" else None)
+        self.err_count = torch.zeros(1, dtype=torch.int32, device=dev)
+        if w.has_decode:
+            self.q = _t(w.q(), dev, self.tdtype if w.dtype == "bf16" else None)
+            self.out = torch.empty_like(self.q)
+            self.workspace = bkv.alloc_workspace(w.num_rows, w.q_len, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                                 w.kernel_block_size, self.max_context_len, device=dev)
+        if fill_prior:
+            self.fill_prior()
+
+    # -- prior context ------------------------------------------------------
+    def fill_prior(self, rows=None):
+        """Write prior tokens of ``rows`` (default all) through slot mapping + cache write."""
+        w, dev = self.w, self.device
+        rows = list(range(w.num_rows)) if rows is None else list(rows)
+        batch: list[int] = []
+        ntok = 0
+        for r in rows + [None]:
+            if r is not None and int(w.prior_lens[r]) == 0:
+                continue
+            if r is None or (batch and ntok + int(w.prior_lens[r]) > PRIOR_FILL_TOKENS):
+                if batch:
+                    self._write_rows(batch)
+                batch, ntok = [], 0
+            if r is not None:
+                batch.append(r)
+                ntok += int(w.prior_lens[r])
+        torch.cuda.synchronize(dev)
+
+    def _write_rows(self, rows):
+        w, dev = self.w, self.device
+        req, pos = w.prior_tokens(rows)
+        ks, vs = zip(*(w.kv_rows(r, 0, int(w.prior_lens[r])) for r in rows))
+        k = np.concatenate(ks)
+        v = np.concatenate(vs)
+        cast = self.tdtype if w.dtype == "bf16" else None
+        kt, vt = _t(k, dev, cast), _t(v, dev, cast)
+        slots = torch.empty(len(pos), dtype=torch.int64, device=dev)
+        bkv.bkv_compute_slot_mapping(self.kernel_table, _t(req, dev), _t(pos, dev), w.kernel_block_size, slots,
+                                     err_count=self.err_count)
+        bkv.bkv_cache_write(kt, vt, slots, self.k_cache, self.v_cache, err_count=self.err_count)
+
+    # -- the hot path ---------------------------------------------------------
+    def expand_blocks(self, stream=None):
+        w = self.w
+        bkv.bkv_map_to_kernel_blocks(self.mgr_table, w.block_size, w.kernel_block_size, self.kernel_table,
+                                     stream=stream)
+
+    def write_step(self, stream=None):
+        w = self.w
+        bkv.bkv_compute_slot_mapping(self.kernel_table, self.req_indices, self.positions, w.kernel_block_size,
+                                     self.slot_mapping, num_tokens=w.num_tokens, err_count=self.err_count,
+                                     stream=stream)
+        bkv.bkv_cache_write(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
+                            num_tokens=w.num_tokens, err_count=self.err_count, stream=stream)
+
+    def decode(self, stream=None, out=None, table=None, mask_mode=bkv.BKV_MASK_CAUSAL):
+        out = self.out if out is None else out
+        table = self.kernel_table if table is None else table
+        bkv.bkv_paged_decode(self.q, self.k_cache, self.v_cache, table, self.context_lens, self.max_context_len,
+                             out, self.workspace, mask_mode=mask_mode, err_count=self.err_count, stream=stream)
+        return out
+
+    def step(self, stream=None):
+        """One pass of the whole path: a2 -> a1 -> a3 -> a4 + a5."""
+        self.expand_blocks(stream)
+        self.write_step(stream)
+        if self.w.has_decode:
+            self.decode(stream)
+
+    # -- byte accounting (algorithmic, token granularity) ---------------------
+    def decode_kv_bytes(self) -> int:
+        """K and V bytes the decode must read: cache_len rows per request and KV head."""
+        w = self.w
+        return int(w.context_lens.astype(np.int64).sum()) * 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+
+    def write_bytes(self) -> int:
+        """Cache-write traffic: new K/V rows read + written, plus the slot ids."""
+        w = self.w
+        return w.num_tokens * (4 * w.num_kv_heads * w.head_dim * w.elem_bytes + 8)

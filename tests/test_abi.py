@@ -1,0 +1,113 @@
+"""CPU checks of the C ABI: libbkv.so builds, loads, exports every entry point
+include/bkv.h declares, and rejects bad arguments on the host (before any
+CUDA call) with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_slot_gb300 import bkv
+from paged_kv_cache_slot_gb300 import build as bkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bkv_build.build()
+    return bkv.load()
+
+
+def _declared():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(bkv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("bkv_compute_slot_mapping", "bkv_map_to_kernel_blocks", "bkv_cache_write", "bkv_paged_decode",
+              "bkv_paged_decode_workspace_size"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    assert lib.bkv_status_string(0) == b"ok"
+    assert b"invalid" in lib.bkv_status_string(1)
+    assert lib.bkv_version().startswith(b"bkv ")
+
+
+NULL = None
+
+
+def test_slot_mapping_rejects_bad_arguments(lib):
+    f = lib.bkv_compute_slot_mapping
+    # block_size <= 0
+    assert f(NULL, 1, 4, 4, NULL, NULL, 1, 1, 0, NULL, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
+    # max_num_tokens < num_tokens
+    assert f(NULL, 1, 4, 4, NULL, NULL, 5, 4, 16, NULL, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
+    # bt_stride < bt_cols
+    assert f(NULL, 1, 2, 4, NULL, NULL, 1, 1, 16, NULL, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
+    # null output / inputs
+    assert f(NULL, 1, 4, 4, NULL, NULL, 1, 1, 16, NULL, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
+    # nothing to do is fine and launches nothing
+    assert f(NULL, 0, 0, 0, NULL, NULL, 0, 0, 16, NULL, NULL, NULL) == bkv.BKV_OK
+
+
+def test_block_expansion_rejects_indivisible(lib):
+    f = lib.bkv_map_to_kernel_blocks
+    assert f(NULL, 2, 4, 4, 32, 12, NULL, 16, NULL) == bkv.BKV_ERR_INVALID_ARG
+    assert f(NULL, 2, 4, 4, 32, 0, NULL, 16, NULL) == bkv.BKV_ERR_INVALID_ARG
+    assert f(NULL, 2, 4, 4, 32, 16, NULL, 7, NULL) == bkv.BKV_ERR_INVALID_ARG   # kernel_stride < 4 * 2
+    assert f(NULL, 0, 4, 4, 32, 16, NULL, 8, NULL) == bkv.BKV_OK                 # empty
+
+
+def test_cache_write_rejects_bad_arguments(lib):
+    f = lib.bkv_cache_write
+    assert f(NULL, NULL, 1, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 7, NULL, NULL) == bkv.BKV_ERR_UNSUPPORTED
+    assert f(NULL, NULL, 1, 1023, NULL, NULL, NULL, 4, 16, 8, 128, 0, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
+    assert f(NULL, NULL, 1, 1024, NULL, NULL, NULL, 4, 0, 8, 128, 0, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
+    assert f(NULL, NULL, 1, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 0, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
+    assert f(NULL, NULL, 0, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 0, NULL, NULL) == bkv.BKV_OK
+
+
+def test_paged_decode_rejects_bad_arguments(lib):
+    f = lib.bkv_paged_decode
+    base = dict(q=NULL, k=NULL, v=NULL, bt=NULL, bt_stride=4, bt_cols=4, ctx=NULL, max_ctx=16, num_reqs=2, q_len=1,
+                hq=32, hkv=8, d=128, bs=16, tb=8, scale=0.0, mask=0, dtype=0, out=NULL, ws=NULL, wsb=0, err=NULL,
+                stream=NULL)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return f(*a.values())
+
+    assert call(dtype=5) == bkv.BKV_ERR_UNSUPPORTED
+    assert call(d=512) == bkv.BKV_ERR_UNSUPPORTED
+    assert call(mask=2) == bkv.BKV_ERR_INVALID_ARG
+    assert call(bt_stride=2) == bkv.BKV_ERR_INVALID_ARG
+    assert call(hq=30) == bkv.BKV_ERR_INVALID_ARG          # 30 % 8 != 0
+    assert call(num_reqs=0) == bkv.BKV_ERR_INVALID_ARG
+    assert call() == bkv.BKV_ERR_INVALID_ARG                # null pointers / no workspace
+
+
+def test_workspace_size_is_zero_for_invalid_sizes(lib):
+    assert lib.bkv_paged_decode_workspace_size(2, 1, 30, 8, 128, 16, 100) == 0
+    assert lib.bkv_paged_decode_workspace_size(0, 1, 32, 8, 128, 16, 100) == 0
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(bkv, "_lib", None)
+    monkeypatch.setattr(bkv, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        bkv.load()

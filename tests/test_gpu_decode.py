@@ -1,0 +1,237 @@
+"""GPU parity for the paged decode (partition + merge kernels) against the fp64
+oracle, plus bitwise invariants of the GPU path itself.
+
+Tolerance: max abs error <= 1e-2 for bf16 inputs/outputs (fp32 accumulation
+against the fp64 oracle) and <= 1e-5 for fp32, the bars the benchmark
+configuration states.  Caches start as NaN everywhere, so a read of any
+position that was never written (block 0, slack blocks, the tail of a
+request's last block) poisons the output and fails the comparison.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.cases import fill_oracle_cache
+from paged_kv_cache_slot_gb300 import bkv
+from paged_kv_cache_slot_gb300 import workloads as wl
+from paged_kv_cache_slot_gb300.staging import DeviceWorkload
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 1e-2, "f32": 1e-5}
+
+
+def _f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _oracle_rows(w, rows, mask_mode=0, table=None):
+    kc, vc, ktable = fill_oracle_cache(w, rows=rows)
+    table = ktable if table is None else table
+    q = w.q()
+    out = {}
+    for r in rows:
+        out[r], _ = oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens, mask_mode=mask_mode)
+    return out
+
+
+def _check(dw, rows, mask_mode=0, label=""):
+    w = dw.w
+    got = _f64(dw.decode(mask_mode=mask_mode))
+    torch.cuda.synchronize()
+    want = _oracle_rows(w, rows, mask_mode)
+    worst = 0.0
+    for r in rows:
+        assert np.isfinite(got[r]).all(), f"{label} row {r}: non-finite output"
+        worst = max(worst, float(np.abs(got[r] - want[r]).max()))
+    assert worst <= TOL[w.dtype], f"{label}: max abs err {worst:.3e} > {TOL[w.dtype]}"
+    return got, worst
+
+
+def _custom(q_len, H_q, H_kv, D, bs, prior, dtype="bf16", width=None, seed=4242, null_rows=(), sharp=False,
+            holes=()):
+    """A small seeded workload spanning several tiles and partitions, with ragged tails."""
+    prior = np.array(prior, np.int64)
+    nr = len(prior)
+    new = np.full(nr, q_len, np.int64)
+    for r in null_rows:
+        prior[r] = 0
+        new[r] = 0
+    need = -(-(prior + new) // bs)
+    width = int(need.max()) + 2 if width is None else width
+    rng = np.random.default_rng(seed)
+    total = 1 + int(need.sum()) + 7
+    ids = rng.permutation(np.arange(1, total))[: int(need.sum())]
+    table = np.full((nr, width), -1, np.int32)
+    k = 0
+    for r, n in enumerate(need):
+        table[r, :n] = ids[k:k + n]
+        k += int(n)
+    for r, lb in holes:  # null entries inside a request's range: masked, never read
+        table[r, lb] = 0
+    s = 1.0 / np.sqrt(D)
+    return wl.Workload("custom", seed, dtype, nr, nr - len(null_rows), q_len, H_q, H_kv, D, bs, bs, prior, new,
+                       table, total, max_num_tokens=int(new.sum()) + 3, qk_scale=1.0 if sharp else s, v_scale=s)
+
+
+@pytest.mark.parametrize("reading", ["record", "other"])
+@pytest.mark.parametrize("mask_mode", [0, 1])
+def test_tiny_fp32(reading, mask_mode):
+    w = wl.make("tiny", tiny_reading=reading)
+    dw = DeviceWorkload(w)
+    dw.write_step()
+    _check(dw, range(w.num_rows), mask_mode, f"tiny/{reading}/{mask_mode}")
+
+
+SMALL = [
+    # q_len, H_q, H_kv, D, bs, prior, dtype
+    (1, 32, 8, 128, 64, (511, 1, 1300, 64, 2047, 129), "bf16"),
+    (4, 32, 8, 128, 16, (0, 3, 700, 1025, 17, 250), "bf16"),
+    (1, 64, 8, 128, 64, (3000, 70, 1), "bf16"),
+    (2, 8, 8, 128, 32, (100, 600, 33), "bf16"),
+    (3, 16, 2, 64, 16, (90, 1100, 5, 400), "bf16"),
+    (1, 4, 1, 256, 8, (300, 17), "bf16"),
+    (4, 8, 2, 32, 4, (50, 3, 260), "f32"),
+    (1, 2, 1, 8, 4, (1, 2, 3, 9), "f32"),
+    (5, 40, 8, 128, 64, (200, 1500), "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"q{c[0]}_h{c[1]}x{c[2]}_d{c[3]}_bs{c[4]}_{c[6]}")
+@pytest.mark.parametrize("mask_mode", [0, 1])
+def test_small_shapes(case, mask_mode):
+    q_len, H_q, H_kv, D, bs, prior, dtype = case
+    w = _custom(q_len, H_q, H_kv, D, bs, list(prior) + [0], dtype, null_rows=(len(prior),),
+                holes=((0, 1),) if prior[0] >= 2 * bs else ())
+    dw = DeviceWorkload(w)
+    dw.write_step()
+    got, _ = _check(dw, range(w.num_rows), mask_mode, f"{case}")
+    assert (got[w.num_rows - 1] == 0).all()
+
+
+@pytest.mark.parametrize("sharp", [False, True])
+def test_llama3_decode_all_rows(sharp):
+    w = wl.make("llama3_decode", sharp=sharp)
+    dw = DeviceWorkload(w)
+    dw.step()
+    _check(dw, range(w.num_rows), 0, f"llama3/sharp={sharp}")
+    assert int(dw.err_count.item()) == 0
+
+
+def test_long_context_sampled_rows():
+    w = wl.make("long_context", sharp=True)
+    dw = DeviceWorkload(w)
+    dw.step()
+    lens = w.context_lens
+    rows = sorted({int(np.argmax(lens)), int(np.argmin(lens)), 0, 5})
+    _check(dw, rows, 0, "long_context")
+
+
+def test_hybrid_spec_sampled_rows_and_null_rows():
+    w = wl.make("hybrid_spec", sharp=True)
+    dw = DeviceWorkload(w)
+    dw.step()
+    lens = w.context_lens
+    real = lens[: w.num_real]
+    rows = sorted({int(np.argmax(real)), int(np.argmin(real)), 1, 17, 100, 255, 256, 319})
+    got, _ = _check(dw, rows, 0, "hybrid")
+    assert (got[w.num_real:] == 0).all()          # padded NULL rows
+    assert int(dw.err_count.item()) == 0
+
+
+def _filled(w):
+    dw = DeviceWorkload(w)
+    dw.write_step()
+    torch.cuda.synchronize()
+    return dw
+
+
+def test_block_permutation_invariance_bitwise():
+    w = _custom(4, 32, 8, 128, 16, (900, 40, 1700, 333), "bf16", sharp=True)
+    dw = _filled(w)
+    base = dw.decode().clone()
+    tb = dw.k_cache.shape[0]
+    g = torch.Generator().manual_seed(8)
+    perm = torch.cat([torch.zeros(1, dtype=torch.int64), torch.randperm(tb - 1, generator=g) + 1]).cuda()
+    kc2, vc2 = torch.empty_like(dw.k_cache), torch.empty_like(dw.v_cache)
+    kc2[perm] = dw.k_cache
+    vc2[perm] = dw.v_cache
+    t = dw.kernel_table.long()
+    t2 = torch.where(t > 0, perm[t.clamp(min=0)], t).int()
+    dw.k_cache, dw.v_cache = kc2, vc2
+    moved = dw.decode(out=torch.empty_like(base), table=t2)
+    torch.cuda.synchronize()
+    assert torch.equal(moved.view(torch.int16), base.view(torch.int16))
+
+
+def test_trim_and_garbage_past_range_and_zero_vs_minus_one_bitwise():
+    w = _custom(1, 32, 8, 128, 64, (1000, 64, 3000, 5), "bf16", width=80, sharp=True, holes=((2, 3),))
+    dw = _filled(w)
+    base = dw.decode().clone()
+    n_max = int(-(-w.context_lens.max() // w.kernel_block_size))
+    trimmed = dw.kernel_table[:, :n_max].contiguous()
+    a = dw.decode(out=torch.empty_like(base), table=trimmed)
+    garbage = dw.kernel_table.clone()
+    for r in range(w.num_rows):
+        n = int(-(-int(w.context_lens[r]) // w.kernel_block_size))
+        garbage[r, n:] = 10**7
+    b = dw.decode(out=torch.empty_like(base), table=garbage)
+    zero = dw.kernel_table.clone()
+    zero[2, 3] = 0          # the hole as upstream 0 instead of -1
+    c = dw.decode(out=torch.empty_like(base), table=zero)
+    torch.cuda.synchronize()
+    for x in (a, b, c):
+        assert torch.equal(x.view(torch.int16), base.view(torch.int16))
+    assert int(dw.err_count.item()) == 0
+
+
+def test_out_of_range_block_id_is_masked_and_counted():
+    w = _custom(1, 16, 4, 128, 16, (300, 90), "bf16")
+    dw = _filled(w)
+    bad = dw.kernel_table.clone()
+    bad[0, 2] = dw.k_cache.shape[0] + 5
+    dw.err_count.zero_()
+    got = _f64(dw.decode(table=bad))
+    torch.cuda.synchronize()
+    assert int(dw.err_count.item()) > 0
+    tab = w.block_table.copy()
+    tab[0, 2] = dw.k_cache.shape[0] + 5
+    want = _oracle_rows(w, [0, 1], table=tab)
+    for r in (0, 1):
+        assert np.abs(got[r] - want[r]).max() <= 1e-2
+
+
+def test_context_len_above_host_bound_is_clamped_and_counted():
+    w = _custom(1, 8, 8, 128, 16, (100, 50), "bf16")
+    dw = _filled(w)
+    dw.err_count.zero_()
+    dw.max_context_len = 80          # below request 0's cache length of 101
+    ws = bkv.alloc_workspace(w.num_rows, 1, 8, 8, 128, 16, 80)
+    dw.workspace = ws
+    got = _f64(dw.decode())
+    torch.cuda.synchronize()
+    assert int(dw.err_count.item()) > 0
+    assert np.isfinite(got).all()
+
+
+def test_workspace_too_small_is_rejected():
+    w = _custom(1, 8, 8, 128, 16, (100, 50), "bf16")
+    dw = _filled(w)
+    dw.workspace = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(bkv.BkvError) as ei:
+        dw.decode()
+    assert ei.value.status == bkv.BKV_ERR_INVALID_ARG
+
+
+def test_repeated_steps_are_deterministic():
+    w = wl.make("llama3_decode")
+    dw = DeviceWorkload(w)
+    dw.step()
+    a = dw.out.clone()
+    for _ in range(3):
+        dw.step()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), dw.out.view(torch.int16))

@@ -20,7 +20,7 @@ import torch
 
 import oracle
 from paged_kv_cache_slot_gb300 import workloads as wl
-from oracle_cases import fill_oracle_cache, nan_cache
+from oracle.cases import fill_oracle_cache, nan_cache
 
 F64 = torch.float64
 
