@@ -346,6 +346,7 @@ extern "C" int bkv_paged_decode(const void *q, const void *k_cache, const void *
     a.total_blocks = total_blocks;
     a.scale_log2 = softmax_scale * bkv::kLog2e;
     a.mask_mode = mask_mode;
+    a.dtype = dtype;
     a.chunk = plan.chunk;
     a.n_chunks = plan.n_chunks;
     a.G = num_q_heads / num_kv_heads;

@@ -19,6 +19,7 @@ struct DecodeArgs {
     int64_t total_blocks;
     float scale_log2;  // softmax_scale * log2(e): scores are kept in base 2
     int mask_mode;
+    int dtype;         // BKV_BF16 or BKV_F32 (q, caches and out share it)
     int32_t chunk;     // tokens per split-KV partition (multiple of the tile and of bs)
     int32_t n_chunks;  // partitions per request at max_ctx
     int32_t G;         // query heads per KV head

@@ -1,12 +1,737 @@
-// bkv_decode_tc.cu -- tensor-core (tcgen05) partition kernel for the paged
-// decode.  Placeholder until the kernel lands: reports every shape as
-// unsupported so the generic kernel runs.
+// bkv_decode_tc.cu -- tensor-core (tcgen05 + TMA) partition kernel of the
+// paged decode, bf16, head_dim 128, up to 16 query rows per KV head.
+//
+// Operation ("Padding and Batching with Block KV", Cache Masking; Special
+// Block and Slot Values): for one unit = (request r, KV head g, partition
+// of `chunk` logical positions) compute, for every query row n = t * G + hh
+// of the GQA group, the online-softmax partial (o, m, l) over the visible
+// positions of the partition.  The merge kernel in bkv_decode.cu combines
+// partitions.
+//
+// Design (sm_103a):
+// * Persistent CTAs (one per SM, ~210 KB of shared memory), units dealt
+//   round-robin.  Warp 0 is the TMA producer, warp 1 issues tcgen05.mma from
+//   one thread and owns the TMEM allocation, warps 2..5 (128 threads) run the
+//   softmax and the rescaling of the output.
+// * A tile is 128 logical positions.  The producer gathers the tile's K and
+//   V rows of KV head g through the block table with 3-D TMA loads
+//   (cp.async.bulk.tensor; map over (head_dim, H_kv, total_blocks *
+//   block_size), box = 64 x 1 x min(block_size, 128) rows, 128-byte
+//   swizzle), one load per block segment and head_dim half, into a 3-stage
+//   ring of 64 KB stages.  Null (<= 0) and out-of-range table entries are
+//   not loaded at all, and blocks past the request's length are never
+//   touched, so traffic is the ceil(len / block_size) blocks actually needed.
+// * S^T[128 x 16] = K_tile[128 x 128] . Q^T (M = positions, N = query rows
+//   padded to 16, K = head_dim), fp32 in TMEM.  Each softmax thread owns one
+//   position (one TMEM lane): masks by select, reduces the tile max per query
+//   row across the 128 threads, exponentiates in base 2, keeps its partial
+//   row sums, and writes P (bf16) to shared memory in the K-major layout.
+// * O^T[128 x 16] = V_tile^T . P^T (M = head_dim, V read MN-major straight
+//   from the TMA tile, K = positions).  Each softmax thread owns one head_dim
+//   row of O^T and accumulates o = o * 2^(m_old - m_new) + O_tile in
+//   registers, one tile behind the softmax so the MMA overlaps it.
+// * V rows that were loaded but lie past the request's end are zeroed in
+//   shared memory before the P.V MMA, so unwritten cache memory (which may
+//   hold NaN) never reaches the output; K rows there are masked by select.
+// * Every wait is bounded: after ~2 s a wait gives up, the CTA records an
+//   error in *err_count (+ 1 << 24), lets copies in flight land, frees its
+//   TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "bkv_decode.cuh"
 
 namespace bkv {
+namespace tc {
 
-bool decode_tc_supported(const DecodeArgs &) { return false; }
+constexpr int kTile = 128;            // positions per tile
+constexpr int kD = 128;               // head_dim handled
+constexpr int kN = 16;                // query rows per MMA (padded)
+constexpr int kStages = 3;
+constexpr int kHalfBytes = kTile * 128;          // 128 rows x 64 bf16 (128 B): one head_dim half
+constexpr int kTileBytes = 2 * kHalfBytes;       // K or V tile: 32 KB
+constexpr int kStageBytes = 2 * kTileBytes;      // K + V: 64 KB
+constexpr int kQBytes = 2 * kN * 128;            // 16 rows x 128 B x 2 halves: 4 KB
+constexpr int kPBytes = 2 * kN * 128;            // 16 rows x 128 positions (2 x 64) bf16: 4 KB
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 64;                    // S x2 (16 cols each) + O x2
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr int kTimeoutErr = 1 << 24;
 
-int launch_decode_tc(const DecodeArgs &, cudaStream_t) { return BKV_ERR_UNSUPPORTED; }
+// Shared-memory layout (offsets from a 1024-aligned base).
+constexpr int kOffStages = 0;
+constexpr int kOffQ = kOffStages + kStages * kStageBytes;
+constexpr int kOffP = kOffQ + 2 * kQBytes;
+constexpr int kOffMask = kOffP + 2 * kPBytes;             // kStages x 4 words
+constexpr int kOffRedMax = kOffMask + kStages * 16;       // 2 x 16 x 4 floats
+constexpr int kOffRedSum = kOffRedMax + 2 * kN * 4 * 4;   // 16 x 4 floats
+constexpr int kOffBar = kOffRedSum + kN * 4 * 4;          // barriers (8 B each)
+constexpr int kNumBars = 2 * kStages + 2 * 5 + 1;
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+constexpr int kSmemUsed = kOffAbort + 4;
+constexpr int kSmemBytes = kSmemUsed + 1024;              // slack for 1024 alignment
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on a phase parity; false on timeout or when another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Warp-uniform bounded wait: every lane observes the phase itself (acquire),
+// and the give-up decision is taken by lane 0 for the whole warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const unsigned full = 0xffffffffu;
+    if (__all_sync(full, mbar_try_wait(bar, parity))) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (__all_sync(full, mbar_try_wait(bar, parity))) return true;
+        int stop = 0;
+        if ((threadIdx.x & 31) == 0) {
+            stop = *abort_flag;
+            if (!stop && global_ns() - t0 > kTimeoutNs) {
+                *abort_flag = 1;
+                stop = 1;
+            }
+        }
+        if (__shfl_sync(full, stop, 0)) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+        "[%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: 128-byte swizzle, version 1 (sm_100 family).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+
+// ---------------------------------------------------------------------------
+// The static schedule every role walks: unit u -> (r, g, c) and its tiles.
+// ---------------------------------------------------------------------------
+struct Unit {
+    int r, g, c;
+    int32_t L, start, cend, ntiles;
+};
+
+__device__ __forceinline__ bool unit_at(const DecodeArgs &a, int64_t u, Unit &x) {
+    const int64_t rg = u / a.n_chunks;
+    x.c = (int)(u - rg * a.n_chunks);
+    x.r = (int)(rg / a.H_kv);
+    x.g = (int)(rg - (int64_t)x.r * a.H_kv);
+    int32_t L = __ldg(a.ctx + x.r);
+    if (L > a.max_ctx) L = a.max_ctx;
+    if (L < 0) L = 0;
+    x.L = L;
+    x.start = x.c * a.chunk;
+    if (x.start >= L) return false;
+    x.cend = min(x.start + a.chunk, L);
+    x.ntiles = (x.cend - x.start + kTile - 1) / kTile;
+    return true;
+}
+
+// Transposed butterfly over a warp: on return lanes 2k and 2k+1 hold the
+// reduction of v[k] over all 32 lanes (k = 0..15).
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
+    auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
+    float a8[8];
+    {
+        const bool hi = lane & 16;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float send = hi ? v[i] : v[i + 8];
+            const float keep = hi ? v[i + 8] : v[i];
+            a8[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+        }
+    }
+    float a4[4];
+    {
+        const bool hi = lane & 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float send = hi ? a8[i] : a8[i + 4];
+            const float keep = hi ? a8[i + 4] : a8[i];
+            a4[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+        }
+    }
+    float a2[2];
+    {
+        const bool hi = lane & 4;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float send = hi ? a4[i] : a4[i + 2];
+            const float keep = hi ? a4[i + 2] : a4[i];
+            a2[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+        }
+    }
+    float a1;
+    {
+        const bool hi = lane & 2;
+        const float send = hi ? a2[0] : a2[1];
+        const float keep = hi ? a2[1] : a2[0];
+        a1 = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    }
+    return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a, int seg_rows) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    uint32_t *mask_words = reinterpret_cast<uint32_t *>(smem + kOffMask);
+    float *red_max = reinterpret_cast<float *>(smem + kOffRedMax);
+    float *red_sum = reinterpret_cast<float *>(smem + kOffRedSum);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemSlot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
+    const uint32_t bar0 = sbase + kOffBar;
+    auto bar_full = [&](int s) { return bar0 + 8u * s; };
+    auto bar_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto bar_qfull = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+    auto bar_qempty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+    auto bar_sfull = [&](int b) { return bar0 + 8u * (2 * kStages + 4 + b); };
+    auto bar_pfull = [&](int b) { return bar0 + 8u * (2 * kStages + 6 + b); };
+    auto bar_ofull = [&](int b) { return bar0 + 8u * (2 * kStages + 8 + b); };
+    const uint32_t bar_group = bar0 + 8u * (2 * kStages + 10);   // the four softmax warps
+    const uint32_t sm_stage = sbase + kOffStages;
+    const uint32_t sm_q = sbase + kOffQ;
+    const uint32_t sm_p = sbase + kOffP;
+
+    // ---- set-up: barriers, zeroed V / Q / P buffers, TMEM ----
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_full(s), 1);
+            mbar_init(bar_empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_qfull(b), 1);
+            mbar_init(bar_qempty(b), 1);
+            mbar_init(bar_sfull(b), 1);
+            mbar_init(bar_pfull(b), 4);
+            mbar_init(bar_ofull(b), 1);
+        }
+        mbar_init(bar_group, 4);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmQ);
+    }
+    {
+        // V tiles must never hold NaN where nothing was loaded; Q rows past
+        // the group and P start at zero.
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int s = 0; s < kStages; ++s) {
+            uint4 *v = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes);
+            for (int i = threadIdx.x; i < kTileBytes / 16; i += kThreads) v[i] = z;
+        }
+        uint4 *qp = reinterpret_cast<uint4 *>(smem + kOffQ);
+        for (int i = threadIdx.x; i < (2 * kQBytes + 2 * kPBytes) / 16; i += kThreads) qp[i] = z;
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int64_t num_units = (int64_t)a.num_reqs * a.H_kv * a.n_chunks;
+    const int G = a.G;
+    const int nq = a.nq;
+    const int nseg = kTile / seg_rows;         // block segments per tile (1..16)
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        int64_t j = 0;   // tile sequence number in this CTA
+        int us = 0;      // unit sequence number in this CTA
+        for (int64_t u = blockIdx.x; u < num_units && !*abort_flag; u += gridDim.x) {
+            Unit x;
+            if (!unit_at(a, u, x)) continue;
+            if (lane == 0 && x.c == 0 && x.g == 0 && __ldg(a.ctx + x.r) > a.max_ctx && a.err) atomicAdd(a.err, 1);
+            const int qb = us & 1;
+            if (!mbar_wait_warp(bar_qempty(qb), ((us >> 1) & 1) ^ 1, abort_flag)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar_qfull(qb), 2u * 128u * (uint32_t)nq);
+                const uint32_t dq = sm_q + qb * kQBytes;
+                tma_load_3d(dq, &tmQ, bar_qfull(qb), 0, x.g * G, x.r * a.q_len);
+                tma_load_3d(dq + kN * 128, &tmQ, bar_qfull(qb), 64, x.g * G, x.r * a.q_len);
+            }
+            for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
+                const int s = (int)(j % kStages);
+                if (!mbar_wait_warp(bar_empty(s), (uint32_t)((j / kStages) & 1) ^ 1u, abort_flag)) break;
+                const int32_t ts = x.start + jt * kTile;
+                // lane i looks up block segment i of the tile
+                bool load = false;
+                int64_t row0 = 0;
+                if (lane < nseg) {
+                    const int32_t p0 = ts + lane * seg_rows;
+                    if (p0 < x.cend) {
+                        const int32_t lb = p0 / a.bs;
+                        if (lb >= a.bt_cols) {
+                            if (a.err) atomicAdd(a.err, 1);
+                        } else {
+                            const int64_t e = __ldg(a.bt + (int64_t)x.r * a.bt_stride + lb);
+                            if (e >= a.total_blocks) {
+                                if (a.err) atomicAdd(a.err, 1);
+                            } else if (e > 0) {
+                                load = true;
+                                row0 = e * a.bs + (p0 - lb * a.bs);
+                            }
+                        }
+                    }
+                }
+                const uint32_t ballot = __ballot_sync(0xffffffffu, load);
+                if (lane == 0) {
+                    uint32_t words[4] = {0u, 0u, 0u, 0u};
+                    for (int i = 0; i < nseg; ++i) {
+                        if (!((ballot >> i) & 1u)) continue;
+                        for (int rr = i * seg_rows; rr < (i + 1) * seg_rows; rr += 32) {
+                            const int n = min(32, seg_rows);
+                            const uint32_t bits = n == 32 ? 0xffffffffu : ((1u << n) - 1u) << (rr & 31);
+                            words[rr >> 5] |= bits;
+                        }
+                    }
+                    for (int w = 0; w < 4; ++w) mask_words[s * 4 + w] = words[w];
+                    const uint32_t bytes = (uint32_t)__popc(ballot) * (uint32_t)seg_rows * 128u * 4u;
+                    mbar_arrive_expect_tx(bar_full(s), bytes);
+                }
+                __syncwarp();
+                if (load) {
+                    const uint32_t dk = sm_stage + s * kStageBytes + lane * seg_rows * 128;
+                    const uint32_t dv = dk + kTileBytes;
+                    const int z = (int)row0;
+                    tma_load_3d(dk, &tmK, bar_full(s), 0, x.g, z);
+                    tma_load_3d(dk + kHalfBytes, &tmK, bar_full(s), 64, x.g, z);
+                    tma_load_3d(dv, &tmV, bar_full(s), 0, x.g, z);
+                    tma_load_3d(dv + kHalfBytes, &tmV, bar_full(s), 64, x.g, z);
+                }
+                __syncwarp();
+            }
+            ++us;
+        }
+        if (*abort_flag) {
+            // let copies already issued land before the CTA retires
+            const unsigned long long t0 = global_ns();
+            while (global_ns() - t0 < 200000ull) {
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer (one thread) =================
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = idesc_bf16(128, kN, 0, 0);   // K (K-major) x Q (K-major)
+            constexpr uint32_t kIdescO = idesc_bf16(128, kN, 1, 0);   // V^T (MN-major) x P (K-major)
+            int64_t j = 0;
+            int us = 0;
+            int64_t pending = -1;        // tile whose P.V MMA is still to be issued
+            int pending_stage = 0;
+            bool ok = true;
+            auto issue_pv = [&](int64_t jp, int stage) -> bool {
+                const int b = (int)(jp & 1);
+                if (!mbar_wait(bar_pfull(b), (uint32_t)((jp >> 1) & 1), abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t v_base = sm_stage + stage * kStageBytes + kTileBytes;
+                const uint32_t p_base = sm_p + b * kPBytes;
+                const uint32_t d_tmem = tmem + 32u + 16u * b;
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    const uint64_t adesc = sdesc(v_base + kk * 2048, kHalfBytes, 1024);
+                    const uint64_t bdesc = sdesc(p_base + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+                    mma_bf16(d_tmem, adesc, bdesc, kIdescO, kk > 0);
+                }
+                mma_commit(bar_ofull(b));
+                mma_commit(bar_empty(stage));
+                return true;
+            };
+            for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+                Unit x;
+                if (!unit_at(a, u, x)) continue;
+                const int qb = us & 1;
+                if (!mbar_wait(bar_qfull(qb), (uint32_t)((us >> 1) & 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
+                    const int s = (int)(j % kStages);
+                    if (!mbar_wait(bar_full(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t k_base = sm_stage + s * kStageBytes;
+                    const uint32_t q_base = sm_q + qb * kQBytes;
+                    const uint32_t d_tmem = tmem + 16u * (uint32_t)(j & 1);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t half = (uint32_t)(kk >> 2) * kHalfBytes;
+                        const uint64_t adesc = sdesc(k_base + half + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bdesc = sdesc(q_base + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+                        mma_bf16(d_tmem, adesc, bdesc, kIdescS, kk > 0);
+                    }
+                    mma_commit(bar_sfull((int)(j & 1)));
+                    if (jt == x.ntiles - 1) mma_commit(bar_qempty(qb));
+                    if (pending >= 0 && !issue_pv(pending, pending_stage)) {
+                        ok = false;
+                        break;
+                    }
+                    pending = j;
+                    pending_stage = s;
+                }
+                ++us;
+            }
+            if (ok && pending >= 0) issue_pv(pending, pending_stage);
+        }
+        __syncwarp();
+    } else {
+        // ================= softmax + output (128 threads) =================
+        const int row = 32 * (warp & 3) + lane;          // TMEM lane: position in tile / head_dim row
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int wq = warp & 3;
+        float o[kN], lsum[kN], mrun[kN], corr_prev[kN];
+        int64_t j = 0;
+        bool ok = true;
+        uint32_t gphase = 0;
+        // Bounded barrier of the four softmax warps (an mbarrier, so that a
+        // timed-out wait elsewhere can never leave a warp stuck here).
+        auto group_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_group);
+            const bool r = mbar_wait_warp(bar_group, gphase, abort_flag);
+            gphase ^= 1u;
+            return r;
+        };
+        for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+            Unit x;
+            if (!unit_at(a, u, x)) continue;
+            int32_t lastv[kN];
+#pragma unroll
+            for (int n = 0; n < kN; ++n) {
+                o[n] = 0.f;
+                lsum[n] = 0.f;
+                mrun[n] = -INFINITY;
+                corr_prev[n] = 1.f;
+                const int t = n / G;
+                lastv[n] = (n < nq) ? (a.mask_mode == 0 ? x.L - a.q_len + t : x.L - 1) : -1;
+            }
+            for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
+                const int s = (int)(j % kStages);
+                const int b = (int)(j & 1);
+                if (!mbar_wait_warp(bar_sfull(b), (uint32_t)((j >> 1) & 1), abort_flag) ||
+                    !mbar_wait_warp(bar_full(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float sv[kN];
+                tmem_ld16(tmem + lane_base + 16u * b, sv);
+                const int32_t pos = x.start + jt * kTile + row;
+                const bool loaded = (mask_words[s * 4 + (row >> 5)] >> (row & 31)) & 1u;
+                const bool inrange = loaded && pos < x.cend;
+#pragma unroll
+                for (int n = 0; n < kN; ++n) sv[n] = (inrange && pos <= lastv[n]) ? sv[n] * a.scale_log2 : -INFINITY;
+                // tile max per query row across the 128 threads
+                float tmp[kN];
+#pragma unroll
+                for (int n = 0; n < kN; ++n) tmp[n] = sv[n];
+                const float wmax = warp_reduce16<true>(tmp, lane);
+                float *rm = red_max + b * (kN * 4);
+                if ((lane & 1) == 0) rm[((lane >> 1) & 15) * 4 + wq] = wmax;
+                if (!group_sync()) {
+                    ok = false;
+                    break;
+                }
+                float corr[kN];
+                uint8_t *pgen = smem + kOffP + b * kPBytes;
+#pragma unroll
+                for (int n = 0; n < kN; ++n) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(rm + n * 4);
+                    const float mt = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
+                    const float mn = fmaxf(mrun[n], mt);
+                    corr[n] = (mn == -INFINITY) ? 1.f : exp2f(mrun[n] - mn);
+                    mrun[n] = mn;
+                    const float p = (sv[n] == -INFINITY) ? 0.f : exp2f(sv[n] - mn);
+                    const __nv_bfloat16 pbv = __float2bfloat16_rn(p);
+                    lsum[n] = fmaf(lsum[n], corr[n], __bfloat162float(pbv));
+                    // P^T operand, K-major, 128-byte swizzle: row n, position `row`
+                    const int off = (row >> 6) * (kN * 128) + n * 128 + ((((row & 63) >> 3) ^ (n & 7)) << 4) +
+                                    (row & 7) * 2;
+                    *reinterpret_cast<__nv_bfloat16 *>(pgen + off) = pbv;
+                }
+                // V rows that were loaded but lie past the end must be zero for P.V
+                if (loaded && pos >= x.cend) {
+                    uint4 *vrow0 = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes +
+                                                             row * 128);
+                    uint4 *vrow1 = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes +
+                                                             kHalfBytes + row * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        vrow0[c] = make_uint4(0, 0, 0, 0);
+                        vrow1[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_pfull(b));
+                // fold in the previous tile's P.V, one tile behind
+                if (jt > 0) {
+                    const int64_t jp = j - 1;
+                    if (!mbar_wait_warp(bar_ofull((int)(jp & 1)), (uint32_t)((jp >> 1) & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    float ot[kN];
+                    tmem_ld16(tmem + lane_base + 32u + 16u * (uint32_t)(jp & 1), ot);
+#pragma unroll
+                    for (int n = 0; n < kN; ++n) o[n] = fmaf(o[n], corr_prev[n], ot[n]);
+                }
+#pragma unroll
+                for (int n = 0; n < kN; ++n) corr_prev[n] = corr[n];
+            }
+            if (!ok) break;
+            // last tile of the unit
+            {
+                const int64_t jl = j - 1;
+                if (!mbar_wait_warp(bar_ofull((int)(jl & 1)), (uint32_t)((jl >> 1) & 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float ot[kN];
+                tmem_ld16(tmem + lane_base + 32u + 16u * (uint32_t)(jl & 1), ot);
+#pragma unroll
+                for (int n = 0; n < kN; ++n) o[n] = fmaf(o[n], corr_prev[n], ot[n]);
+            }
+            // row sums across the 128 threads, then the partial (o, m, l)
+            {
+                float tmp[kN];
+#pragma unroll
+                for (int n = 0; n < kN; ++n) tmp[n] = lsum[n];
+                const float ws = warp_reduce16<false>(tmp, lane);
+                if ((lane & 1) == 0) red_sum[((lane >> 1) & 15) * 4 + wq] = ws;
+                if (!group_sync()) {
+                    ok = false;
+                    break;
+                }
+                const int64_t prow0 = u * nq;
+#pragma unroll
+                for (int n = 0; n < kN; ++n)
+                    if (n < nq) a.ws_o[(prow0 + n) * kD + row] = o[n];
+                if (row < nq) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(red_sum + row * 4);
+                    float m_row = -INFINITY;
+#pragma unroll
+                    for (int n = 0; n < kN; ++n)
+                        if (n == row) m_row = mrun[n];
+                    a.ws_ml[(prow0 + row) * 2 + 0] = m_row;
+                    a.ws_ml[(prow0 + row) * 2 + 1] = (t4.x + t4.y) + (t4.z + t4.w);
+                }
+                if (!group_sync()) {   // red_sum is reused by the next unit
+                    ok = false;
+                    break;
+                }
+            }
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0 && a.err) atomicAdd(a.err, kTimeoutErr);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+static bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
+                      uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+bool decode_tc_supported(const DecodeArgs &a) {
+    if (a.dtype != BKV_BF16 || a.D != tc::kD || a.nq > tc::kN || a.nq <= 0) return false;
+    if (a.bs < 8 || !((tc::kTile % a.bs == 0) || (a.bs % tc::kTile == 0))) return false;
+    if (a.G > 256 || a.q_len > 256 || a.H_kv > 65535) return false;
+    if ((int64_t)a.total_blocks * a.bs >= ((int64_t)1 << 31)) return false;
+    if ((int64_t)a.num_reqs * a.q_len >= ((int64_t)1 << 31)) return false;
+    if (!aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.q, 16)) return false;
+    return tc::encode_fn() != nullptr;
+}
+
+int launch_decode_tc(const DecodeArgs &a, cudaStream_t st) {
+    using namespace tc;
+    const int seg_rows = a.bs < kTile ? a.bs : kTile;
+    CUtensorMap mk, mv, mq;
+    const uint64_t rows = (uint64_t)a.total_blocks * (uint64_t)a.bs;
+    if (rows == 0) return BKV_ERR_UNSUPPORTED;
+    const uint64_t row_stride = (uint64_t)a.H_kv * kD * 2;
+    if (!encode_3d(&mk, a.k, kD, a.H_kv, rows, kD * 2, row_stride, 64, 1, seg_rows) ||
+        !encode_3d(&mv, a.v, kD, a.H_kv, rows, kD * 2, row_stride, 64, 1, seg_rows) ||
+        !encode_3d(&mq, a.q, kD, a.H_q, (uint64_t)a.num_reqs * a.q_len, kD * 2, (uint64_t)a.H_q * kD * 2, 64, a.G,
+                   a.q_len))
+        return BKV_ERR_UNSUPPORTED;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess)
+            return launch_status();
+        attr_set[dev] = true;
+    }
+    const int64_t units = (int64_t)a.num_reqs * a.H_kv * a.n_chunks;
+    int64_t grid = current_sm_count();
+    if (grid > units) grid = units;
+    if (grid < 1) grid = 1;
+    decode_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, a, seg_rows);
+    return launch_status();
+}
 
 }  // namespace bkv
