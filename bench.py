@@ -209,12 +209,25 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def torch_int64():
+    import torch
+    return torch.int64
+
+
+def _flush_l2(flush):
+    """Evict L2 before a timed step: write a buffer of 2x the L2 size, then
+    read it back, so that the dirty lines of the write are written back here
+    and not during the timed step."""
+    flush.zero_()
+    flush.view(torch_int64()).amax()
+
+
 def _time_steps(torch, fn, steps, flush, stream):
     """Per-step device times (ms) with an L2 flush before each step, outside the events."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     with torch.cuda.stream(stream):
         for a, b in evs:
-            flush.zero_()
+            _flush_l2(flush)
             a.record(stream)
             fn()
             b.record(stream)
@@ -274,15 +287,35 @@ def run_bkv(args):
             decode_only()
     torch.cuda.synchronize()
 
+    # CUDA graphs of the three timed bodies (a serving engine replays its
+    # decode step as a graph); captured after the warm-up so that one-time
+    # set-up (kernel attributes, driver entry points) is outside the graphs.
+    graphs = {}
+    if not args.eager:
+        for name, fn in (("step", step), ("decode", decode_only), ("e2e", e2e_step)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            graphs[name] = g
+        torch.cuda.synchronize()
+        for g in graphs.values():
+            g.replay()
+        torch.cuda.synchronize()
+    body = {name: (graphs[name].replay if name in graphs else fn)
+            for name, fn in (("step", step), ("decode", decode_only), ("e2e", e2e_step))}
+
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
-        step_ms = _time_steps(torch, step, args.steps, flush, stream)
-        dec_ms = _time_steps(torch, decode_only, args.steps, flush, stream)
-        e2e_ms = _time_steps(torch, e2e_step, args.steps, flush, stream)
+        step_ms = _time_steps(torch, body["step"], args.steps, flush, stream)
+        dec_ms = _time_steps(torch, body["decode"], args.steps, flush, stream)
+        e2e_ms = _time_steps(torch, body["e2e"], args.steps, flush, stream)
         t_wall = time.perf_counter() - t_wall0
+    eager_ms = None
+    if graphs:
+        eager_ms = statistics.mean(_time_steps(torch, step, args.steps, flush, stream))
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -307,11 +340,20 @@ def run_bkv(args):
         with torch.cuda.stream(stream):
             for _ in range(3):
                 wstep()
-        wms = _time_steps(torch, wstep, max(args.steps, 20), flush, stream)
+        torch.cuda.synchronize()
+        wbody = wstep
+        if not args.eager:
+            wg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(wg, stream=stream):
+                wstep()
+            wbody = wg.replay
+        wms = _time_steps(torch, wbody, max(args.steps, 20), flush, stream)
         wm = statistics.median(wms)
+        wme = statistics.median(_time_steps(torch, wstep, max(args.steps, 20), flush, stream))
         secondary = {"workload": f"ragged_step: {rw.num_tokens} tokens of 64 requests, bs 16, H_kv 8, D 128, bf16",
                      "tokens_per_s": rw.num_tokens / (wm / 1e3), "GB_per_s": rdw.write_bytes() / (wm / 1e3) / 1e9,
-                     "ms_per_step": wm, "kernels_per_step": 2}
+                     "ms_per_step": wm, "eager_ms_per_step": wme, "kernels_per_step": 2,
+                     "cuda_graph": not args.eager}
         del rdw
 
     if rank != 0:
@@ -327,14 +369,17 @@ def run_bkv(args):
         "config": {"workload": "llama3_decode: 32 req, ctx U[512,4096] + 1 new token, H_q 32, H_kv 8, D 128, "
                                "bs 64, bf16, fp32 accumulate",
                    "kv_bytes_per_step": kv_bytes, "l2": "flushed before every timed step (2x L2 write)",
-                   "parallelism": f"replicas x{world}", "step": "expand + slot map + write + decode + merge"},
-        # library kernels in the timed region: step (5) + decode alone (2) + end-to-end step (5), per step
-        "gpu_launches": args.steps * (5 + 2 + 5),
+                   "parallelism": f"replicas x{world}", "step": "expand + slot map + write + decode + merge",
+                   "cuda_graph": bool(graphs)},
+        # library kernels in the timed region: step (5) + decode alone (2) + end-to-end step (5), per step,
+        # plus the eager reference pass (5 per step) when graphs are used
+        "gpu_launches": args.steps * (5 + 2 + 5) + (args.steps * 5 if graphs else 0),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic(),
                      "kernel": "bkv_paged_decode (partition + merge, CUDA events around the call)",
                      "peak_kind": f"{peak_kind} copy bandwidth"},
         "decode_ms": dms,
+        "eager_ms_per_step": eager_ms,
         "e2e": {"value": world * kv_bytes / (ems / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ems},
         "clocks": clocks,
@@ -356,6 +401,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA graphs")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

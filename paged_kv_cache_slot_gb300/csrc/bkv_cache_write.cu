@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(kCwWarps * 32) cache_write_vec16_kernel(
     const char *__restrict__ k_new, const char *__restrict__ v_new, int64_t num_tokens, int64_t src_stride_bytes,
     const int64_t *__restrict__ slot_mapping, char *__restrict__ k_cache, char *__restrict__ v_cache,
     int64_t capacity, int64_t row_bytes, int32_t *err_count) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (int64_t)blockIdx.x * kCwWarps + (threadIdx.x >> 5);
     const int64_t wstep = (int64_t)gridDim.x * kCwWarps;
@@ -64,6 +66,8 @@ __global__ void __launch_bounds__(kCwWarps * 32) cache_write_elem_kernel(
     const E *__restrict__ k_new, const E *__restrict__ v_new, int64_t num_tokens, int64_t src_stride,
     const int64_t *__restrict__ slot_mapping, E *__restrict__ k_cache, E *__restrict__ v_cache, int64_t capacity,
     int64_t row, int32_t *err_count) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (int64_t)blockIdx.x * kCwWarps + (threadIdx.x >> 5);
     const int64_t wstep = (int64_t)gridDim.x * kCwWarps;
@@ -101,18 +105,20 @@ extern "C" int bkv_cache_write(const void *k_new, const void *v_new, int64_t num
     cudaStream_t st = (cudaStream_t)stream;
     const bool vec16 = (row * eb) % 16 == 0 && (new_token_stride * eb) % 16 == 0 && bkv::aligned(k_new, 16) &&
                        bkv::aligned(v_new, 16) && bkv::aligned(k_cache, 16) && bkv::aligned(v_cache, 16);
+    cudaError_t e;
     if (vec16) {
-        bkv::cache_write_vec16_kernel<<<grid, threads, 0, st>>>(
-            (const char *)k_new, (const char *)v_new, num_tokens, new_token_stride * eb, slot_mapping,
-            (char *)k_cache, (char *)v_cache, capacity, row * eb, err_count);
+        e = bkv::launch_pdl(bkv::cache_write_vec16_kernel, grid, threads, 0, st, (const char *)k_new,
+                            (const char *)v_new, num_tokens, new_token_stride * eb, slot_mapping, (char *)k_cache,
+                            (char *)v_cache, capacity, row * eb, err_count);
     } else if (eb == 2) {
-        bkv::cache_write_elem_kernel<uint16_t><<<grid, threads, 0, st>>>(
-            (const uint16_t *)k_new, (const uint16_t *)v_new, num_tokens, new_token_stride, slot_mapping,
-            (uint16_t *)k_cache, (uint16_t *)v_cache, capacity, row, err_count);
+        e = bkv::launch_pdl(bkv::cache_write_elem_kernel<uint16_t>, grid, threads, 0, st, (const uint16_t *)k_new,
+                            (const uint16_t *)v_new, num_tokens, new_token_stride, slot_mapping, (uint16_t *)k_cache,
+                            (uint16_t *)v_cache, capacity, row, err_count);
     } else {
-        bkv::cache_write_elem_kernel<uint32_t><<<grid, threads, 0, st>>>(
-            (const uint32_t *)k_new, (const uint32_t *)v_new, num_tokens, new_token_stride, slot_mapping,
-            (uint32_t *)k_cache, (uint32_t *)v_cache, capacity, row, err_count);
+        e = bkv::launch_pdl(bkv::cache_write_elem_kernel<uint32_t>, grid, threads, 0, st, (const uint32_t *)k_new,
+                            (const uint32_t *)v_new, num_tokens, new_token_stride, slot_mapping, (uint32_t *)k_cache,
+                            (uint32_t *)v_cache, capacity, row, err_count);
     }
+    if (e != cudaSuccess) bkv::set_cuda_error(e);
     return bkv::launch_status();
 }

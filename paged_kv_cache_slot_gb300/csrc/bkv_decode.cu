@@ -57,6 +57,8 @@ __device__ __forceinline__ int32_t clamped_len(const DecodeArgs &a, int r, bool 
 template <typename T, int DPL, int QR>
 __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a) {
     constexpr int NW = 4;
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int rg = blockIdx.x / a.n_chunks;
@@ -196,49 +198,88 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
 
 // ---------------------------------------------------------------------------
 // Merge: out = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the
-// request's partitions; 0 when no partition saw a visible key.  One warp per
-// output row (r, t, h).
+// request's partitions, M = max_c m_c; 0 when no partition saw a visible key.
+// One CTA per output row (request, KV head, query row of the group).  Warp 0
+// turns every partition's (m, l) into a weight in shared memory; then the
+// four warps split the partitions, each lane summing four head_dim elements
+// (one 16-byte load per partition), and combine through shared memory.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ float sw[];   // [n_chunks] weights, 1 / denominator, then (16-byte aligned) [4][D] warp sums
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int64_t rows = (int64_t)a.num_reqs * a.q_len * a.H_q;
-    if (row >= rows) return;
-    const int h = (int)(row % a.H_q);
-    const int64_t rt = row / a.H_q;
-    const int t = (int)(rt % a.q_len);
-    const int r = (int)(rt / a.q_len);
-    const int g = h / a.G;
-    const int i = t * a.G + (h - g * a.G);
+    const int warp = threadIdx.x >> 5;
+    const int64_t idx = blockIdx.x;           // (r * H_kv + g) * nq + row
+    const int row = (int)(idx % a.nq);
+    const int64_t rg = idx / a.nq;
+    const int r = (int)(rg / a.H_kv);
+    const int g = (int)(rg - (int64_t)r * a.H_kv);
     const int32_t L = clamped_len(a, r, false);
     const int nch = L > 0 ? (int)ceil_div<int32_t>(L, a.chunk) : 0;
-    const int64_t unit0 = ((int64_t)r * a.H_kv + g) * a.n_chunks;
-    T *out = static_cast<T *>(a.out) + row * a.D;
-
-    float M = -INFINITY;
-    for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.ws_ml[((unit0 + c) * a.nq + i) * 2]);
+    const int64_t unit0 = rg * a.n_chunks;
+    float *inv = sw + a.n_chunks;
+    float *part = sw + ((a.n_chunks + 1 + 3) & ~3);   // 16-byte aligned
+    if (warp == 0) {
+        float M = -INFINITY;
+        for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.ws_ml[((unit0 + c) * a.nq + row) * 2]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (M == -INFINITY) {
-        for (int d = lane; d < a.D; d += 32) store_out(out + d, 0.f);
-        return;
-    }
-    float lsum = 0.f;
-    for (int c = lane; c < nch; c += 32) {
-        const float *ml = a.ws_ml + ((unit0 + c) * a.nq + i) * 2;
-        lsum += exp2f(ml[0] - M) * ml[1];
-    }
-    lsum = warp_sum(lsum);
-    const float inv = 1.f / lsum;
-    for (int d = lane; d < a.D; d += 32) {
-        float acc = 0.f;
-        for (int c = 0; c < nch; ++c) {
-            const int64_t prow = (unit0 + c) * a.nq + i;
-            const float w = exp2f(a.ws_ml[prow * 2] - M);
-            acc = fmaf(w, a.ws_o[prow * a.D + d], acc);
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float lsum = 0.f;
+        for (int c = lane; c < nch; c += 32) {
+            const float2 ml = *reinterpret_cast<const float2 *>(a.ws_ml + ((unit0 + c) * a.nq + row) * 2);
+            const float wgt = M == -INFINITY ? 0.f : exp2f(ml.x - M);
+            sw[c] = wgt;
+            lsum = fmaf(wgt, ml.y, lsum);
         }
-        store_out(out + d, acc * inv);
+        lsum = warp_sum(lsum);
+        if (lane == 0) inv[0] = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : 1.f / lsum;
+    }
+    __syncthreads();
+    const int t = row / a.G;
+    const int h = g * a.G + (row - t * a.G);
+    T *out = static_cast<T *>(a.out) + (((int64_t)r * a.q_len + t) * a.H_q + h) * a.D;
+    const float iv = inv[0];
+    if ((a.D & 3) == 0) {
+        for (int d4 = lane; d4 < a.D / 4; d4 += 32) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            int c = warp;
+            for (; c + 12 < nch; c += 16) {
+                float4 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    v[k] = *reinterpret_cast<const float4 *>(a.ws_o + ((unit0 + c + 4 * k) * a.nq + row) * a.D + 4 * d4);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float wgt = sw[c + 4 * k];
+                    acc.x = fmaf(wgt, v[k].x, acc.x);
+                    acc.y = fmaf(wgt, v[k].y, acc.y);
+                    acc.z = fmaf(wgt, v[k].z, acc.z);
+                    acc.w = fmaf(wgt, v[k].w, acc.w);
+                }
+            }
+            for (; c < nch; c += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(a.ws_o + ((unit0 + c) * a.nq + row) * a.D + 4 * d4);
+                const float wgt = sw[c];
+                acc.x = fmaf(wgt, v.x, acc.x);
+                acc.y = fmaf(wgt, v.y, acc.y);
+                acc.z = fmaf(wgt, v.z, acc.z);
+                acc.w = fmaf(wgt, v.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(part + warp * a.D + 4 * d4) = acc;
+        }
+    } else {
+        for (int d = lane; d < a.D; d += 32) {
+            float acc = 0.f;
+            for (int c = warp; c < nch; c += 4) acc = fmaf(sw[c], a.ws_o[((unit0 + c) * a.nq + row) * a.D + d], acc);
+            part[warp * a.D + d] = acc;
+        }
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+        const float acc = (part[d] + part[a.D + d]) + (part[2 * a.D + d] + part[3 * a.D + d]);
+        store_out(out + d, acc * iv);
     }
 }
 
@@ -259,16 +300,25 @@ bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int3
     if (num_reqs <= 0 || q_len <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         max_context_len < 0 || num_q_heads % num_kv_heads != 0 || block_size > 65536)
         return false;
-    // Partitions are whole 128-position tiles and whole blocks.
+    // Partitions are whole 128-position tiles and whole blocks.  512
+    // positions keeps the partial outputs near 2% of the K/V bytes while
+    // leaving enough units for an even spread over the SMs; large batches of
+    // long requests take bigger partitions (up to 2048) to cut partial
+    // traffic, small ones smaller partitions to fill the device.
     const int64_t align = (int64_t)block_size / gcd64(block_size, 128) * 128;
     const int64_t units = (int64_t)num_reqs * num_kv_heads;
     const int64_t sms = current_sm_count();
-    int64_t chunk = ceil_div<int64_t>(512, align) * align;
+    int64_t chunk = 512;
+    const int64_t big = (int64_t)max_context_len * units / (32 * sms);
+    if (big > chunk) chunk = big < 2048 ? big : 2048;
+    chunk = ceil_div<int64_t>(chunk, align) * align;
     if (units * ceil_div<int64_t>(max_context_len, chunk) < 4 * sms) {
         // Few, short units: split finer so the grid still fills the device.
         const int64_t want = ceil_div<int64_t>((int64_t)max_context_len * units, 4 * sms);
         chunk = ceil_div<int64_t>(want > 0 ? want : 1, align) * align;
     }
+    // keep the merge's per-row weight table small
+    if (ceil_div<int64_t>(max_context_len, chunk) > 4096) chunk = ceil_div<int64_t>(ceil_div<int64_t>(max_context_len, 4096), align) * align;
     if (chunk > (int64_t)1 << 30) return false;
     const int64_t n_chunks = max_context_len > 0 ? ceil_div<int64_t>(max_context_len, chunk) : 1;
     const int64_t nq = (int64_t)q_len * (num_q_heads / num_kv_heads);
@@ -286,7 +336,8 @@ template <typename T, int DPL>
 static void launch_generic(const DecodeArgs &a, cudaStream_t st) {
     constexpr int QR = 8;
     dim3 grid(a.n_chunks * a.num_reqs * a.H_kv, ceil_div(a.nq, QR));
-    decode_generic_kernel<T, DPL, QR><<<grid, 128, 0, st>>>(a);
+    const cudaError_t e = launch_pdl(decode_generic_kernel<T, DPL, QR>, grid, dim3(128), 0, st, a);
+    if (e != cudaSuccess) set_cuda_error(e);
 }
 
 template <typename T>
@@ -368,9 +419,11 @@ extern "C" int bkv_paged_decode(const void *q, const void *k_cache, const void *
     }
     if (rc != BKV_OK) return rc;
 
-    const int64_t rows = (int64_t)num_reqs * q_len * num_q_heads;
-    const unsigned mgrid = (unsigned)bkv::ceil_div<int64_t>(rows, 4);
-    if (dtype == BKV_BF16) bkv::decode_merge_kernel<__nv_bfloat16><<<mgrid, 128, 0, st>>>(a);
-    else bkv::decode_merge_kernel<float><<<mgrid, 128, 0, st>>>(a);
+    const size_t msmem = ((((size_t)plan.n_chunks + 1 + 3) & ~(size_t)3) + 4 * (size_t)head_dim) * 4;
+    const dim3 mgrid((unsigned)((int64_t)num_reqs * num_kv_heads * plan.nq));
+    const cudaError_t e = dtype == BKV_BF16
+                              ? bkv::launch_pdl(bkv::decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(128), msmem, st, a)
+                              : bkv::launch_pdl(bkv::decode_merge_kernel<float>, mgrid, dim3(128), msmem, st, a);
+    if (e != cudaSuccess) bkv::set_cuda_error(e);
     return bkv::launch_status();
 }

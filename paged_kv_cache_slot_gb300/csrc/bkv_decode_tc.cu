@@ -9,8 +9,10 @@
 // partitions.
 //
 // Design (sm_103a):
-// * Persistent CTAs (one per SM, ~210 KB of shared memory), units dealt
-//   round-robin.  Warp 0 is the TMA producer, warp 1 issues tcgen05.mma from
+// * Persistent CTAs (one per SM, ~222 KB of shared memory).  Each CTA sorts
+//   the non-empty units by size (largest first) in its set-up and takes
+//   every gridDim-th one, which keeps the busiest SM within a few percent of
+//   the average (natural order left it 1.7x above on the Llama-shaped batch).  Warp 0 is the TMA producer, warp 1 issues tcgen05.mma from
 //   one thread and owns the TMEM allocation, warps 2..5 (128 threads) run the
 //   softmax and the rescaling of the output.
 // * A tile is 128 logical positions.  The producer gathers the tile's K and
@@ -72,7 +74,15 @@ constexpr int kOffBar = kOffRedSum + kN * 4 * 4;          // barriers (8 B each)
 constexpr int kNumBars = 2 * kStages + 2 * 5 + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kSmemUsed = kOffAbort + 4;
+// Per-CTA schedule: units sorted by tile count (largest first), dealt round-robin.
+constexpr int kMaxReqsSorted = 2048;                      // requests the in-kernel sort handles
+constexpr int kMaxListed = 1024;                          // units one CTA can list
+constexpr int kMaxBuckets = 32;                           // tiles per partition the sort handles
+constexpr int kOffInfo = kOffAbort + 4;                   // per request: full partitions | tail tiles << 24
+constexpr int kOffList = kOffInfo + kMaxReqsSorted * 4;   // this CTA's units in order
+constexpr int kOffBucket = kOffList + kMaxListed * 4;     // units per bucket, then bucket offsets
+constexpr int kOffSched = kOffBucket + 2 * (kMaxBuckets + 1) * 4;   // [0] = units listed, [1] = mode
+constexpr int kSmemUsed = kOffSched + 8;
 constexpr int kSmemBytes = kSmemUsed + 1024;              // slack for 1024 alignment
 
 // ---------------------------------------------------------------------------
@@ -195,7 +205,7 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
     uint32_t r[16];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -209,6 +219,35 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float *v) {
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// The first NQ accumulator columns of this thread's TMEM lane.
+template <int NQ>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NQ]) {
+    if constexpr (NQ == 16) tmem_ld16(taddr, v);
+    else if constexpr (NQ == 8) tmem_ld8(taddr, v);
+    else tmem_ld4(taddr, v);
+}
 
 // ---------------------------------------------------------------------------
 // The static schedule every role walks: unit u -> (r, g, c) and its tiles.
@@ -234,54 +273,157 @@ __device__ __forceinline__ bool unit_at(const DecodeArgs &a, int64_t u, Unit &x)
     return true;
 }
 
-// Transposed butterfly over a warp: on return lanes 2k and 2k+1 hold the
-// reduction of v[k] over all 32 lanes (k = 0..15).
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
+// Builds this CTA's list of units: every non-empty unit, sorted by its tile
+// count (largest first, natural order within a count), dealt round-robin to
+// the CTAs.  Partitions are `chunk` positions, so a request of length L has
+// L / chunk full units of T = chunk / 128 tiles per KV head and at most one
+// shorter tail unit.  Runs on all threads of the CTA.  When the batch is too
+// large for the shared-memory tables, falls back to natural order.
+__device__ void build_schedule(const DecodeArgs &a, uint8_t *smem) {
+    uint32_t *info = reinterpret_cast<uint32_t *>(smem + kOffInfo);
+    int32_t *list = reinterpret_cast<int32_t *>(smem + kOffList);
+    int32_t *tot = reinterpret_cast<int32_t *>(smem + kOffBucket);
+    int32_t *off = tot + (kMaxBuckets + 1);
+    int32_t *sched = reinterpret_cast<int32_t *>(smem + kOffSched);
+    const int T = a.chunk / kTile;
+    const int tid = threadIdx.x;
+    const int nthreads = blockDim.x;
+    const bool fits = a.num_reqs <= kMaxReqsSorted && T <= kMaxBuckets;
+    if (tid <= kMaxBuckets) tot[tid] = 0;
+    __syncthreads();
+    if (fits) {
+        for (int r = tid; r < a.num_reqs; r += nthreads) {
+            int32_t L = __ldg(a.ctx + r);
+            L = L > a.max_ctx ? a.max_ctx : (L < 0 ? 0 : L);
+            const int32_t nfull = L / a.chunk;
+            const int32_t trem = (L - nfull * a.chunk + kTile - 1) / kTile;
+            info[r] = (uint32_t)nfull | ((uint32_t)trem << 24);
+            if (nfull) atomicAdd(&tot[T], nfull * a.H_kv);
+            if (trem) atomicAdd(&tot[trem], a.H_kv);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int64_t run = 0;
+        for (int t = T; t >= 1; --t) {
+            off[t] = (int32_t)run;
+            run += tot[t];
+        }
+        const int64_t k = blockIdx.x;
+        const int64_t mine = run > k ? (run - k + gridDim.x - 1) / gridDim.x : 0;
+        sched[0] = (int32_t)mine;
+        sched[1] = (fits && mine <= kMaxListed) ? 1 : 0;
+    }
+    __syncthreads();
+    if (sched[1] == 0) return;
+    // one warp per bucket: a scan over requests places this CTA's targets
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
+    const int64_t k = blockIdx.x, grid = gridDim.x;
+    for (int t = T - warp; t >= 1; t -= nwarps) {
+        int64_t run = off[t];
+        for (int base = 0; base < a.num_reqs; base += 32) {
+            const int r = base + lane;
+            uint32_t nfull = 0, trem = 0;
+            if (r < a.num_reqs) {
+                nfull = info[r] & 0xFFFFFFu;
+                trem = info[r] >> 24;
+            }
+            // bucket t holds the full units (t == T) and the tail units of t tiles
+            const int32_t cnt_full = (t == T) ? (int32_t)nfull * a.H_kv : 0;
+            const int32_t cnt = cnt_full + (trem == (uint32_t)t ? a.H_kv : 0);
+            int32_t inc = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += v;
+            }
+            const int64_t lo = run + inc - cnt, hi = lo + cnt;
+            // targets i = k + m * grid inside [lo, hi)
+            int64_t m = lo <= k ? 0 : (lo - k + grid - 1) / grid;
+            for (int64_t i = k + m * grid; i < hi; i += grid, ++m) {
+                const int64_t o2 = i - lo;
+                int g, c;
+                if (o2 < cnt_full) {
+                    g = (int)(o2 / nfull);
+                    c = (int)(o2 - (int64_t)g * nfull);
+                } else {
+                    g = (int)(o2 - cnt_full);
+                    c = (int)nfull;
+                }
+                list[m] = (int32_t)(((int64_t)r * a.H_kv + g) * a.n_chunks + c);
+            }
+            run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+    }
+}
+
+// The m-th unit of this CTA (sorted schedule), or the natural round-robin
+// order when the sorted list did not fit.
+struct Sched {
+    const int32_t *list;
+    int32_t count;
+    bool sorted;
+    int64_t num_units;
+    __device__ __forceinline__ int64_t first() const { return sorted ? 0 : (int64_t)blockIdx.x; }
+    __device__ __forceinline__ bool more(int64_t it) const { return sorted ? it < count : it < num_units; }
+    __device__ __forceinline__ int64_t next(int64_t it) const { return sorted ? it + 1 : it + gridDim.x; }
+    __device__ __forceinline__ int64_t unit(int64_t it) const { return sorted ? (int64_t)list[it] : it; }
+};
+
+// Transposed butterfly over a warp: NQ values per lane in, one value out.
+// Each halving step exchanges half of the remaining values with the partner
+// lane, so after log2(NQ) steps lane l holds query row (l >> (5 - log2 NQ)) &
+// (NQ - 1), reduced over the lanes that differ in the high bits; the last
+// steps reduce over the low lane bits.  NQ + 5 - log2(NQ) - ... shuffles in
+// all (16 for NQ = 16, 6 for NQ = 4).
+template <bool kMax, int NQ>
+__device__ __forceinline__ float warp_reduce_rows(const float (&v)[NQ], int lane) {
     auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
-    float a8[8];
-    {
-        const bool hi = lane & 16;
+    float cur[NQ];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float send = hi ? v[i] : v[i + 8];
-            const float keep = hi ? v[i + 8] : v[i];
-            a8[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    for (int i = 0; i < NQ; ++i) cur[i] = v[i];
+    int width = NQ;
+    int shift = 16;
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+        if (width > 1) {
+            const bool hi = lane & shift;
+            const int h = width / 2;
+#pragma unroll
+            for (int i = 0; i < NQ / 2; ++i) {
+                if (i < h) {
+                    const float send = hi ? cur[i] : cur[i + h];
+                    const float keep = hi ? cur[i + h] : cur[i];
+                    cur[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, shift));
+                }
+            }
+            width = h;
+            shift >>= 1;
         }
     }
-    float a4[4];
-    {
-        const bool hi = lane & 8;
+    float x = cur[0];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float send = hi ? a8[i] : a8[i + 4];
-            const float keep = hi ? a8[i + 4] : a8[i];
-            a4[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-        }
-    }
-    float a2[2];
-    {
-        const bool hi = lane & 4;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float send = hi ? a4[i] : a4[i + 2];
-            const float keep = hi ? a4[i + 2] : a4[i];
-            a2[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-        }
-    }
-    float a1;
-    {
-        const bool hi = lane & 2;
-        const float send = hi ? a2[0] : a2[1];
-        const float keep = hi ? a2[1] : a2[0];
-        a1 = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-    }
-    return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+    for (int o = 16; o > 0; o >>= 1)
+        if (o <= shift) x = op(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+template <int NQ>
+__device__ __forceinline__ int reduced_row(int lane) {
+    constexpr int k = NQ == 16 ? 4 : (NQ == 8 ? 3 : 2);
+    return (lane >> (5 - k)) & (NQ - 1);
+}
+
+template <int NQ>
+__device__ __forceinline__ bool reduced_writer(int lane) {
+    constexpr int k = NQ == 16 ? 4 : (NQ == 8 ? 3 : 2);
+    return (lane & ((1 << (5 - k)) - 1)) == 0;
 }
 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+template <int NQ>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a, int seg_rows) {
@@ -348,6 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    pdl_wait();                // global memory is read from here on
+    pdl_trigger();
+    build_schedule(a, smem);   // contains __syncthreads
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -355,6 +500,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     const int64_t num_units = (int64_t)a.num_reqs * a.H_kv * a.n_chunks;
+    Sched sch;
+    sch.list = reinterpret_cast<const int32_t *>(smem + kOffList);
+    sch.count = reinterpret_cast<const int32_t *>(smem + kOffSched)[0];
+    sch.sorted = reinterpret_cast<const int32_t *>(smem + kOffSched)[1] != 0;
+    sch.num_units = num_units;
     const int G = a.G;
     const int nq = a.nq;
     const int nseg = kTile / seg_rows;         // block segments per tile (1..16)
@@ -363,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= TMA producer =================
         int64_t j = 0;   // tile sequence number in this CTA
         int us = 0;      // unit sequence number in this CTA
-        for (int64_t u = blockIdx.x; u < num_units && !*abort_flag; u += gridDim.x) {
+        for (int64_t it = sch.first(); sch.more(it) && !*abort_flag; it = sch.next(it)) {
+            const int64_t u = sch.unit(it);
             Unit x;
             if (!unit_at(a, u, x)) continue;
             if (lane == 0 && x.c == 0 && x.g == 0 && __ldg(a.ctx + x.r) > a.max_ctx && a.err) atomicAdd(a.err, 1);
@@ -461,7 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(bar_empty(stage));
                 return true;
             };
-            for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+            for (int64_t it = sch.first(); sch.more(it) && ok; it = sch.next(it)) {
+                const int64_t u = sch.unit(it);
                 Unit x;
                 if (!unit_at(a, u, x)) continue;
                 const int qb = us & 1;
@@ -505,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 32 * (warp & 3) + lane;          // TMEM lane: position in tile / head_dim row
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const int wq = warp & 3;
-        float o[kN], lsum[kN], mrun[kN], corr_prev[kN];
+        float o[NQ], lsum[NQ], mrun[NQ], corr_prev[NQ];
         int64_t j = 0;
         bool ok = true;
         uint32_t gphase = 0;
@@ -518,12 +670,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             gphase ^= 1u;
             return r;
         };
-        for (int64_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        // This thread's byte offset in the P^T operand (K-major, 128-byte
+        // swizzle): position `row`, query row n adds n * 128 and swizzles the
+        // 16-byte chunk index with n & 7.
+        const int p_row_off = (row >> 6) * (kN * 128) + (row & 7) * 2;
+        const int p_chunk = (row & 63) >> 3;
+        const int red_row = reduced_row<NQ>(lane);
+        const bool red_writer = reduced_writer<NQ>(lane);
+        for (int64_t it = sch.first(); sch.more(it) && ok; it = sch.next(it)) {
+            const int64_t u = sch.unit(it);
             Unit x;
             if (!unit_at(a, u, x)) continue;
-            int32_t lastv[kN];
+            int32_t lastv[NQ];
 #pragma unroll
-            for (int n = 0; n < kN; ++n) {
+            for (int n = 0; n < NQ; ++n) {
                 o[n] = 0.f;
                 lsum[n] = 0.f;
                 mrun[n] = -INFINITY;
@@ -540,28 +700,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                float sv[kN];
-                tmem_ld16(tmem + lane_base + 16u * b, sv);
+                float sv[NQ];
+                tmem_ld_cols<NQ>(tmem + lane_base + 16u * b, sv);
                 const int32_t pos = x.start + jt * kTile + row;
                 const bool loaded = (mask_words[s * 4 + (row >> 5)] >> (row & 31)) & 1u;
                 const bool inrange = loaded && pos < x.cend;
 #pragma unroll
-                for (int n = 0; n < kN; ++n) sv[n] = (inrange && pos <= lastv[n]) ? sv[n] * a.scale_log2 : -INFINITY;
+                for (int n = 0; n < NQ; ++n) sv[n] = (inrange && pos <= lastv[n]) ? sv[n] * a.scale_log2 : -INFINITY;
                 // tile max per query row across the 128 threads
-                float tmp[kN];
-#pragma unroll
-                for (int n = 0; n < kN; ++n) tmp[n] = sv[n];
-                const float wmax = warp_reduce16<true>(tmp, lane);
+                const float wmax = warp_reduce_rows<true, NQ>(sv, lane);
                 float *rm = red_max + b * (kN * 4);
-                if ((lane & 1) == 0) rm[((lane >> 1) & 15) * 4 + wq] = wmax;
+                if (red_writer) rm[red_row * 4 + wq] = wmax;
                 if (!group_sync()) {
                     ok = false;
                     break;
                 }
-                float corr[kN];
-                uint8_t *pgen = smem + kOffP + b * kPBytes;
+                float corr[NQ];
+                uint8_t *pgen = smem + kOffP + b * kPBytes + p_row_off;
 #pragma unroll
-                for (int n = 0; n < kN; ++n) {
+                for (int n = 0; n < NQ; ++n) {
                     const float4 t4 = *reinterpret_cast<const float4 *>(rm + n * 4);
                     const float mt = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
                     const float mn = fmaxf(mrun[n], mt);
@@ -570,10 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float p = (sv[n] == -INFINITY) ? 0.f : exp2f(sv[n] - mn);
                     const __nv_bfloat16 pbv = __float2bfloat16_rn(p);
                     lsum[n] = fmaf(lsum[n], corr[n], __bfloat162float(pbv));
-                    // P^T operand, K-major, 128-byte swizzle: row n, position `row`
-                    const int off = (row >> 6) * (kN * 128) + n * 128 + ((((row & 63) >> 3) ^ (n & 7)) << 4) +
-                                    (row & 7) * 2;
-                    *reinterpret_cast<__nv_bfloat16 *>(pgen + off) = pbv;
+                    *reinterpret_cast<__nv_bfloat16 *>(pgen + n * 128 + ((p_chunk ^ (n & 7)) << 4)) = pbv;
                 }
                 // V rows that were loaded but lie past the end must be zero for P.V
                 if (loaded && pos >= x.cend) {
@@ -599,13 +753,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    float ot[kN];
-                    tmem_ld16(tmem + lane_base + 32u + 16u * (uint32_t)(jp & 1), ot);
+                    float ot[NQ];
+                    tmem_ld_cols<NQ>(tmem + lane_base + 32u + 16u * (uint32_t)(jp & 1), ot);
 #pragma unroll
-                    for (int n = 0; n < kN; ++n) o[n] = fmaf(o[n], corr_prev[n], ot[n]);
+                    for (int n = 0; n < NQ; ++n) o[n] = fmaf(o[n], corr_prev[n], ot[n]);
                 }
 #pragma unroll
-                for (int n = 0; n < kN; ++n) corr_prev[n] = corr[n];
+                for (int n = 0; n < NQ; ++n) corr_prev[n] = corr[n];
             }
             if (!ok) break;
             // last tile of the unit
@@ -616,31 +770,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                float ot[kN];
-                tmem_ld16(tmem + lane_base + 32u + 16u * (uint32_t)(jl & 1), ot);
+                float ot[NQ];
+                tmem_ld_cols<NQ>(tmem + lane_base + 32u + 16u * (uint32_t)(jl & 1), ot);
 #pragma unroll
-                for (int n = 0; n < kN; ++n) o[n] = fmaf(o[n], corr_prev[n], ot[n]);
+                for (int n = 0; n < NQ; ++n) o[n] = fmaf(o[n], corr_prev[n], ot[n]);
             }
             // row sums across the 128 threads, then the partial (o, m, l)
             {
-                float tmp[kN];
-#pragma unroll
-                for (int n = 0; n < kN; ++n) tmp[n] = lsum[n];
-                const float ws = warp_reduce16<false>(tmp, lane);
-                if ((lane & 1) == 0) red_sum[((lane >> 1) & 15) * 4 + wq] = ws;
+                const float wsum = warp_reduce_rows<false, NQ>(lsum, lane);
+                if (red_writer) red_sum[red_row * 4 + wq] = wsum;
                 if (!group_sync()) {
                     ok = false;
                     break;
                 }
                 const int64_t prow0 = u * nq;
 #pragma unroll
-                for (int n = 0; n < kN; ++n)
+                for (int n = 0; n < NQ; ++n)
                     if (n < nq) a.ws_o[(prow0 + n) * kD + row] = o[n];
                 if (row < nq) {
                     const float4 t4 = *reinterpret_cast<const float4 *>(red_sum + row * 4);
                     float m_row = -INFINITY;
 #pragma unroll
-                    for (int n = 0; n < kN; ++n)
+                    for (int n = 0; n < NQ; ++n)
                         if (n == row) m_row = mrun[n];
                     a.ws_ml[(prow0 + row) * 2 + 0] = m_row;
                     a.ws_ml[(prow0 + row) * 2 + 1] = (t4.x + t4.y) + (t4.z + t4.w);
@@ -717,20 +868,23 @@ int launch_decode_tc(const DecodeArgs &a, cudaStream_t st) {
         !encode_3d(&mq, a.q, kD, a.H_q, (uint64_t)a.num_reqs * a.q_len, kD * 2, (uint64_t)a.H_q * kD * 2, 64, a.G,
                    a.q_len))
         return BKV_ERR_UNSUPPORTED;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
-            return launch_status();
-        attr_set[dev] = true;
-    }
     const int64_t units = (int64_t)a.num_reqs * a.H_kv * a.n_chunks;
     int64_t grid = current_sm_count();
     if (grid > units) grid = units;
     if (grid < 1) grid = 1;
-    decode_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, a, seg_rows);
+    // the softmax handles only the query rows that exist (4, 8 or 16 columns)
+    auto kern = a.nq <= 4 ? decode_tc_kernel<4> : (a.nq <= 8 ? decode_tc_kernel<8> : decode_tc_kernel<16>);
+    const int slot = a.nq <= 4 ? 0 : (a.nq <= 8 ? 1 : 2);
+    static bool attr_set[64][3] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev][slot]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+            return launch_status();
+        attr_set[dev][slot] = true;
+    }
+    const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, mk, mv, mq, a, seg_rows);
+    if (e != cudaSuccess) set_cuda_error(e);
     return launch_status();
 }
 

@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(256) slot_mapping_kernel(
     const int32_t *__restrict__ block_table, int32_t num_reqs, int64_t bt_stride, int32_t bt_cols,
     const int32_t *__restrict__ req_indices, const int64_t *__restrict__ positions, int64_t num_tokens,
     int64_t max_num_tokens, int32_t block_size, int64_t *__restrict__ slot_mapping, int32_t *err_count) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < max_num_tokens; i += step) {
         int64_t slot = -1;
@@ -43,6 +45,8 @@ __global__ void __launch_bounds__(256) slot_mapping_kernel(
 __global__ void __launch_bounds__(256) kernel_blocks_kernel(
     const int32_t *__restrict__ mgr, int32_t rows, int64_t mgr_stride, int32_t mgr_cols, int32_t bpk,
     int32_t *__restrict__ out, int64_t out_stride) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t cols = (int64_t)mgr_cols * bpk;
     const int64_t total = (int64_t)rows * cols;
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
@@ -70,9 +74,10 @@ extern "C" int bkv_compute_slot_mapping(const int32_t *block_table, int32_t num_
     if (num_tokens > 0 && (!req_indices || !positions)) return BKV_ERR_INVALID_ARG;
     if (num_tokens > 0 && num_reqs > 0 && bt_cols > 0 && !block_table) return BKV_ERR_INVALID_ARG;
     const int threads = 256;
-    bkv::slot_mapping_kernel<<<bkv::grid_for(max_num_tokens, threads), threads, 0, (cudaStream_t)stream>>>(
-        block_table, num_reqs, bt_stride, bt_cols, req_indices, positions, num_tokens, max_num_tokens, block_size,
-        slot_mapping, err_count);
+    const cudaError_t e = bkv::launch_pdl(bkv::slot_mapping_kernel, bkv::grid_for(max_num_tokens, threads), threads, 0,
+                                          (cudaStream_t)stream, block_table, num_reqs, bt_stride, bt_cols, req_indices,
+                                          positions, num_tokens, max_num_tokens, block_size, slot_mapping, err_count);
+    if (e != cudaSuccess) bkv::set_cuda_error(e);
     return bkv::launch_status();
 }
 
@@ -88,7 +93,9 @@ extern "C" int bkv_map_to_kernel_blocks(const int32_t *mgr_table, int32_t rows, 
     if (total == 0) return BKV_OK;
     if (!mgr_table || !kernel_table) return BKV_ERR_INVALID_ARG;
     const int threads = 256;
-    bkv::kernel_blocks_kernel<<<bkv::grid_for(total, threads), threads, 0, (cudaStream_t)stream>>>(
-        mgr_table, rows, mgr_stride, mgr_cols, bpk, kernel_table, kernel_stride);
+    const cudaError_t e = bkv::launch_pdl(bkv::kernel_blocks_kernel, bkv::grid_for(total, threads), threads, 0,
+                                          (cudaStream_t)stream, mgr_table, rows, mgr_stride, mgr_cols, bpk,
+                                          kernel_table, kernel_stride);
+    if (e != cudaSuccess) bkv::set_cuda_error(e);
     return bkv::launch_status();
 }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/bkv.h"
 
 namespace bkv {
@@ -39,6 +41,32 @@ inline unsigned grid_for(int64_t n, int threads, int waves = 8) {
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return (unsigned)blocks;
+}
+
+// Programmatic dependent launch.  Every library kernel starts with
+// pdl_wait() before it touches global memory: the wait returns only once the
+// preceding kernel in the stream has completed and its writes are visible,
+// so launching with the programmatic-serialisation attribute changes no
+// result; it lets the launch (and any set-up that needs no global memory)
+// overlap the preceding kernel.  pdl_trigger() lets the next such kernel
+// launch early; it is always safe for the same reason.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace bkv
