@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
                 lsum = fmaf(f, sm_l[w][i], lsum);
             }
         }
-        const int64_t prow = unit * a.nq + i0 + i;
+        const int64_t prow = unit * a.parts * a.nq + i0 + i;
         a.ws_o[prow * a.D + d] = acc;
         if (d == 0) {
             a.ws_ml[prow * 2 + 0] = M;
@@ -208,7 +208,7 @@ template <typename T>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     pdl_wait();
     pdl_trigger();
-    extern __shared__ float sw[];   // [n_chunks] weights, 1 / denominator, then (16-byte aligned) [4][D] warp sums
+    extern __shared__ float sw[];   // [n_chunks * parts] weights, 1 / denominator, then [4][D] warp sums
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int64_t idx = blockIdx.x;           // (r * H_kv + g) * nq + row
@@ -217,10 +217,12 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     const int r = (int)(rg / a.H_kv);
     const int g = (int)(rg - (int64_t)r * a.H_kv);
     const int32_t L = clamped_len(a, r, false);
-    const int nch = L > 0 ? (int)ceil_div<int32_t>(L, a.chunk) : 0;
-    const int64_t unit0 = rg * a.n_chunks;
-    float *inv = sw + a.n_chunks;
-    float *part = sw + ((a.n_chunks + 1 + 3) & ~3);   // 16-byte aligned
+    // a request's partial slots are contiguous: `parts` per partition
+    const int nch = L > 0 ? (int)ceil_div<int32_t>(L, a.chunk) * a.parts : 0;
+    const int64_t unit0 = rg * a.n_chunks * a.parts;
+    const int nslots = a.n_chunks * a.parts;
+    float *inv = sw + nslots;
+    float *part = sw + ((nslots + 1 + 3) & ~3);   // 16-byte aligned
     if (warp == 0) {
         float M = -INFINITY;
         for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.ws_ml[((unit0 + c) * a.nq + row) * 2]);
@@ -326,7 +328,7 @@ bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int3
     plan->chunk = (int32_t)chunk;
     plan->n_chunks = (int32_t)n_chunks;
     plan->nq = (int32_t)nq;
-    const int64_t prows = units * n_chunks * nq;
+    const int64_t prows = units * n_chunks * 2 * nq;   // up to two partial slots per unit
     const int64_t o_bytes = ceil_div<int64_t>(prows * head_dim * 4, 256) * 256;
     plan->ws_bytes = (size_t)(o_bytes + prows * 2 * 4);
     return true;
@@ -402,7 +404,8 @@ extern "C" int bkv_paged_decode(const void *q, const void *k_cache, const void *
     a.n_chunks = plan.n_chunks;
     a.G = num_q_heads / num_kv_heads;
     a.nq = plan.nq;
-    const int64_t prows = (int64_t)num_reqs * num_kv_heads * plan.n_chunks * plan.nq;
+    const int64_t prows = (int64_t)num_reqs * num_kv_heads * plan.n_chunks * 2 * plan.nq;
+    a.parts = 2;
     a.ws_o = static_cast<float *>(workspace);
     a.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                         bkv::ceil_div<int64_t>(prows * head_dim * 4, 256) * 256);
@@ -413,13 +416,15 @@ extern "C" int bkv_paged_decode(const void *q, const void *k_cache, const void *
     int rc = BKV_ERR_UNSUPPORTED;
     if (bkv::decode_tc_supported(a)) rc = bkv::launch_decode_tc(a, st);
     if (rc == BKV_ERR_UNSUPPORTED) {
+        a.parts = 1;
         if (dtype == BKV_BF16) bkv::launch_generic_dpl<__nv_bfloat16>(a, st);
         else bkv::launch_generic_dpl<float>(a, st);
         rc = bkv::launch_status();
     }
     if (rc != BKV_OK) return rc;
 
-    const size_t msmem = ((((size_t)plan.n_chunks + 1 + 3) & ~(size_t)3) + 4 * (size_t)head_dim) * 4;
+    const size_t nslots = (size_t)plan.n_chunks * a.parts;
+    const size_t msmem = (((nslots + 1 + 3) & ~(size_t)3) + 4 * (size_t)head_dim) * 4;
     const dim3 mgrid((unsigned)((int64_t)num_reqs * num_kv_heads * plan.nq));
     const cudaError_t e = dtype == BKV_BF16
                               ? bkv::launch_pdl(bkv::decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(128), msmem, st, a)

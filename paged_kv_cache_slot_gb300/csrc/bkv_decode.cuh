@@ -24,8 +24,9 @@ struct DecodeArgs {
     int32_t n_chunks;  // partitions per request at max_ctx
     int32_t G;         // query heads per KV head
     int32_t nq;        // query rows per KV head: q_len * G, row i = t * G + (h % G)
-    float *ws_o;       // [num_reqs * H_kv * n_chunks][nq][D] unnormalised partial outputs
-    float *ws_ml;      // [num_reqs * H_kv * n_chunks][nq][2]  (running max in base 2, sum of weights)
+    int32_t parts;     // partials per unit (slots): 1 for the generic kernel, 2 for the tensor-core one
+    float *ws_o;       // [num_reqs * H_kv * n_chunks * parts][nq][D] unnormalised partial outputs
+    float *ws_ml;      // [num_reqs * H_kv * n_chunks * parts][nq][2]  (running max in base 2, sum of weights)
     void *out;
     int32_t *err;
 };

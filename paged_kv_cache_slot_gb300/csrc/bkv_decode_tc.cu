@@ -9,12 +9,14 @@
 // partitions.
 //
 // Design (sm_103a):
-// * Persistent CTAs (one per SM, ~222 KB of shared memory).  Each CTA sorts
+// * Persistent CTAs (one per SM, ~225 KB of shared memory).  Each CTA sorts
 //   the non-empty units by size (largest first) in its set-up and takes
 //   every gridDim-th one, which keeps the busiest SM within a few percent of
 //   the average (natural order left it 1.7x above on the Llama-shaped batch).  Warp 0 is the TMA producer, warp 1 issues tcgen05.mma from
-//   one thread and owns the TMEM allocation, warps 2..5 (128 threads) run the
-//   softmax and the rescaling of the output.
+//   one thread and owns the TMEM allocation, and two warpgroups (warps 2..5
+//   and 6..9) run the softmax and the output update on alternate tiles, so
+//   one group's waits overlap the other's arithmetic.  Each group keeps its
+//   own online-softmax state and writes its own partial per unit.
 // * A tile is 128 logical positions.  The producer gathers the tile's K and
 //   V rows of KV head g through the block table with 3-D TMA loads
 //   (cp.async.bulk.tensor; map over (head_dim, H_kv, total_blocks *
@@ -31,7 +33,7 @@
 // * O^T[128 x 16] = V_tile^T . P^T (M = head_dim, V read MN-major straight
 //   from the TMA tile, K = positions).  Each softmax thread owns one head_dim
 //   row of O^T and accumulates o = o * 2^(m_old - m_new) + O_tile in
-//   registers, one tile behind the softmax so the MMA overlaps it.
+//   registers.
 // * V rows that were loaded but lie past the request's end are zeroed in
 //   shared memory before the P.V MMA, so unwritten cache memory (which may
 //   hold NaN) never reaches the output; K rows there are masked by select.
@@ -58,7 +60,7 @@ constexpr int kTileBytes = 2 * kHalfBytes;       // K or V tile: 32 KB
 constexpr int kStageBytes = 2 * kTileBytes;      // K + V: 64 KB
 constexpr int kQBytes = 2 * kN * 128;            // 16 rows x 128 B x 2 halves: 4 KB
 constexpr int kPBytes = 2 * kN * 128;            // 16 rows x 128 positions (2 x 64) bf16: 4 KB
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;                    // producer, MMA, two softmax warpgroups
 constexpr int kTmemCols = 64;                    // S x2 (16 cols each) + O x2
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr int kTimeoutErr = 1 << 24;
@@ -67,23 +69,27 @@ constexpr int kTimeoutErr = 1 << 24;
 constexpr int kOffStages = 0;
 constexpr int kOffQ = kOffStages + kStages * kStageBytes;
 constexpr int kOffP = kOffQ + 2 * kQBytes;
-constexpr int kOffMask = kOffP + 2 * kPBytes;             // kStages x 4 words
-constexpr int kOffRedMax = kOffMask + kStages * 16;       // 2 x 16 x 4 floats
-constexpr int kOffRedSum = kOffRedMax + 2 * kN * 4 * 4;   // 16 x 4 floats
-constexpr int kOffBar = kOffRedSum + kN * 4 * 4;          // barriers (8 B each)
-constexpr int kNumBars = 2 * kStages + 2 * 5 + 1;
+constexpr int kOffMask = kOffP + 2 * kPBytes;             // kStages x 4 words (word 0: loaded segments)
+constexpr int kOffRedMax = kOffMask + kStages * 16;       // [warpgroup][2][16 rows][4 warps] floats
+constexpr int kOffRedSum = kOffRedMax + 4 * kN * 4 * 4;   // [warpgroup][16 rows][4 warps] floats
+constexpr int kOffBar = kOffRedSum + 2 * kN * 4 * 4;      // barriers (8 B each)
+constexpr int kNumBars = 2 * kStages + 2 * 5 + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 // Per-CTA schedule: units sorted by tile count (largest first), dealt round-robin.
+// The same pass leaves every request's (clamped) length in shared memory.
 constexpr int kMaxReqsSorted = 2048;                      // requests the in-kernel sort handles
 constexpr int kMaxListed = 1024;                          // units one CTA can list
 constexpr int kMaxBuckets = 32;                           // tiles per partition the sort handles
-constexpr int kOffInfo = kOffAbort + 4;                   // per request: full partitions | tail tiles << 24
+constexpr int kOffInfo = kOffAbort + 4;                   // per request: clamped length
 constexpr int kOffList = kOffInfo + kMaxReqsSorted * 4;   // this CTA's units in order
 constexpr int kOffBucket = kOffList + kMaxListed * 4;     // units per bucket, then bucket offsets
 constexpr int kOffSched = kOffBucket + 2 * (kMaxBuckets + 1) * 4;   // [0] = units listed, [1] = mode
-constexpr int kSmemUsed = kOffSched + 8;
+constexpr int kMaxUnitBlocks = 256;                       // table entries the producer caches per unit
+constexpr int kOffEnt = kOffSched + 8;                    // 2 x kMaxUnitBlocks table entries
+constexpr int kSmemUsed = kOffEnt + 2 * kMaxUnitBlocks * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;              // slack for 1024 alignment
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -174,6 +180,13 @@ __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// 2^x with the MUFU approximation (ex2.approx.ftz); 2^-inf = +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Shared-memory matrix descriptor: 128-byte swizzle, version 1 (sm_100 family).
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
@@ -257,12 +270,12 @@ struct Unit {
     int32_t L, start, cend, ntiles;
 };
 
-__device__ __forceinline__ bool unit_at(const DecodeArgs &a, int64_t u, Unit &x) {
+__device__ __forceinline__ bool unit_at(const DecodeArgs &a, int64_t u, Unit &x, const int32_t *lens) {
     const int64_t rg = u / a.n_chunks;
     x.c = (int)(u - rg * a.n_chunks);
     x.r = (int)(rg / a.H_kv);
     x.g = (int)(rg - (int64_t)x.r * a.H_kv);
-    int32_t L = __ldg(a.ctx + x.r);
+    int32_t L = lens ? lens[x.r] : __ldg(a.ctx + x.r);
     if (L > a.max_ctx) L = a.max_ctx;
     if (L < 0) L = 0;
     x.L = L;
@@ -297,7 +310,7 @@ __device__ void build_schedule(const DecodeArgs &a, uint8_t *smem) {
             L = L > a.max_ctx ? a.max_ctx : (L < 0 ? 0 : L);
             const int32_t nfull = L / a.chunk;
             const int32_t trem = (L - nfull * a.chunk + kTile - 1) / kTile;
-            info[r] = (uint32_t)nfull | ((uint32_t)trem << 24);
+            info[r] = (uint32_t)L;
             if (nfull) atomicAdd(&tot[T], nfull * a.H_kv);
             if (trem) atomicAdd(&tot[trem], a.H_kv);
         }
@@ -325,8 +338,9 @@ __device__ void build_schedule(const DecodeArgs &a, uint8_t *smem) {
             const int r = base + lane;
             uint32_t nfull = 0, trem = 0;
             if (r < a.num_reqs) {
-                nfull = info[r] & 0xFFFFFFu;
-                trem = info[r] >> 24;
+                const int32_t L = (int32_t)info[r];
+                nfull = (uint32_t)(L / a.chunk);
+                trem = (uint32_t)((L - (int32_t)nfull * a.chunk + kTile - 1) / kTile);
             }
             // bucket t holds the full units (t == T) and the tail units of t tiles
             const int32_t cnt_full = (t == T) ? (int32_t)nfull * a.H_kv : 0;
@@ -446,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_sfull = [&](int b) { return bar0 + 8u * (2 * kStages + 4 + b); };
     auto bar_pfull = [&](int b) { return bar0 + 8u * (2 * kStages + 6 + b); };
     auto bar_ofull = [&](int b) { return bar0 + 8u * (2 * kStages + 8 + b); };
-    const uint32_t bar_group = bar0 + 8u * (2 * kStages + 10);   // the four softmax warps
+    auto bar_group = [&](int k) { return bar0 + 8u * (2 * kStages + 10 + k); };   // four warps of warpgroup k
     const uint32_t sm_stage = sbase + kOffStages;
     const uint32_t sm_q = sbase + kOffQ;
     const uint32_t sm_p = sbase + kOffP;
@@ -464,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_pfull(b), 4);
             mbar_init(bar_ofull(b), 1);
         }
-        mbar_init(bar_group, 4);
+        mbar_init(bar_group(0), 4);
+        mbar_init(bar_group(1), 4);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -502,21 +517,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t num_units = (int64_t)a.num_reqs * a.H_kv * a.n_chunks;
     Sched sch;
     sch.list = reinterpret_cast<const int32_t *>(smem + kOffList);
+    const int32_t *lens = reinterpret_cast<const int32_t *>(smem + kOffSched)[1] != 0
+                              ? reinterpret_cast<const int32_t *>(smem + kOffInfo)
+                              : nullptr;
     sch.count = reinterpret_cast<const int32_t *>(smem + kOffSched)[0];
     sch.sorted = reinterpret_cast<const int32_t *>(smem + kOffSched)[1] != 0;
     sch.num_units = num_units;
     const int G = a.G;
     const int nq = a.nq;
     const int nseg = kTile / seg_rows;         // block segments per tile (1..16)
+    const int seg_shift = 31 - __clz(seg_rows);   // seg_rows is a power of two
 
     if (warp == 0) {
         // ================= TMA producer =================
+        // The table entries of a unit (one per block it covers) are loaded
+        // into registers one unit ahead and parked in shared memory, so no
+        // table lookup sits between a stage becoming free and its refill.
+        // An entry past the table width is parked as INT32_MIN.
+        int32_t *ent_buf = reinterpret_cast<int32_t *>(smem + kOffEnt);
+        constexpr int kEntRegs = kMaxUnitBlocks / 32;
+        int32_t ent_reg[kEntRegs];
+        auto unit_blocks = [&](const Unit &x) { return (x.cend - x.start + a.bs - 1) / a.bs; };
+        auto fetch_entries = [&](const Unit &x) {
+            const int32_t lb0 = x.start / a.bs;
+            const int32_t nblk = unit_blocks(x);
+#pragma unroll
+            for (int kk = 0; kk < kEntRegs; ++kk) {
+                const int32_t lbl = kk * 32 + lane;
+                if (lbl < nblk) {
+                    const int32_t lb = lb0 + lbl;
+                    ent_reg[kk] = lb < a.bt_cols ? __ldg(a.bt + (int64_t)x.r * a.bt_stride + lb) : INT32_MIN;
+                }
+            }
+        };
+        auto park_entries = [&](const Unit &x, int buf) {
+            const int32_t nblk = unit_blocks(x);
+#pragma unroll
+            for (int kk = 0; kk < kEntRegs; ++kk) {
+                const int32_t lbl = kk * 32 + lane;
+                if (lbl < nblk) ent_buf[buf * kMaxUnitBlocks + lbl] = ent_reg[kk];
+            }
+            __syncwarp();
+        };
+        // next non-empty unit at or after schedule position `it`
+        auto find_unit = [&](int64_t it, Unit &x) -> int64_t {
+            for (; sch.more(it); it = sch.next(it))
+                if (unit_at(a, sch.unit(it), x, lens)) return it;
+            return -1;
+        };
         int64_t j = 0;   // tile sequence number in this CTA
         int us = 0;      // unit sequence number in this CTA
-        for (int64_t it = sch.first(); sch.more(it) && !*abort_flag; it = sch.next(it)) {
-            const int64_t u = sch.unit(it);
-            Unit x;
-            if (!unit_at(a, u, x)) continue;
+        Unit x;
+        int64_t it = find_unit(sch.first(), x);
+        if (it >= 0 && unit_blocks(x) <= kMaxUnitBlocks) {
+            fetch_entries(x);
+            park_entries(x, 0);
+        }
+        while (it >= 0 && !*abort_flag) {
+            Unit nx;
+            const int64_t it_next = find_unit(sch.next(it), nx);
+            const bool cached = unit_blocks(x) <= kMaxUnitBlocks;
+            const bool next_cached = it_next >= 0 && unit_blocks(nx) <= kMaxUnitBlocks;
+            if (next_cached) fetch_entries(nx);     // in flight while this unit's tiles are issued
+            const int32_t *ents = ent_buf + (us & 1) * kMaxUnitBlocks;
             if (lane == 0 && x.c == 0 && x.g == 0 && __ldg(a.ctx + x.r) > a.max_ctx && a.err) atomicAdd(a.err, 1);
             const int qb = us & 1;
             if (!mbar_wait_warp(bar_qempty(qb), ((us >> 1) & 1) ^ 1, abort_flag)) break;
@@ -530,38 +593,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = (int)(j % kStages);
                 if (!mbar_wait_warp(bar_empty(s), (uint32_t)((j / kStages) & 1) ^ 1u, abort_flag)) break;
                 const int32_t ts = x.start + jt * kTile;
-                // lane i looks up block segment i of the tile
+                // lane i handles block segment i of the tile
                 bool load = false;
                 int64_t row0 = 0;
                 if (lane < nseg) {
                     const int32_t p0 = ts + lane * seg_rows;
                     if (p0 < x.cend) {
-                        const int32_t lb = p0 / a.bs;
-                        if (lb >= a.bt_cols) {
-                            if (a.err) atomicAdd(a.err, 1);
+                        const int32_t lbl = (p0 - x.start) / a.bs;
+                        const int32_t lb = x.start / a.bs + lbl;
+                        int64_t e;
+                        if (cached) {
+                            e = ents[lbl];
                         } else {
-                            const int64_t e = __ldg(a.bt + (int64_t)x.r * a.bt_stride + lb);
-                            if (e >= a.total_blocks) {
-                                if (a.err) atomicAdd(a.err, 1);
-                            } else if (e > 0) {
-                                load = true;
-                                row0 = e * a.bs + (p0 - lb * a.bs);
-                            }
+                            e = lb < a.bt_cols ? (int64_t)__ldg(a.bt + (int64_t)x.r * a.bt_stride + lb) : INT32_MIN;
+                        }
+                        if (e == INT32_MIN || e >= a.total_blocks) {
+                            if (a.err) atomicAdd(a.err, 1);
+                        } else if (e > 0) {
+                            load = true;
+                            row0 = e * a.bs + (p0 - (int64_t)lb * a.bs);
                         }
                     }
                 }
                 const uint32_t ballot = __ballot_sync(0xffffffffu, load);
                 if (lane == 0) {
-                    uint32_t words[4] = {0u, 0u, 0u, 0u};
-                    for (int i = 0; i < nseg; ++i) {
-                        if (!((ballot >> i) & 1u)) continue;
-                        for (int rr = i * seg_rows; rr < (i + 1) * seg_rows; rr += 32) {
-                            const int n = min(32, seg_rows);
-                            const uint32_t bits = n == 32 ? 0xffffffffu : ((1u << n) - 1u) << (rr & 31);
-                            words[rr >> 5] |= bits;
-                        }
-                    }
-                    for (int w = 0; w < 4; ++w) mask_words[s * 4 + w] = words[w];
+                    mask_words[s * 4] = ballot;   // bit i: segment i was loaded
                     const uint32_t bytes = (uint32_t)__popc(ballot) * (uint32_t)seg_rows * 128u * 4u;
                     mbar_arrive_expect_tx(bar_full(s), bytes);
                 }
@@ -577,7 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
+            if (next_cached) park_entries(nx, (us + 1) & 1);
             ++us;
+            it = it_next;
+            x = nx;
         }
         if (*abort_flag) {
             // let copies already issued land before the CTA retires
@@ -615,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t it = sch.first(); sch.more(it) && ok; it = sch.next(it)) {
                 const int64_t u = sch.unit(it);
                 Unit x;
-                if (!unit_at(a, u, x)) continue;
+                if (!unit_at(a, u, x, lens)) continue;
                 const int qb = us & 1;
                 if (!mbar_wait(bar_qfull(qb), (uint32_t)((us >> 1) & 1), abort_flag)) {
                     ok = false;
@@ -653,20 +712,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ================= softmax + output (128 threads) =================
+        // ================= softmax + output (two warpgroups of 128 threads) =================
+        // Warpgroup k takes the tiles with (tile sequence number & 1) == k,
+        // i.e. the S / P / O buffers of parity k, and writes partial slot k
+        // of every unit.
+        const int wg = (warp - 2) >> 2;
         const int row = 32 * (warp & 3) + lane;          // TMEM lane: position in tile / head_dim row
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const int wq = warp & 3;
-        float o[NQ], lsum[NQ], mrun[NQ], corr_prev[NQ];
+        float o[NQ], lsum[NQ], mrun[NQ];
         int64_t j = 0;
         bool ok = true;
         uint32_t gphase = 0;
-        // Bounded barrier of the four softmax warps (an mbarrier, so that a
+        // Bounded barrier of the warpgroup's four warps (an mbarrier, so that a
         // timed-out wait elsewhere can never leave a warp stuck here).
         auto group_sync = [&]() -> bool {
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_group);
-            const bool r = mbar_wait_warp(bar_group, gphase, abort_flag);
+            if (lane == 0) mbar_arrive(bar_group(wg));
+            const bool r = mbar_wait_warp(bar_group(wg), gphase, abort_flag);
             gphase ^= 1u;
             return r;
         };
@@ -677,24 +740,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int p_chunk = (row & 63) >> 3;
         const int red_row = reduced_row<NQ>(lane);
         const bool red_writer = reduced_writer<NQ>(lane);
+        float *my_red_sum = red_sum + wg * (kN * 4);
         for (int64_t it = sch.first(); sch.more(it) && ok; it = sch.next(it)) {
             const int64_t u = sch.unit(it);
             Unit x;
-            if (!unit_at(a, u, x)) continue;
+            if (!unit_at(a, u, x, lens)) continue;
             int32_t lastv[NQ];
 #pragma unroll
             for (int n = 0; n < NQ; ++n) {
                 o[n] = 0.f;
                 lsum[n] = 0.f;
                 mrun[n] = -INFINITY;
-                corr_prev[n] = 1.f;
                 const int t = n / G;
                 lastv[n] = (n < nq) ? (a.mask_mode == 0 ? x.L - a.q_len + t : x.L - 1) : -1;
             }
             for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
+                if ((int)(j & 1) != wg) continue;
                 const int s = (int)(j % kStages);
-                const int b = (int)(j & 1);
-                if (!mbar_wait_warp(bar_sfull(b), (uint32_t)((j >> 1) & 1), abort_flag) ||
+                const int b = wg;
+                const uint32_t par = (uint32_t)((j >> 1) & 1);
+                if (!mbar_wait_warp(bar_sfull(b), par, abort_flag) ||
                     !mbar_wait_warp(bar_full(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
                     ok = false;
                     break;
@@ -703,13 +768,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float sv[NQ];
                 tmem_ld_cols<NQ>(tmem + lane_base + 16u * b, sv);
                 const int32_t pos = x.start + jt * kTile + row;
-                const bool loaded = (mask_words[s * 4 + (row >> 5)] >> (row & 31)) & 1u;
+                const bool loaded = (mask_words[s * 4] >> (row >> seg_shift)) & 1u;
                 const bool inrange = loaded && pos < x.cend;
 #pragma unroll
                 for (int n = 0; n < NQ; ++n) sv[n] = (inrange && pos <= lastv[n]) ? sv[n] * a.scale_log2 : -INFINITY;
-                // tile max per query row across the 128 threads
+                // tile max per query row across the warpgroup's 128 threads
                 const float wmax = warp_reduce_rows<true, NQ>(sv, lane);
-                float *rm = red_max + b * (kN * 4);
+                float *rm = red_max + (wg * 2 + (int)par) * (kN * 4);
                 if (red_writer) rm[red_row * 4 + wq] = wmax;
                 if (!group_sync()) {
                     ok = false;
@@ -722,9 +787,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float4 t4 = *reinterpret_cast<const float4 *>(rm + n * 4);
                     const float mt = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
                     const float mn = fmaxf(mrun[n], mt);
-                    corr[n] = (mn == -INFINITY) ? 1.f : exp2f(mrun[n] - mn);
+                    corr[n] = (mn == -INFINITY) ? 1.f : fast_exp2(mrun[n] - mn);
                     mrun[n] = mn;
-                    const float p = (sv[n] == -INFINITY) ? 0.f : exp2f(sv[n] - mn);
+                    const float p = (sv[n] == -INFINITY) ? 0.f : fast_exp2(sv[n] - mn);
                     const __nv_bfloat16 pbv = __float2bfloat16_rn(p);
                     lsum[n] = fmaf(lsum[n], corr[n], __bfloat162float(pbv));
                     *reinterpret_cast<__nv_bfloat16 *>(pgen + n * 128 + ((p_chunk ^ (n & 7)) << 4)) = pbv;
@@ -745,50 +810,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_pfull(b));
-                // fold in the previous tile's P.V, one tile behind
-                if (jt > 0) {
-                    const int64_t jp = j - 1;
-                    if (!mbar_wait_warp(bar_ofull((int)(jp & 1)), (uint32_t)((jp >> 1) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    float ot[NQ];
-                    tmem_ld_cols<NQ>(tmem + lane_base + 32u + 16u * (uint32_t)(jp & 1), ot);
-#pragma unroll
-                    for (int n = 0; n < NQ; ++n) o[n] = fmaf(o[n], corr_prev[n], ot[n]);
-                }
-#pragma unroll
-                for (int n = 0; n < NQ; ++n) corr_prev[n] = corr[n];
-            }
-            if (!ok) break;
-            // last tile of the unit
-            {
-                const int64_t jl = j - 1;
-                if (!mbar_wait_warp(bar_ofull((int)(jl & 1)), (uint32_t)((jl >> 1) & 1), abort_flag)) {
+                // this tile's P.V (the other warpgroup works meanwhile)
+                if (!mbar_wait_warp(bar_ofull(b), par, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 float ot[NQ];
-                tmem_ld_cols<NQ>(tmem + lane_base + 32u + 16u * (uint32_t)(jl & 1), ot);
+                tmem_ld_cols<NQ>(tmem + lane_base + 32u + 16u * b, ot);
 #pragma unroll
-                for (int n = 0; n < NQ; ++n) o[n] = fmaf(o[n], corr_prev[n], ot[n]);
+                for (int n = 0; n < NQ; ++n) o[n] = fmaf(o[n], corr[n], ot[n]);
             }
-            // row sums across the 128 threads, then the partial (o, m, l)
+            if (!ok) break;
+            // row sums across the warpgroup, then this warpgroup's partial (o, m, l)
             {
                 const float wsum = warp_reduce_rows<false, NQ>(lsum, lane);
-                if (red_writer) red_sum[red_row * 4 + wq] = wsum;
+                if (red_writer) my_red_sum[red_row * 4 + wq] = wsum;
                 if (!group_sync()) {
                     ok = false;
                     break;
                 }
-                const int64_t prow0 = u * nq;
+                const int64_t prow0 = (u * 2 + wg) * nq;
 #pragma unroll
                 for (int n = 0; n < NQ; ++n)
                     if (n < nq) a.ws_o[(prow0 + n) * kD + row] = o[n];
                 if (row < nq) {
-                    const float4 t4 = *reinterpret_cast<const float4 *>(red_sum + row * 4);
+                    const float4 t4 = *reinterpret_cast<const float4 *>(my_red_sum + row * 4);
                     float m_row = -INFINITY;
 #pragma unroll
                     for (int n = 0; n < NQ; ++n)
@@ -796,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     a.ws_ml[(prow0 + row) * 2 + 0] = m_row;
                     a.ws_ml[(prow0 + row) * 2 + 1] = (t4.x + t4.y) + (t4.z + t4.w);
                 }
-                if (!group_sync()) {   // red_sum is reused by the next unit
+                if (!group_sync()) {   // the row-sum buffer is reused by the next unit
                     ok = false;
                     break;
                 }
