@@ -187,6 +187,42 @@ int bkv_paged_decode(const void *q, const void *k_cache, const void *v_cache,
                      int dtype, void *out, void *workspace, size_t workspace_bytes,
                      int32_t *err_count, bkv_stream_t stream);
 
+/*
+ * bkv_paged_decode_noalloc
+ *   No counterpart on the pages: this is a convenience of this library.
+ *
+ *   Same operation, arguments and results as bkv_paged_decode, but with no
+ *   workspace argument and no device allocation of any kind.  It is for
+ *   callers that cannot call cudaMalloc: code running while a stream is
+ *   being captured into a CUDA graph under a mode that forbids allocation,
+ *   plugins whose host framework owns all device memory and refuses new
+ *   allocations after start-up, or plain C callers that hold only raw
+ *   pointers to their inputs and outputs and no allocator.
+ *
+ *   The split-KV scratch lives in one fixed device array of
+ *   BKV_NOALLOC_SCRATCH_BYTES inside this library; every GPU on which the
+ *   library is used holds that array until the process exits.  Shapes whose
+ *   bkv_paged_decode_workspace_size(...) exceeds it are rejected with
+ *   BKV_ERR_UNSUPPORTED before anything is enqueued (use bkv_paged_decode
+ *   with your own workspace for those).
+ *
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.  All calls share the one array and leave the
+ *   last call's partial results in it (nothing in it has to start at zero):
+ *   calls whose kernels overlap on the GPU (on different streams without
+ *   ordering between them) race on it and give undefined results.
+ */
+#define BKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+int bkv_paged_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
+                             const int32_t *context_lens, int32_t max_context_len,
+                             int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int64_t total_blocks, float softmax_scale, int mask_mode, int dtype,
+                             void *out, int32_t *err_count, bkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
