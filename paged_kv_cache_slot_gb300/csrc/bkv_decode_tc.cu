@@ -60,7 +60,8 @@ constexpr int kTileBytes = 2 * kHalfBytes;       // K or V tile: 32 KB
 constexpr int kStageBytes = 2 * kTileBytes;      // K + V: 64 KB
 constexpr int kQBytes = 2 * kN * 128;            // 16 rows x 128 B x 2 halves: 4 KB
 constexpr int kPBytes = 2 * kN * 128;            // 16 rows x 128 positions (2 x 64) bf16: 4 KB
-constexpr int kThreads = 320;                    // producer, MMA, two softmax warpgroups
+constexpr int kThreads = 352;                    // K producer, MMA, two softmax warpgroups, V producer
+constexpr int kWarpV = kThreads / 32 - 1;        // the V producer's warp
 constexpr int kTmemCols = 64;                    // S x2 (16 cols each) + O x2
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr int kTimeoutErr = 1 << 24;
@@ -69,11 +70,11 @@ constexpr int kTimeoutErr = 1 << 24;
 constexpr int kOffStages = 0;
 constexpr int kOffQ = kOffStages + kStages * kStageBytes;
 constexpr int kOffP = kOffQ + 2 * kQBytes;
-constexpr int kOffMask = kOffP + 2 * kPBytes;             // kStages x 4 words (word 0: loaded segments)
-constexpr int kOffRedMax = kOffMask + kStages * 16;       // [warpgroup][2][16 rows][4 warps] floats
+constexpr int kOffMask = kOffP + 2 * kPBytes;             // 8 words: loaded segments per tile (ring)
+constexpr int kOffRedMax = kOffMask + 64;                 // [warpgroup][2][16 rows][4 warps] floats
 constexpr int kOffRedSum = kOffRedMax + 4 * kN * 4 * 4;   // [warpgroup][16 rows][4 warps] floats
 constexpr int kOffBar = kOffRedSum + 2 * kN * 4 * 4;      // barriers (8 B each)
-constexpr int kNumBars = 2 * kStages + 2 * 5 + 2;
+constexpr int kNumBars = 4 * kStages + 2 * 5 + 2 + 8;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 // Per-CTA schedule: units sorted by tile count (largest first), dealt round-robin.
@@ -85,9 +86,9 @@ constexpr int kOffInfo = kOffAbort + 4;                   // per request: clampe
 constexpr int kOffList = kOffInfo + kMaxReqsSorted * 4;   // this CTA's units in order
 constexpr int kOffBucket = kOffList + kMaxListed * 4;     // units per bucket, then bucket offsets
 constexpr int kOffSched = kOffBucket + 2 * (kMaxBuckets + 1) * 4;   // [0] = units listed, [1] = mode
-constexpr int kMaxUnitBlocks = 256;                       // table entries the producer caches per unit
-constexpr int kOffEnt = kOffSched + 8;                    // 2 x kMaxUnitBlocks table entries
-constexpr int kSmemUsed = kOffEnt + 2 * kMaxUnitBlocks * 4;
+constexpr int kMaxUnitBlocks = 128;                       // table entries a producer caches per unit
+constexpr int kOffEnt = kOffSched + 8;                    // [producer][2][kMaxUnitBlocks] table entries
+constexpr int kSmemUsed = kOffEnt + 4 * kMaxUnitBlocks * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;              // slack for 1024 alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
 
@@ -453,14 +454,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
     const uint32_t bar0 = sbase + kOffBar;
-    auto bar_full = [&](int s) { return bar0 + 8u * s; };
-    auto bar_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto bar_qfull = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-    auto bar_qempty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-    auto bar_sfull = [&](int b) { return bar0 + 8u * (2 * kStages + 4 + b); };
-    auto bar_pfull = [&](int b) { return bar0 + 8u * (2 * kStages + 6 + b); };
-    auto bar_ofull = [&](int b) { return bar0 + 8u * (2 * kStages + 8 + b); };
-    auto bar_group = [&](int k) { return bar0 + 8u * (2 * kStages + 10 + k); };   // four warps of warpgroup k
+    // K and V tiles have separate rings (same slot numbering): a K slot is
+    // released as soon as the S MMA that reads it completes.
+    auto bar_kfull = [&](int s) { return bar0 + 8u * s; };
+    auto bar_kempty = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto bar_vfull = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
+    auto bar_vempty = [&](int s) { return bar0 + 8u * (3 * kStages + s); };
+    auto bar_qfull = [&](int b) { return bar0 + 8u * (4 * kStages + b); };
+    auto bar_qempty = [&](int b) { return bar0 + 8u * (4 * kStages + 2 + b); };
+    auto bar_sfull = [&](int b) { return bar0 + 8u * (4 * kStages + 4 + b); };
+    auto bar_pfull = [&](int b) { return bar0 + 8u * (4 * kStages + 6 + b); };
+    auto bar_ofull = [&](int b) { return bar0 + 8u * (4 * kStages + 8 + b); };
+    auto bar_group = [&](int k) { return bar0 + 8u * (4 * kStages + 10 + k); };   // four warps of warpgroup k
+    // "loaded segments" word of tile j: mask_words[j & 7], published with bar_mask(j & 7)
+    auto bar_mask = [&](int m) { return bar0 + 8u * (4 * kStages + 12 + m); };
     const uint32_t sm_stage = sbase + kOffStages;
     const uint32_t sm_q = sbase + kOffQ;
     const uint32_t sm_p = sbase + kOffP;
@@ -468,8 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- set-up: barriers, zeroed V / Q / P buffers, TMEM ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_full(s), 1);
-            mbar_init(bar_empty(s), 1);
+            mbar_init(bar_kfull(s), 1);
+            mbar_init(bar_kempty(s), 1);
+            mbar_init(bar_vfull(s), 1);
+            mbar_init(bar_vempty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_qfull(b), 1);
@@ -480,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar_group(0), 4);
         mbar_init(bar_group(1), 4);
+        for (int m = 0; m < 8; ++m) mbar_init(bar_mask(m), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -528,13 +538,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nseg = kTile / seg_rows;         // block segments per tile (1..16)
     const int seg_shift = 31 - __clz(seg_rows);   // seg_rows is a power of two
 
-    if (warp == 0) {
-        // ================= TMA producer =================
+    if (warp == 0 || warp == kWarpV) {
+        // ================= TMA producers (warp 0: K and Q, last warp: V) =================
+        const bool is_v = warp == kWarpV;
         // The table entries of a unit (one per block it covers) are loaded
         // into registers one unit ahead and parked in shared memory, so no
         // table lookup sits between a stage becoming free and its refill.
         // An entry past the table width is parked as INT32_MIN.
-        int32_t *ent_buf = reinterpret_cast<int32_t *>(smem + kOffEnt);
+        int32_t *ent_buf = reinterpret_cast<int32_t *>(smem + kOffEnt) + (is_v ? 2 * kMaxUnitBlocks : 0);
         constexpr int kEntRegs = kMaxUnitBlocks / 32;
         int32_t ent_reg[kEntRegs];
         auto unit_blocks = [&](const Unit &x) { return (x.cend - x.start + a.bs - 1) / a.bs; };
@@ -580,10 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool next_cached = it_next >= 0 && unit_blocks(nx) <= kMaxUnitBlocks;
             if (next_cached) fetch_entries(nx);     // in flight while this unit's tiles are issued
             const int32_t *ents = ent_buf + (us & 1) * kMaxUnitBlocks;
-            if (lane == 0 && x.c == 0 && x.g == 0 && __ldg(a.ctx + x.r) > a.max_ctx && a.err) atomicAdd(a.err, 1);
+            if (!is_v && lane == 0 && x.c == 0 && x.g == 0 && __ldg(a.ctx + x.r) > a.max_ctx && a.err)
+                atomicAdd(a.err, 1);
             const int qb = us & 1;
-            if (!mbar_wait_warp(bar_qempty(qb), ((us >> 1) & 1) ^ 1, abort_flag)) break;
-            if (lane == 0) {
+            if (!is_v && !mbar_wait_warp(bar_qempty(qb), ((us >> 1) & 1) ^ 1, abort_flag)) break;
+            if (!is_v && lane == 0) {
                 mbar_arrive_expect_tx(bar_qfull(qb), 2u * 128u * (uint32_t)nq);
                 const uint32_t dq = sm_q + qb * kQBytes;
                 tma_load_3d(dq, &tmQ, bar_qfull(qb), 0, x.g * G, x.r * a.q_len);
@@ -591,7 +603,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
                 const int s = (int)(j % kStages);
-                if (!mbar_wait_warp(bar_empty(s), (uint32_t)((j / kStages) & 1) ^ 1u, abort_flag)) break;
+                const uint32_t bar_e = is_v ? bar_vempty(s) : bar_kempty(s);
+                const uint32_t bar_f = is_v ? bar_vfull(s) : bar_kfull(s);
+                if (!mbar_wait_warp(bar_e, (uint32_t)((j / kStages) & 1) ^ 1u, abort_flag)) break;
                 const int32_t ts = x.start + jt * kTile;
                 // lane i handles block segment i of the tile
                 bool load = false;
@@ -608,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             e = lb < a.bt_cols ? (int64_t)__ldg(a.bt + (int64_t)x.r * a.bt_stride + lb) : INT32_MIN;
                         }
                         if (e == INT32_MIN || e >= a.total_blocks) {
-                            if (a.err) atomicAdd(a.err, 1);
+                            if (!is_v && a.err) atomicAdd(a.err, 1);
                         } else if (e > 0) {
                             load = true;
                             row0 = e * a.bs + (p0 - (int64_t)lb * a.bs);
@@ -617,19 +631,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t ballot = __ballot_sync(0xffffffffu, load);
                 if (lane == 0) {
-                    mask_words[s * 4] = ballot;   // bit i: segment i was loaded
-                    const uint32_t bytes = (uint32_t)__popc(ballot) * (uint32_t)seg_rows * 128u * 4u;
-                    mbar_arrive_expect_tx(bar_full(s), bytes);
+                    // bit i: segment i was loaded.  A ring of 8 words by tile number with
+                    // its own barriers: the K producer writes tile j's word only after
+                    // the S MMA of tile j - 3 completed, which is issued only after the
+                    // softmax released tile j - 5, so it is never more than 5 tiles ahead
+                    // of the reader and a slot's phases cannot alias.
+                    if (!is_v) {
+                        mask_words[j & 7] = ballot;
+                        mbar_arrive(bar_mask((int)(j & 7)));
+                    }
+                    const uint32_t bytes = (uint32_t)__popc(ballot) * (uint32_t)seg_rows * 128u * 2u;
+                    mbar_arrive_expect_tx(bar_f, bytes);
                 }
                 __syncwarp();
                 if (load) {
-                    const uint32_t dk = sm_stage + s * kStageBytes + lane * seg_rows * 128;
-                    const uint32_t dv = dk + kTileBytes;
+                    const uint32_t dst = sm_stage + s * kStageBytes + (is_v ? kTileBytes : 0) + lane * seg_rows * 128;
+                    const CUtensorMap *map = is_v ? &tmV : &tmK;
                     const int z = (int)row0;
-                    tma_load_3d(dk, &tmK, bar_full(s), 0, x.g, z);
-                    tma_load_3d(dk + kHalfBytes, &tmK, bar_full(s), 64, x.g, z);
-                    tma_load_3d(dv, &tmV, bar_full(s), 0, x.g, z);
-                    tma_load_3d(dv + kHalfBytes, &tmV, bar_full(s), 64, x.g, z);
+                    tma_load_3d(dst, map, bar_f, 0, x.g, z);
+                    tma_load_3d(dst + kHalfBytes, map, bar_f, 64, x.g, z);
                 }
                 __syncwarp();
             }
@@ -656,7 +676,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             auto issue_pv = [&](int64_t jp, int stage) -> bool {
                 const int b = (int)(jp & 1);
-                if (!mbar_wait(bar_pfull(b), (uint32_t)((jp >> 1) & 1), abort_flag)) return false;
+                if (!mbar_wait(bar_vfull(stage), (uint32_t)((jp / kStages) & 1), abort_flag) ||
+                    !mbar_wait(bar_pfull(b), (uint32_t)((jp >> 1) & 1), abort_flag))
+                    return false;
                 tc_fence_after();
                 const uint32_t v_base = sm_stage + stage * kStageBytes + kTileBytes;
                 const uint32_t p_base = sm_p + b * kPBytes;
@@ -668,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16(d_tmem, adesc, bdesc, kIdescO, kk > 0);
                 }
                 mma_commit(bar_ofull(b));
-                mma_commit(bar_empty(stage));
+                mma_commit(bar_vempty(stage));
                 return true;
             };
             for (int64_t it = sch.first(); sch.more(it) && ok; it = sch.next(it)) {
@@ -682,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
                     const int s = (int)(j % kStages);
-                    if (!mbar_wait(bar_full(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
+                    if (!mbar_wait(bar_kfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -698,6 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(d_tmem, adesc, bdesc, kIdescS, kk > 0);
                     }
                     mma_commit(bar_sfull((int)(j & 1)));
+                    mma_commit(bar_kempty(s));
                     if (jt == x.ntiles - 1) mma_commit(bar_qempty(qb));
                     if (pending >= 0 && !issue_pv(pending, pending_stage)) {
                         ok = false;
@@ -760,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = wg;
                 const uint32_t par = (uint32_t)((j >> 1) & 1);
                 if (!mbar_wait_warp(bar_sfull(b), par, abort_flag) ||
-                    !mbar_wait_warp(bar_full(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
+                    !mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -768,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float sv[NQ];
                 tmem_ld_cols<NQ>(tmem + lane_base + 16u * b, sv);
                 const int32_t pos = x.start + jt * kTile + row;
-                const bool loaded = (mask_words[s * 4] >> (row >> seg_shift)) & 1u;
+                const bool loaded = (mask_words[j & 7] >> (row >> seg_shift)) & 1u;
                 const bool inrange = loaded && pos < x.cend;
 #pragma unroll
                 for (int n = 0; n < NQ; ++n) sv[n] = (inrange && pos <= lastv[n]) ? sv[n] * a.scale_log2 : -INFINITY;
@@ -795,7 +818,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<__nv_bfloat16 *>(pgen + n * 128 + ((p_chunk ^ (n & 7)) << 4)) = pbv;
                 }
                 // V rows that were loaded but lie past the end must be zero for P.V
-                if (loaded && pos >= x.cend) {
+                // (after the V tile has landed)
+                const bool zero_row = loaded && pos >= x.cend;
+                if (__any_sync(0xffffffffu, zero_row) &&
+                    !mbar_wait_warp(bar_vfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (zero_row) {
                     uint4 *vrow0 = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes +
                                                              row * 128);
                     uint4 *vrow1 = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes +
