@@ -197,33 +197,50 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// Merge: out = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the
-// request's partitions, M = max_c m_c; 0 when no partition saw a visible key.
-// One CTA per output row (request, KV head, query row of the group).  Warp 0
-// turns every partition's (m, l) into a weight in shared memory; then the
-// four warps split the partitions, each lane summing four head_dim elements
-// (one 16-byte load per partition), and combine through shared memory.
+// Merge: out = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over a stream's
+// partial slots, M = max_c m_c; 0 when no slot saw a visible key.  One CTA
+// per stream (request, KV head); each warp takes query rows warp, warp + 4,
+// ...: the lanes read the slots' (m, l) pairs in one round, turn them into
+// weights in the warp's own shared-memory strip, and then each lane sums
+// four head_dim elements over the slots with 16-byte loads.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int max_slots) {
     pdl_wait();
     pdl_trigger();
-    extern __shared__ float sw[];   // [n_chunks * parts] weights, 1 / denominator, then [4][D] warp sums
+    extern __shared__ float sw[];   // [4 warps][max_slots] weights
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int64_t idx = blockIdx.x;           // (r * H_kv + g) * nq + row
-    const int row = (int)(idx % a.nq);
-    const int64_t rg = idx / a.nq;
+    const int64_t rg = blockIdx.x;            // stream: r * H_kv + g
     const int r = (int)(rg / a.H_kv);
     const int g = (int)(rg - (int64_t)r * a.H_kv);
     const int32_t L = clamped_len(a, r, false);
-    // a request's partial slots are contiguous: `parts` per partition
-    const int nch = L > 0 ? (int)ceil_div<int32_t>(L, a.chunk) * a.parts : 0;
-    const int64_t unit0 = rg * a.n_chunks * a.parts;
-    const int nslots = a.n_chunks * a.parts;
-    float *inv = sw + nslots;
-    float *part = sw + ((nslots + 1 + 3) & ~3);   // 16-byte aligned
-    if (warp == 0) {
+    // a stream's partial slots are contiguous
+    int nch = 0;          // slots of this stream
+    int64_t unit0 = 0;    // its first slot
+    if (a.sk_pre) {
+        // stream-K: stream s has T tiles starting at global tile S; CTA k of
+        // geff = min(sk_grid, TT) covers [k TT / geff, (k + 1) TT / geff) and
+        // writes slots 2 (k + s) and 2 (k + s) + 1 for its overlap with s
+        const int64_t T = a.sk_pre[r + 1] - a.sk_pre[r];
+        const int64_t TT = (int64_t)a.H_kv * a.sk_pre[a.num_reqs];
+        if (T > 0 && L > 0) {
+            const int64_t geff = TT < (int64_t)a.sk_grid ? TT : (int64_t)a.sk_grid;   // CTAs with tiles
+            const int64_t S = (int64_t)a.H_kv * a.sk_pre[r] + g * T;
+            const int64_t k0 = ((S + 1) * geff - 1) / TT;
+            const int64_t k1 = ((S + T) * geff - 1) / TT;
+            nch = (int)(2 * (k1 - k0 + 1));
+            unit0 = 2 * (k0 + rg);
+        }
+    } else {
+        nch = L > 0 ? (int)ceil_div<int32_t>(L, a.chunk) * a.parts : 0;
+        unit0 = rg * a.n_chunks * a.parts;
+    }
+    float *wts = sw + (size_t)warp * max_slots;
+    for (int row = warp; row < a.nq; row += 4) {
+        const int t = row / a.G;
+        const int h = g * a.G + (row - t * a.G);
+        T *out = static_cast<T *>(a.out) + (((int64_t)r * a.q_len + t) * a.H_q + h) * a.D;
         float M = -INFINITY;
         for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.ws_ml[((unit0 + c) * a.nq + row) * 2]);
 #pragma unroll
@@ -232,56 +249,51 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
         for (int c = lane; c < nch; c += 32) {
             const float2 ml = *reinterpret_cast<const float2 *>(a.ws_ml + ((unit0 + c) * a.nq + row) * 2);
             const float wgt = M == -INFINITY ? 0.f : exp2f(ml.x - M);
-            sw[c] = wgt;
+            wts[c] = wgt;
             lsum = fmaf(wgt, ml.y, lsum);
         }
         lsum = warp_sum(lsum);
-        if (lane == 0) inv[0] = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : 1.f / lsum;
-    }
-    __syncthreads();
-    const int t = row / a.G;
-    const int h = g * a.G + (row - t * a.G);
-    T *out = static_cast<T *>(a.out) + (((int64_t)r * a.q_len + t) * a.H_q + h) * a.D;
-    const float iv = inv[0];
-    if ((a.D & 3) == 0) {
-        for (int d4 = lane; d4 < a.D / 4; d4 += 32) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            int c = warp;
-            for (; c + 12 < nch; c += 16) {
-                float4 v[4];
+        const float iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : 1.f / lsum;
+        __syncwarp();
+        if ((a.D & 3) == 0) {
+            for (int d4 = lane; d4 < a.D / 4; d4 += 32) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                int c = 0;
+                for (; c + 4 <= nch; c += 4) {
+                    float4 v[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    v[k] = *reinterpret_cast<const float4 *>(a.ws_o + ((unit0 + c + 4 * k) * a.nq + row) * a.D + 4 * d4);
+                    for (int k = 0; k < 4; ++k)
+                        v[k] = *reinterpret_cast<const float4 *>(a.ws_o + ((unit0 + c + k) * a.nq + row) * a.D + 4 * d4);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float wgt = sw[c + 4 * k];
-                    acc.x = fmaf(wgt, v[k].x, acc.x);
-                    acc.y = fmaf(wgt, v[k].y, acc.y);
-                    acc.z = fmaf(wgt, v[k].z, acc.z);
-                    acc.w = fmaf(wgt, v[k].w, acc.w);
+                    for (int k = 0; k < 4; ++k) {
+                        const float wgt = wts[c + k];
+                        acc.x = fmaf(wgt, v[k].x, acc.x);
+                        acc.y = fmaf(wgt, v[k].y, acc.y);
+                        acc.z = fmaf(wgt, v[k].z, acc.z);
+                        acc.w = fmaf(wgt, v[k].w, acc.w);
+                    }
                 }
+                for (; c < nch; ++c) {
+                    const float4 v = *reinterpret_cast<const float4 *>(a.ws_o + ((unit0 + c) * a.nq + row) * a.D + 4 * d4);
+                    const float wgt = wts[c];
+                    acc.x = fmaf(wgt, v.x, acc.x);
+                    acc.y = fmaf(wgt, v.y, acc.y);
+                    acc.z = fmaf(wgt, v.z, acc.z);
+                    acc.w = fmaf(wgt, v.w, acc.w);
+                }
+                store_out(out + 4 * d4 + 0, acc.x * iv);
+                store_out(out + 4 * d4 + 1, acc.y * iv);
+                store_out(out + 4 * d4 + 2, acc.z * iv);
+                store_out(out + 4 * d4 + 3, acc.w * iv);
             }
-            for (; c < nch; c += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(a.ws_o + ((unit0 + c) * a.nq + row) * a.D + 4 * d4);
-                const float wgt = sw[c];
-                acc.x = fmaf(wgt, v.x, acc.x);
-                acc.y = fmaf(wgt, v.y, acc.y);
-                acc.z = fmaf(wgt, v.z, acc.z);
-                acc.w = fmaf(wgt, v.w, acc.w);
+        } else {
+            for (int d = lane; d < a.D; d += 32) {
+                float acc = 0.f;
+                for (int c = 0; c < nch; ++c) acc = fmaf(wts[c], a.ws_o[((unit0 + c) * a.nq + row) * a.D + d], acc);
+                store_out(out + d, acc * iv);
             }
-            *reinterpret_cast<float4 *>(part + warp * a.D + 4 * d4) = acc;
         }
-    } else {
-        for (int d = lane; d < a.D; d += 32) {
-            float acc = 0.f;
-            for (int c = warp; c < nch; c += 4) acc = fmaf(sw[c], a.ws_o[((unit0 + c) * a.nq + row) * a.D + d], acc);
-            part[warp * a.D + d] = acc;
-        }
-    }
-    __syncthreads();
-    for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
-        const float acc = (part[d] + part[a.D + d]) + (part[2 * a.D + d] + part[3 * a.D + d]);
-        store_out(out + d, acc * iv);
+        __syncwarp();   // the weight strip is rewritten for the warp's next row
     }
 }
 
@@ -319,8 +331,9 @@ bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int3
         const int64_t want = ceil_div<int64_t>((int64_t)max_context_len * units, 4 * sms);
         chunk = ceil_div<int64_t>(want > 0 ? want : 1, align) * align;
     }
-    // keep the merge's per-row weight table small
-    if (ceil_div<int64_t>(max_context_len, chunk) > 4096) chunk = ceil_div<int64_t>(ceil_div<int64_t>(max_context_len, 4096), align) * align;
+    // keep the merge's weight tables (4 warps x partitions, fp32) within 32 KB
+    if (ceil_div<int64_t>(max_context_len, chunk) > 2048)
+        chunk = ceil_div<int64_t>(ceil_div<int64_t>(max_context_len, 2048), align) * align;
     if (chunk > (int64_t)1 << 30) return false;
     const int64_t n_chunks = max_context_len > 0 ? ceil_div<int64_t>(max_context_len, chunk) : 1;
     const int64_t nq = (int64_t)q_len * (num_q_heads / num_kv_heads);
@@ -328,9 +341,14 @@ bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int3
     plan->chunk = (int32_t)chunk;
     plan->n_chunks = (int32_t)n_chunks;
     plan->nq = (int32_t)nq;
-    const int64_t prows = units * n_chunks * 2 * nq;   // up to two partial slots per unit
+    plan->sk_grid = (int32_t)sms;
+    plan->header_bytes = (size_t)ceil_div<int64_t>(((int64_t)num_reqs + 1) * 4, 256) * 256;
+    const int64_t slots_generic = units * n_chunks;
+    const int64_t slots_sk = 2 * (sms + units);
+    const int64_t slots = slots_generic > slots_sk ? slots_generic : slots_sk;
+    const int64_t prows = slots * nq;
     const int64_t o_bytes = ceil_div<int64_t>(prows * head_dim * 4, 256) * 256;
-    plan->ws_bytes = (size_t)(o_bytes + prows * 2 * 4);
+    plan->ws_bytes = plan->header_bytes + (size_t)(o_bytes + prows * 2 * 4);
     return true;
 }
 
@@ -404,11 +422,17 @@ extern "C" int bkv_paged_decode(const void *q, const void *k_cache, const void *
     a.n_chunks = plan.n_chunks;
     a.G = num_q_heads / num_kv_heads;
     a.nq = plan.nq;
-    const int64_t prows = (int64_t)num_reqs * num_kv_heads * plan.n_chunks * 2 * plan.nq;
+    // partial-slot layout of the kernel that runs (see DecodePlan)
+    auto set_slots = [&](int64_t slots) {
+        char *base = static_cast<char *>(workspace) + plan.header_bytes;
+        a.ws_o = reinterpret_cast<float *>(base);
+        a.ws_ml = reinterpret_cast<float *>(base + bkv::ceil_div<int64_t>(slots * plan.nq * head_dim * 4, 256) * 256);
+    };
+    const int64_t units = (int64_t)num_reqs * num_kv_heads;
     a.parts = 2;
-    a.ws_o = static_cast<float *>(workspace);
-    a.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                        bkv::ceil_div<int64_t>(prows * head_dim * 4, 256) * 256);
+    a.sk_pre = static_cast<int32_t *>(workspace);
+    a.sk_grid = plan.sk_grid;
+    set_slots(2 * (plan.sk_grid + units));
     a.out = out;
     a.err = err_count;
 
@@ -417,18 +441,21 @@ extern "C" int bkv_paged_decode(const void *q, const void *k_cache, const void *
     if (bkv::decode_tc_supported(a)) rc = bkv::launch_decode_tc(a, st);
     if (rc == BKV_ERR_UNSUPPORTED) {
         a.parts = 1;
+        a.sk_pre = nullptr;
+        set_slots(units * plan.n_chunks);
         if (dtype == BKV_BF16) bkv::launch_generic_dpl<__nv_bfloat16>(a, st);
         else bkv::launch_generic_dpl<float>(a, st);
         rc = bkv::launch_status();
     }
     if (rc != BKV_OK) return rc;
 
-    const size_t nslots = (size_t)plan.n_chunks * a.parts;
-    const size_t msmem = (((nslots + 1 + 3) & ~(size_t)3) + 4 * (size_t)head_dim) * 4;
-    const dim3 mgrid((unsigned)((int64_t)num_reqs * num_kv_heads * plan.nq));
-    const cudaError_t e = dtype == BKV_BF16
-                              ? bkv::launch_pdl(bkv::decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(128), msmem, st, a)
-                              : bkv::launch_pdl(bkv::decode_merge_kernel<float>, mgrid, dim3(128), msmem, st, a);
+    const int max_slots = a.sk_pre ? 2 * plan.sk_grid : plan.n_chunks * a.parts;
+    const size_t msmem = 4 * (size_t)max_slots * 4;
+    const dim3 mgrid((unsigned)((int64_t)num_reqs * num_kv_heads));
+    const cudaError_t e =
+        dtype == BKV_BF16
+            ? bkv::launch_pdl(bkv::decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(128), msmem, st, a, max_slots)
+            : bkv::launch_pdl(bkv::decode_merge_kernel<float>, mgrid, dim3(128), msmem, st, a, max_slots);
     if (e != cudaSuccess) bkv::set_cuda_error(e);
     return bkv::launch_status();
 }

@@ -25,18 +25,26 @@ struct DecodeArgs {
     int32_t G;         // query heads per KV head
     int32_t nq;        // query rows per KV head: q_len * G, row i = t * G + (h % G)
     int32_t parts;     // partials per unit (slots): 1 for the generic kernel, 2 for the tensor-core one
-    float *ws_o;       // [num_reqs * H_kv * n_chunks * parts][nq][D] unnormalised partial outputs
-    float *ws_ml;      // [num_reqs * H_kv * n_chunks * parts][nq][2]  (running max in base 2, sum of weights)
+    int32_t *sk_pre;   // tensor-core kernel: [num_reqs + 1] tiles-per-request prefix (written by its CTA 0)
+    int32_t sk_grid;   // tensor-core kernel: CTAs of the stream-K split
+    float *ws_o;       // [slots][nq][D] unnormalised partial outputs
+    float *ws_ml;      // [slots][nq][2]  (running max in base 2, sum of weights)
     void *out;
     int32_t *err;
 };
 
 // Split of each request's context into partitions; identical for the
-// workspace query and the decode call.
+// workspace query and the decode call.  The workspace holds, in order, the
+// stream-K header ([num_reqs + 1] int32, 256-byte padded) and the partials
+// of whichever kernel runs: the generic kernel's (request, KV head,
+// partition) slots or the tensor-core kernel's 2 (sk_grid + num_reqs * H_kv)
+// stream-K slots.
 struct DecodePlan {
     int32_t chunk;
     int32_t n_chunks;
     int32_t nq;
+    int32_t sk_grid;
+    size_t header_bytes;
     size_t ws_bytes;
 };
 

@@ -2,38 +2,47 @@
 // paged decode, bf16, head_dim 128, up to 16 query rows per KV head.
 //
 // Operation ("Padding and Batching with Block KV", Cache Masking; Special
-// Block and Slot Values): for one unit = (request r, KV head g, partition
-// of `chunk` logical positions) compute, for every query row n = t * G + hh
-// of the GQA group, the online-softmax partial (o, m, l) over the visible
-// positions of the partition.  The merge kernel in bkv_decode.cu combines
-// partitions.
+// Block and Slot Values): for a run of consecutive 128-position tiles of one
+// stream (request r, KV head g), compute for every query row n = t * G + hh
+// of the GQA group the online-softmax partial (o, m, l) over the visible
+// positions of those tiles.  The merge kernel in bkv_decode.cu combines the
+// partials of each stream.
 //
 // Design (sm_103a):
-// * Persistent CTAs (one per SM, ~225 KB of shared memory).  Each CTA sorts
-//   the non-empty units by size (largest first) in its set-up and takes
-//   every gridDim-th one, which keeps the busiest SM within a few percent of
-//   the average (natural order left it 1.7x above on the Llama-shaped batch).  Warp 0 is the TMA producer, warp 1 issues tcgen05.mma from
-//   one thread and owns the TMEM allocation, and two warpgroups (warps 2..5
-//   and 6..9) run the softmax and the output update on alternate tiles, so
-//   one group's waits overlap the other's arithmetic.  Each group keeps its
-//   own online-softmax state and writes its own partial per unit.
-// * A tile is 128 logical positions.  The producer gathers the tile's K and
-//   V rows of KV head g through the block table with 3-D TMA loads
-//   (cp.async.bulk.tensor; map over (head_dim, H_kv, total_blocks *
-//   block_size), box = 64 x 1 x min(block_size, 128) rows, 128-byte
-//   swizzle), one load per block segment and head_dim half, into a 3-stage
-//   ring of 64 KB stages.  Null (<= 0) and out-of-range table entries are
-//   not loaded at all, and blocks past the request's length are never
-//   touched, so traffic is the ceil(len / block_size) blocks actually needed.
-// * S^T[128 x 16] = K_tile[128 x 128] . Q^T (M = positions, N = query rows
-//   padded to 16, K = head_dim), fp32 in TMEM.  Each softmax thread owns one
-//   position (one TMEM lane): masks by select, reduces the tile max per query
-//   row across the 128 threads, exponentiates in base 2, keeps its partial
-//   row sums, and writes P (bf16) to shared memory in the K-major layout.
+// * Stream-K schedule.  The streams' tiles (ceil(len / 128) per request and
+//   KV head, requests in order, heads in order) are laid end to end; the
+//   persistent CTA k (one per SM) takes the global tiles
+//   [k * TT / grid, (k + 1) * TT / grid), so every SM gets the same number
+//   of tiles to within one, whatever the mix of lengths (grid = min(SMs,
+//   TT), so that no participating CTA has an empty range).  Each overlap of a
+//   CTA range with a stream is a unit; the i-th unit along the sequence is
+//   the overlap of CTA k and stream s with k + s increasing by at least one
+//   per step, so unit (k, s) writes partial slots 2 (k + s) and
+//   2 (k + s) + 1 (one per softmax warpgroup), and stream s's slots are the
+//   contiguous range the merge recomputes from the per-request tile prefix
+//   sums that CTA 0 leaves in the workspace.
+// * Warp roles: warp 0 gathers K tiles (and Q), the last warp gathers V
+//   tiles, warp 1 issues tcgen05.mma from one thread and owns the TMEM
+//   allocation, and two warpgroups (warps 2..5 and 6..9) run the softmax and
+//   the output update on alternate tiles.  K and V have separate 3-slot
+//   rings of 32 KB: a K slot is released as soon as the S MMA that reads it
+//   completes.
+// * A tile's K (or V) rows of KV head g are gathered through the block
+//   table with 3-D TMA loads (cp.async.bulk.tensor; map over (head_dim,
+//   H_kv, total_blocks * block_size), box = 64 x 1 x min(block_size, 128)
+//   rows, 128-byte swizzle), one load per block segment and head_dim half.
+//   Null (<= 0) and out-of-range entries are not loaded at all and blocks
+//   past the request's end are never touched, so the traffic is the
+//   ceil(len / block_size) blocks actually needed.  Table entries are loaded
+//   a window ahead into registers and parked in shared memory.
+// * S^T[128 x 16] = K_tile . Q^T (M = positions, N = query rows padded to
+//   16, K = head_dim), fp32 in TMEM.  Each softmax thread owns one position
+//   (TMEM lane): masks by select, reduces the tile max per query row across
+//   its warpgroup, exponentiates in base 2, keeps its partial row sums, and
+//   writes P (bf16) to shared memory in the K-major swizzled layout.
 // * O^T[128 x 16] = V_tile^T . P^T (M = head_dim, V read MN-major straight
-//   from the TMA tile, K = positions).  Each softmax thread owns one head_dim
-//   row of O^T and accumulates o = o * 2^(m_old - m_new) + O_tile in
-//   registers.
+//   from the TMA tile, K = positions); each softmax thread owns one head_dim
+//   row of O^T and accumulates o = o * 2^(m_old - m_new) + O_tile.
 // * V rows that were loaded but lie past the request's end are zeroed in
 //   shared memory before the P.V MMA, so unwritten cache memory (which may
 //   hold NaN) never reaches the output; K rows there are masked by select.
@@ -57,7 +66,7 @@ constexpr int kN = 16;                // query rows per MMA (padded)
 constexpr int kStages = 3;
 constexpr int kHalfBytes = kTile * 128;          // 128 rows x 64 bf16 (128 B): one head_dim half
 constexpr int kTileBytes = 2 * kHalfBytes;       // K or V tile: 32 KB
-constexpr int kStageBytes = 2 * kTileBytes;      // K + V: 64 KB
+constexpr int kStageBytes = 2 * kTileBytes;      // K + V slot pair: 64 KB
 constexpr int kQBytes = 2 * kN * 128;            // 16 rows x 128 B x 2 halves: 4 KB
 constexpr int kPBytes = 2 * kN * 128;            // 16 rows x 128 positions (2 x 64) bf16: 4 KB
 constexpr int kThreads = 352;                    // K producer, MMA, two softmax warpgroups, V producer
@@ -65,6 +74,8 @@ constexpr int kWarpV = kThreads / 32 - 1;        // the V producer's warp
 constexpr int kTmemCols = 64;                    // S x2 (16 cols each) + O x2
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr int kTimeoutErr = 1 << 24;
+constexpr int kMaxReqs = 2048;                   // requests the in-kernel tile prefix handles
+constexpr int kWinBlocks = 128;                  // table entries a producer caches per window
 
 // Shared-memory layout (offsets from a 1024-aligned base).
 constexpr int kOffStages = 0;
@@ -77,20 +88,12 @@ constexpr int kOffBar = kOffRedSum + 2 * kN * 4 * 4;      // barriers (8 B each)
 constexpr int kNumBars = 4 * kStages + 2 * 5 + 2 + 8;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
-// Per-CTA schedule: units sorted by tile count (largest first), dealt round-robin.
-// The same pass leaves every request's (clamped) length in shared memory.
-constexpr int kMaxReqsSorted = 2048;                      // requests the in-kernel sort handles
-constexpr int kMaxListed = 1024;                          // units one CTA can list
-constexpr int kMaxBuckets = 32;                           // tiles per partition the sort handles
-constexpr int kOffInfo = kOffAbort + 4;                   // per request: clamped length
-constexpr int kOffList = kOffInfo + kMaxReqsSorted * 4;   // this CTA's units in order
-constexpr int kOffBucket = kOffList + kMaxListed * 4;     // units per bucket, then bucket offsets
-constexpr int kOffSched = kOffBucket + 2 * (kMaxBuckets + 1) * 4;   // [0] = units listed, [1] = mode
-constexpr int kMaxUnitBlocks = 128;                       // table entries a producer caches per unit
-constexpr int kOffEnt = kOffSched + 8;                    // [producer][2][kMaxUnitBlocks] table entries
-constexpr int kSmemUsed = kOffEnt + 4 * kMaxUnitBlocks * 4;
+constexpr int kOffPre = kOffAbort + 4;                    // [kMaxReqs + 1] tile prefix per request
+constexpr int kOffEnt = (kOffPre + (kMaxReqs + 1) * 4 + 15) / 16 * 16;   // [producer][2][kWinBlocks] entries
+constexpr int kSmemUsed = kOffEnt + 4 * kWinBlocks * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;              // slack for 1024 alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
+static_assert(kOffEnt % 16 == 0, "entry buffers must stay aligned");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -264,125 +267,98 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NQ]) {
 }
 
 // ---------------------------------------------------------------------------
-// The static schedule every role walks: unit u -> (r, g, c) and its tiles.
+// Stream-K schedule
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ int32_t clamp_len(const DecodeArgs &a, int r) {
+    int32_t L = __ldg(a.ctx + r);
+    return L > a.max_ctx ? a.max_ctx : (L < 0 ? 0 : L);
+}
+
+// pre[r] = sum of ceil(len / 128) over requests before r (r <= num_reqs),
+// built in shared memory by warp 0; CTA 0 also stores it in the workspace for
+// the merge.  Ends with a __syncthreads.
+__device__ void build_prefix(const DecodeArgs &a, int32_t *pre) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = a.num_reqs;
+    if (warp == 0) {
+        const int per = (n + 31) / 32;
+        const int lo = min(n, lane * per), hi = min(n, lo + per);
+        int32_t sum = 0;
+        for (int r = lo; r < hi; ++r) sum += (clamp_len(a, r) + kTile - 1) / kTile;
+        int32_t inc = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        int32_t run = inc - sum;
+        for (int r = lo; r < hi; ++r) {
+            pre[r] = run;
+            run += (clamp_len(a, r) + kTile - 1) / kTile;
+        }
+        if (lane == 31) pre[n] = inc;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int r = threadIdx.x; r <= n; r += blockDim.x) a.sk_pre[r] = pre[r];
+}
+
+// One unit: tiles [lo, hi) of stream s = r * H_kv + g (positions
+// [start, cend) with start = lo * 128, cend = min(hi * 128, L)).
 struct Unit {
-    int r, g, c;
+    int r, g;
+    int64_t s;
     int32_t L, start, cend, ntiles;
 };
 
-__device__ __forceinline__ bool unit_at(const DecodeArgs &a, int64_t u, Unit &x, const int32_t *lens) {
-    const int64_t rg = u / a.n_chunks;
-    x.c = (int)(u - rg * a.n_chunks);
-    x.r = (int)(rg / a.H_kv);
-    x.g = (int)(rg - (int64_t)x.r * a.H_kv);
-    int32_t L = lens ? lens[x.r] : __ldg(a.ctx + x.r);
-    if (L > a.max_ctx) L = a.max_ctx;
-    if (L < 0) L = 0;
-    x.L = L;
-    x.start = x.c * a.chunk;
-    if (x.start >= L) return false;
-    x.cend = min(x.start + a.chunk, L);
-    x.ntiles = (x.cend - x.start + kTile - 1) / kTile;
-    return true;
-}
-
-// Builds this CTA's list of units: every non-empty unit, sorted by its tile
-// count (largest first, natural order within a count), dealt round-robin to
-// the CTAs.  Partitions are `chunk` positions, so a request of length L has
-// L / chunk full units of T = chunk / 128 tiles per KV head and at most one
-// shorter tail unit.  Runs on all threads of the CTA.  When the batch is too
-// large for the shared-memory tables, falls back to natural order.
-__device__ void build_schedule(const DecodeArgs &a, uint8_t *smem) {
-    uint32_t *info = reinterpret_cast<uint32_t *>(smem + kOffInfo);
-    int32_t *list = reinterpret_cast<int32_t *>(smem + kOffList);
-    int32_t *tot = reinterpret_cast<int32_t *>(smem + kOffBucket);
-    int32_t *off = tot + (kMaxBuckets + 1);
-    int32_t *sched = reinterpret_cast<int32_t *>(smem + kOffSched);
-    const int T = a.chunk / kTile;
-    const int tid = threadIdx.x;
-    const int nthreads = blockDim.x;
-    const bool fits = a.num_reqs <= kMaxReqsSorted && T <= kMaxBuckets;
-    if (tid <= kMaxBuckets) tot[tid] = 0;
-    __syncthreads();
-    if (fits) {
-        for (int r = tid; r < a.num_reqs; r += nthreads) {
-            int32_t L = __ldg(a.ctx + r);
-            L = L > a.max_ctx ? a.max_ctx : (L < 0 ? 0 : L);
-            const int32_t nfull = L / a.chunk;
-            const int32_t trem = (L - nfull * a.chunk + kTile - 1) / kTile;
-            info[r] = (uint32_t)L;
-            if (nfull) atomicAdd(&tot[T], nfull * a.H_kv);
-            if (trem) atomicAdd(&tot[trem], a.H_kv);
+// Walks this CTA's units in order.
+struct StreamK {
+    const int32_t *pre;
+    int n, H;
+    int64_t t, t1;   // next global tile, end of this CTA's range
+    int r;
+    __device__ void init(const DecodeArgs &a, const int32_t *pre_) {
+        pre = pre_;
+        n = a.num_reqs;
+        H = a.H_kv;
+        // split over min(grid, TT) CTAs so every participating CTA has at
+        // least one tile (the merge recomputes the slots with the same rule)
+        const int64_t TT = (int64_t)H * pre[n];
+        const int64_t geff = TT < (int64_t)gridDim.x ? TT : (int64_t)gridDim.x;
+        if ((int64_t)blockIdx.x < geff) {
+            t = TT * blockIdx.x / geff;
+            t1 = TT * (blockIdx.x + 1) / geff;
+        } else {
+            t = t1 = TT;
         }
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int64_t run = 0;
-        for (int t = T; t >= 1; --t) {
-            off[t] = (int32_t)run;
-            run += tot[t];
+        // first request whose tiles end after t
+        int lo = 0, hi = n;   // invariant: answer in [lo, hi]
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((int64_t)H * pre[mid + 1] > t) hi = mid;
+            else lo = mid + 1;
         }
-        const int64_t k = blockIdx.x;
-        const int64_t mine = run > k ? (run - k + gridDim.x - 1) / gridDim.x : 0;
-        sched[0] = (int32_t)mine;
-        sched[1] = (fits && mine <= kMaxListed) ? 1 : 0;
+        r = lo;
     }
-    __syncthreads();
-    if (sched[1] == 0) return;
-    // one warp per bucket: a scan over requests places this CTA's targets
-    const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
-    const int64_t k = blockIdx.x, grid = gridDim.x;
-    for (int t = T - warp; t >= 1; t -= nwarps) {
-        int64_t run = off[t];
-        for (int base = 0; base < a.num_reqs; base += 32) {
-            const int r = base + lane;
-            uint32_t nfull = 0, trem = 0;
-            if (r < a.num_reqs) {
-                const int32_t L = (int32_t)info[r];
-                nfull = (uint32_t)(L / a.chunk);
-                trem = (uint32_t)((L - (int32_t)nfull * a.chunk + kTile - 1) / kTile);
-            }
-            // bucket t holds the full units (t == T) and the tail units of t tiles
-            const int32_t cnt_full = (t == T) ? (int32_t)nfull * a.H_kv : 0;
-            const int32_t cnt = cnt_full + (trem == (uint32_t)t ? a.H_kv : 0);
-            int32_t inc = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += v;
-            }
-            const int64_t lo = run + inc - cnt, hi = lo + cnt;
-            // targets i = k + m * grid inside [lo, hi)
-            int64_t m = lo <= k ? 0 : (lo - k + grid - 1) / grid;
-            for (int64_t i = k + m * grid; i < hi; i += grid, ++m) {
-                const int64_t o2 = i - lo;
-                int g, c;
-                if (o2 < cnt_full) {
-                    g = (int)(o2 / nfull);
-                    c = (int)(o2 - (int64_t)g * nfull);
-                } else {
-                    g = (int)(o2 - cnt_full);
-                    c = (int)nfull;
-                }
-                list[m] = (int32_t)(((int64_t)r * a.H_kv + g) * a.n_chunks + c);
-            }
-            run += __shfl_sync(0xffffffffu, inc, 31);
-        }
+    __device__ bool next(const DecodeArgs &a, Unit &x) {
+        if (t >= t1) return false;
+        while (r < n && (int64_t)H * pre[r + 1] <= t) ++r;
+        const int64_t Tr = pre[r + 1] - pre[r];
+        const int64_t S0 = (int64_t)H * pre[r];
+        const int g = (int)((t - S0) / Tr);
+        const int64_t S = S0 + g * Tr;
+        const int64_t lo = t - S;
+        const int64_t hi = (t1 - S) < Tr ? (t1 - S) : Tr;
+        x.r = r;
+        x.g = g;
+        x.s = (int64_t)r * H + g;
+        x.L = clamp_len(a, r);
+        x.start = (int32_t)(lo * kTile);
+        x.cend = (int32_t)(hi * kTile < (int64_t)x.L ? hi * kTile : (int64_t)x.L);
+        x.ntiles = (int32_t)(hi - lo);
+        t = S + hi;
+        return true;
     }
-}
-
-// The m-th unit of this CTA (sorted schedule), or the natural round-robin
-// order when the sorted list did not fit.
-struct Sched {
-    const int32_t *list;
-    int32_t count;
-    bool sorted;
-    int64_t num_units;
-    __device__ __forceinline__ int64_t first() const { return sorted ? 0 : (int64_t)blockIdx.x; }
-    __device__ __forceinline__ bool more(int64_t it) const { return sorted ? it < count : it < num_units; }
-    __device__ __forceinline__ int64_t next(int64_t it) const { return sorted ? it + 1 : it + gridDim.x; }
-    __device__ __forceinline__ int64_t unit(int64_t it) const { return sorted ? (int64_t)list[it] : it; }
 };
 
 // Transposed butterfly over a warp: NQ values per lane in, one value out.
@@ -453,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *red_sum = reinterpret_cast<float *>(smem + kOffRedSum);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
+    int32_t *pre = reinterpret_cast<int32_t *>(smem + kOffPre);
     const uint32_t bar0 = sbase + kOffBar;
     // K and V tiles have separate rings (same slot numbering): a K slot is
     // released as soon as the S MMA that reads it completes.
@@ -472,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sm_q = sbase + kOffQ;
     const uint32_t sm_p = sbase + kOffP;
 
-    // ---- set-up: barriers, zeroed V / Q / P buffers, TMEM ----
+    // ---- set-up (no global memory): barriers, zeroed V / Q / P buffers, TMEM ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar_kfull(s), 1);
@@ -515,93 +492,107 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    pdl_wait();                // global memory is read from here on
-    pdl_trigger();
-    build_schedule(a, smem);   // contains __syncthreads
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();                // global memory is read from here on
+    pdl_trigger();
+    build_prefix(a, pre);      // ends with __syncthreads
     const uint32_t tmem = *tmem_slot;
 
-    const int64_t num_units = (int64_t)a.num_reqs * a.H_kv * a.n_chunks;
-    Sched sch;
-    sch.list = reinterpret_cast<const int32_t *>(smem + kOffList);
-    const int32_t *lens = reinterpret_cast<const int32_t *>(smem + kOffSched)[1] != 0
-                              ? reinterpret_cast<const int32_t *>(smem + kOffInfo)
-                              : nullptr;
-    sch.count = reinterpret_cast<const int32_t *>(smem + kOffSched)[0];
-    sch.sorted = reinterpret_cast<const int32_t *>(smem + kOffSched)[1] != 0;
-    sch.num_units = num_units;
     const int G = a.G;
     const int nq = a.nq;
-    const int nseg = kTile / seg_rows;         // block segments per tile (1..16)
-    const int seg_shift = 31 - __clz(seg_rows);   // seg_rows is a power of two
+    const int nseg = kTile / seg_rows;              // block segments per tile (1..16)
+    const int seg_shift = 31 - __clz(seg_rows);     // seg_rows is a power of two
 
     if (warp == 0 || warp == kWarpV) {
         // ================= TMA producers (warp 0: K and Q, last warp: V) =================
+        // Units are walked in windows of at most kWinBlocks table entries; a
+        // window's entries are loaded into registers while the previous
+        // window's tiles are issued, then parked in shared memory, so no
+        // table lookup sits between a slot becoming free and its refill.  An
+        // entry past the table width is parked as INT32_MIN.
         const bool is_v = warp == kWarpV;
-        // The table entries of a unit (one per block it covers) are loaded
-        // into registers one unit ahead and parked in shared memory, so no
-        // table lookup sits between a stage becoming free and its refill.
-        // An entry past the table width is parked as INT32_MIN.
-        int32_t *ent_buf = reinterpret_cast<int32_t *>(smem + kOffEnt) + (is_v ? 2 * kMaxUnitBlocks : 0);
-        constexpr int kEntRegs = kMaxUnitBlocks / 32;
+        int32_t *ent_buf = reinterpret_cast<int32_t *>(smem + kOffEnt) + (is_v ? 2 * kWinBlocks : 0);
+        const int win_tiles = max(1, ((kWinBlocks - 1) * a.bs) / kTile);
+        struct Win {
+            Unit u;
+            int32_t t0, t1;   // tiles of the unit
+        };
+        StreamK sk;
+        sk.init(a, pre);
+        Unit cu = {};
+        bool have_u = false;
+        int32_t wt = 0;
+        auto next_win = [&](Win &w) -> bool {
+            if (!have_u || wt >= cu.ntiles) {
+                if (!sk.next(a, cu)) return false;
+                have_u = true;
+                wt = 0;
+            }
+            w.u = cu;
+            w.t0 = wt;
+            w.t1 = min(cu.ntiles, wt + win_tiles);
+            wt = w.t1;
+            return true;
+        };
+        auto win_first_block = [&](const Win &w) { return (w.u.start + w.t0 * kTile) / a.bs; };
+        auto win_blocks = [&](const Win &w) {
+            const int32_t p1 = min(w.u.start + w.t1 * kTile, w.u.cend);
+            return (p1 - 1) / a.bs - win_first_block(w) + 1;
+        };
+        constexpr int kEntRegs = kWinBlocks / 32;
         int32_t ent_reg[kEntRegs];
-        auto unit_blocks = [&](const Unit &x) { return (x.cend - x.start + a.bs - 1) / a.bs; };
-        auto fetch_entries = [&](const Unit &x) {
-            const int32_t lb0 = x.start / a.bs;
-            const int32_t nblk = unit_blocks(x);
+        auto fetch_entries = [&](const Win &w) {
+            const int32_t lb0 = win_first_block(w);
+            const int32_t nblk = win_blocks(w);
 #pragma unroll
             for (int kk = 0; kk < kEntRegs; ++kk) {
                 const int32_t lbl = kk * 32 + lane;
                 if (lbl < nblk) {
                     const int32_t lb = lb0 + lbl;
-                    ent_reg[kk] = lb < a.bt_cols ? __ldg(a.bt + (int64_t)x.r * a.bt_stride + lb) : INT32_MIN;
+                    ent_reg[kk] = lb < a.bt_cols ? __ldg(a.bt + (int64_t)w.u.r * a.bt_stride + lb) : INT32_MIN;
                 }
             }
         };
-        auto park_entries = [&](const Unit &x, int buf) {
-            const int32_t nblk = unit_blocks(x);
+        auto park_entries = [&](const Win &w, int buf) {
+            const int32_t nblk = win_blocks(w);
 #pragma unroll
             for (int kk = 0; kk < kEntRegs; ++kk) {
                 const int32_t lbl = kk * 32 + lane;
-                if (lbl < nblk) ent_buf[buf * kMaxUnitBlocks + lbl] = ent_reg[kk];
+                if (lbl < nblk) ent_buf[buf * kWinBlocks + lbl] = ent_reg[kk];
             }
             __syncwarp();
         };
-        // next non-empty unit at or after schedule position `it`
-        auto find_unit = [&](int64_t it, Unit &x) -> int64_t {
-            for (; sch.more(it); it = sch.next(it))
-                if (unit_at(a, sch.unit(it), x, lens)) return it;
-            return -1;
-        };
         int64_t j = 0;   // tile sequence number in this CTA
         int us = 0;      // unit sequence number in this CTA
-        Unit x;
-        int64_t it = find_unit(sch.first(), x);
-        if (it >= 0 && unit_blocks(x) <= kMaxUnitBlocks) {
-            fetch_entries(x);
-            park_entries(x, 0);
+        int ws = 0;      // window sequence number
+        Win cur, nxt;
+        bool have = next_win(cur);
+        if (have) {
+            fetch_entries(cur);
+            park_entries(cur, 0);
         }
-        while (it >= 0 && !*abort_flag) {
-            Unit nx;
-            const int64_t it_next = find_unit(sch.next(it), nx);
-            const bool cached = unit_blocks(x) <= kMaxUnitBlocks;
-            const bool next_cached = it_next >= 0 && unit_blocks(nx) <= kMaxUnitBlocks;
-            if (next_cached) fetch_entries(nx);     // in flight while this unit's tiles are issued
-            const int32_t *ents = ent_buf + (us & 1) * kMaxUnitBlocks;
-            if (!is_v && lane == 0 && x.c == 0 && x.g == 0 && __ldg(a.ctx + x.r) > a.max_ctx && a.err)
-                atomicAdd(a.err, 1);
-            const int qb = us & 1;
-            if (!is_v && !mbar_wait_warp(bar_qempty(qb), ((us >> 1) & 1) ^ 1, abort_flag)) break;
-            if (!is_v && lane == 0) {
-                mbar_arrive_expect_tx(bar_qfull(qb), 2u * 128u * (uint32_t)nq);
-                const uint32_t dq = sm_q + qb * kQBytes;
-                tma_load_3d(dq, &tmQ, bar_qfull(qb), 0, x.g * G, x.r * a.q_len);
-                tma_load_3d(dq + kN * 128, &tmQ, bar_qfull(qb), 64, x.g * G, x.r * a.q_len);
+        while (have && !*abort_flag) {
+            const bool have_n = next_win(nxt);
+            if (have_n) fetch_entries(nxt);   // in flight while this window's tiles are issued
+            const int32_t *ents = ent_buf + (ws & 1) * kWinBlocks;
+            const int32_t lb_first = win_first_block(cur);
+            const Unit &x = cur.u;
+            if (cur.t0 == 0 && !is_v) {
+                if (lane == 0 && x.start == 0 && x.g == 0 && __ldg(a.ctx + x.r) > a.max_ctx && a.err)
+                    atomicAdd(a.err, 1);
+                const int qb = us & 1;
+                if (!mbar_wait_warp(bar_qempty(qb), ((us >> 1) & 1) ^ 1, abort_flag)) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar_qfull(qb), 2u * 128u * (uint32_t)nq);
+                    const uint32_t dq = sm_q + qb * kQBytes;
+                    tma_load_3d(dq, &tmQ, bar_qfull(qb), 0, x.g * G, x.r * a.q_len);
+                    tma_load_3d(dq + kN * 128, &tmQ, bar_qfull(qb), 64, x.g * G, x.r * a.q_len);
+                }
             }
-            for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
+            for (int jt = cur.t0; jt < cur.t1; ++jt, ++j) {
                 const int s = (int)(j % kStages);
                 const uint32_t bar_e = is_v ? bar_vempty(s) : bar_kempty(s);
                 const uint32_t bar_f = is_v ? bar_vfull(s) : bar_kfull(s);
@@ -613,14 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane < nseg) {
                     const int32_t p0 = ts + lane * seg_rows;
                     if (p0 < x.cend) {
-                        const int32_t lbl = (p0 - x.start) / a.bs;
-                        const int32_t lb = x.start / a.bs + lbl;
-                        int64_t e;
-                        if (cached) {
-                            e = ents[lbl];
-                        } else {
-                            e = lb < a.bt_cols ? (int64_t)__ldg(a.bt + (int64_t)x.r * a.bt_stride + lb) : INT32_MIN;
-                        }
+                        const int32_t lb = p0 / a.bs;
+                        const int64_t e = ents[lb - lb_first];
                         if (e == INT32_MIN || e >= a.total_blocks) {
                             if (!is_v && a.err) atomicAdd(a.err, 1);
                         } else if (e > 0) {
@@ -653,10 +638,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            if (next_cached) park_entries(nx, (us + 1) & 1);
-            ++us;
-            it = it_next;
-            x = nx;
+            if (have_n) park_entries(nxt, (ws + 1) & 1);
+            if (cur.t1 == x.ntiles) ++us;
+            ++ws;
+            cur = nxt;
+            have = have_n;
         }
         if (*abort_flag) {
             // let copies already issued land before the CTA retires
@@ -693,10 +679,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(bar_vempty(stage));
                 return true;
             };
-            for (int64_t it = sch.first(); sch.more(it) && ok; it = sch.next(it)) {
-                const int64_t u = sch.unit(it);
-                Unit x;
-                if (!unit_at(a, u, x, lens)) continue;
+            StreamK sk;
+            sk.init(a, pre);
+            Unit x;
+            while (ok && sk.next(a, x)) {
                 const int qb = us & 1;
                 if (!mbar_wait(bar_qfull(qb), (uint32_t)((us >> 1) & 1), abort_flag)) {
                     ok = false;
@@ -737,8 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ================= softmax + output (two warpgroups of 128 threads) =================
         // Warpgroup k takes the tiles with (tile sequence number & 1) == k,
-        // i.e. the S / P / O buffers of parity k, and writes partial slot k
-        // of every unit.
+        // i.e. the S / P / O buffers of parity k, and writes partial slot
+        // 2 (CTA + stream) + k of every unit.
         const int wg = (warp - 2) >> 2;
         const int row = 32 * (warp & 3) + lane;          // TMEM lane: position in tile / head_dim row
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -764,10 +750,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int red_row = reduced_row<NQ>(lane);
         const bool red_writer = reduced_writer<NQ>(lane);
         float *my_red_sum = red_sum + wg * (kN * 4);
-        for (int64_t it = sch.first(); sch.more(it) && ok; it = sch.next(it)) {
-            const int64_t u = sch.unit(it);
-            Unit x;
-            if (!unit_at(a, u, x, lens)) continue;
+        StreamK sk;
+        sk.init(a, pre);
+        Unit x;
+        while (ok && sk.next(a, x)) {
             int32_t lastv[NQ];
 #pragma unroll
             for (int n = 0; n < NQ; ++n) {
@@ -860,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const int64_t prow0 = (u * 2 + wg) * nq;
+                const int64_t prow0 = (2 * ((int64_t)blockIdx.x + x.s) + wg) * nq;
 #pragma unroll
                 for (int n = 0; n < NQ; ++n)
                     if (n < nq) a.ws_o[(prow0 + n) * kD + row] = o[n];
@@ -926,7 +912,7 @@ static bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1
 bool decode_tc_supported(const DecodeArgs &a) {
     if (a.dtype != BKV_BF16 || a.D != tc::kD || a.nq > tc::kN || a.nq <= 0) return false;
     if (a.bs < 8 || !((tc::kTile % a.bs == 0) || (a.bs % tc::kTile == 0))) return false;
-    if (a.G > 256 || a.q_len > 256 || a.H_kv > 65535) return false;
+    if (a.G > 256 || a.q_len > 256 || a.H_kv > 65535 || a.num_reqs > tc::kMaxReqs || !a.sk_pre) return false;
     if ((int64_t)a.total_blocks * a.bs >= ((int64_t)1 << 31)) return false;
     if ((int64_t)a.num_reqs * a.q_len >= ((int64_t)1 << 31)) return false;
     if (!aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.q, 16)) return false;
@@ -945,10 +931,8 @@ int launch_decode_tc(const DecodeArgs &a, cudaStream_t st) {
         !encode_3d(&mq, a.q, kD, a.H_q, (uint64_t)a.num_reqs * a.q_len, kD * 2, (uint64_t)a.H_q * kD * 2, 64, a.G,
                    a.q_len))
         return BKV_ERR_UNSUPPORTED;
-    const int64_t units = (int64_t)a.num_reqs * a.H_kv * a.n_chunks;
-    int64_t grid = current_sm_count();
-    if (grid > units) grid = units;
-    if (grid < 1) grid = 1;
+    // the grid is the stream-K CTA count the workspace was laid out for
+    const int64_t grid = a.sk_grid;
     // the softmax handles only the query rows that exist (4, 8 or 16 columns)
     auto kern = a.nq <= 4 ? decode_tc_kernel<4> : (a.nq <= 8 ? decode_tc_kernel<8> : decode_tc_kernel<16>);
     const int slot = a.nq <= 4 ? 0 : (a.nq <= 8 ? 1 : 2);

@@ -51,6 +51,7 @@ def test_noalloc_matches_workspace_entry_point(name):
     w = wl.make(name)
     dw = DeviceWorkload(w)
     dw.write_step()
+    dw.workspace.fill_(0xFF)                     # NaN: no unwritten partial may be read
     ref = dw.decode().clone()                    # bkv_paged_decode with a caller workspace
     torch.cuda.synchronize()
     need = bkv.bkv_paged_decode_workspace_size(w.num_rows, w.q_len, w.num_q_heads, w.num_kv_heads, w.head_dim,
