@@ -368,7 +368,7 @@ def run_bkv(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "llama3_decode: 32 req, ctx U[512,4096] + 1 new token, H_q 32, H_kv 8, D 128, "
                                "bs 64, bf16, fp32 accumulate",
-                   "kv_bytes_per_step": kv_bytes, "l2": "flushed before every timed step (2x L2 write)",
+                   "kv_bytes_per_step": kv_bytes, "l2": "flushed before every timed step (write 2x L2, read it back)",
                    "parallelism": f"replicas x{world}", "step": "expand + slot map + write + decode + merge",
                    "cuda_graph": bool(graphs)},
         # library kernels in the timed region: step (5) + decode alone (2) + end-to-end step (5), per step,
