@@ -241,6 +241,39 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
         const int t = row / a.G;
         const int h = g * a.G + (row - t * a.G);
         T *out = static_cast<T *>(a.out) + (((int64_t)r * a.q_len + t) * a.H_q + h) * a.D;
+        if (nch <= 8 && a.D == 128) {
+            // few slots: every load of the row (each lane's slot (m, l) and its four
+            // head_dim elements of every slot) is issued in one round
+            const float2 ml = lane < nch
+                                  ? *reinterpret_cast<const float2 *>(a.ws_ml + ((unit0 + lane) * a.nq + row) * 2)
+                                  : make_float2(-INFINITY, 0.f);
+            float4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < nch) v[k] = *reinterpret_cast<const float4 *>(a.ws_o + ((unit0 + k) * a.nq + row) * a.D + 4 * lane);
+            float M = ml.x;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float wl = (M == -INFINITY || lane >= nch) ? 0.f : exp2f(ml.x - M);
+            const float lsum = warp_sum(wl * ml.y);
+            const float iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : 1.f / lsum;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (k < nch) {
+                    const float wgt = __shfl_sync(0xffffffffu, wl, k);
+                    acc.x = fmaf(wgt, v[k].x, acc.x);
+                    acc.y = fmaf(wgt, v[k].y, acc.y);
+                    acc.z = fmaf(wgt, v[k].z, acc.z);
+                    acc.w = fmaf(wgt, v[k].w, acc.w);
+                }
+            }
+            store_out(out + 4 * lane + 0, acc.x * iv);
+            store_out(out + 4 * lane + 1, acc.y * iv);
+            store_out(out + 4 * lane + 2, acc.z * iv);
+            store_out(out + 4 * lane + 3, acc.w * iv);
+            continue;
+        }
         float M = -INFINITY;
         for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.ws_ml[((unit0 + c) * a.nq + row) * 2]);
 #pragma unroll

@@ -63,10 +63,18 @@ namespace tc {
 constexpr int kTile = 128;            // positions per tile
 constexpr int kD = 128;               // head_dim handled
 constexpr int kN = 16;                // query rows per MMA (padded)
-constexpr int kStages = 3;
+// K and V tiles have separate rings of 32 KB slots
+#ifndef BKV_K_STAGES
+#define BKV_K_STAGES 3
+#endif
+#ifndef BKV_V_STAGES
+#define BKV_V_STAGES 3
+#endif
+constexpr int kKStages = BKV_K_STAGES;
+constexpr int kVStages = BKV_V_STAGES;
+static_assert(kKStages >= 2 && kKStages <= 3, "the 8-entry mask ring assumes at most 3 K slots");
 constexpr int kHalfBytes = kTile * 128;          // 128 rows x 64 bf16 (128 B): one head_dim half
 constexpr int kTileBytes = 2 * kHalfBytes;       // K or V tile: 32 KB
-constexpr int kStageBytes = 2 * kTileBytes;      // K + V slot pair: 64 KB
 constexpr int kQBytes = 2 * kN * 128;            // 16 rows x 128 B x 2 halves: 4 KB
 constexpr int kPBytes = 2 * kN * 128;            // 16 rows x 128 positions (2 x 64) bf16: 4 KB
 constexpr int kThreads = 352;                    // K producer, MMA, two softmax warpgroups, V producer
@@ -78,14 +86,15 @@ constexpr int kMaxReqs = 2048;                   // requests the in-kernel tile 
 constexpr int kWinBlocks = 128;                  // table entries a producer caches per window
 
 // Shared-memory layout (offsets from a 1024-aligned base).
-constexpr int kOffStages = 0;
-constexpr int kOffQ = kOffStages + kStages * kStageBytes;
+constexpr int kOffK = 0;                                  // kKStages K slots
+constexpr int kOffV = kOffK + kKStages * kTileBytes;      // kVStages V slots
+constexpr int kOffQ = kOffV + kVStages * kTileBytes;
 constexpr int kOffP = kOffQ + 2 * kQBytes;
 constexpr int kOffMask = kOffP + 2 * kPBytes;             // 8 words: loaded segments per tile (ring)
 constexpr int kOffRedMax = kOffMask + 64;                 // [warpgroup][2][16 rows][4 warps] floats
 constexpr int kOffRedSum = kOffRedMax + 4 * kN * 4 * 4;   // [warpgroup][16 rows][4 warps] floats
 constexpr int kOffBar = kOffRedSum + 2 * kN * 4 * 4;      // barriers (8 B each)
-constexpr int kNumBars = 4 * kStages + 2 * 5 + 2 + 8;
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 8;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffPre = kOffAbort + 4;                    // [kMaxReqs + 1] tile prefix per request
@@ -433,27 +442,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar0 = sbase + kOffBar;
     // K and V tiles have separate rings (same slot numbering): a K slot is
     // released as soon as the S MMA that reads it completes.
+    constexpr int kB = 2 * kKStages + 2 * kVStages;   // first barrier after the rings
     auto bar_kfull = [&](int s) { return bar0 + 8u * s; };
-    auto bar_kempty = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto bar_vfull = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
-    auto bar_vempty = [&](int s) { return bar0 + 8u * (3 * kStages + s); };
-    auto bar_qfull = [&](int b) { return bar0 + 8u * (4 * kStages + b); };
-    auto bar_qempty = [&](int b) { return bar0 + 8u * (4 * kStages + 2 + b); };
-    auto bar_sfull = [&](int b) { return bar0 + 8u * (4 * kStages + 4 + b); };
-    auto bar_pfull = [&](int b) { return bar0 + 8u * (4 * kStages + 6 + b); };
-    auto bar_ofull = [&](int b) { return bar0 + 8u * (4 * kStages + 8 + b); };
-    auto bar_group = [&](int k) { return bar0 + 8u * (4 * kStages + 10 + k); };   // four warps of warpgroup k
+    auto bar_kempty = [&](int s) { return bar0 + 8u * (kKStages + s); };
+    auto bar_vfull = [&](int s) { return bar0 + 8u * (2 * kKStages + s); };
+    auto bar_vempty = [&](int s) { return bar0 + 8u * (2 * kKStages + kVStages + s); };
+    auto bar_qfull = [&](int b) { return bar0 + 8u * (kB + b); };
+    auto bar_qempty = [&](int b) { return bar0 + 8u * (kB + 2 + b); };
+    auto bar_sfull = [&](int b) { return bar0 + 8u * (kB + 4 + b); };
+    auto bar_pfull = [&](int b) { return bar0 + 8u * (kB + 6 + b); };
+    auto bar_ofull = [&](int b) { return bar0 + 8u * (kB + 8 + b); };
+    auto bar_group = [&](int k) { return bar0 + 8u * (kB + 10 + k); };   // four warps of warpgroup k
     // "loaded segments" word of tile j: mask_words[j & 7], published with bar_mask(j & 7)
-    auto bar_mask = [&](int m) { return bar0 + 8u * (4 * kStages + 12 + m); };
-    const uint32_t sm_stage = sbase + kOffStages;
+    auto bar_mask = [&](int m) { return bar0 + 8u * (kB + 12 + m); };
+    const uint32_t sm_k = sbase + kOffK;
+    const uint32_t sm_v = sbase + kOffV;
     const uint32_t sm_q = sbase + kOffQ;
     const uint32_t sm_p = sbase + kOffP;
 
     // ---- set-up (no global memory): barriers, zeroed V / Q / P buffers, TMEM ----
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar_kfull(s), 1);
             mbar_init(bar_kempty(s), 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(bar_vfull(s), 1);
             mbar_init(bar_vempty(s), 1);
         }
@@ -479,10 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // V tiles must never hold NaN where nothing was loaded; Q rows past
         // the group and P start at zero.
         const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int s = 0; s < kStages; ++s) {
-            uint4 *v = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes);
-            for (int i = threadIdx.x; i < kTileBytes / 16; i += kThreads) v[i] = z;
-        }
+        uint4 *v = reinterpret_cast<uint4 *>(smem + kOffV);
+        for (int i = threadIdx.x; i < kVStages * kTileBytes / 16; i += kThreads) v[i] = z;
         uint4 *qp = reinterpret_cast<uint4 *>(smem + kOffQ);
         for (int i = threadIdx.x; i < (2 * kQBytes + 2 * kPBytes) / 16; i += kThreads) qp[i] = z;
     }
@@ -593,10 +604,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             for (int jt = cur.t0; jt < cur.t1; ++jt, ++j) {
-                const int s = (int)(j % kStages);
+                const int nst = is_v ? kVStages : kKStages;
+                const int s = (int)(j % nst);
                 const uint32_t bar_e = is_v ? bar_vempty(s) : bar_kempty(s);
                 const uint32_t bar_f = is_v ? bar_vfull(s) : bar_kfull(s);
-                if (!mbar_wait_warp(bar_e, (uint32_t)((j / kStages) & 1) ^ 1u, abort_flag)) break;
+                if (!mbar_wait_warp(bar_e, (uint32_t)((j / nst) & 1) ^ 1u, abort_flag)) break;
                 const int32_t ts = x.start + jt * kTile;
                 // lane i handles block segment i of the tile
                 bool load = false;
@@ -618,9 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     // bit i: segment i was loaded.  A ring of 8 words by tile number with
                     // its own barriers: the K producer writes tile j's word only after
-                    // the S MMA of tile j - 3 completed, which is issued only after the
-                    // softmax released tile j - 5, so it is never more than 5 tiles ahead
-                    // of the reader and a slot's phases cannot alias.
+                    // the S MMA of tile j - kKStages completed, which is issued only after
+                    // the softmax released tile j - kKStages - 2, so it is never more than
+                    // kKStages + 2 <= 5 tiles ahead of the reader and phases cannot alias.
                     if (!is_v) {
                         mask_words[j & 7] = ballot;
                         mbar_arrive(bar_mask((int)(j & 7)));
@@ -630,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (load) {
-                    const uint32_t dst = sm_stage + s * kStageBytes + (is_v ? kTileBytes : 0) + lane * seg_rows * 128;
+                    const uint32_t dst = (is_v ? sm_v : sm_k) + s * kTileBytes + lane * seg_rows * 128;
                     const CUtensorMap *map = is_v ? &tmV : &tmK;
                     const int z = (int)row0;
                     tma_load_3d(dst, map, bar_f, 0, x.g, z);
@@ -662,11 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             auto issue_pv = [&](int64_t jp, int stage) -> bool {
                 const int b = (int)(jp & 1);
-                if (!mbar_wait(bar_vfull(stage), (uint32_t)((jp / kStages) & 1), abort_flag) ||
+                if (!mbar_wait(bar_vfull(stage), (uint32_t)((jp / kVStages) & 1), abort_flag) ||
                     !mbar_wait(bar_pfull(b), (uint32_t)((jp >> 1) & 1), abort_flag))
                     return false;
                 tc_fence_after();
-                const uint32_t v_base = sm_stage + stage * kStageBytes + kTileBytes;
+                const uint32_t v_base = sm_v + stage * kTileBytes;
                 const uint32_t p_base = sm_p + b * kPBytes;
                 const uint32_t d_tmem = tmem + 32u + 16u * b;
 #pragma unroll
@@ -689,13 +701,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
-                    const int s = (int)(j % kStages);
-                    if (!mbar_wait(bar_kfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
+                    const int s = (int)(j % kKStages);
+                    if (!mbar_wait(bar_kfull(s), (uint32_t)((j / kKStages) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t k_base = sm_stage + s * kStageBytes;
+                    const uint32_t k_base = sm_k + s * kTileBytes;
                     const uint32_t q_base = sm_q + qb * kQBytes;
                     const uint32_t d_tmem = tmem + 16u * (uint32_t)(j & 1);
 #pragma unroll
@@ -713,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     pending = j;
-                    pending_stage = s;
+                    pending_stage = (int)(j % kVStages);
                 }
                 ++us;
             }
@@ -765,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
                 if ((int)(j & 1) != wg) continue;
-                const int s = (int)(j % kStages);
+                const int sv_slot = (int)(j % kVStages);
                 const int b = wg;
                 const uint32_t par = (uint32_t)((j >> 1) & 1);
                 if (!mbar_wait_warp(bar_sfull(b), par, abort_flag) ||
@@ -807,15 +819,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (after the V tile has landed)
                 const bool zero_row = loaded && pos >= x.cend;
                 if (__any_sync(0xffffffffu, zero_row) &&
-                    !mbar_wait_warp(bar_vfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
+                    !mbar_wait_warp(bar_vfull(sv_slot), (uint32_t)((j / kVStages) & 1), abort_flag)) {
                     ok = false;
                     break;
                 }
                 if (zero_row) {
-                    uint4 *vrow0 = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes +
-                                                             row * 128);
-                    uint4 *vrow1 = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes +
-                                                             kHalfBytes + row * 128);
+                    uint4 *vrow0 = reinterpret_cast<uint4 *>(smem + kOffV + sv_slot * kTileBytes + row * 128);
+                    uint4 *vrow1 = reinterpret_cast<uint4 *>(smem + kOffV + sv_slot * kTileBytes + kHalfBytes + row * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         vrow0[c] = make_uint4(0, 0, 0, 0);
