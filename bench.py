@@ -13,7 +13,9 @@ value  = decode KV bytes needed per step (cache_len rows x K,V x H_kv x D x 2B)
          / device time of the step (CUDA events), aggregated over ranks.
 e2e    = the same bytes / time of a step that also copies the step's inputs
          from pinned host memory and reads the output back.
-roofline.achieved = the same bytes / device time of the decode call alone.
+roofline.achieved = the same bytes / device time of the decode partition
+         kernel alone (the dominant kernel; bkv_paged_decode_partition);
+         decode_ms is the whole decode call (partition + merge).
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bkv|reference]
@@ -267,6 +269,9 @@ def run_bkv(args):
     def decode_only():
         dw.decode(stream=stream)
 
+    def partition_only():
+        dw.decode_partition(stream=stream)
+
     # pinned host copies of the step's inputs for the end-to-end leg
     host_in = {name: getattr(dw, name).cpu().pin_memory()
                for name in ("mgr_table", "req_indices", "positions", "k_new", "v_new", "q", "context_lens")}
@@ -285,14 +290,16 @@ def run_bkv(args):
             step()
             e2e_step()
             decode_only()
+            partition_only()
     torch.cuda.synchronize()
 
     # CUDA graphs of the three timed bodies (a serving engine replays its
     # decode step as a graph); captured after the warm-up so that one-time
     # set-up (kernel attributes, driver entry points) is outside the graphs.
+    BODIES = (("step", step), ("decode", decode_only), ("partition", partition_only), ("e2e", e2e_step))
     graphs = {}
     if not args.eager:
-        for name, fn in (("step", step), ("decode", decode_only), ("e2e", e2e_step)):
+        for name, fn in BODIES:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 fn()
@@ -302,7 +309,7 @@ def run_bkv(args):
             g.replay()
         torch.cuda.synchronize()
     body = {name: (graphs[name].replay if name in graphs else fn)
-            for name, fn in (("step", step), ("decode", decode_only), ("e2e", e2e_step))}
+            for name, fn in BODIES}
 
     if dist:
         dist.barrier()
@@ -311,6 +318,7 @@ def run_bkv(args):
         t_wall0 = time.perf_counter()
         step_ms = _time_steps(torch, body["step"], args.steps, flush, stream)
         dec_ms = _time_steps(torch, body["decode"], args.steps, flush, stream)
+        part_ms = _time_steps(torch, body["partition"], args.steps, flush, stream)
         e2e_ms = _time_steps(torch, body["e2e"], args.steps, flush, stream)
         t_wall = time.perf_counter() - t_wall0
     eager_ms = None
@@ -323,10 +331,11 @@ def run_bkv(args):
     ms = sum(step_ms) / len(step_ms)
     dms = sum(dec_ms) / len(dec_ms)
     ems = sum(e2e_ms) / len(e2e_ms)
+    pms = sum(part_ms) / len(part_ms)
     if dist:
-        t = torch.tensor([ms, dms, ems], dtype=torch.float64, device=f"cuda:{local}")
+        t = torch.tensor([ms, dms, ems, pms], dtype=torch.float64, device=f"cuda:{local}")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, dms, ems = t.tolist()
+        ms, dms, ems, pms = t.tolist()
 
     # secondary half of the metric: slot mapping + cache write on the ragged mixed step
     secondary = None
@@ -359,7 +368,7 @@ def run_bkv(args):
     if rank != 0:
         return
     peak, peak_kind = _peaks()
-    achieved = kv_bytes / (dms / 1e3) / 1e9
+    achieved = kv_bytes / (pms / 1e3) / 1e9
     value = world * kv_bytes / (ms / 1e3) / 1e9
     clocks = clk.summary()
     line = {
@@ -371,14 +380,16 @@ def run_bkv(args):
                    "kv_bytes_per_step": kv_bytes, "l2": "flushed before every timed step (write 2x L2, read it back)",
                    "parallelism": f"replicas x{world}", "step": "expand + slot map + write + decode + merge",
                    "cuda_graph": bool(graphs)},
-        # library kernels in the timed region: step (5) + decode alone (2) + end-to-end step (5), per step,
-        # plus the eager reference pass (5 per step) when graphs are used
-        "gpu_launches": args.steps * (5 + 2 + 5) + (args.steps * 5 if graphs else 0),
+        # library kernels in the timed region: step (5) + decode alone (2) + partition alone (1) + end-to-end
+        # step (5), per step, plus the eager reference pass (5 per step) when graphs are used
+        "gpu_launches": args.steps * (5 + 2 + 1 + 5) + (args.steps * 5 if graphs else 0),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic(),
-                     "kernel": "bkv_paged_decode (partition + merge, CUDA events around the call)",
+                     "kernel": "decode partition kernel (bkv_paged_decode_partition, CUDA events around it)",
+                     "decode_call_GBps": kv_bytes / (dms / 1e3) / 1e9,
                      "peak_kind": f"{peak_kind} copy bandwidth"},
         "decode_ms": dms,
+        "partition_ms": pms,
         "eager_ms_per_step": eager_ms,
         "e2e": {"value": world * kv_bytes / (ems / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ems},

@@ -188,6 +188,39 @@ int bkv_paged_decode(const void *q, const void *k_cache, const void *v_cache,
                      int32_t *err_count, bkv_stream_t stream);
 
 /*
+ * bkv_paged_decode_partition, bkv_paged_decode_merge
+ *   The two phases of bkv_paged_decode, with exactly its arguments and
+ *   checks: the partition phase reads the cache and writes every split-KV
+ *   partial (o, max, sum of weights) into `workspace`; the merge phase,
+ *   enqueued later with the same arguments and the same workspace contents,
+ *   combines them into `out`.  The operation is the one bkv_paged_decode
+ *   defines ("Padding and Batching with Block KV", Cache Masking); the pages
+ *   prescribe no split, so the split itself and its exact log-sum-exp merge
+ *   of partial softmaxes belong to this library (no counterpart on the
+ *   pages).  bkv_paged_decode is exactly partition followed by merge, so the
+ *   two-call form gives bit-identical results.  Between the calls the caller
+ *   may run other work on the stream; the workspace layout is private to
+ *   this library version, so it must reach the merge unchanged.
+ *   Errors: as bkv_paged_decode; each call validates its arguments again.
+ */
+int bkv_paged_decode_partition(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
+                               const int32_t *context_lens, int32_t max_context_len,
+                               int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int64_t total_blocks, float softmax_scale, int mask_mode, int dtype,
+                               void *out, void *workspace, size_t workspace_bytes,
+                               int32_t *err_count, bkv_stream_t stream);
+int bkv_paged_decode_merge(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
+                           const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs,
+                           int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, int64_t total_blocks,
+                           float softmax_scale, int mask_mode, int dtype, void *out,
+                           void *workspace, size_t workspace_bytes, int32_t *err_count,
+                           bkv_stream_t stream);
+
+/*
  * bkv_paged_decode_noalloc
  *   No counterpart on the pages: this is a convenience of this library.
  *

@@ -64,9 +64,11 @@ def load() -> ctypes.CDLL:
         lib.bkv_cache_write.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i32, i32, i32, cint, vp, vp]
         lib.bkv_paged_decode_workspace_size.restype = sz
         lib.bkv_paged_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
-        lib.bkv_paged_decode.restype = cint
-        lib.bkv_paged_decode.argtypes = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i32, i64, f32,
-                                         cint, cint, vp, vp, sz, vp, vp]
+        dec = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i32, i64, f32, cint, cint, vp, vp, sz, vp,
+               vp]
+        for fn in ("bkv_paged_decode", "bkv_paged_decode_partition", "bkv_paged_decode_merge"):
+            getattr(lib, fn).restype = cint
+            getattr(lib, fn).argtypes = dec
         _lib = lib
         return lib
 
@@ -163,6 +165,26 @@ def bkv_paged_decode_workspace_size(num_reqs, q_len, num_q_heads, num_kv_heads, 
 def bkv_paged_decode(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
                      softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None):
     """GQA paged decode attention into ``out`` (num_reqs, q_len, H_q, D) (see include/bkv.h)."""
+    return _decode("bkv_paged_decode", q, k_cache, v_cache, block_table, context_lens, max_context_len, out,
+                   workspace, softmax_scale, mask_mode, err_count, stream)
+
+
+def bkv_paged_decode_partition(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
+                               softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None):
+    """Phase 1 of bkv_paged_decode: split-KV partials into ``workspace`` (see include/bkv.h)."""
+    return _decode("bkv_paged_decode_partition", q, k_cache, v_cache, block_table, context_lens, max_context_len,
+                   out, workspace, softmax_scale, mask_mode, err_count, stream)
+
+
+def bkv_paged_decode_merge(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
+                           softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None):
+    """Phase 2 of bkv_paged_decode: merge the workspace partials into ``out`` (see include/bkv.h)."""
+    return _decode("bkv_paged_decode_merge", q, k_cache, v_cache, block_table, context_lens, max_context_len, out,
+                   workspace, softmax_scale, mask_mode, err_count, stream)
+
+
+def _decode(fn, q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace, softmax_scale,
+            mask_mode, err_count, stream):
     if q.dim() != 4 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
         raise ValueError("q/out must be (num_reqs, q_len, H_q, D); caches (total_blocks, bs, H_kv, D)")
     nr, ql, hq, d = q.shape
@@ -179,7 +201,7 @@ def bkv_paged_decode(q, k_cache, v_cache, block_table, context_lens, max_context
         raise TypeError("workspace must be a uint8 tensor")
     ws_ptr = None if workspace is None else _dev(workspace, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel()
-    _check("bkv_paged_decode", load().bkv_paged_decode(
+    _check(fn, getattr(load(), fn)(
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_table, "block_table", torch.int32, contiguous=False), block_table.stride(0),
         block_table.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), nr, ql, hq, hkv,

@@ -413,26 +413,36 @@ extern "C" size_t bkv_paged_decode_workspace_size(int32_t num_reqs, int32_t q_le
     return p.ws_bytes;
 }
 
-extern "C" int bkv_paged_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
-                                int64_t bt_stride, int32_t bt_cols, const int32_t *context_lens,
-                                int32_t max_context_len, int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
-                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t total_blocks,
-                                float softmax_scale, int mask_mode, int dtype, void *out, void *workspace,
-                                size_t workspace_bytes, int32_t *err_count, bkv_stream_t stream) {
+namespace bkv {
+
+// Everything one decode call needs, decided from its arguments alone (so the
+// partition and merge entry points, called separately with the same
+// arguments, agree on the kernel, the plan and the workspace layout).
+struct DecodeCall {
+    DecodeArgs a;
+    DecodePlan plan;
+    bool tc;
+    TcLaunch t;
+};
+
+static int decode_setup(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                        int64_t bt_stride, int32_t bt_cols, const int32_t *context_lens, int32_t max_context_len,
+                        int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int64_t total_blocks, float softmax_scale, int mask_mode, int dtype,
+                        void *out, void *workspace, size_t workspace_bytes, int32_t *err_count, DecodeCall *c) {
     if (dtype != BKV_BF16 && dtype != BKV_F32) return BKV_ERR_UNSUPPORTED;
     if (head_dim > 256 || head_dim % 2 != 0) return BKV_ERR_UNSUPPORTED;
     if (mask_mode != BKV_MASK_CAUSAL && mask_mode != BKV_MASK_ALL) return BKV_ERR_INVALID_ARG;
     if (bt_cols < 0 || bt_stride < bt_cols || total_blocks < 0) return BKV_ERR_INVALID_ARG;
-    bkv::DecodePlan plan;
-    if (!bkv::make_decode_plan(num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
-                               &plan))
+    DecodePlan &plan = c->plan;
+    if (!make_decode_plan(num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, &plan))
         return BKV_ERR_INVALID_ARG;
     if (!q || !out || !context_lens || (bt_cols > 0 && !block_table)) return BKV_ERR_INVALID_ARG;
     if (max_context_len > 0 && (!k_cache || !v_cache)) return BKV_ERR_INVALID_ARG;
-    if (workspace_bytes < plan.ws_bytes || !workspace || !bkv::aligned(workspace, 16)) return BKV_ERR_INVALID_ARG;
+    if (workspace_bytes < plan.ws_bytes || !workspace || !aligned(workspace, 16)) return BKV_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / sqrtf((float)head_dim);
 
-    bkv::DecodeArgs a;
+    DecodeArgs &a = c->a;
     a.q = q;
     a.k = k_cache;
     a.v = v_cache;
@@ -448,47 +458,87 @@ extern "C" int bkv_paged_decode(const void *q, const void *k_cache, const void *
     a.D = head_dim;
     a.bs = block_size;
     a.total_blocks = total_blocks;
-    a.scale_log2 = softmax_scale * bkv::kLog2e;
+    a.scale_log2 = softmax_scale * kLog2e;
     a.mask_mode = mask_mode;
     a.dtype = dtype;
     a.chunk = plan.chunk;
     a.n_chunks = plan.n_chunks;
     a.G = num_q_heads / num_kv_heads;
     a.nq = plan.nq;
+    a.out = out;
+    a.err = err_count;
     // partial-slot layout of the kernel that runs (see DecodePlan)
     auto set_slots = [&](int64_t slots) {
         char *base = static_cast<char *>(workspace) + plan.header_bytes;
         a.ws_o = reinterpret_cast<float *>(base);
-        a.ws_ml = reinterpret_cast<float *>(base + bkv::ceil_div<int64_t>(slots * plan.nq * head_dim * 4, 256) * 256);
+        a.ws_ml = reinterpret_cast<float *>(base + ceil_div<int64_t>(slots * plan.nq * head_dim * 4, 256) * 256);
     };
     const int64_t units = (int64_t)num_reqs * num_kv_heads;
     a.parts = 2;
     a.sk_pre = static_cast<int32_t *>(workspace);
     a.sk_grid = plan.sk_grid;
     set_slots(2 * (plan.sk_grid + units));
-    a.out = out;
-    a.err = err_count;
-
-    cudaStream_t st = (cudaStream_t)stream;
-    int rc = BKV_ERR_UNSUPPORTED;
-    if (bkv::decode_tc_supported(a)) rc = bkv::launch_decode_tc(a, st);
-    if (rc == BKV_ERR_UNSUPPORTED) {
+    c->tc = prepare_decode_tc(a, &c->t);
+    if (!c->tc) {
         a.parts = 1;
         a.sk_pre = nullptr;
         set_slots(units * plan.n_chunks);
-        if (dtype == BKV_BF16) bkv::launch_generic_dpl<__nv_bfloat16>(a, st);
-        else bkv::launch_generic_dpl<float>(a, st);
-        rc = bkv::launch_status();
     }
-    if (rc != BKV_OK) return rc;
+    return BKV_OK;
+}
 
-    const int max_slots = a.sk_pre ? 2 * plan.sk_grid : plan.n_chunks * a.parts;
+static int decode_partition(DecodeCall &c, cudaStream_t st) {
+    if (c.tc) return launch_decode_tc(c.a, c.t, st);
+    if (c.a.dtype == BKV_BF16) launch_generic_dpl<__nv_bfloat16>(c.a, st);
+    else launch_generic_dpl<float>(c.a, st);
+    return launch_status();
+}
+
+static int decode_merge(DecodeCall &c, cudaStream_t st) {
+    const DecodeArgs &a = c.a;
+    const int max_slots = a.sk_pre ? 2 * c.plan.sk_grid : c.plan.n_chunks * a.parts;
     const size_t msmem = 4 * (size_t)max_slots * 4;
-    const dim3 mgrid((unsigned)((int64_t)num_reqs * num_kv_heads));
+    const dim3 mgrid((unsigned)((int64_t)a.num_reqs * a.H_kv));
     const cudaError_t e =
-        dtype == BKV_BF16
-            ? bkv::launch_pdl(bkv::decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(128), msmem, st, a, max_slots)
-            : bkv::launch_pdl(bkv::decode_merge_kernel<float>, mgrid, dim3(128), msmem, st, a, max_slots);
-    if (e != cudaSuccess) bkv::set_cuda_error(e);
-    return bkv::launch_status();
+        a.dtype == BKV_BF16
+            ? launch_pdl(decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(128), msmem, st, a, max_slots)
+            : launch_pdl(decode_merge_kernel<float>, mgrid, dim3(128), msmem, st, a, max_slots);
+    if (e != cudaSuccess) set_cuda_error(e);
+    return launch_status();
+}
+
+}  // namespace bkv
+
+#define BKV_DECODE_PARAMS                                                                                         \
+    const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table, int64_t bt_stride,      \
+        int32_t bt_cols, const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs, int32_t q_len,  \
+        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t total_blocks,   \
+        float softmax_scale, int mask_mode, int dtype, void *out, void *workspace, size_t workspace_bytes,       \
+        int32_t *err_count, bkv_stream_t stream
+#define BKV_DECODE_SETUP(c)                                                                                       \
+    bkv::decode_setup(q, k_cache, v_cache, block_table, bt_stride, bt_cols, context_lens, max_context_len,       \
+                      num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, total_blocks, softmax_scale, \
+                      mask_mode, dtype, out, workspace, workspace_bytes, err_count, &(c))
+
+extern "C" int bkv_paged_decode(BKV_DECODE_PARAMS) {
+    bkv::DecodeCall c;
+    int rc = BKV_DECODE_SETUP(c);
+    if (rc != BKV_OK) return rc;
+    rc = bkv::decode_partition(c, (cudaStream_t)stream);
+    if (rc != BKV_OK) return rc;
+    return bkv::decode_merge(c, (cudaStream_t)stream);
+}
+
+extern "C" int bkv_paged_decode_partition(BKV_DECODE_PARAMS) {
+    bkv::DecodeCall c;
+    const int rc = BKV_DECODE_SETUP(c);
+    if (rc != BKV_OK) return rc;
+    return bkv::decode_partition(c, (cudaStream_t)stream);
+}
+
+extern "C" int bkv_paged_decode_merge(BKV_DECODE_PARAMS) {
+    bkv::DecodeCall c;
+    const int rc = BKV_DECODE_SETUP(c);
+    if (rc != BKV_OK) return rc;
+    return bkv::decode_merge(c, (cudaStream_t)stream);
 }

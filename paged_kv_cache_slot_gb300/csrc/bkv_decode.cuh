@@ -1,6 +1,8 @@
 // bkv_decode.cuh -- shared declarations of the paged decode kernels.
 #pragma once
 
+#include <cuda.h>
+
 #include "bkv_internal.cuh"
 
 namespace bkv {
@@ -52,8 +54,14 @@ bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int3
                       int32_t head_dim, int32_t block_size, int32_t max_context_len, DecodePlan *plan);
 
 // tcgen05 / TMA partition kernel for bf16, head_dim 128 (bkv_decode_tc.cu).
-// Returns BKV_ERR_UNSUPPORTED when the shape is outside what it handles.
-int launch_decode_tc(const DecodeArgs &a, cudaStream_t stream);
-bool decode_tc_supported(const DecodeArgs &a);
+// prepare_decode_tc decides, from the arguments alone, whether it handles
+// this call (and encodes its tensor maps); the partition and merge entry
+// points take the same decision independently.
+struct TcLaunch {
+    CUtensorMap mk, mv, mq;
+    int seg_rows;
+};
+bool prepare_decode_tc(const DecodeArgs &a, TcLaunch *t);
+int launch_decode_tc(const DecodeArgs &a, const TcLaunch &t, cudaStream_t stream);
 
 }  // namespace bkv

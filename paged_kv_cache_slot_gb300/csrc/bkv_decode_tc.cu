@@ -919,28 +919,26 @@ static bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1
 
 }  // namespace tc
 
-bool decode_tc_supported(const DecodeArgs &a) {
+bool prepare_decode_tc(const DecodeArgs &a, TcLaunch *t) {
     if (a.dtype != BKV_BF16 || a.D != tc::kD || a.nq > tc::kN || a.nq <= 0) return false;
     if (a.bs < 8 || !((tc::kTile % a.bs == 0) || (a.bs % tc::kTile == 0))) return false;
     if (a.G > 256 || a.q_len > 256 || a.H_kv > 65535 || a.num_reqs > tc::kMaxReqs || !a.sk_pre) return false;
-    if ((int64_t)a.total_blocks * a.bs >= ((int64_t)1 << 31)) return false;
+    if ((int64_t)a.total_blocks * a.bs >= ((int64_t)1 << 31) || a.total_blocks <= 0) return false;
     if ((int64_t)a.num_reqs * a.q_len >= ((int64_t)1 << 31)) return false;
-    if (!aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.q, 16)) return false;
-    return tc::encode_fn() != nullptr;
+    if (!aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.q, 16) || !aligned(a.out, 16)) return false;
+    if (!tc::encode_fn()) return false;
+    using namespace tc;
+    t->seg_rows = a.bs < kTile ? a.bs : kTile;
+    const uint64_t rows = (uint64_t)a.total_blocks * (uint64_t)a.bs;
+    const uint64_t row_stride = (uint64_t)a.H_kv * kD * 2;
+    return encode_3d(&t->mk, a.k, kD, a.H_kv, rows, kD * 2, row_stride, 64, 1, t->seg_rows) &&
+           encode_3d(&t->mv, a.v, kD, a.H_kv, rows, kD * 2, row_stride, 64, 1, t->seg_rows) &&
+           encode_3d(&t->mq, a.q, kD, a.H_q, (uint64_t)a.num_reqs * a.q_len, kD * 2, (uint64_t)a.H_q * kD * 2, 64,
+                     a.G, a.q_len);
 }
 
-int launch_decode_tc(const DecodeArgs &a, cudaStream_t st) {
+int launch_decode_tc(const DecodeArgs &a, const TcLaunch &t, cudaStream_t st) {
     using namespace tc;
-    const int seg_rows = a.bs < kTile ? a.bs : kTile;
-    CUtensorMap mk, mv, mq;
-    const uint64_t rows = (uint64_t)a.total_blocks * (uint64_t)a.bs;
-    if (rows == 0) return BKV_ERR_UNSUPPORTED;
-    const uint64_t row_stride = (uint64_t)a.H_kv * kD * 2;
-    if (!encode_3d(&mk, a.k, kD, a.H_kv, rows, kD * 2, row_stride, 64, 1, seg_rows) ||
-        !encode_3d(&mv, a.v, kD, a.H_kv, rows, kD * 2, row_stride, 64, 1, seg_rows) ||
-        !encode_3d(&mq, a.q, kD, a.H_q, (uint64_t)a.num_reqs * a.q_len, kD * 2, (uint64_t)a.H_q * kD * 2, 64, a.G,
-                   a.q_len))
-        return BKV_ERR_UNSUPPORTED;
     // the grid is the stream-K CTA count the workspace was laid out for
     const int64_t grid = a.sk_grid;
     // the softmax handles only the query rows that exist (4, 8 or 16 columns)
@@ -954,7 +952,8 @@ int launch_decode_tc(const DecodeArgs &a, cudaStream_t st) {
             return launch_status();
         attr_set[dev][slot] = true;
     }
-    const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, mk, mv, mq, a, seg_rows);
+    const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, t.mk, t.mv, t.mq, a,
+                                     t.seg_rows);
     if (e != cudaSuccess) set_cuda_error(e);
     return launch_status();
 }

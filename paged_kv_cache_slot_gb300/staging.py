@@ -112,6 +112,12 @@ class DeviceWorkload:
                              out, self.workspace, mask_mode=mask_mode, err_count=self.err_count, stream=stream)
         return out
 
+    def decode_partition(self, stream=None):
+        """Phase 1 of the decode alone (the partition kernel), for timing."""
+        bkv.bkv_paged_decode_partition(self.q, self.k_cache, self.v_cache, self.kernel_table, self.context_lens,
+                                       self.max_context_len, self.out, self.workspace, err_count=self.err_count,
+                                       stream=stream)
+
     def step(self, stream=None):
         """One pass of the whole path: a2 -> a1 -> a3 -> a4 + a5."""
         self.expand_blocks(stream)

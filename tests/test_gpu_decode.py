@@ -236,3 +236,18 @@ def test_repeated_steps_are_deterministic():
         dw.step()
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), dw.out.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["llama3_decode", "hybrid_spec"])
+def test_partition_then_merge_equals_one_call_bitwise(name):
+    w = wl.make(name)
+    dw = DeviceWorkload(w)
+    dw.write_step()
+    one = dw.decode(out=torch.empty_like(dw.out)).clone()
+    two = torch.empty_like(dw.out)
+    args = (dw.q, dw.k_cache, dw.v_cache, dw.kernel_table, dw.context_lens, dw.max_context_len, two, dw.workspace)
+    bkv.bkv_paged_decode_partition(*args, err_count=dw.err_count)
+    bkv.bkv_paged_decode_merge(*args, err_count=dw.err_count)
+    torch.cuda.synchronize()
+    assert torch.equal(one.view(torch.int16), two.view(torch.int16))
+    assert int(dw.err_count.item()) == 0
