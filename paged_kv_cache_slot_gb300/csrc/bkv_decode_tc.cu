@@ -99,7 +99,10 @@ constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffPre = kOffAbort + 4;                    // [kMaxReqs + 1] tile prefix per request
 constexpr int kOffEnt = (kOffPre + (kMaxReqs + 1) * 4 + 15) / 16 * 16;   // [producer][2][kWinBlocks] entries
-constexpr int kSmemUsed = kOffEnt + 4 * kWinBlocks * 4;
+// [kMaxReqs] last-tile fill of each request minus one: with the tile count it
+// gives the clamped length without a global read, len = (tiles - 1) * 128 + fill
+constexpr int kOffLrem = kOffEnt + 4 * kWinBlocks * 4;
+constexpr int kSmemUsed = kOffLrem + kMaxReqs;
 constexpr int kSmemBytes = kSmemUsed + 1024;              // slack for 1024 alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
 static_assert(kOffEnt % 16 == 0, "entry buffers must stay aligned");
@@ -186,6 +189,10 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -278,35 +285,92 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NQ]) {
 // ---------------------------------------------------------------------------
 // Stream-K schedule
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int32_t clamp_len(const DecodeArgs &a, int r) {
-    int32_t L = __ldg(a.ctx + r);
-    return L > a.max_ctx ? a.max_ctx : (L < 0 ? 0 : L);
+// The schedule's global reads, issued together right after the grid
+// dependency wait: every thread loads its share of context_lens (one round
+// trip for up to kMaxReqs requests) and prefetches a slice of the block table
+// into L2, so that the producers' first table reads hit L2; the V ring is
+// zeroed while those loads are in flight (a V row that no TMA load writes
+// must hold zeros, never uninitialised bits, for the P.V MMA).  Leaves the
+// tile count of request r in pre[r] and its last tile's fill in lrem[r]; a
+// length above the host bound is clamped to it and counted once (CTA 0).
+// The caller orders the V-ring stores before the TMA writes (proxy fence +
+// barrier).
+constexpr int kLensPerThread = (kMaxReqs + kThreads - 1) / kThreads;
+
+__device__ void schedule_loads(const DecodeArgs &a, int32_t *pre, uint8_t *lrem, uint8_t *smem) {
+    const int n = a.num_reqs;
+    int32_t lens[kLensPerThread];
+#pragma unroll
+    for (int i = 0; i < kLensPerThread; ++i) {
+        const int r = threadIdx.x + i * kThreads;
+        lens[i] = r < n ? __ldg(a.ctx + r) : 0;
+    }
+    {
+        // 128-byte lines of the table rows, at most two per thread of the grid
+        const int64_t lines_per_row = ((int64_t)a.bt_cols + 31) / 32;
+        const int64_t lines = lines_per_row * n;
+        const int64_t nthr = (int64_t)gridDim.x * kThreads;
+        int64_t l = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+        for (int k = 0; k < 2 && l < lines; ++k, l += nthr) {
+            const int64_t r = l / lines_per_row;
+            prefetch_l2(a.bt + r * a.bt_stride + (l - r * lines_per_row) * 32);
+        }
+    }
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    uint4 *v = reinterpret_cast<uint4 *>(smem + kOffV);
+    for (int i = threadIdx.x; i < kVStages * kTileBytes / 16; i += kThreads) v[i] = z;
+#pragma unroll
+    for (int i = 0; i < kLensPerThread; ++i) {
+        const int r = threadIdx.x + i * kThreads;
+        if (r < n) {
+            if (lens[i] > a.max_ctx && blockIdx.x == 0 && a.err) atomicAdd(a.err, 1);
+            const int32_t L = lens[i] > a.max_ctx ? a.max_ctx : (lens[i] < 0 ? 0 : lens[i]);
+            pre[r] = (L + kTile - 1) / kTile;
+            lrem[r] = (uint8_t)((L - 1) & (kTile - 1));
+        }
+    }
 }
 
-// pre[r] = sum of ceil(len / 128) over requests before r (r <= num_reqs),
-// built in shared memory by warp 0; CTA 0 also stores it in the workspace for
-// the merge.  Ends with a __syncthreads.
-__device__ void build_prefix(const DecodeArgs &a, int32_t *pre) {
+// Exclusive prefix sum of the tile counts in place, pre[n] = total, over all
+// threads of the CTA (tot: 12 ints of scratch); CTA 0 also stores it in the
+// workspace for the merge.  Starts and ends with a __syncthreads.
+__device__ void scan_prefix(const DecodeArgs &a, int32_t *pre, int32_t *tot) {
+    constexpr int kWarps = kThreads / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = a.num_reqs;
+    __syncthreads();
+    const int per = (n + kThreads - 1) / kThreads;
+    const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
+    int32_t sum = 0;
+    for (int r = lo; r < hi; ++r) sum += pre[r];
+    int32_t inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t x = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += x;
+    }
+    if (lane == 31) tot[warp] = inc;
+    __syncthreads();
     if (warp == 0) {
-        const int per = (n + 31) / 32;
-        const int lo = min(n, lane * per), hi = min(n, lo + per);
-        int32_t sum = 0;
-        for (int r = lo; r < hi; ++r) sum += (clamp_len(a, r) + kTile - 1) / kTile;
-        int32_t inc = sum;
+        const int32_t w = lane < kWarps ? tot[lane] : 0;
+        int32_t wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += v;
+            const int32_t x = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += x;
         }
-        int32_t run = inc - sum;
-        for (int r = lo; r < hi; ++r) {
-            pre[r] = run;
-            run += (clamp_len(a, r) + kTile - 1) / kTile;
-        }
-        if (lane == 31) pre[n] = inc;
+        __syncwarp();
+        if (lane < kWarps) tot[lane] = wi - w;
+        if (lane == kWarps - 1) tot[kWarps] = wi;
     }
+    __syncthreads();
+    int32_t run = tot[warp] + inc - sum;
+    for (int r = lo; r < hi; ++r) {
+        const int32_t t = pre[r];
+        pre[r] = run;
+        run += t;
+    }
+    if (threadIdx.x == 0) pre[n] = tot[kWarps];
     __syncthreads();
     if (blockIdx.x == 0)
         for (int r = threadIdx.x; r <= n; r += blockDim.x) a.sk_pre[r] = pre[r];
@@ -323,11 +387,13 @@ struct Unit {
 // Walks this CTA's units in order.
 struct StreamK {
     const int32_t *pre;
+    const uint8_t *lrem;
     int n, H;
     int64_t t, t1;   // next global tile, end of this CTA's range
     int r;
-    __device__ void init(const DecodeArgs &a, const int32_t *pre_) {
+    __device__ void init(const DecodeArgs &a, const int32_t *pre_, const uint8_t *lrem_) {
         pre = pre_;
+        lrem = lrem_;
         n = a.num_reqs;
         H = a.H_kv;
         // split over min(grid, TT) CTAs so every participating CTA has at
@@ -361,7 +427,7 @@ struct StreamK {
         x.r = r;
         x.g = g;
         x.s = (int64_t)r * H + g;
-        x.L = clamp_len(a, r);
+        x.L = (int32_t)(Tr - 1) * kTile + lrem[r] + 1;   // Tr > 0: the stream has this tile
         x.start = (int32_t)(lo * kTile);
         x.cend = (int32_t)(hi * kTile < (int64_t)x.L ? hi * kTile : (int64_t)x.L);
         x.ntiles = (int32_t)(hi - lo);
@@ -460,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sm_q = sbase + kOffQ;
     const uint32_t sm_p = sbase + kOffP;
 
-    // ---- set-up (no global memory): barriers, zeroed V / Q / P buffers, TMEM ----
+    // ---- set-up (no global memory): barriers, zeroed Q / P buffers, TMEM ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar_kfull(s), 1);
@@ -489,11 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmQ);
     }
     {
-        // V tiles must never hold NaN where nothing was loaded; Q rows past
-        // the group and P start at zero.
+        // Q rows past the group and P start at zero
         const uint4 z = make_uint4(0, 0, 0, 0);
-        uint4 *v = reinterpret_cast<uint4 *>(smem + kOffV);
-        for (int i = threadIdx.x; i < kVStages * kTileBytes / 16; i += kThreads) v[i] = z;
         uint4 *qp = reinterpret_cast<uint4 *>(smem + kOffQ);
         for (int i = threadIdx.x; i < (2 * kQBytes + 2 * kPBytes) / 16; i += kThreads) qp[i] = z;
     }
@@ -509,7 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     pdl_wait();                // global memory is read from here on
     pdl_trigger();
-    build_prefix(a, pre);      // ends with __syncthreads
+    uint8_t *lrem = smem + kOffLrem;
+    schedule_loads(a, pre, lrem, smem);
+    fence_proxy_async();       // the zeroed V ring before any TMA write to it
+    // red_max is free until the softmax starts: scratch for the scan
+    scan_prefix(a, pre, reinterpret_cast<int32_t *>(red_max));
     const uint32_t tmem = *tmem_slot;
 
     const int G = a.G;
@@ -532,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t t0, t1;   // tiles of the unit
         };
         StreamK sk;
-        sk.init(a, pre);
+        sk.init(a, pre, lrem);
         Unit cu = {};
         bool have_u = false;
         int32_t wt = 0;
@@ -592,8 +659,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t lb_first = win_first_block(cur);
             const Unit &x = cur.u;
             if (cur.t0 == 0 && !is_v) {
-                if (lane == 0 && x.start == 0 && x.g == 0 && __ldg(a.ctx + x.r) > a.max_ctx && a.err)
-                    atomicAdd(a.err, 1);
                 const int qb = us & 1;
                 if (!mbar_wait_warp(bar_qempty(qb), ((us >> 1) & 1) ^ 1, abort_flag)) break;
                 if (lane == 0) {
@@ -692,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             StreamK sk;
-            sk.init(a, pre);
+            sk.init(a, pre, lrem);
             Unit x;
             while (ok && sk.next(a, x)) {
                 const int qb = us & 1;
@@ -763,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool red_writer = reduced_writer<NQ>(lane);
         float *my_red_sum = red_sum + wg * (kN * 4);
         StreamK sk;
-        sk.init(a, pre);
+        sk.init(a, pre, lrem);
         Unit x;
         while (ok && sk.next(a, x)) {
             int32_t lastv[NQ];
@@ -925,6 +990,8 @@ bool prepare_decode_tc(const DecodeArgs &a, TcLaunch *t) {
     if (a.G > 256 || a.q_len > 256 || a.H_kv > 65535 || a.num_reqs > tc::kMaxReqs || !a.sk_pre) return false;
     if ((int64_t)a.total_blocks * a.bs >= ((int64_t)1 << 31) || a.total_blocks <= 0) return false;
     if ((int64_t)a.num_reqs * a.q_len >= ((int64_t)1 << 31)) return false;
+    // the tile prefix sums and the global tile numbers stay within int32
+    if ((int64_t)a.num_reqs * ((a.max_ctx + tc::kTile - 1) / tc::kTile) * a.H_kv >= ((int64_t)1 << 31)) return false;
     if (!aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.q, 16) || !aligned(a.out, 16)) return false;
     if (!tc::encode_fn()) return false;
     using namespace tc;
