@@ -67,7 +67,8 @@ def _load():
             lib.orc_map_to_kernel_blocks.argtypes = [vp, i32, i64, i32, i32, i32, vp, i64]
             lib.orc_cache_write.restype = i64
             lib.orc_cache_write.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int]
-            dec = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i64, dbl, ctypes.c_int, ctypes.c_int, vp]
+            dec = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i64, dbl, ctypes.c_int, i32,
+                   ctypes.c_int, vp]
             lib.orc_paged_decode.restype = i64
             lib.orc_paged_decode.argtypes = dec
             lib.orc_paged_decode_request.restype = i64
@@ -157,7 +158,7 @@ def cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens=None, i
     return kc, vc, int(err)
 
 
-def _decode_args(q, k_cache, v_cache, block_table, context_lens, scale, mask_mode):
+def _decode_args(q, k_cache, v_cache, block_table, context_lens, scale, mask_mode, sliding_window=0):
     qa = np.ascontiguousarray(q)
     kc = np.ascontiguousarray(k_cache)
     vc = np.ascontiguousarray(v_cache)
@@ -172,13 +173,17 @@ def _decode_args(q, k_cache, v_cache, block_table, context_lens, scale, mask_mod
         raise ValueError("head_dim mismatch")
     sc = (1.0 / np.sqrt(d)) if scale is None else float(scale)
     args = (_ptr(qa), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], bt.shape[1], _ptr(cl), nr, ql, hq, hkv, d, bs, tb,
-            sc, int(mask_mode), dt)
+            sc, int(mask_mode), int(sliding_window), dt)
     return args, (qa, kc, vc, bt, cl), (nr, ql, hq, d)
 
 
-def paged_decode(q, k_cache, v_cache, block_table, context_lens, scale=None, mask_mode=0):
-    """fp64 attention output (num_reqs, q_len, H_q, D) and the bad-entry count."""
-    args, keep, shape = _decode_args(q, k_cache, v_cache, block_table, context_lens, scale, mask_mode)
+def paged_decode(q, k_cache, v_cache, block_table, context_lens, scale=None, mask_mode=0, sliding_window=0):
+    """fp64 attention output (num_reqs, q_len, H_q, D) and the bad-entry count.
+
+    ``sliding_window`` W > 0: query t of a request of length L sees only keys
+    j >= L - q_len + t - W + 1 (reading R13 of the C source)."""
+    args, keep, shape = _decode_args(q, k_cache, v_cache, block_table, context_lens, scale, mask_mode,
+                                     sliding_window)
     out = np.zeros(shape, np.float64)
     err = _load().orc_paged_decode(*args, _ptr(out))
     if err < 0:
@@ -187,9 +192,11 @@ def paged_decode(q, k_cache, v_cache, block_table, context_lens, scale=None, mas
     return out, int(err)
 
 
-def paged_decode_request(r, q, k_cache, v_cache, block_table, context_lens, scale=None, mask_mode=0):
+def paged_decode_request(r, q, k_cache, v_cache, block_table, context_lens, scale=None, mask_mode=0,
+                         sliding_window=0):
     """fp64 output of request ``r`` only, (q_len, H_q, D)."""
-    args, keep, shape = _decode_args(q, k_cache, v_cache, block_table, context_lens, scale, mask_mode)
+    args, keep, shape = _decode_args(q, k_cache, v_cache, block_table, context_lens, scale, mask_mode,
+                                     sliding_window)
     out = np.zeros(shape, np.float64)
     err = _load().orc_paged_decode_request(int(r), *args, _ptr(out))
     if err < 0:

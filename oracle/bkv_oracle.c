@@ -24,6 +24,8 @@
  *        - 設計動機 (kernel block_size vs manager block_size; CUDA-graph
  *          padding of the slot-mapping tail)
  *        - 境界と失敗 (block_size % kernel_block_size != 0 is an error)
+ *   [P3] "KV Caching with vLLM" (Neuron)
+ *        - Layer-specific cache specification (sliding-window layers)
  *   [P4] "Decode Context-Length Bucketing"
  *        - Design / Per-step bucket selection (needed_seq), Block-table
  *          head-trim vs. SWA tail-trim
@@ -44,6 +46,13 @@
  *       row) outputs 0.
  *   R10 a key whose block-table entry is <= 0 is masked out, not read.
  *   R12 a position past the table width gives slot -1 and counts an error.
+ *   R13 sliding window W > 0 ([P4 Block-table head-trim vs. SWA tail-trim;
+ *       [P3] Layer-specific cache specification: an SWA layer keeps only
+ *       the recent tokens within the window): query t at position p_t =
+ *       L - q_len + t sees only keys j >= p_t - W + 1, in both mask modes
+ *       (the upper bound is R7's); blocks wholly before every query's window
+ *       are never read, so they may be null or hold anything.  W <= 0: no
+ *       window.
  */
 #include <math.h>
 #include <stdint.h>
@@ -238,8 +247,9 @@ int64_t orc_cache_write(const void *k_new, const void *v_new,
  * its q_len query tokens t, each query head h:
  *
  *   key position j is visible iff  j < L,  j <= L - q_len + t (mask_mode 0,
- *   R7), and its table entry b = block_table[r][j / bs] is a real block
- *   (b > 0, R10; b < total_blocks, otherwise counted as an error);
+ *   R7),  j >= L - q_len + t - W + 1 (sliding window W > 0, R13), and its
+ *   table entry b = block_table[r][j / bs] is a real block (b > 0, R10;
+ *   b < total_blocks, otherwise counted as an error);
  *   s_j = scale * sum_d q[r,t,h,d] * K[b, j % bs, h / G, d]        (R6)
  *   out[r,t,h,:] = sum_j softmax(s)_j * V[b, j % bs, h / G, :]
  *
@@ -247,8 +257,9 @@ int64_t orc_cache_write(const void *k_new, const void *v_new,
  * before exponentiating; that changes no value, only avoids overflow.
  *
  * q and out are (num_reqs, q_len, num_q_heads, head_dim); out is fp64.
- * Returns the number of bad table entries met (positions past the table
- * width or ids past the cache), or -1 for invalid arguments.
+ * Returns the number of bad table entries met among the blocks some query
+ * may see (positions past the table width or ids past the cache), or -1 for
+ * invalid arguments.
  */
 int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
                                  const void *v_cache, const int32_t *block_table,
@@ -257,8 +268,8 @@ int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
                                  int32_t q_len, int32_t num_q_heads,
                                  int32_t num_kv_heads, int32_t head_dim,
                                  int32_t block_size, int64_t total_blocks,
-                                 double scale, int mask_mode, int dtype,
-                                 double *out)
+                                 double scale, int mask_mode, int32_t sliding_window,
+                                 int dtype, double *out)
 {
     if (orc_elem_bytes(dtype) == 0 || r < 0 || r >= num_reqs || q_len <= 0 ||
         num_q_heads <= 0 || num_kv_heads <= 0 ||
@@ -268,9 +279,15 @@ int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
     const int64_t D = head_dim;
     const int64_t G = num_q_heads / num_kv_heads;
     const int64_t L = context_lens[r] > 0 ? context_lens[r] : 0;
+    const int64_t W = sliding_window > 0 ? sliding_window : 0;
+    /* R13: no query sees a key before lo (the window of query 0) */
+    int64_t lo = 0;
+    if (W > 0 && L - q_len - W + 1 > 0)
+        lo = L - q_len - W + 1;
     int64_t errors = 0;
 
-    /* Which key positions may be read at all: j < L with a real block. */
+    /* Which key positions may be read at all: lo <= j < L with a real block
+     * (a bad entry counts once per block, at its first position read). */
     unsigned char *readable = (unsigned char *)malloc((size_t)(L > 0 ? L : 1));
     double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
     if (!readable || !s) {
@@ -280,9 +297,12 @@ int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
     }
     for (int64_t j = 0; j < L; ++j) {
         readable[j] = 0;
+        if (j < lo)
+            continue;
+        const int first = (j == lo) || (j % block_size == 0);
         int64_t lb = j / block_size;
         if (lb >= bt_cols) {
-            if (j % block_size == 0)
+            if (first)
                 errors += 1;
             continue;
         }
@@ -290,7 +310,7 @@ int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
         if (b <= 0)
             continue;
         if (b >= total_blocks) {
-            if (j % block_size == 0)
+            if (first)
                 errors += 1;
             continue;
         }
@@ -299,6 +319,7 @@ int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
 
     for (int64_t t = 0; t < q_len; ++t) {
         int64_t last_visible = (mask_mode == 0) ? (L - q_len + t) : (L - 1);
+        int64_t first_visible = (W > 0) ? (L - q_len + t - W + 1) : 0;
         for (int64_t h = 0; h < num_q_heads; ++h) {
             int64_t g = h / G;
             const int64_t qoff = (((int64_t)r * q_len + t) * num_q_heads + h) * D;
@@ -309,7 +330,7 @@ int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
             double m = -INFINITY;
             int any = 0;
             for (int64_t j = 0; j < L && j <= last_visible; ++j) {
-                if (!readable[j])
+                if (!readable[j] || j < first_visible)
                     continue;
                 int64_t b = block_table[(int64_t)r * bt_stride + j / block_size];
                 int64_t krow = ((b * block_size + j % block_size) * num_kv_heads + g) * D;
@@ -326,7 +347,7 @@ int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
 
             double denom = 0.0;
             for (int64_t j = 0; j < L && j <= last_visible; ++j) {
-                if (!readable[j])
+                if (!readable[j] || j < first_visible)
                     continue;
                 int64_t b = block_table[(int64_t)r * bt_stride + j / block_size];
                 int64_t vrow = ((b * block_size + j % block_size) * num_kv_heads + g) * D;
@@ -351,7 +372,7 @@ int64_t orc_paged_decode(const void *q, const void *k_cache, const void *v_cache
                          int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim,
                          int32_t block_size, int64_t total_blocks, double scale,
-                         int mask_mode, int dtype, double *out)
+                         int mask_mode, int32_t sliding_window, int dtype, double *out)
 {
     int64_t errors = 0;
     for (int32_t r = 0; r < num_reqs; ++r) {
@@ -360,7 +381,7 @@ int64_t orc_paged_decode(const void *q, const void *k_cache, const void *v_cache
                                              num_reqs, q_len, num_q_heads,
                                              num_kv_heads, head_dim, block_size,
                                              total_blocks, scale, mask_mode,
-                                             dtype, out);
+                                             sliding_window, dtype, out);
         if (e < 0)
             return e;
         errors += e;

@@ -11,6 +11,10 @@
   poisoning unreferenced memory with NaN, trimming the table, and writing 0
   instead of -1 for unused entries leave every output bit unchanged;
   padded (NULL) rows give 0.
+* Sliding window (reading R13): SDPA with the banded mask; a window that
+  covers every key changes no bit; a window of one returns the query's own
+  V row exactly; blocks wholly before the window may be null, garbage or
+  NaN without changing a bit or counting an error.
 """
 import dataclasses
 
@@ -20,12 +24,12 @@ import torch
 
 import oracle
 from paged_kv_cache_slot_gb300 import workloads as wl
-from oracle.cases import fill_oracle_cache, nan_cache
+from oracle.cases import BF16_NAN, fill_oracle_cache, nan_cache
 
 F64 = torch.float64
 
 
-def _sdpa_request(w, r, mask_mode, drop_logical_blocks=()):
+def _sdpa_request(w, r, mask_mode, drop_logical_blocks=(), window=0):
     """torch SDPA (fp64, CPU) for request r on its contiguous generator rows."""
     L = int(w.context_lens[r])
     q = wl.to_f32(w.q()[r]).astype(np.float64)                # (q_len, H_q, D)
@@ -46,6 +50,8 @@ def _sdpa_request(w, r, mask_mode, drop_logical_blocks=()):
         allowed = kpos[None, :] <= qpos[:, None]
     else:
         allowed = np.ones((w.q_len, len(kpos)), bool)
+    if window > 0:
+        allowed &= kpos[None, :] > qpos[:, None] - window
     G = w.group_size
     qt = torch.from_numpy(q).permute(1, 0, 2)                  # (H_q, q_len, D)
     kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(G, dim=0)
@@ -204,3 +210,70 @@ def test_query_rows_before_position_zero_are_zero():
     out, _ = _oracle_all(w, kc, vc, table)
     assert (out[:, :2] == 0).all() and np.isfinite(out).all()
     assert (out[0, 2] != 0).any()
+
+
+# ---------------------------------------------------------------------------
+# sliding window (R13)
+# ---------------------------------------------------------------------------
+def _oracle_win(w, kc, vc, table, window, mask_mode=0):
+    return oracle.paged_decode(w.q(), kc, vc, table, w.context_lens, mask_mode=mask_mode, sliding_window=window)
+
+
+@pytest.mark.parametrize("mask_mode", [0, 1])
+@pytest.mark.parametrize("window", [1, 2, 5, 9, 17])
+def test_window_matches_sdpa_with_banded_mask(mask_mode, window):
+    w = _small(prior=(30, 0, 17, 22, 9))
+    kc, vc, table = fill_oracle_cache(w)
+    out, err = _oracle_win(w, kc, vc, table, window, mask_mode)
+    assert err == 0
+    for r in range(w.num_rows):
+        np.testing.assert_allclose(out[r], _sdpa_request(w, r, mask_mode, window=window), rtol=0, atol=1e-12)
+
+
+def test_window_covering_every_key_changes_no_bit():
+    w = _small(prior=(30, 0, 17, 22, 9))
+    kc, vc, table = fill_oracle_cache(w)
+    base, _ = _oracle_all(w, kc, vc, table)
+    wide = int(w.context_lens.max()) + w.q_len
+    out, _ = _oracle_win(w, kc, vc, table, wide)
+    assert out.tobytes() == base.tobytes()
+    out0, _ = _oracle_win(w, kc, vc, table, 0)
+    assert out0.tobytes() == base.tobytes()
+
+
+def test_window_of_one_returns_the_query_positions_value_row():
+    w = _small(prior=(30, 0, 17, 22, 9), q_len=3)
+    kc, vc, table = fill_oracle_cache(w)
+    out, _ = _oracle_win(w, kc, vc, table, 1)
+    for r in (0, 2, 3, 4):
+        L = int(w.context_lens[r])
+        _, v = w.kv_rows(r, 0, L)
+        v = wl.to_f32(v).astype(np.float64)
+        for t in range(w.q_len):
+            p = L - w.q_len + t
+            assert (out[r, t] == np.repeat(v[p], w.group_size, axis=0)).all()
+
+
+def test_blocks_before_the_window_are_never_read():
+    w = _small(prior=(30, 0, 17, 22, 9), q_len=2)
+    kc, vc, table = fill_oracle_cache(w)
+    window = 5
+    base, err = _oracle_win(w, kc, vc, table, window)
+    assert err == 0 and np.isfinite(base).all()
+    bs = w.kernel_block_size
+    t_null, t_junk = table.copy(), table.copy()
+    kp, vp = kc.copy(), vc.copy()
+    for r in range(w.num_rows):
+        L = int(w.context_lens[r])
+        lo = max(0, L - w.q_len - window + 1)          # first key any query of the row sees
+        for lb in range(lo // bs):                     # logical blocks wholly before it
+            b = int(table[r, lb])
+            if b > 0:
+                kp[b] = BF16_NAN if w.dtype == "bf16" else np.nan
+                vp[b] = BF16_NAN if w.dtype == "bf16" else np.nan
+            t_null[r, lb] = -1
+            t_junk[r, lb] = 10**6
+    for tab, k_, v_ in ((t_null, kc, vc), (t_junk, kc, vc), (table, kp, vp)):
+        out, err = _oracle_win(w, k_, v_, tab, window)
+        assert err == 0
+        assert out.tobytes() == base.tobytes()
