@@ -155,7 +155,8 @@ size_t bkv_paged_decode_workspace_size(int32_t num_reqs, int32_t q_len, int32_t 
  *   For request r with L = context_lens[r] (cache length INCLUDING this
  *   step's q_len tokens), query token t < q_len, query head h, G =
  *   num_q_heads / num_kv_heads:
- *     key j is visible iff j < L, j <= L - q_len + t (BKV_MASK_CAUSAL only)
+ *     key j is visible iff j < L, j <= L - q_len + t (BKV_MASK_CAUSAL only),
+ *     j >= L - q_len + t - sliding_window + 1 (sliding_window > 0 only)
  *     and b = block_table[r * bt_stride + j / block_size] > 0;
  *     out[r][t][h] = softmax_j(softmax_scale * q[r][t][h] . K[b][j % block_size][h / G])
  *                    . V[b][j % block_size][h / G]
@@ -171,12 +172,22 @@ size_t bkv_paged_decode_workspace_size(int32_t num_reqs, int32_t q_len, int32_t 
  *   max_context_len  host-side upper bound on context_lens (sizes the grid);
  *             a larger context_lens[r] is clamped to it and counted as an error.
  *   softmax_scale    <= 0 selects 1 / sqrt(head_dim).
+ *   sliding_window   W > 0: a sliding-window attention layer ("KV Caching
+ *             with vLLM", Layer-specific cache specification: an SWA layer
+ *             keeps only the recent tokens within the window; "Decode
+ *             Context-Length Bucketing", Block-table head-trim vs. SWA
+ *             tail-trim): query t sees only the last W positions up to its
+ *             own, and only the blocks that overlap some query's window are
+ *             read, so the entries of older blocks may already be null (-1)
+ *             and their memory reused.  The table keeps logical block
+ *             numbering (entry j covers positions [j * block_size, ...)), so
+ *             no position offset is passed.  0: full attention.
  *   workspace        device scratch of workspace_bytes >=
  *                    bkv_paged_decode_workspace_size(...); may be null when
  *                    that size is 0.  Used only while the call's kernels run.
  *   Ids >= total_blocks and positions past bt_cols are masked and counted.
  *   INVALID_ARG: num_q_heads % num_kv_heads != 0, non-positive sizes, bad
- *   mask_mode, workspace too small, null pointers.
+ *   mask_mode, negative sliding_window, workspace too small, null pointers.
  *   UNSUPPORTED: dtype not BKV_BF16 / BKV_F32, head_dim > 256 or odd.
  */
 int bkv_paged_decode(const void *q, const void *k_cache, const void *v_cache,
@@ -184,8 +195,8 @@ int bkv_paged_decode(const void *q, const void *k_cache, const void *v_cache,
                      const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs,
                      int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                      int32_t block_size, int64_t total_blocks, float softmax_scale, int mask_mode,
-                     int dtype, void *out, void *workspace, size_t workspace_bytes,
-                     int32_t *err_count, bkv_stream_t stream);
+                     int32_t sliding_window, int dtype, void *out, void *workspace,
+                     size_t workspace_bytes, int32_t *err_count, bkv_stream_t stream);
 
 /*
  * bkv_paged_decode_partition, bkv_paged_decode_merge
@@ -208,16 +219,16 @@ int bkv_paged_decode_partition(const void *q, const void *k_cache, const void *v
                                const int32_t *context_lens, int32_t max_context_len,
                                int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                               int64_t total_blocks, float softmax_scale, int mask_mode, int dtype,
-                               void *out, void *workspace, size_t workspace_bytes,
-                               int32_t *err_count, bkv_stream_t stream);
+                               int64_t total_blocks, float softmax_scale, int mask_mode,
+                               int32_t sliding_window, int dtype, void *out, void *workspace,
+                               size_t workspace_bytes, int32_t *err_count, bkv_stream_t stream);
 int bkv_paged_decode_merge(const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
                            const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs,
                            int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
                            int32_t head_dim, int32_t block_size, int64_t total_blocks,
-                           float softmax_scale, int mask_mode, int dtype, void *out,
-                           void *workspace, size_t workspace_bytes, int32_t *err_count,
+                           float softmax_scale, int mask_mode, int32_t sliding_window, int dtype,
+                           void *out, void *workspace, size_t workspace_bytes, int32_t *err_count,
                            bkv_stream_t stream);
 
 /*

@@ -64,8 +64,8 @@ def load() -> ctypes.CDLL:
         lib.bkv_cache_write.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i32, i32, i32, cint, vp, vp]
         lib.bkv_paged_decode_workspace_size.restype = sz
         lib.bkv_paged_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
-        dec = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i32, i64, f32, cint, cint, vp, vp, sz, vp,
-               vp]
+        dec = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i32, i64, f32, cint, i32, cint, vp, vp, sz,
+               vp, vp]
         for fn in ("bkv_paged_decode", "bkv_paged_decode_partition", "bkv_paged_decode_merge"):
             getattr(lib, fn).restype = cint
             getattr(lib, fn).argtypes = dec
@@ -163,28 +163,30 @@ def bkv_paged_decode_workspace_size(num_reqs, q_len, num_q_heads, num_kv_heads, 
 
 
 def bkv_paged_decode(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
-                     softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None):
+                     softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None, sliding_window=0):
     """GQA paged decode attention into ``out`` (num_reqs, q_len, H_q, D) (see include/bkv.h)."""
     return _decode("bkv_paged_decode", q, k_cache, v_cache, block_table, context_lens, max_context_len, out,
-                   workspace, softmax_scale, mask_mode, err_count, stream)
+                   workspace, softmax_scale, mask_mode, sliding_window, err_count, stream)
 
 
 def bkv_paged_decode_partition(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
-                               softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None):
+                               softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None,
+                               sliding_window=0):
     """Phase 1 of bkv_paged_decode: split-KV partials into ``workspace`` (see include/bkv.h)."""
     return _decode("bkv_paged_decode_partition", q, k_cache, v_cache, block_table, context_lens, max_context_len,
-                   out, workspace, softmax_scale, mask_mode, err_count, stream)
+                   out, workspace, softmax_scale, mask_mode, sliding_window, err_count, stream)
 
 
 def bkv_paged_decode_merge(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
-                           softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None):
+                           softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None,
+                           sliding_window=0):
     """Phase 2 of bkv_paged_decode: merge the workspace partials into ``out`` (see include/bkv.h)."""
     return _decode("bkv_paged_decode_merge", q, k_cache, v_cache, block_table, context_lens, max_context_len, out,
-                   workspace, softmax_scale, mask_mode, err_count, stream)
+                   workspace, softmax_scale, mask_mode, sliding_window, err_count, stream)
 
 
 def _decode(fn, q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace, softmax_scale,
-            mask_mode, err_count, stream):
+            mask_mode, sliding_window, err_count, stream):
     if q.dim() != 4 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
         raise ValueError("q/out must be (num_reqs, q_len, H_q, D); caches (total_blocks, bs, H_kv, D)")
     nr, ql, hq, d = q.shape
@@ -205,7 +207,7 @@ def _decode(fn, q, k_cache, v_cache, block_table, context_lens, max_context_len,
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_table, "block_table", torch.int32, contiguous=False), block_table.stride(0),
         block_table.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), nr, ql, hq, hkv,
-        d, bs, tb, float(softmax_scale), int(mask_mode), dt, _dev(out, "out"), ws_ptr, ws_bytes,
+        d, bs, tb, float(softmax_scale), int(mask_mode), int(sliding_window), dt, _dev(out, "out"), ws_ptr, ws_bytes,
         _opt(err_count, "err_count", torch.int32), _stream(stream)))
     return out
 

@@ -78,8 +78,9 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
     const T *V = static_cast<const T *>(a.v);
 
     float q[QR][DPL];
-    int32_t lastv[QR];
+    int32_t lastv[QR], firstv[QR];
     int32_t jmax = -1;
+    const int32_t jmin = window_lo(a, L);   // no query sees a key before this one
 #pragma unroll
     for (int i = 0; i < QR; ++i) {
         if (i < nrows) {
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
             const int h = g * a.G + (row - t * a.G);
             const int64_t qb = (((int64_t)r * a.q_len + t) * a.H_q + h) * a.D;
             lastv[i] = a.mask_mode == 0 ? L - a.q_len + t : L - 1;
+            firstv[i] = a.window > 0 ? L - a.q_len + t - a.window + 1 : INT32_MIN;
             jmax = max(jmax, lastv[i]);
 #pragma unroll
             for (int e = 0; e < DPL; ++e) {
@@ -96,6 +98,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
             }
         } else {
             lastv[i] = -1;
+            firstv[i] = 0;
 #pragma unroll
             for (int e = 0; e < DPL; ++e) q[i][e] = 0.f;
         }
@@ -110,10 +113,11 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
         for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
     }
 
-    for (int32_t j = start + warp; j < end && j <= jmax; j += NW) {
+    const int32_t j0 = max(start, jmin);
+    for (int32_t j = j0 + warp; j < end && j <= jmax; j += NW) {
         const int32_t lb = j / a.bs;
         const int32_t off = j - lb * a.bs;
-        const bool first = (j == start) || (off == 0);  // count a bad entry once per CTA
+        const bool first = (j == j0) || (off == 0);  // count a bad entry once per CTA
         if (lb >= a.bt_cols) {
             if (first && lane == 0 && a.err) atomicAdd(a.err, 1);
             continue;
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
         }
 #pragma unroll
         for (int i = 0; i < QR; ++i) {
-            if (i < nrows && j <= lastv[i]) {
+            if (i < nrows && j <= lastv[i] && j >= firstv[i]) {
                 const float mn = fmaxf(m[i], s[i]);
                 const float corr = exp2f(m[i] - mn);
                 const float p = exp2f(s[i] - mn);
@@ -429,8 +433,10 @@ static int decode_setup(const void *q, const void *k_cache, const void *v_cache,
                         int64_t bt_stride, int32_t bt_cols, const int32_t *context_lens, int32_t max_context_len,
                         int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                         int32_t block_size, int64_t total_blocks, float softmax_scale, int mask_mode, int dtype,
-                        void *out, void *workspace, size_t workspace_bytes, int32_t *err_count, DecodeCall *c) {
+                        int32_t sliding_window, void *out, void *workspace, size_t workspace_bytes,
+                        int32_t *err_count, DecodeCall *c) {
     if (dtype != BKV_BF16 && dtype != BKV_F32) return BKV_ERR_UNSUPPORTED;
+    if (sliding_window < 0) return BKV_ERR_INVALID_ARG;
     if (head_dim > 256 || head_dim % 2 != 0) return BKV_ERR_UNSUPPORTED;
     if (mask_mode != BKV_MASK_CAUSAL && mask_mode != BKV_MASK_ALL) return BKV_ERR_INVALID_ARG;
     if (bt_cols < 0 || bt_stride < bt_cols || total_blocks < 0) return BKV_ERR_INVALID_ARG;
@@ -460,6 +466,7 @@ static int decode_setup(const void *q, const void *k_cache, const void *v_cache,
     a.total_blocks = total_blocks;
     a.scale_log2 = softmax_scale * kLog2e;
     a.mask_mode = mask_mode;
+    a.window = sliding_window;
     a.dtype = dtype;
     a.chunk = plan.chunk;
     a.n_chunks = plan.n_chunks;
@@ -513,12 +520,12 @@ static int decode_merge(DecodeCall &c, cudaStream_t st) {
     const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table, int64_t bt_stride,      \
         int32_t bt_cols, const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs, int32_t q_len,  \
         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t total_blocks,   \
-        float softmax_scale, int mask_mode, int dtype, void *out, void *workspace, size_t workspace_bytes,       \
-        int32_t *err_count, bkv_stream_t stream
+        float softmax_scale, int mask_mode, int32_t sliding_window, int dtype, void *out, void *workspace,       \
+        size_t workspace_bytes, int32_t *err_count, bkv_stream_t stream
 #define BKV_DECODE_SETUP(c)                                                                                       \
     bkv::decode_setup(q, k_cache, v_cache, block_table, bt_stride, bt_cols, context_lens, max_context_len,       \
                       num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, total_blocks, softmax_scale, \
-                      mask_mode, dtype, out, workspace, workspace_bytes, err_count, &(c))
+                      mask_mode, dtype, sliding_window, out, workspace, workspace_bytes, err_count, &(c))
 
 extern "C" int bkv_paged_decode(BKV_DECODE_PARAMS) {
     bkv::DecodeCall c;

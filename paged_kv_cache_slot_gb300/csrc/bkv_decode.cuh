@@ -21,6 +21,7 @@ struct DecodeArgs {
     int64_t total_blocks;
     float scale_log2;  // softmax_scale * log2(e): scores are kept in base 2
     int mask_mode;
+    int32_t window;    // sliding window W (> 0): query t sees keys j >= L - q_len + t - W + 1; 0: none
     int dtype;         // BKV_BF16 or BKV_F32 (q, caches and out share it)
     int32_t chunk;     // tokens per split-KV partition (multiple of the tile and of bs)
     int32_t n_chunks;  // partitions per request at max_ctx
@@ -41,6 +42,14 @@ struct DecodeArgs {
 // of whichever kernel runs: the generic kernel's (request, KV head,
 // partition) slots or the tensor-core kernel's 2 (sk_grid + num_reqs * H_kv)
 // stream-K slots.
+// First key position any query of a request of cache length L may see (the
+// window of its first query token); 0 without a sliding window.
+__host__ __device__ inline int32_t window_lo(const DecodeArgs &a, int32_t L) {
+    if (a.window <= 0) return 0;
+    const int64_t lo = (int64_t)L - a.q_len - a.window + 1;
+    return lo > 0 ? (int32_t)lo : 0;
+}
+
 struct DecodePlan {
     int32_t chunk;
     int32_t n_chunks;

@@ -325,7 +325,8 @@ __device__ void schedule_loads(const DecodeArgs &a, int32_t *pre, uint8_t *lrem,
         if (r < n) {
             if (lens[i] > a.max_ctx && blockIdx.x == 0 && a.err) atomicAdd(a.err, 1);
             const int32_t L = lens[i] > a.max_ctx ? a.max_ctx : (lens[i] < 0 ? 0 : lens[i]);
-            pre[r] = (L + kTile - 1) / kTile;
+            // a sliding window drops the tiles wholly before its first visible key
+            pre[r] = (L + kTile - 1) / kTile - window_lo(a, L) / kTile;
             lrem[r] = (uint8_t)((L - 1) & (kTile - 1));
         }
     }
@@ -376,8 +377,10 @@ __device__ void scan_prefix(const DecodeArgs &a, int32_t *pre, int32_t *tot) {
         for (int r = threadIdx.x; r <= n; r += blockDim.x) a.sk_pre[r] = pre[r];
 }
 
-// One unit: tiles [lo, hi) of stream s = r * H_kv + g (positions
-// [start, cend) with start = lo * 128, cend = min(hi * 128, L)).
+// One unit: tiles [lo, hi) of stream s = r * H_kv + g, counted from the
+// stream's first tile f (0, or the tile holding the sliding window's first
+// visible key): positions [start, cend) with start = (f + lo) * 128, cend =
+// min((f + hi) * 128, L).
 struct Unit {
     int r, g;
     int64_t s;
@@ -427,9 +430,17 @@ struct StreamK {
         x.r = r;
         x.g = g;
         x.s = (int64_t)r * H + g;
-        x.L = (int32_t)(Tr - 1) * kTile + lrem[r] + 1;   // Tr > 0: the stream has this tile
-        x.start = (int32_t)(lo * kTile);
-        x.cend = (int32_t)(hi * kTile < (int64_t)x.L ? hi * kTile : (int64_t)x.L);
+        int64_t f = 0;
+        if (a.window > 0) {
+            // the tile count no longer gives the length: read it (clamped) again
+            const int32_t Lg = __ldg(a.ctx + r);
+            x.L = Lg > a.max_ctx ? a.max_ctx : Lg;
+            f = window_lo(a, x.L) / kTile;
+        } else {
+            x.L = (int32_t)(Tr - 1) * kTile + lrem[r] + 1;   // Tr > 0: the stream has this tile
+        }
+        x.start = (int32_t)((f + lo) * kTile);
+        x.cend = (int32_t)((f + hi) * kTile < (int64_t)x.L ? (f + hi) * kTile : (int64_t)x.L);
         x.ntiles = (int32_t)(hi - lo);
         t = S + hi;
         return true;
@@ -658,6 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t *ents = ent_buf + (ws & 1) * kWinBlocks;
             const int32_t lb_first = win_first_block(cur);
             const Unit &x = cur.u;
+            const int32_t wlo = window_lo(a, x.L);   // segments ending at or before it are not needed
             if (cur.t0 == 0 && !is_v) {
                 const int qb = us & 1;
                 if (!mbar_wait_warp(bar_qempty(qb), ((us >> 1) & 1) ^ 1, abort_flag)) break;
@@ -680,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int64_t row0 = 0;
                 if (lane < nseg) {
                     const int32_t p0 = ts + lane * seg_rows;
-                    if (p0 < x.cend) {
+                    if (p0 < x.cend && p0 + seg_rows > wlo) {
                         const int32_t lb = p0 / a.bs;
                         const int64_t e = ents[lb - lb_first];
                         if (e == INT32_MIN || e >= a.total_blocks) {
@@ -831,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sk.init(a, pre, lrem);
         Unit x;
         while (ok && sk.next(a, x)) {
-            int32_t lastv[NQ];
+            int32_t lastv[NQ], firstv[NQ];
 #pragma unroll
             for (int n = 0; n < NQ; ++n) {
                 o[n] = 0.f;
@@ -839,6 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mrun[n] = -INFINITY;
                 const int t = n / G;
                 lastv[n] = (n < nq) ? (a.mask_mode == 0 ? x.L - a.q_len + t : x.L - 1) : -1;
+                firstv[n] = a.window > 0 ? x.L - a.q_len + t - a.window + 1 : INT32_MIN;
             }
             for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
                 if ((int)(j & 1) != wg) continue;
@@ -857,7 +870,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool loaded = (mask_words[j & 7] >> (row >> seg_shift)) & 1u;
                 const bool inrange = loaded && pos < x.cend;
 #pragma unroll
-                for (int n = 0; n < NQ; ++n) sv[n] = (inrange && pos <= lastv[n]) ? sv[n] * a.scale_log2 : -INFINITY;
+                for (int n = 0; n < NQ; ++n)
+                    sv[n] = (inrange && pos <= lastv[n] && pos >= firstv[n]) ? sv[n] * a.scale_log2 : -INFINITY;
                 // tile max per query row across the warpgroup's 128 threads
                 const float wmax = warp_reduce_rows<true, NQ>(sv, lane);
                 float *rm = red_max + (wg * 2 + (int)par) * (kN * 4);

@@ -58,6 +58,6 @@ extern "C" int bkv_paged_decode_noalloc(const void *q, const void *k_cache, cons
     if (rc != BKV_OK) return rc;
     return bkv_paged_decode(q, k_cache, v_cache, block_table, bt_stride, bt_cols, context_lens, max_context_len,
                             num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, total_blocks,
-                            softmax_scale, mask_mode, dtype, out, scratch, BKV_NOALLOC_SCRATCH_BYTES, err_count,
+                            softmax_scale, mask_mode, 0, dtype, out, scratch, BKV_NOALLOC_SCRATCH_BYTES, err_count,
                             stream);
 }

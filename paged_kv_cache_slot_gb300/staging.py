@@ -105,11 +105,12 @@ class DeviceWorkload:
         bkv.bkv_cache_write(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
                             num_tokens=w.num_tokens, err_count=self.err_count, stream=stream)
 
-    def decode(self, stream=None, out=None, table=None, mask_mode=bkv.BKV_MASK_CAUSAL):
+    def decode(self, stream=None, out=None, table=None, mask_mode=bkv.BKV_MASK_CAUSAL, sliding_window=0):
         out = self.out if out is None else out
         table = self.kernel_table if table is None else table
         bkv.bkv_paged_decode(self.q, self.k_cache, self.v_cache, table, self.context_lens, self.max_context_len,
-                             out, self.workspace, mask_mode=mask_mode, err_count=self.err_count, stream=stream)
+                             out, self.workspace, mask_mode=mask_mode, err_count=self.err_count, stream=stream,
+                             sliding_window=sliding_window)
         return out
 
     def decode_partition(self, stream=None):

@@ -85,8 +85,8 @@ def test_cache_write_rejects_bad_arguments(lib):
 def test_paged_decode_rejects_bad_arguments(lib):
     f = lib.bkv_paged_decode
     base = dict(q=NULL, k=NULL, v=NULL, bt=NULL, bt_stride=4, bt_cols=4, ctx=NULL, max_ctx=16, num_reqs=2, q_len=1,
-                hq=32, hkv=8, d=128, bs=16, tb=8, scale=0.0, mask=0, dtype=0, out=NULL, ws=NULL, wsb=0, err=NULL,
-                stream=NULL)
+                hq=32, hkv=8, d=128, bs=16, tb=8, scale=0.0, mask=0, window=0, dtype=0, out=NULL, ws=NULL, wsb=0,
+                err=NULL, stream=NULL)
 
     def call(**kw):
         a = dict(base, **kw)
@@ -95,6 +95,7 @@ def test_paged_decode_rejects_bad_arguments(lib):
     assert call(dtype=5) == bkv.BKV_ERR_UNSUPPORTED
     assert call(d=512) == bkv.BKV_ERR_UNSUPPORTED
     assert call(mask=2) == bkv.BKV_ERR_INVALID_ARG
+    assert call(window=-1) == bkv.BKV_ERR_INVALID_ARG
     assert call(bt_stride=2) == bkv.BKV_ERR_INVALID_ARG
     assert call(hq=30) == bkv.BKV_ERR_INVALID_ARG          # 30 % 8 != 0
     assert call(num_reqs=0) == bkv.BKV_ERR_INVALID_ARG

@@ -28,22 +28,23 @@ def _f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def _oracle_rows(w, rows, mask_mode=0, table=None):
+def _oracle_rows(w, rows, mask_mode=0, table=None, window=0):
     kc, vc, ktable = fill_oracle_cache(w, rows=rows)
     table = ktable if table is None else table
     q = w.q()
     out = {}
     for r in rows:
-        out[r], _ = oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens, mask_mode=mask_mode)
+        out[r], _ = oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens, mask_mode=mask_mode,
+                                                sliding_window=window)
     return out
 
 
-def _check(dw, rows, mask_mode=0, label=""):
+def _check(dw, rows, mask_mode=0, label="", window=0):
     w = dw.w
     dw.workspace.fill_(0xFF)   # NaN everywhere: reading a partial nobody wrote poisons the output
-    got = _f64(dw.decode(mask_mode=mask_mode))
+    got = _f64(dw.decode(mask_mode=mask_mode, sliding_window=window))
     torch.cuda.synchronize()
-    want = _oracle_rows(w, rows, mask_mode)
+    want = _oracle_rows(w, rows, mask_mode, window=window)
     worst = 0.0
     for r in rows:
         assert np.isfinite(got[r]).all(), f"{label} row {r}: non-finite output"
@@ -251,3 +252,80 @@ def test_partition_then_merge_equals_one_call_bitwise(name):
     torch.cuda.synchronize()
     assert torch.equal(one.view(torch.int16), two.view(torch.int16))
     assert int(dw.err_count.item()) == 0
+
+
+# ---------------------------------------------------------------------------
+# sliding window: key j visible for query t iff j >= L - q_len + t - W + 1
+# ---------------------------------------------------------------------------
+SWA_CASES = [(c, W, m) for c in range(len(SMALL)) for (W, m) in ((1, 0), (77, 0), (77, 1), (1000, 0))]
+
+
+@pytest.mark.parametrize("ci,window,mask_mode", SWA_CASES,
+                         ids=lambda v: str(v))
+def test_sliding_window_small_shapes(ci, window, mask_mode):
+    q_len, H_q, H_kv, D, bs, prior, dtype = SMALL[ci]
+    w = _custom(q_len, H_q, H_kv, D, bs, list(prior) + [0], dtype, null_rows=(len(prior),))
+    dw = DeviceWorkload(w)
+    dw.write_step()
+    got, _ = _check(dw, range(w.num_rows), mask_mode, f"{SMALL[ci]} W={window}", window=window)
+    assert (got[w.num_rows - 1] == 0).all()
+
+
+def test_sliding_window_long_context_sampled_rows():
+    w = wl.make("long_context", sharp=True)
+    dw = DeviceWorkload(w)
+    dw.step()
+    lens = w.context_lens
+    rows = sorted({int(np.argmax(lens)), int(np.argmin(lens)), 0, 5})
+    _check(dw, rows, 0, "long_context W=4096", window=4096)
+    assert int(dw.err_count.item()) == 0
+
+
+def test_sliding_window_hybrid_sampled_rows():
+    w = wl.make("hybrid_spec", sharp=True)
+    dw = DeviceWorkload(w)
+    dw.step()
+    real = w.context_lens[: w.num_real]
+    rows = sorted({int(np.argmax(real)), int(np.argmin(real)), 1, 17, 100, 255, 256, 319})
+    got, _ = _check(dw, rows, 0, "hybrid W=512", window=512)
+    assert (got[w.num_real:] == 0).all()
+    assert int(dw.err_count.item()) == 0
+
+
+def test_sliding_window_never_reads_blocks_before_it_bitwise():
+    w = _custom(2, 32, 8, 128, 16, (900, 40, 1700, 333), "bf16", sharp=True)
+    dw = _filled(w)
+    window = 300
+    base = dw.decode(sliding_window=window).clone()
+    torch.cuda.synchronize()
+    bs = w.kernel_block_size
+    t_null, t_junk = dw.kernel_table.clone(), dw.kernel_table.clone()
+    dropped = []
+    for r in range(w.num_rows):
+        L = int(w.context_lens[r])
+        lo = max(0, L - w.q_len - window + 1)
+        for lb in range(lo // bs):
+            dropped.append(int(dw.kernel_table[r, lb]))
+            t_null[r, lb] = -1
+            t_junk[r, lb] = 10**7
+    assert dropped
+    dw.err_count.zero_()
+    a = dw.decode(out=torch.empty_like(base), table=t_null, sliding_window=window)
+    b = dw.decode(out=torch.empty_like(base), table=t_junk, sliding_window=window)
+    ids = torch.tensor(dropped, device="cuda", dtype=torch.int64)
+    dw.k_cache[ids] = float("nan")
+    dw.v_cache[ids] = float("nan")
+    c = dw.decode(out=torch.empty_like(base), sliding_window=window)
+    torch.cuda.synchronize()
+    for x in (a, b, c):
+        assert torch.equal(x.view(torch.int16), base.view(torch.int16))
+    assert int(dw.err_count.item()) == 0
+
+
+def test_sliding_window_covering_every_key_is_bitwise_full_attention():
+    w = _custom(3, 32, 8, 128, 64, (1000, 64, 3000, 5), "bf16", sharp=True)
+    dw = _filled(w)
+    base = dw.decode().clone()
+    wide = dw.decode(out=torch.empty_like(base), sliding_window=int(w.context_lens.max()) + w.q_len)
+    torch.cuda.synchronize()
+    assert torch.equal(wide.view(torch.int16), base.view(torch.int16))
