@@ -19,6 +19,10 @@ roofline.achieved = the same bytes / device time of the decode partition
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bkv|reference]
+                  [--workload NAME] [--sliding-window W]
+--workload / --sliding-window time another seeded workload (long_context,
+hybrid_spec, ...) or a sliding-window decode on the same harness; the
+default is the headline configuration above.
 Under torchrun every rank runs an independent replica (the path has no
 exchange step); rank 0 prints one JSON line.
 """
@@ -61,6 +65,21 @@ def _peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def _describe(w, window):
+    """The workload's name and sizes, as the JSON line's config.workload."""
+    if w.name == WORKLOAD and window == 0:
+        return ("llama3_decode: 32 req, ctx U[512,4096] + 1 new token, H_q 32, H_kv 8, D 128, bs 64, bf16, "
+                "fp32 accumulate")
+    lens = w.context_lens[: w.num_real]
+    bs = (f"bs {w.block_size} -> kernel bs {w.kernel_block_size}" if w.block_size != w.kernel_block_size
+          else f"bs {w.block_size}")
+    d = (f"{w.name}: {w.num_real} req" + (f" + {w.num_rows - w.num_real} NULL rows" if w.num_rows > w.num_real
+                                          else "")
+         + f", ctx {int(lens.min())}..{int(lens.max())} (mean {lens.mean():.0f}), q_len {w.q_len}, H_q "
+         f"{w.num_q_heads}, H_kv {w.num_kv_heads}, D {w.head_dim}, {bs}, {w.dtype}, fp32 accumulate")
+    return d + (f", sliding window {window}" if window else "")
 
 
 def _decode_source_sha():
@@ -145,7 +164,7 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _cpu_baseline(budget_s: float, workload: str = WORKLOAD):
+def _cpu_baseline(budget_s: float, workload: str = WORKLOAD, window: int = 0):
     """The oracle, as it stands, on a bounded sample of the workload: every
     request decoded (single thread, fp64), each repeated ``reps`` times so that
     the timed CPU work comes to about ``budget_s``; ``reps`` is calibrated on
@@ -158,21 +177,23 @@ def _cpu_baseline(budget_s: float, workload: str = WORKLOAD):
     q = w.q()
     order = [int(r) for r in np.argsort(w.context_lens)[::-1]]      # fixed order, longest first
     per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
-    total_ctx = int(w.context_lens.astype(np.int64).sum())
+    Ls = w.context_lens.astype(np.int64)
+    eff = Ls - (np.maximum(0, Ls - w.q_len - window + 1) if window > 0 else 0)   # rows each request reads
+    total_ctx = int(eff.sum())
     done_bytes, done_t, reps = 0, 0.0, None
     for r in order:
         kc, vc, table = fill_oracle_cache(w, rows=[r])
         if reps is None:
             t0 = time.perf_counter()
-            oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens)
+            oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens, sliding_window=window)
             t_row = time.perf_counter() - t0
-            pass_est = t_row * total_ctx / max(int(w.context_lens[r]), 1)
+            pass_est = t_row * total_ctx / max(int(eff[r]), 1)
             reps = max(1, math.ceil(budget_s / max(pass_est, 1e-6)))
         t0 = time.perf_counter()
         for _ in range(reps):
-            oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens)
+            oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens, sliding_window=window)
         done_t += time.perf_counter() - t0
-        done_bytes += reps * int(w.context_lens[r]) * per_tok
+        done_bytes += reps * int(eff[r]) * per_tok
         del kc, vc
     return {"value": done_bytes / done_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"all {w.num_rows} requests of {workload} x {reps} repeats decoded by the fp64 C oracle "
@@ -263,8 +284,9 @@ def run_bkv(args):
         dist.barrier()
     bkv.load()
 
-    w = wl.make(WORKLOAD)
-    dw = DeviceWorkload(w, device=f"cuda:{local}")
+    w = wl.make(args.workload)
+    dw = DeviceWorkload(w, device=f"cuda:{local}", sliding_window=args.sliding_window)
+    headline = args.workload == WORKLOAD and args.sliding_window == 0
     stream = torch.cuda.Stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=f"cuda:{local}")
@@ -346,7 +368,7 @@ def run_bkv(args):
 
     # secondary half of the metric: slot mapping + cache write on the ragged mixed step
     secondary = None
-    if rank == 0 and not args.no_secondary:
+    if rank == 0 and not args.no_secondary and headline:
         rw = wl.make("ragged_step")
         rdw = DeviceWorkload(rw, device=f"cuda:{local}", fill_prior=False)
 
@@ -382,8 +404,7 @@ def run_bkv(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "llama3_decode: 32 req, ctx U[512,4096] + 1 new token, H_q 32, H_kv 8, D 128, "
-                               "bs 64, bf16, fp32 accumulate",
+        "config": {"workload": _describe(w, args.sliding_window),
                    "kv_bytes_per_step": kv_bytes, "l2": "flushed before every timed step (write 2x L2, read it back)",
                    "parallelism": f"replicas x{world}", "step": "expand + slot map + write + decode + merge",
                    "cuda_graph": bool(graphs)},
@@ -391,7 +412,7 @@ def run_bkv(args):
         # step (5), per step, plus the eager reference pass (5 per step) when graphs are used
         "gpu_launches": args.steps * (5 + 2 + 1 + 5) + (args.steps * 5 if graphs else 0),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _profiled_traffic(),
+                     "frac": achieved / peak, "traffic": _profiled_traffic() if headline else None,
                      "kernel": "decode partition kernel (bkv_paged_decode_partition, CUDA events around it)",
                      "decode_call_GBps": kv_bytes / (dms / 1e3) / 1e9,
                      "peak_kind": f"{peak_kind} copy bandwidth"},
@@ -406,7 +427,7 @@ def run_bkv(args):
     if secondary:
         line["secondary"] = secondary
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = _cpu_baseline(args.cpu_budget)
+        line["cpu_baseline"] = _cpu_baseline(args.cpu_budget, args.workload, args.sliding_window)
     print(json.dumps(line), flush=True)
 
 
@@ -420,6 +441,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA graphs")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="seeded workload to time (default: the Llama-3-8B-shaped decode batch)")
+    ap.add_argument("--sliding-window", type=int, default=0, help="decode with this sliding window (0: none)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -29,8 +29,10 @@ def _t(a: np.ndarray, device, dtype=None):
 
 
 class DeviceWorkload:
-    def __init__(self, w: Workload, device="cuda", background: str = "nan", fill_prior: bool = True):
+    def __init__(self, w: Workload, device="cuda", background: str = "nan", fill_prior: bool = True,
+                 sliding_window: int = 0):
         self.w = w
+        self.window = int(sliding_window)   # decode's default sliding window (0: full attention)
         self.device = torch.device(device)
         dev = self.device
         self.tdtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -105,8 +107,9 @@ class DeviceWorkload:
         bkv.bkv_cache_write(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
                             num_tokens=w.num_tokens, err_count=self.err_count, stream=stream)
 
-    def decode(self, stream=None, out=None, table=None, mask_mode=bkv.BKV_MASK_CAUSAL, sliding_window=0):
+    def decode(self, stream=None, out=None, table=None, mask_mode=bkv.BKV_MASK_CAUSAL, sliding_window=None):
         out = self.out if out is None else out
+        sliding_window = self.window if sliding_window is None else sliding_window
         table = self.kernel_table if table is None else table
         bkv.bkv_paged_decode(self.q, self.k_cache, self.v_cache, table, self.context_lens, self.max_context_len,
                              out, self.workspace, mask_mode=mask_mode, err_count=self.err_count, stream=stream,
@@ -117,7 +120,7 @@ class DeviceWorkload:
         """Phase 1 of the decode alone (the partition kernel), for timing."""
         bkv.bkv_paged_decode_partition(self.q, self.k_cache, self.v_cache, self.kernel_table, self.context_lens,
                                        self.max_context_len, self.out, self.workspace, err_count=self.err_count,
-                                       stream=stream)
+                                       stream=stream, sliding_window=self.window)
 
     def step(self, stream=None):
         """One pass of the whole path: a2 -> a1 -> a3 -> a4 + a5."""
@@ -128,9 +131,13 @@ class DeviceWorkload:
 
     # -- byte accounting (algorithmic, token granularity) ---------------------
     def decode_kv_bytes(self) -> int:
-        """K and V bytes the decode must read: cache_len rows per request and KV head."""
+        """K and V bytes the decode must read: cache_len rows per request and KV head (with a
+        sliding window W, only the rows from the first query's window start, L - q_len - W + 1)."""
         w = self.w
-        return int(w.context_lens.astype(np.int64).sum()) * 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+        L = w.context_lens.astype(np.int64)
+        if self.window > 0:
+            L = L - np.maximum(0, L - w.q_len - self.window + 1)
+        return int(L.sum()) * 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
 
     def write_bytes(self) -> int:
         """Cache-write traffic: new K/V rows read + written, plus the slot ids."""
