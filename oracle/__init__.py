@@ -17,6 +17,10 @@ Functions and the passages they follow (page titles and sections):
   Batching with Block KV", Cache Masking (mask_cache, mask_active).
 * :func:`decode_bucket` -- "Decode Context-Length Bucketing", Design /
   Per-step bucket selection (used to report bytes only).
+* :func:`compute_slot_mapping_cp`, :func:`paged_decode_cp`,
+  :func:`merge_attn_states` -- "ブロック表" 設計動機 (DCP / PCP interleave:
+  a rank writes real slots only for the tokens it owns); the ownership,
+  local-position and merge readings are R14 of the C source.
 
 Every function is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_*.py`` against worked values printed on the pages, brute
@@ -73,6 +77,14 @@ def _load():
             lib.orc_paged_decode.argtypes = dec
             lib.orc_paged_decode_request.restype = i64
             lib.orc_paged_decode_request.argtypes = [i32] + dec
+            lib.orc_compute_slot_mapping_cp.restype = i64
+            lib.orc_compute_slot_mapping_cp.argtypes = [vp, i32, i64, i32, vp, vp, i64, i64, i32, i32, i32, i32, vp]
+            lib.orc_paged_decode_cp_request.restype = i64
+            lib.orc_paged_decode_cp_request.argtypes = [i32, vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32,
+                                                        i32, i64, dbl, ctypes.c_int, i32, i32, i32, i32,
+                                                        ctypes.c_int, vp, vp]
+            lib.orc_merge_attn_states.restype = ctypes.c_int
+            lib.orc_merge_attn_states.argtypes = [vp, vp, i32, i64, i32, vp, vp]
             lib.orc_decode_bucket.restype = i64
             lib.orc_decode_bucket.argtypes = [vp, i64, i64, vp, i64, i64]
             _lib = lib
@@ -109,6 +121,25 @@ def compute_slot_mapping(block_table, req_indices, positions, block_size, num_to
     out = np.empty(max(mx, 1), np.int64)
     err = _load().orc_compute_slot_mapping(_ptr(bt), bt.shape[0], bt.shape[1], bt.shape[1], _ptr(req), _ptr(pos),
                                            n, mx, int(block_size), _ptr(out))
+    if err < 0:
+        raise ValueError("invalid slot-mapping arguments")
+    return out[:mx], int(err)
+
+
+def compute_slot_mapping_cp(block_table, req_indices, positions, block_size, cp_world, cp_rank, cp_interleave,
+                            num_tokens=None, max_num_tokens=None):
+    """Slot ids of rank ``cp_rank`` under decode context parallelism (reading R14) and the bad-token count."""
+    bt = _c(block_table, np.int32)
+    if bt.ndim != 2:
+        raise ValueError("block_table must be 2-D")
+    req = _c(req_indices, np.int32)
+    pos = _c(positions, np.int64)
+    n = len(pos) if num_tokens is None else int(num_tokens)
+    mx = n if max_num_tokens is None else int(max_num_tokens)
+    out = np.empty(max(mx, 1), np.int64)
+    err = _load().orc_compute_slot_mapping_cp(_ptr(bt), bt.shape[0], bt.shape[1], bt.shape[1], _ptr(req),
+                                              _ptr(pos), n, mx, int(block_size), int(cp_world), int(cp_rank),
+                                              int(cp_interleave), _ptr(out))
     if err < 0:
         raise ValueError("invalid slot-mapping arguments")
     return out[:mx], int(err)
@@ -203,6 +234,44 @@ def paged_decode_request(r, q, k_cache, v_cache, block_table, context_lens, scal
         raise ValueError("invalid paged_decode arguments")
     del keep
     return out[r], int(err)
+
+
+def paged_decode_cp(q, k_cache, v_cache, block_table, context_lens, cp_world=1, cp_rank=0, cp_interleave=1,
+                    scale=None, mask_mode=0, sliding_window=0, rows=None):
+    """Rank ``cp_rank``'s decode over its own keys (reading R14; context_lens are global lengths).
+
+    Returns fp64 out (num_reqs, q_len, H_q, D), lse (num_reqs, q_len, H_q) (natural log of the sum of
+    exp of the scaled scores over the visible keys, -inf where none) and the bad-entry count; ``rows``
+    limits the work to those requests (the others stay 0 / -inf)."""
+    args, keep, shape = _decode_args(q, k_cache, v_cache, block_table, context_lens, scale, mask_mode,
+                                     sliding_window)
+    out = np.zeros(shape, np.float64)
+    lse = np.full(shape[:3], -np.inf, np.float64)
+    err = 0
+    lib = _load()
+    base, tail = args[:-2], args[-1]   # everything up to the mask / window, then dtype
+    for r in (range(shape[0]) if rows is None else rows):
+        e = lib.orc_paged_decode_cp_request(int(r), *base, int(sliding_window), int(cp_world), int(cp_rank),
+                                            int(cp_interleave), tail, _ptr(out), _ptr(lse))
+        if e < 0:
+            raise ValueError("invalid paged_decode_cp arguments")
+        err += e
+    del keep
+    return out, lse, int(err)
+
+
+def merge_attn_states(outs, lses):
+    """Merge of partial attention results (R14): outs (parts, rows, D), lses (parts, rows) -> (out, lse)."""
+    o = np.ascontiguousarray(outs, np.float64)
+    l = np.ascontiguousarray(lses, np.float64)
+    parts, rows, d = o.shape
+    if l.shape != (parts, rows):
+        raise ValueError("lses must be (parts, rows)")
+    out = np.zeros((rows, d), np.float64)
+    lse = np.zeros(rows, np.float64)
+    if _load().orc_merge_attn_states(_ptr(o), _ptr(l), parts, rows, d, _ptr(out), _ptr(lse)) != 0:
+        raise ValueError("invalid merge arguments")
+    return out, lse
 
 
 def decode_bucket(num_computed, num_speculative_tokens, buckets, max_model_len):

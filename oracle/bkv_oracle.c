@@ -53,6 +53,20 @@
  *       (the upper bound is R7's); blocks wholly before every query's window
  *       are never read, so they may be null or hold anything.  W <= 0: no
  *       window.
+ *   R14 decode context parallelism ([P2 設計動機]: under DCP the slot
+ *       kernel writes real slots only for the tokens its rank owns and
+ *       PAD_ID for the rest; the ownership formula is not printed): with
+ *       world size Wc, rank k and interleave size I, position p belongs to
+ *       rank (p / I) mod Wc (runs of I consecutive positions dealt round
+ *       robin); its owner stores it at local position
+ *       p_l = (p / (I Wc)) I + p mod I, and the owner's block table indexes
+ *       local positions, so slot = table[r][p_l / bs] * bs + p_l mod bs.  A
+ *       rank's decode attends over its own keys with the masks in global
+ *       positions (local key j stands for (j / I) I Wc + k I + j mod I) and
+ *       reports its normalised output and lse = log sum_j exp(s_j) over its
+ *       visible keys (-inf if none); merging the ranks' (out, lse) by
+ *       out = sum_k exp(lse_k - LSE) out_k, LSE = log sum_k exp(lse_k), is
+ *       the attention over all keys.
  */
 #include <math.h>
 #include <stdint.h>
@@ -131,6 +145,57 @@ int64_t orc_compute_slot_mapping(const int32_t *block_table, int32_t num_reqs,
         if (block_number <= 0)
             continue; /* null block 0 or sentinel -1 (R2) */
         slot_mapping[i] = block_number * block_size + offset;
+    }
+    return errors;
+}
+
+/*
+ * O1 under decode context parallelism (R14): the token's position p is
+ * real on rank cp_rank only if (p / cp_interleave) mod cp_world == cp_rank;
+ * there the slot follows the core formula at the local position
+ * p_l = (p / (cp_interleave * cp_world)) * cp_interleave + p mod cp_interleave.
+ * A token another rank owns gets -1 without counting an error.
+ * Returns the number of bad indices (as O1), or -1 for invalid arguments.
+ */
+int64_t orc_compute_slot_mapping_cp(const int32_t *block_table, int32_t num_reqs,
+                                    int64_t bt_stride, int32_t bt_cols,
+                                    const int32_t *req_indices,
+                                    const int64_t *positions, int64_t num_tokens,
+                                    int64_t max_num_tokens, int32_t block_size,
+                                    int32_t cp_world, int32_t cp_rank,
+                                    int32_t cp_interleave, int64_t *slot_mapping)
+{
+    if (block_size <= 0 || num_tokens < 0 || max_num_tokens < num_tokens ||
+        num_reqs < 0 || bt_cols < 0 || bt_stride < bt_cols || cp_world <= 0 ||
+        cp_rank < 0 || cp_rank >= cp_world || cp_interleave <= 0)
+        return -1;
+    int64_t errors = 0;
+    for (int64_t i = 0; i < max_num_tokens; ++i) {
+        slot_mapping[i] = -1;
+        if (i >= num_tokens)
+            continue;
+        int32_t r = req_indices[i];
+        int64_t p = positions[i];
+        if (r < 0)
+            continue;
+        if (r >= num_reqs || p < 0) {
+            errors += 1;
+            continue;
+        }
+        int64_t owner = (p / cp_interleave) % cp_world;
+        if (owner != cp_rank)
+            continue; /* another rank's token: PAD */
+        int64_t local = (p / ((int64_t)cp_interleave * cp_world)) * cp_interleave +
+                        p % cp_interleave;
+        int64_t logical_block = local / block_size;
+        if (logical_block >= bt_cols) {
+            errors += 1;
+            continue;
+        }
+        int64_t block_number = block_table[(int64_t)r * bt_stride + logical_block];
+        if (block_number <= 0)
+            continue;
+        slot_mapping[i] = block_number * block_size + local % block_size;
     }
     return errors;
 }
@@ -261,45 +326,66 @@ int64_t orc_cache_write(const void *k_new, const void *v_new,
  * may see (positions past the table width or ids past the cache), or -1 for
  * invalid arguments.
  */
-int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
-                                 const void *v_cache, const int32_t *block_table,
-                                 int64_t bt_stride, int32_t bt_cols,
-                                 const int32_t *context_lens, int32_t num_reqs,
-                                 int32_t q_len, int32_t num_q_heads,
-                                 int32_t num_kv_heads, int32_t head_dim,
-                                 int32_t block_size, int64_t total_blocks,
-                                 double scale, int mask_mode, int32_t sliding_window,
-                                 int dtype, double *out)
+/*
+ * The general form: the keys are this rank's (R14; cp_world 1 is the plain
+ * cache) and, when lse is not NULL, lse[(r * q_len + t) * num_q_heads + h]
+ * receives log sum_j exp(s_j) over the visible keys (-inf if none).  Key
+ * positions, masks and windows are global; j below is a local key index and
+ * g its global position.
+ */
+int64_t orc_paged_decode_cp_request(int32_t r, const void *q, const void *k_cache,
+                                    const void *v_cache, const int32_t *block_table,
+                                    int64_t bt_stride, int32_t bt_cols,
+                                    const int32_t *context_lens, int32_t num_reqs,
+                                    int32_t q_len, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int64_t total_blocks,
+                                    double scale, int mask_mode, int32_t sliding_window,
+                                    int32_t cp_world, int32_t cp_rank, int32_t cp_interleave,
+                                    int dtype, double *out, double *lse)
 {
     if (orc_elem_bytes(dtype) == 0 || r < 0 || r >= num_reqs || q_len <= 0 ||
         num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_q_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 ||
-        bt_cols < 0 || bt_stride < bt_cols || (mask_mode != 0 && mask_mode != 1))
+        bt_cols < 0 || bt_stride < bt_cols || (mask_mode != 0 && mask_mode != 1) ||
+        cp_world <= 0 || cp_rank < 0 || cp_rank >= cp_world || cp_interleave <= 0)
         return -1;
     const int64_t D = head_dim;
     const int64_t G = num_q_heads / num_kv_heads;
-    const int64_t L = context_lens[r] > 0 ? context_lens[r] : 0;
+    const int64_t L = context_lens[r] > 0 ? context_lens[r] : 0;   /* global cache length */
     const int64_t W = sliding_window > 0 ? sliding_window : 0;
+    const int64_t I = cp_interleave, Wc = cp_world;
+    /* R14: this rank's keys are the global positions g < L it owns */
+    int64_t Lk = 0;
+    for (int64_t g = 0; g < L; ++g)
+        if ((g / I) % Wc == cp_rank)
+            Lk += 1;
     /* R13: no query sees a key before lo (the window of query 0) */
     int64_t lo = 0;
     if (W > 0 && L - q_len - W + 1 > 0)
         lo = L - q_len - W + 1;
     int64_t errors = 0;
 
-    /* Which key positions may be read at all: lo <= j < L with a real block
-     * (a bad entry counts once per block, at its first position read). */
-    unsigned char *readable = (unsigned char *)malloc((size_t)(L > 0 ? L : 1));
-    double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
-    if (!readable || !s) {
+    /* Which local keys may be read at all: global position >= lo, a real
+     * block (a bad entry counts once per block, at its first key read). */
+    unsigned char *readable = (unsigned char *)malloc((size_t)(Lk > 0 ? Lk : 1));
+    int64_t *gpos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(Lk > 0 ? Lk : 1));
+    double *s = (double *)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
+    if (!readable || !gpos || !s) {
         free(readable);
+        free(gpos);
         free(s);
         return -1;
     }
-    for (int64_t j = 0; j < L; ++j) {
+    int64_t first_read = -1;
+    for (int64_t j = 0; j < Lk; ++j) {
+        gpos[j] = (j / I) * I * Wc + cp_rank * I + j % I;
         readable[j] = 0;
-        if (j < lo)
+        if (gpos[j] < lo)
             continue;
-        const int first = (j == lo) || (j % block_size == 0);
+        if (first_read < 0)
+            first_read = j;
+        const int first = (j == first_read) || (j % block_size == 0);
         int64_t lb = j / block_size;
         if (lb >= bt_cols) {
             if (first)
@@ -326,11 +412,13 @@ int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
             double *o = out + qoff;
             for (int64_t d = 0; d < D; ++d)
                 o[d] = 0.0;
+            if (lse)
+                lse[((int64_t)r * q_len + t) * num_q_heads + h] = -INFINITY;
 
             double m = -INFINITY;
             int any = 0;
-            for (int64_t j = 0; j < L && j <= last_visible; ++j) {
-                if (!readable[j] || j < first_visible)
+            for (int64_t j = 0; j < Lk; ++j) {
+                if (!readable[j] || gpos[j] > last_visible || gpos[j] < first_visible)
                     continue;
                 int64_t b = block_table[(int64_t)r * bt_stride + j / block_size];
                 int64_t krow = ((b * block_size + j % block_size) * num_kv_heads + g) * D;
@@ -346,8 +434,8 @@ int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
                 continue; /* R9: nothing visible -> 0 */
 
             double denom = 0.0;
-            for (int64_t j = 0; j < L && j <= last_visible; ++j) {
-                if (!readable[j] || j < first_visible)
+            for (int64_t j = 0; j < Lk; ++j) {
+                if (!readable[j] || gpos[j] > last_visible || gpos[j] < first_visible)
                     continue;
                 int64_t b = block_table[(int64_t)r * bt_stride + j / block_size];
                 int64_t vrow = ((b * block_size + j % block_size) * num_kv_heads + g) * D;
@@ -358,11 +446,71 @@ int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
             }
             for (int64_t d = 0; d < D; ++d)
                 o[d] /= denom;
+            if (lse)
+                lse[((int64_t)r * q_len + t) * num_q_heads + h] = m + log(denom);
         }
     }
     free(readable);
+    free(gpos);
     free(s);
     return errors;
+}
+
+/* One request of the plain (single-rank) decode. */
+int64_t orc_paged_decode_request(int32_t r, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_table,
+                                 int64_t bt_stride, int32_t bt_cols,
+                                 const int32_t *context_lens, int32_t num_reqs,
+                                 int32_t q_len, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int64_t total_blocks,
+                                 double scale, int mask_mode, int32_t sliding_window,
+                                 int dtype, double *out)
+{
+    return orc_paged_decode_cp_request(r, q, k_cache, v_cache, block_table, bt_stride,
+                                       bt_cols, context_lens, num_reqs, q_len,
+                                       num_q_heads, num_kv_heads, head_dim, block_size,
+                                       total_blocks, scale, mask_mode, sliding_window,
+                                       1, 0, 1, dtype, out, NULL);
+}
+
+/*
+ * Merge of attention states (R14): rows of `parts` partial results, each a
+ * normalised output (fp64 [parts][rows][head_dim]) and its lse
+ * ([parts][rows]); out = sum_k exp(lse_k - M) out_k / sum_k exp(lse_k - M),
+ * lse_out = M + log sum_k exp(lse_k - M), M = max_k lse_k; a row whose parts
+ * are all -inf gives 0 and -inf.
+ */
+int orc_merge_attn_states(const double *outs, const double *lses, int32_t parts,
+                          int64_t rows, int32_t head_dim, double *out, double *lse_out)
+{
+    if (parts <= 0 || rows < 0 || head_dim <= 0)
+        return 1;
+    for (int64_t i = 0; i < rows; ++i) {
+        double M = -INFINITY;
+        for (int32_t k = 0; k < parts; ++k)
+            if (lses[(int64_t)k * rows + i] > M)
+                M = lses[(int64_t)k * rows + i];
+        double *o = out + i * head_dim;
+        for (int32_t d = 0; d < head_dim; ++d)
+            o[d] = 0.0;
+        if (M == -INFINITY) {
+            lse_out[i] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int32_t k = 0; k < parts; ++k) {
+            double w = exp(lses[(int64_t)k * rows + i] - M);
+            sum += w;
+            const double *ok = outs + ((int64_t)k * rows + i) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d)
+                o[d] += w * ok[d];
+        }
+        for (int32_t d = 0; d < head_dim; ++d)
+            o[d] /= sum;
+        lse_out[i] = M + log(sum);
+    }
+    return 0;
 }
 
 /* The whole batch: every request in turn. */

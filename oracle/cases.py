@@ -3,7 +3,7 @@ own slot mapping and cache write.  TEST INFRASTRUCTURE, like the rest of
 this package; it calls only the oracle and the seeded input generators."""
 import numpy as np
 
-from . import compute_slot_mapping, cache_write, map_to_kernel_blocks
+from . import cache_write, compute_slot_mapping, compute_slot_mapping_cp, map_to_kernel_blocks
 from paged_kv_cache_slot_gb300 import workloads as wl
 
 BF16_NAN = np.uint16(0x7FC0)
@@ -49,3 +49,27 @@ def fill_oracle_cache(w: wl.Workload, rows=None, kcache=None, vcache=None, table
         kc, vc, err = cache_write(k, v, slots, kc, vc, inplace=True)
         assert err == 0
     return kc, vc, table
+
+
+def fill_oracle_cache_cp(w: wl.Workload, world: int, interleave: int, tables, rows=None):
+    """Each context-parallel rank's caches, written through the oracle's CP slot
+    mapping (reading R14) and cache write from every token of ``rows``;
+    ``tables`` are the ranks' (table, total_blocks) pairs.  Returns [(k, v)]."""
+    rows = range(w.num_rows) if rows is None else rows
+    out = []
+    for k, (table, total) in enumerate(tables):
+        kc = nan_cache(w, total_blocks=total)
+        vc = nan_cache(w, total_blocks=total)
+        for r in rows:
+            L = int(w.context_lens[r])
+            if L == 0:
+                continue
+            kr, vr = w.kv_rows(r, 0, L)
+            req = np.full(L, r, np.int32)
+            pos = np.arange(L, dtype=np.int64)
+            slots, err = compute_slot_mapping_cp(table, req, pos, w.kernel_block_size, world, k, interleave)
+            assert err == 0
+            kc, vc, err = cache_write(kr, vr, slots, kc, vc, inplace=True)
+            assert err == 0
+        out.append((kc, vc))
+    return out

@@ -200,6 +200,22 @@ class Workload:
         return np.concatenate(reqs), np.concatenate(poss)
 
 
+def cp_block_tables(w: Workload, world: int, slack: float = 0.25):
+    """Per-rank kernel-block tables for splitting ``w``'s cache over ``world``
+    context-parallel ranks: rank k draws its own seeded permutation of physical
+    ids 1..total-1 and gives every request as many blocks as its unsplit row
+    needs (more than any rank's share), so each rank's cache holds whichever
+    positions the split gives it.  Returns [(table int32 (rows, width), total)]."""
+    kbs = w.kernel_block_size
+    needed = np.array([_ceil_div(int(n), kbs) for n in w.context_lens], np.int64)
+    width = max(int(needed.max()) if len(needed) else 0, 1) + 1
+    out = []
+    for k in range(world):
+        rng = np.random.default_rng([w.seed, 11, k])
+        out.append(_assign_blocks(rng, needed, width, slack))
+    return out
+
+
 def _assign_blocks(rng, needed: np.ndarray, width: int, slack: float = 0.25):
     """Random distinct physical ids 1..total-1 for each row's needed blocks; -1 elsewhere."""
     total_needed = int(needed.sum())
