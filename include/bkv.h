@@ -232,6 +232,75 @@ int bkv_paged_decode_merge(const void *q, const void *k_cache, const void *v_cac
                            bkv_stream_t stream);
 
 /*
+ * bkv_compute_slot_mapping_cp
+ *   bkv_compute_slot_mapping under decode context parallelism ("ブロック表"
+ *   設計動機: with DCP the slot kernel writes the real slot only for the
+ *   tokens its own rank holds and PAD for the others; the page names the
+ *   world size, rank and interleave size but prints no formula).  Reading
+ *   taken: global position p belongs to rank (p / cp_interleave) %
+ *   cp_world (runs of cp_interleave consecutive positions dealt round
+ *   robin) and is stored on that rank at the local position
+ *   p_l = (p / (cp_interleave * cp_world)) * cp_interleave + p % cp_interleave;
+ *   `block_table` is this rank's table over local positions, so the slot is
+ *   block_table[r][p_l / block_size] * block_size + p_l % block_size.  A
+ *   token another rank holds gets -1 and is not an error.  When
+ *   cp_interleave divides block_size this is the same as one table shared
+ *   by all ranks with blocks of block_size * cp_world global positions.
+ *   cp_world = 1 is bkv_compute_slot_mapping exactly.
+ *   INVALID_ARG: as bkv_compute_slot_mapping, or cp_world < 1, cp_rank
+ *   outside [0, cp_world), cp_interleave < 1.
+ */
+int bkv_compute_slot_mapping_cp(const int32_t *block_table, int32_t num_reqs, int64_t bt_stride,
+                                int32_t bt_cols, const int32_t *req_indices, const int64_t *positions,
+                                int64_t num_tokens, int64_t max_num_tokens, int32_t block_size,
+                                int32_t cp_world, int32_t cp_rank, int32_t cp_interleave,
+                                int64_t *slot_mapping, int32_t *err_count, bkv_stream_t stream);
+
+/*
+ * bkv_paged_decode_cp
+ *   One rank's part of a context-parallel paged decode: bkv_paged_decode
+ *   over the keys this rank holds (the split of bkv_compute_slot_mapping_cp;
+ *   k_cache, v_cache and block_table are this rank's, context_lens are the
+ *   requests' GLOBAL cache lengths), with the causal mask applied in global
+ *   positions.  `out` receives this rank's normalised result and, when `lse`
+ *   is not NULL, lse[(r * q_len + t) * num_q_heads + h] receives the natural
+ *   log of the sum of exp(softmax_scale * q . k) over this rank's visible
+ *   keys (-inf, with out = 0, where it sees none).  Merging the ranks'
+ *   (out, lse) with bkv_merge_attn_states gives the attention over all keys
+ *   (the exchange between ranks, an all-gather, is the caller's).  The
+ *   workspace is the one bkv_paged_decode_workspace_size gives for the
+ *   global max_context_len.  cp_world = 1 is bkv_paged_decode plus lse.
+ *   Errors: as bkv_paged_decode, plus INVALID_ARG for a bad cp_world /
+ *   cp_rank / cp_interleave.
+ */
+int bkv_paged_decode_cp(const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
+                        const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs,
+                        int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int64_t total_blocks, float softmax_scale, int mask_mode,
+                        int32_t cp_world, int32_t cp_rank, int32_t cp_interleave, int dtype, void *out,
+                        float *lse, void *workspace, size_t workspace_bytes, int32_t *err_count,
+                        bkv_stream_t stream);
+
+/*
+ * bkv_merge_attn_states
+ *   Combines `parts` partial attention results of the same rows, each a
+ *   normalised output and its log-sum-exp as bkv_paged_decode_cp writes
+ *   them: out = sum_k e^(lse_k - M) outs_k / sum_k e^(lse_k - M) and
+ *   lse_out = M + log sum_k e^(lse_k - M), M = max_k lse_k; a row whose parts
+ *   are all -inf gives 0 and -inf.  This is the step after the ranks of a
+ *   context-parallel decode exchange their results ("ブロック表" 設計動機,
+ *   DCP); the pages print no formula for it, and it is the exact split of a
+ *   softmax over disjoint key sets.
+ *   outs   [parts][rows][head_dim] of `dtype`;  lses  fp32 [parts][rows];
+ *   out    [rows][head_dim] of `dtype`;  lse_out fp32 [rows] or NULL.
+ *   INVALID_ARG: parts < 1, rows < 0, head_dim < 1, null pointers.
+ *   UNSUPPORTED: dtype not BKV_BF16 / BKV_F32.
+ */
+int bkv_merge_attn_states(const void *outs, const float *lses, int32_t parts, int64_t rows,
+                          int32_t head_dim, int dtype, void *out, float *lse_out, bkv_stream_t stream);
+
+/*
  * bkv_paged_decode_noalloc
  *   No counterpart on the pages: this is a convenience of this library.
  *

@@ -58,6 +58,14 @@ def load() -> ctypes.CDLL:
         lib.bkv_version.argtypes = []
         lib.bkv_compute_slot_mapping.restype = cint
         lib.bkv_compute_slot_mapping.argtypes = [vp, i32, i64, i32, vp, vp, i64, i64, i32, vp, vp, vp]
+        lib.bkv_compute_slot_mapping_cp.restype = cint
+        lib.bkv_compute_slot_mapping_cp.argtypes = [vp, i32, i64, i32, vp, vp, i64, i64, i32, i32, i32, i32, vp, vp,
+                                                    vp]
+        lib.bkv_paged_decode_cp.restype = cint
+        lib.bkv_paged_decode_cp.argtypes = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i32, i64, f32,
+                                            cint, i32, i32, i32, cint, vp, vp, vp, sz, vp, vp]
+        lib.bkv_merge_attn_states.restype = cint
+        lib.bkv_merge_attn_states.argtypes = [vp, vp, i32, i64, i32, cint, vp, vp, vp]
         lib.bkv_map_to_kernel_blocks.restype = cint
         lib.bkv_map_to_kernel_blocks.argtypes = [vp, i32, i64, i32, i32, i32, vp, i64, vp]
         lib.bkv_cache_write.restype = cint
@@ -108,15 +116,28 @@ def _kv_dtype(t: torch.Tensor) -> int:
 def bkv_compute_slot_mapping(block_table, req_indices, positions, block_size, slot_mapping, num_tokens=None,
                              err_count=None, stream=None):
     """slot_mapping[i] = block_table[req, pos // bs] * bs + pos % bs, -1 for padding (see include/bkv.h)."""
+    return _slot_mapping("bkv_compute_slot_mapping", (), block_table, req_indices, positions, block_size,
+                         slot_mapping, num_tokens, err_count, stream)
+
+
+def bkv_compute_slot_mapping_cp(block_table, req_indices, positions, block_size, slot_mapping, cp_world, cp_rank,
+                                cp_interleave=1, num_tokens=None, err_count=None, stream=None):
+    """Rank ``cp_rank``'s slots under decode context parallelism, -1 for other ranks' tokens (see include/bkv.h)."""
+    return _slot_mapping("bkv_compute_slot_mapping_cp", (int(cp_world), int(cp_rank), int(cp_interleave)),
+                         block_table, req_indices, positions, block_size, slot_mapping, num_tokens, err_count, stream)
+
+
+def _slot_mapping(fn, cp, block_table, req_indices, positions, block_size, slot_mapping, num_tokens, err_count,
+                  stream):
     if block_table.dim() != 2 or block_table.stride(1) != 1:
         raise ValueError("block_table must be 2-D with unit column stride")
     n = positions.numel() if num_tokens is None else int(num_tokens)
     if n > positions.numel() or n > req_indices.numel() or n > slot_mapping.numel():
         raise ValueError("num_tokens exceeds positions / req_indices / slot_mapping")
-    _check("bkv_compute_slot_mapping", load().bkv_compute_slot_mapping(
+    _check(fn, getattr(load(), fn)(
         _dev(block_table, "block_table", torch.int32, contiguous=False), block_table.shape[0],
         block_table.stride(0), block_table.shape[1], _dev(req_indices, "req_indices", torch.int32),
-        _dev(positions, "positions", torch.int64), n, slot_mapping.numel(), int(block_size),
+        _dev(positions, "positions", torch.int64), n, slot_mapping.numel(), int(block_size), *cp,
         _dev(slot_mapping, "slot_mapping", torch.int64), _opt(err_count, "err_count", torch.int32), _stream(stream)))
     return slot_mapping
 
@@ -209,6 +230,53 @@ def _decode(fn, q, k_cache, v_cache, block_table, context_lens, max_context_len,
         block_table.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), nr, ql, hq, hkv,
         d, bs, tb, float(softmax_scale), int(mask_mode), int(sliding_window), dt, _dev(out, "out"), ws_ptr, ws_bytes,
         _opt(err_count, "err_count", torch.int32), _stream(stream)))
+    return out
+
+
+def bkv_paged_decode_cp(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, lse, workspace,
+                        cp_world, cp_rank, cp_interleave=1, softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL,
+                        err_count=None, stream=None):
+    """One rank's part of a context-parallel decode: its normalised ``out`` and fp32 ``lse`` (num_reqs, q_len,
+    H_q) over the keys it holds; ``context_lens`` are global lengths (see include/bkv.h).  ``lse`` may be None."""
+    if q.dim() != 4 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("q/out must be (num_reqs, q_len, H_q, D); caches (total_blocks, bs, H_kv, D)")
+    nr, ql, hq, d = q.shape
+    tb, bs, hkv, d2 = k_cache.shape
+    if d2 != d:
+        raise ValueError("head_dim mismatch")
+    if block_table.dim() != 2 or block_table.shape[0] < nr or block_table.stride(1) != 1:
+        raise ValueError("block_table must be (>= num_reqs, cols) with unit column stride")
+    if lse is not None and tuple(lse.shape) != (nr, ql, hq):
+        raise ValueError("lse must be (num_reqs, q_len, H_q)")
+    dt = _kv_dtype(q)
+    for t, nm in ((k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{nm} dtype differs from q")
+    ws_ptr = None if workspace is None else _dev(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check("bkv_paged_decode_cp", load().bkv_paged_decode_cp(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_table, "block_table", torch.int32, contiguous=False), block_table.stride(0),
+        block_table.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), nr, ql, hq, hkv,
+        d, bs, tb, float(softmax_scale), int(mask_mode), int(cp_world), int(cp_rank), int(cp_interleave), dt,
+        _dev(out, "out"), _opt(lse, "lse", torch.float32), ws_ptr, ws_bytes, _opt(err_count, "err_count", torch.int32),
+        _stream(stream)))
+    return out, lse
+
+
+def bkv_merge_attn_states(outs, lses, out, lse_out=None, stream=None):
+    """Merge ``parts`` partial results: outs (parts, rows, D), lses fp32 (parts, rows) -> out (rows, D) and
+    optionally lse_out (rows) (see include/bkv.h).  Any leading shape with the same element count works."""
+    parts = outs.shape[0]
+    rows = lses[0].numel()
+    d = outs.shape[-1]
+    if outs.numel() != parts * rows * d or lses.numel() != parts * rows or out.numel() != rows * d:
+        raise ValueError("outs (parts, rows, D), lses (parts, rows), out (rows, D) sizes disagree")
+    if out.dtype != outs.dtype:
+        raise TypeError("out dtype differs from outs")
+    _check("bkv_merge_attn_states", load().bkv_merge_attn_states(
+        _dev(outs, "outs"), _dev(lses, "lses", torch.float32), parts, rows, d, _kv_dtype(outs), _dev(out, "out"),
+        _opt(lse_out, "lse_out", torch.float32), _stream(stream)))
     return out
 
 

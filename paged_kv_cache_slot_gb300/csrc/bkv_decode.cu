@@ -24,6 +24,7 @@
 namespace bkv {
 
 static constexpr float kLog2e = 1.4426950408889634f;
+static constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_f(float x) { return x; }
@@ -67,10 +68,12 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
     const int g = rg - r * a.H_kv;
     const int i0 = blockIdx.y * QR;
 
+    // L: global cache length (masks); Lk: the keys this rank holds (loop)
     const int32_t L = clamped_len(a, r, c == 0 && g == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+    const int32_t Lk = cp_local_len(a, L);
     const int32_t start = c * a.chunk;
-    if (start >= L) return;
-    const int32_t end = min(start + a.chunk, L);
+    if (start >= Lk) return;
+    const int32_t end = min(start + a.chunk, Lk);
     const int nrows = min(QR, a.nq - i0);
 
     const T *Q = static_cast<const T *>(a.q);
@@ -113,8 +116,9 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
         for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
     }
 
-    const int32_t j0 = max(start, jmin);
-    for (int32_t j = j0 + warp; j < end && j <= jmax; j += NW) {
+    const int32_t j0 = max(start, jmin);   // a window implies cp_world == 1: local = global
+    for (int32_t j = j0 + warp; j < end && cp_global(a, j) <= jmax; j += NW) {
+        const int64_t gj = cp_global(a, j);
         const int32_t lb = j / a.bs;
         const int32_t off = j - lb * a.bs;
         const bool first = (j == j0) || (off == 0);  // count a bad entry once per CTA
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
         }
 #pragma unroll
         for (int i = 0; i < QR; ++i) {
-            if (i < nrows && j <= lastv[i] && j >= firstv[i]) {
+            if (i < nrows && gj <= lastv[i] && gj >= firstv[i]) {
                 const float mn = fmaxf(m[i], s[i]);
                 const float corr = exp2f(m[i] - mn);
                 const float p = exp2f(s[i] - mn);
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
     const int64_t rg = blockIdx.x;            // stream: r * H_kv + g
     const int r = (int)(rg / a.H_kv);
     const int g = (int)(rg - (int64_t)r * a.H_kv);
-    const int32_t L = clamped_len(a, r, false);
+    const int32_t L = cp_local_len(a, clamped_len(a, r, false));   // keys this rank holds
     // a stream's partial slots are contiguous
     int nch = 0;          // slots of this stream
     int64_t unit0 = 0;    // its first slot
@@ -244,7 +248,13 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
     for (int row = warp; row < a.nq; row += 4) {
         const int t = row / a.G;
         const int h = g * a.G + (row - t * a.G);
-        T *out = static_cast<T *>(a.out) + (((int64_t)r * a.q_len + t) * a.H_q + h) * a.D;
+        const int64_t orow = ((int64_t)r * a.q_len + t) * a.H_q + h;
+        T *out = static_cast<T *>(a.out) + orow * a.D;
+        // log-sum-exp of the row, back from base 2 to natural log (-inf: no visible key)
+        auto put_lse = [&](float M, float lsum) {
+            if (a.lse && lane == 0)
+                a.lse[orow] = (M == -INFINITY || !(lsum > 0.f)) ? -INFINITY : (M + log2f(lsum)) * kLn2;
+        };
         if (nch <= 8 && a.D == 128) {
             // few slots: every load of the row (each lane's slot (m, l) and its four
             // head_dim elements of every slot) is issued in one round
@@ -261,6 +271,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
             const float wl = (M == -INFINITY || lane >= nch) ? 0.f : exp2f(ml.x - M);
             const float lsum = warp_sum(wl * ml.y);
             const float iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : 1.f / lsum;
+            put_lse(M, lsum);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -291,6 +302,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
         }
         lsum = warp_sum(lsum);
         const float iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : 1.f / lsum;
+        put_lse(M, lsum);
         __syncwarp();
         if ((a.D & 3) == 0) {
             for (int d4 = lane; d4 < a.D / 4; d4 += 32) {
@@ -433,10 +445,13 @@ static int decode_setup(const void *q, const void *k_cache, const void *v_cache,
                         int64_t bt_stride, int32_t bt_cols, const int32_t *context_lens, int32_t max_context_len,
                         int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                         int32_t block_size, int64_t total_blocks, float softmax_scale, int mask_mode, int dtype,
-                        int32_t sliding_window, void *out, void *workspace, size_t workspace_bytes,
-                        int32_t *err_count, DecodeCall *c) {
+                        int32_t sliding_window, int32_t cp_world, int32_t cp_rank, int32_t cp_interleave,
+                        void *out, float *lse, void *workspace, size_t workspace_bytes, int32_t *err_count,
+                        DecodeCall *c) {
     if (dtype != BKV_BF16 && dtype != BKV_F32) return BKV_ERR_UNSUPPORTED;
     if (sliding_window < 0) return BKV_ERR_INVALID_ARG;
+    if (cp_world < 1 || cp_rank < 0 || cp_rank >= cp_world || cp_interleave < 1) return BKV_ERR_INVALID_ARG;
+    if (cp_world > 1 && sliding_window > 0) return BKV_ERR_UNSUPPORTED;
     if (head_dim > 256 || head_dim % 2 != 0) return BKV_ERR_UNSUPPORTED;
     if (mask_mode != BKV_MASK_CAUSAL && mask_mode != BKV_MASK_ALL) return BKV_ERR_INVALID_ARG;
     if (bt_cols < 0 || bt_stride < bt_cols || total_blocks < 0) return BKV_ERR_INVALID_ARG;
@@ -467,6 +482,10 @@ static int decode_setup(const void *q, const void *k_cache, const void *v_cache,
     a.scale_log2 = softmax_scale * kLog2e;
     a.mask_mode = mask_mode;
     a.window = sliding_window;
+    a.cp_world = cp_world;
+    a.cp_rank = cp_rank;
+    a.cp_inter = cp_interleave;
+    a.lse = lse;
     a.dtype = dtype;
     a.chunk = plan.chunk;
     a.n_chunks = plan.n_chunks;
@@ -525,7 +544,8 @@ static int decode_merge(DecodeCall &c, cudaStream_t st) {
 #define BKV_DECODE_SETUP(c)                                                                                       \
     bkv::decode_setup(q, k_cache, v_cache, block_table, bt_stride, bt_cols, context_lens, max_context_len,       \
                       num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, total_blocks, softmax_scale, \
-                      mask_mode, dtype, sliding_window, out, workspace, workspace_bytes, err_count, &(c))
+                      mask_mode, dtype, sliding_window, 1, 0, 1, out, nullptr, workspace, workspace_bytes,      \
+                      err_count, &(c))
 
 extern "C" int bkv_paged_decode(BKV_DECODE_PARAMS) {
     bkv::DecodeCall c;
@@ -548,4 +568,87 @@ extern "C" int bkv_paged_decode_merge(BKV_DECODE_PARAMS) {
     const int rc = BKV_DECODE_SETUP(c);
     if (rc != BKV_OK) return rc;
     return bkv::decode_merge(c, (cudaStream_t)stream);
+}
+
+extern "C" int bkv_paged_decode_cp(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
+                                   const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs,
+                                   int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int64_t total_blocks, float softmax_scale, int mask_mode,
+                                   int32_t cp_world, int32_t cp_rank, int32_t cp_interleave, int dtype, void *out,
+                                   float *lse, void *workspace, size_t workspace_bytes, int32_t *err_count,
+                                   bkv_stream_t stream) {
+    bkv::DecodeCall c;
+    int rc = bkv::decode_setup(q, k_cache, v_cache, block_table, bt_stride, bt_cols, context_lens, max_context_len,
+                               num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, total_blocks,
+                               softmax_scale, mask_mode, dtype, 0, cp_world, cp_rank, cp_interleave, out, lse,
+                               workspace, workspace_bytes, err_count, &c);
+    if (rc != BKV_OK) return rc;
+    rc = bkv::decode_partition(c, (cudaStream_t)stream);
+    if (rc != BKV_OK) return rc;
+    return bkv::decode_merge(c, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------------------
+// Merge of attention states: rows of `parts` normalised partial outputs
+// (outs [parts][rows][D]) with their natural-log sums of exponentials
+// (lses [parts][rows]) into out = sum_k e^(lse_k - M) out_k / sum_k
+// e^(lse_k - M) and lse_out = M + log sum_k e^(lse_k - M), M = max_k lse_k;
+// all -inf gives 0 and -inf.  The combination step after the ranks of a
+// context-parallel decode exchange their results.  One warp per row; for up
+// to 32 parts lane k keeps part k's weight and the others take it by shuffle.
+// ---------------------------------------------------------------------------
+namespace bkv {
+
+template <typename T>
+__global__ void __launch_bounds__(128) merge_states_kernel(const T *__restrict__ outs, const float *__restrict__ lses,
+                                                           int parts, int64_t rows, int D, T *__restrict__ out,
+                                                           float *__restrict__ lse_out) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    float M = -INFINITY;
+    for (int k = lane; k < parts; k += 32) M = fmaxf(M, lses[(int64_t)k * rows + row]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    auto weight = [&](int k) { return M == -INFINITY ? 0.f : expf(lses[(int64_t)k * rows + row] - M); };
+    float wsum = 0.f;
+    for (int k = lane; k < parts; k += 32) wsum += weight(k);
+    wsum = warp_sum(wsum);
+    const float iv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const float wl = (parts <= 32 && lane < parts) ? weight(lane) : 0.f;
+    T *o = out + row * D;
+    for (int d = lane; d < D; d += 32) {
+        float acc = 0.f;
+        for (int k = 0; k < parts; ++k) {
+            const float w = parts <= 32 ? __shfl_sync(0xffffffffu, wl, k & 31) : weight(k);
+            acc = fmaf(w, to_f(outs[((int64_t)k * rows + row) * D + d]), acc);
+        }
+        store_out(o + d, acc * iv);
+    }
+    if (lse_out && lane == 0) lse_out[row] = (M == -INFINITY || !(wsum > 0.f)) ? -INFINITY : M + logf(wsum);
+}
+
+}  // namespace bkv
+
+extern "C" int bkv_merge_attn_states(const void *outs, const float *lses, int32_t parts, int64_t rows,
+                                     int32_t head_dim, int dtype, void *out, float *lse_out, bkv_stream_t stream) {
+    if (dtype != BKV_BF16 && dtype != BKV_F32) return BKV_ERR_UNSUPPORTED;
+    if (parts < 1 || rows < 0 || head_dim < 1) return BKV_ERR_INVALID_ARG;
+    if (rows == 0) return BKV_OK;
+    if (!outs || !lses || !out) return BKV_ERR_INVALID_ARG;
+    const int64_t blocks = (rows + 3) / 4;
+    if (blocks > 0x7fffffff) return BKV_ERR_INVALID_ARG;
+    const cudaError_t e =
+        dtype == BKV_BF16
+            ? bkv::launch_pdl(bkv::merge_states_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(128), 0,
+                              (cudaStream_t)stream, static_cast<const __nv_bfloat16 *>(outs), lses, (int)parts, rows,
+                              (int)head_dim, static_cast<__nv_bfloat16 *>(out), lse_out)
+            : bkv::launch_pdl(bkv::merge_states_kernel<float>, dim3((unsigned)blocks), dim3(128), 0,
+                              (cudaStream_t)stream, static_cast<const float *>(outs), lses, (int)parts, rows,
+                              (int)head_dim, static_cast<float *>(out), lse_out);
+    if (e != cudaSuccess) bkv::set_cuda_error(e);
+    return bkv::launch_status();
 }

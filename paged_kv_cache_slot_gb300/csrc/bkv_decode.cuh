@@ -22,6 +22,8 @@ struct DecodeArgs {
     float scale_log2;  // softmax_scale * log2(e): scores are kept in base 2
     int mask_mode;
     int32_t window;    // sliding window W (> 0): query t sees keys j >= L - q_len + t - W + 1; 0: none
+    int32_t cp_world, cp_rank, cp_inter;   // decode context parallelism: this rank's share of the keys
+    float *lse;        // optional [num_reqs, q_len, H_q] natural-log sum of exp of the scaled scores
     int dtype;         // BKV_BF16 or BKV_F32 (q, caches and out share it)
     int32_t chunk;     // tokens per split-KV partition (multiple of the tile and of bs)
     int32_t n_chunks;  // partitions per request at max_ctx
@@ -42,6 +44,34 @@ struct DecodeArgs {
 // of whichever kernel runs: the generic kernel's (request, KV head,
 // partition) slots or the tensor-core kernel's 2 (sk_grid + num_reqs * H_kv)
 // stream-K slots.
+// Decode context parallelism ("ブロック表" 設計動機, DCP interleave): with
+// world size W, rank k and interleave I, global position p belongs to rank
+// (p / I) % W and is its local key (p / (I W)) I + p % I.  cp_local_len is
+// how many of a request's L positions rank k holds; cp_global maps its local
+// key j back to the global position the masks use.  W = 1: identity.
+__host__ __device__ inline int32_t cp_local_len(const DecodeArgs &a, int32_t L) {
+    if (a.cp_world <= 1) return L;
+    const int64_t cyc = (int64_t)a.cp_inter * a.cp_world;
+    const int64_t full = L / cyc;
+    int64_t part = (int64_t)L - full * cyc - (int64_t)a.cp_rank * a.cp_inter;
+    part = part < 0 ? 0 : (part > a.cp_inter ? a.cp_inter : part);
+    return (int32_t)(full * a.cp_inter + part);
+}
+
+__host__ __device__ inline int64_t cp_global(const DecodeArgs &a, int64_t j) {
+    if (a.cp_world <= 1) return j;
+    const int64_t run = j / a.cp_inter;
+    return (run * a.cp_world + a.cp_rank) * a.cp_inter + (j - run * a.cp_inter);
+}
+
+// The same for a key of a request shorter than 2^31 positions (always: cache
+// lengths are int32), in 32-bit arithmetic.
+__host__ __device__ inline int32_t cp_global32(const DecodeArgs &a, int32_t j) {
+    if (a.cp_world <= 1) return j;
+    const int32_t run = j / a.cp_inter;
+    return (run * a.cp_world + a.cp_rank) * a.cp_inter + (j - run * a.cp_inter);
+}
+
 // First key position any query of a request of cache length L may see (the
 // window of its first query token); 0 without a sliding window.
 __host__ __device__ inline int32_t window_lo(const DecodeArgs &a, int32_t L) {

@@ -324,9 +324,12 @@ __device__ void schedule_loads(const DecodeArgs &a, int32_t *pre, uint8_t *lrem,
         const int r = threadIdx.x + i * kThreads;
         if (r < n) {
             if (lens[i] > a.max_ctx && blockIdx.x == 0 && a.err) atomicAdd(a.err, 1);
-            const int32_t L = lens[i] > a.max_ctx ? a.max_ctx : (lens[i] < 0 ? 0 : lens[i]);
-            // a sliding window drops the tiles wholly before its first visible key
-            pre[r] = (L + kTile - 1) / kTile - window_lo(a, L) / kTile;
+            const int32_t Lg = lens[i] > a.max_ctx ? a.max_ctx : (lens[i] < 0 ? 0 : lens[i]);
+            // the keys this rank holds (all of them without context parallelism); a
+            // sliding window (never combined with it) drops the tiles wholly before
+            // its first visible key
+            const int32_t L = cp_local_len(a, Lg);
+            pre[r] = (L + kTile - 1) / kTile - window_lo(a, Lg) / kTile;
             lrem[r] = (uint8_t)((L - 1) & (kTile - 1));
         }
     }
@@ -500,7 +503,7 @@ __device__ __forceinline__ bool reduced_writer(int lane) {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int NQ>
+template <int NQ, bool kCP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a, int seg_rows) {
@@ -843,6 +846,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         sk.init(a, pre, lrem);
         Unit x;
         while (ok && sk.next(a, x)) {
+            // masks are in global positions: with context parallelism x.L counts
+            // only this rank's keys, so the request's length is read again
+            int32_t Lg = x.L;
+            if (kCP) {
+                const int32_t c = __ldg(a.ctx + x.r);
+                Lg = c > a.max_ctx ? a.max_ctx : c;
+            }
             int32_t lastv[NQ], firstv[NQ];
 #pragma unroll
             for (int n = 0; n < NQ; ++n) {
@@ -850,8 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lsum[n] = 0.f;
                 mrun[n] = -INFINITY;
                 const int t = n / G;
-                lastv[n] = (n < nq) ? (a.mask_mode == 0 ? x.L - a.q_len + t : x.L - 1) : -1;
-                firstv[n] = a.window > 0 ? x.L - a.q_len + t - a.window + 1 : INT32_MIN;
+                lastv[n] = (n < nq) ? (a.mask_mode == 0 ? Lg - a.q_len + t : Lg - 1) : -1;
+                firstv[n] = a.window > 0 ? Lg - a.q_len + t - a.window + 1 : INT32_MIN;
             }
             for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
                 if ((int)(j & 1) != wg) continue;
@@ -869,9 +879,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t pos = x.start + jt * kTile + row;
                 const bool loaded = (mask_words[j & 7] >> (row >> seg_shift)) & 1u;
                 const bool inrange = loaded && pos < x.cend;
+                const int32_t gpos = kCP ? cp_global32(a, pos) : pos;
 #pragma unroll
                 for (int n = 0; n < NQ; ++n)
-                    sv[n] = (inrange && pos <= lastv[n] && pos >= firstv[n]) ? sv[n] * a.scale_log2 : -INFINITY;
+                    sv[n] = (inrange && gpos <= lastv[n] && gpos >= firstv[n]) ? sv[n] * a.scale_log2 : -INFINITY;
                 // tile max per query row across the warpgroup's 128 threads
                 const float wmax = warp_reduce_rows<true, NQ>(sv, lane);
                 float *rm = red_max + (wg * 2 + (int)par) * (kN * 4);
@@ -1022,10 +1033,15 @@ int launch_decode_tc(const DecodeArgs &a, const TcLaunch &t, cudaStream_t st) {
     using namespace tc;
     // the grid is the stream-K CTA count the workspace was laid out for
     const int64_t grid = a.sk_grid;
-    // the softmax handles only the query rows that exist (4, 8 or 16 columns)
-    auto kern = a.nq <= 4 ? decode_tc_kernel<4> : (a.nq <= 8 ? decode_tc_kernel<8> : decode_tc_kernel<16>);
-    const int slot = a.nq <= 4 ? 0 : (a.nq <= 8 ? 1 : 2);
-    static bool attr_set[64][3] = {};
+    // the softmax handles only the query rows that exist (4, 8 or 16 columns);
+    // context parallelism (global-position masks) has its own instances
+    const bool cp = a.cp_world > 1;
+    auto kern = cp ? (a.nq <= 4 ? decode_tc_kernel<4, true>
+                                : (a.nq <= 8 ? decode_tc_kernel<8, true> : decode_tc_kernel<16, true>))
+                   : (a.nq <= 4 ? decode_tc_kernel<4, false>
+                                : (a.nq <= 8 ? decode_tc_kernel<8, false> : decode_tc_kernel<16, false>));
+    const int slot = (a.nq <= 4 ? 0 : (a.nq <= 8 ? 1 : 2)) + (cp ? 3 : 0);
+    static bool attr_set[64][6] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev][slot]) {

@@ -10,11 +10,16 @@ namespace bkv {
 // slot = block_table[r][p / bs] * bs + p % bs, with -1 for padding, null or
 // sentinel entries and bad indices ("Padding and Batching with Block KV",
 // The Core Formula; Special Block and Slot Values; "ブロック表" 設計動機 for the
-// padded tail).
+// padded tail).  Under decode context parallelism ("ブロック表" 設計動機: a
+// rank writes real slots only for the tokens it owns, PAD for the rest)
+// position p belongs to rank (p / inter) % world and is stored there at the
+// local position (p / (inter * world)) * inter + p % inter, which the rank's
+// table indexes; world = 1 is the plain formula.
 __global__ void __launch_bounds__(256) slot_mapping_kernel(
     const int32_t *__restrict__ block_table, int32_t num_reqs, int64_t bt_stride, int32_t bt_cols,
     const int32_t *__restrict__ req_indices, const int64_t *__restrict__ positions, int64_t num_tokens,
-    int64_t max_num_tokens, int32_t block_size, int64_t *__restrict__ slot_mapping, int32_t *err_count) {
+    int64_t max_num_tokens, int32_t block_size, int32_t cp_world, int32_t cp_rank, int32_t cp_inter,
+    int64_t *__restrict__ slot_mapping, int32_t *err_count) {
     pdl_wait();
     pdl_trigger();
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
@@ -22,10 +27,16 @@ __global__ void __launch_bounds__(256) slot_mapping_kernel(
         int64_t slot = -1;
         if (i < num_tokens) {
             const int32_t r = req_indices[i];
-            const int64_t p = positions[i];
+            int64_t p = positions[i];
             if (r >= 0) {
                 bool bad = (r >= num_reqs) || (p < 0);
-                if (!bad) {
+                bool mine = true;
+                if (!bad && cp_world > 1) {
+                    const int64_t run = p / cp_inter;
+                    mine = run % cp_world == cp_rank;
+                    p = run / cp_world * cp_inter + (p - run * cp_inter);   // local position
+                }
+                if (!bad && mine) {
                     const int64_t lb = p / block_size;
                     if (lb >= bt_cols) {
                         bad = true;
@@ -66,8 +77,18 @@ extern "C" int bkv_compute_slot_mapping(const int32_t *block_table, int32_t num_
                                         int32_t bt_cols, const int32_t *req_indices, const int64_t *positions,
                                         int64_t num_tokens, int64_t max_num_tokens, int32_t block_size,
                                         int64_t *slot_mapping, int32_t *err_count, bkv_stream_t stream) {
+    return bkv_compute_slot_mapping_cp(block_table, num_reqs, bt_stride, bt_cols, req_indices, positions,
+                                       num_tokens, max_num_tokens, block_size, 1, 0, 1, slot_mapping, err_count,
+                                       stream);
+}
+
+extern "C" int bkv_compute_slot_mapping_cp(const int32_t *block_table, int32_t num_reqs, int64_t bt_stride,
+                                           int32_t bt_cols, const int32_t *req_indices, const int64_t *positions,
+                                           int64_t num_tokens, int64_t max_num_tokens, int32_t block_size,
+                                           int32_t cp_world, int32_t cp_rank, int32_t cp_interleave,
+                                           int64_t *slot_mapping, int32_t *err_count, bkv_stream_t stream) {
     if (block_size <= 0 || num_tokens < 0 || max_num_tokens < num_tokens || num_reqs < 0 || bt_cols < 0 ||
-        bt_stride < bt_cols)
+        bt_stride < bt_cols || cp_world < 1 || cp_rank < 0 || cp_rank >= cp_world || cp_interleave < 1)
         return BKV_ERR_INVALID_ARG;
     if (max_num_tokens == 0) return BKV_OK;
     if (!slot_mapping) return BKV_ERR_INVALID_ARG;
@@ -76,7 +97,8 @@ extern "C" int bkv_compute_slot_mapping(const int32_t *block_table, int32_t num_
     const int threads = 256;
     const cudaError_t e = bkv::launch_pdl(bkv::slot_mapping_kernel, bkv::grid_for(max_num_tokens, threads), threads, 0,
                                           (cudaStream_t)stream, block_table, num_reqs, bt_stride, bt_cols, req_indices,
-                                          positions, num_tokens, max_num_tokens, block_size, slot_mapping, err_count);
+                                          positions, num_tokens, max_num_tokens, block_size, cp_world, cp_rank,
+                                          cp_interleave, slot_mapping, err_count);
     if (e != cudaSuccess) bkv::set_cuda_error(e);
     return bkv::launch_status();
 }
