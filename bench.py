@@ -67,8 +67,11 @@ def _peaks():
     return 6800.0, "fallback"
 
 
-def _describe(w, window):
+def _describe(w, window, cp=(1, 0, 1)):
     """The workload's name and sizes, as the JSON line's config.workload."""
+    if cp[0] > 1:
+        return (_describe(w, window) + f", decode-context-parallel rank {cp[1]} of {cp[0]} (interleave {cp[2]}): "
+                f"its own share of every request's keys")
     if w.name == WORKLOAD and window == 0:
         return ("llama3_decode: 32 req, ctx U[512,4096] + 1 new token, H_q 32, H_kv 8, D 128, bs 64, bf16, "
                 "fp32 accumulate")
@@ -285,8 +288,10 @@ def run_bkv(args):
     bkv.load()
 
     w = wl.make(args.workload)
-    dw = DeviceWorkload(w, device=f"cuda:{local}", sliding_window=args.sliding_window)
-    headline = args.workload == WORKLOAD and args.sliding_window == 0
+    cp = (args.cp_world, 0, args.cp_interleave)
+    dw = DeviceWorkload(w, device=f"cuda:{local}", sliding_window=args.sliding_window, cp_world=cp[0],
+                        cp_rank=cp[1], cp_interleave=cp[2])
+    headline = args.workload == WORKLOAD and args.sliding_window == 0 and cp[0] == 1
     stream = torch.cuda.Stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=f"cuda:{local}")
@@ -299,7 +304,10 @@ def run_bkv(args):
         dw.decode(stream=stream)
 
     def partition_only():
-        dw.decode_partition(stream=stream)
+        if cp[0] > 1:      # no separate phases for a context-parallel rank: the whole decode call
+            dw.decode(stream=stream)
+        else:
+            dw.decode_partition(stream=stream)
 
     # pinned host copies of the step's inputs for the end-to-end leg
     host_in = {name: getattr(dw, name).cpu().pin_memory()
@@ -366,6 +374,30 @@ def run_bkv(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, dms, ems, pms = t.tolist()
 
+    # context parallelism: the merge of cp_world ranks' (out, lse) that follows their exchange
+    cp_merge = None
+    if rank == 0 and cp[0] > 1:
+        outs = torch.stack([dw.out] * cp[0])
+        lses = torch.stack([dw.lse] * cp[0])
+        merged = torch.empty_like(dw.out)
+        mlse = torch.empty_like(dw.lse)
+
+        def mstep():
+            bkv.bkv_merge_attn_states(outs, lses, merged, mlse, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                mstep()
+        torch.cuda.synchronize()
+        mg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(mg, stream=stream):
+            mstep()
+        mms = statistics.median(_time_steps(torch, mg.replay, max(args.steps, 20), flush, stream))
+        mbytes = (outs.numel() * outs.element_size() + lses.numel() * 4 + merged.numel() * merged.element_size()
+                  + mlse.numel() * 4)
+        cp_merge = {"parts": cp[0], "rows": int(dw.lse.numel()), "ms": mms, "bytes": mbytes,
+                    "GB_per_s": mbytes / (mms / 1e3) / 1e9, "kernel": "bkv_merge_attn_states (CUDA graph)"}
+
     # secondary half of the metric: slot mapping + cache write on the ragged mixed step
     secondary = None
     if rank == 0 and not args.no_secondary and headline:
@@ -404,7 +436,7 @@ def run_bkv(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": _describe(w, args.sliding_window),
+        "config": {"workload": _describe(w, args.sliding_window, cp),
                    "kv_bytes_per_step": kv_bytes, "l2": "flushed before every timed step (write 2x L2, read it back)",
                    "parallelism": f"replicas x{world}", "step": "expand + slot map + write + decode + merge",
                    "cuda_graph": bool(graphs)},
@@ -413,7 +445,8 @@ def run_bkv(args):
         "gpu_launches": args.steps * (5 + 2 + 1 + 5) + (args.steps * 5 if graphs else 0),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic() if headline else None,
-                     "kernel": "decode partition kernel (bkv_paged_decode_partition, CUDA events around it)",
+                     "kernel": ("decode partition kernel (bkv_paged_decode_partition, CUDA events around it)"
+                                if cp[0] == 1 else "context-parallel rank's decode call (partition + merge)"),
                      "decode_call_GBps": kv_bytes / (dms / 1e3) / 1e9,
                      "peak_kind": f"{peak_kind} copy bandwidth"},
         "decode_ms": dms,
@@ -426,6 +459,8 @@ def run_bkv(args):
     }
     if secondary:
         line["secondary"] = secondary
+    if cp_merge:
+        line["cp_merge_states"] = cp_merge
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(args.cpu_budget, args.workload, args.sliding_window)
     print(json.dumps(line), flush=True)
@@ -444,6 +479,9 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD,
                     help="seeded workload to time (default: the Llama-3-8B-shaped decode batch)")
     ap.add_argument("--sliding-window", type=int, default=0, help="decode with this sliding window (0: none)")
+    ap.add_argument("--cp-world", type=int, default=1,
+                    help="time rank 0 of a decode-context-parallel split over this many ranks (1: none)")
+    ap.add_argument("--cp-interleave", type=int, default=1, help="context-parallel interleave size")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

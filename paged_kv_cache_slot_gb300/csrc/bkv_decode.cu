@@ -227,16 +227,16 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
     int nch = 0;          // slots of this stream
     int64_t unit0 = 0;    // its first slot
     if (a.sk_pre) {
-        // stream-K: stream s has T tiles starting at global tile S; CTA k of
+        // stream-K: stream s has Ts tiles starting at global tile S; CTA k of
         // geff = min(sk_grid, TT) covers [k TT / geff, (k + 1) TT / geff) and
         // writes slots 2 (k + s) and 2 (k + s) + 1 for its overlap with s
-        const int64_t T = a.sk_pre[r + 1] - a.sk_pre[r];
+        const int64_t Ts = a.sk_pre[r + 1] - a.sk_pre[r];   // tiles of the stream
         const int64_t TT = (int64_t)a.H_kv * a.sk_pre[a.num_reqs];
-        if (T > 0 && L > 0) {
+        if (Ts > 0 && L > 0) {
             const int64_t geff = TT < (int64_t)a.sk_grid ? TT : (int64_t)a.sk_grid;   // CTAs with tiles
-            const int64_t S = (int64_t)a.H_kv * a.sk_pre[r] + g * T;
+            const int64_t S = (int64_t)a.H_kv * a.sk_pre[r] + g * Ts;
             const int64_t k0 = ((S + 1) * geff - 1) / TT;
-            const int64_t k1 = ((S + T) * geff - 1) / TT;
+            const int64_t k1 = ((S + Ts) * geff - 1) / TT;
             nch = (int)(2 * (k1 - k0 + 1));
             unit0 = 2 * (k0 + rg);
         }
@@ -596,9 +596,19 @@ extern "C" int bkv_paged_decode_cp(const void *q, const void *k_cache, const voi
 // e^(lse_k - M) and lse_out = M + log sum_k e^(lse_k - M), M = max_k lse_k;
 // all -inf gives 0 and -inf.  The combination step after the ranks of a
 // context-parallel decode exchange their results.  One warp per row; for up
-// to 32 parts lane k keeps part k's weight and the others take it by shuffle.
+// to 32 parts lane k keeps part k's weight and the others take it by shuffle;
+// with head_dim 128 and up to 8 parts every load of a row is issued at once.
 // ---------------------------------------------------------------------------
 namespace bkv {
+
+// Four consecutive elements of a row as fp32 (one 8- or 16-byte load).
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+    return make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
+}
+__device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 
 template <typename T>
 __global__ void __launch_bounds__(128) merge_states_kernel(const T *__restrict__ outs, const float *__restrict__ lses,
@@ -609,17 +619,49 @@ __global__ void __launch_bounds__(128) merge_states_kernel(const T *__restrict__
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (row >= rows) return;
+    T *o = out + row * D;
+    if (D == 128 && parts <= 8) {
+        // every load of the row at once: lane k < parts its part's lse, each lane
+        // its four elements of every part
+        const float ll = lane < parts ? lses[(int64_t)lane * rows + row] : -INFINITY;
+        float4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k < parts) v[k] = load4(outs + ((int64_t)k * rows + row) * D + 4 * lane);
+        float M = ll;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float wl = (M == -INFINITY || lane >= parts) ? 0.f : expf(ll - M);
+        const float wsum = warp_sum(wl);
+        const float iv = wsum > 0.f ? 1.f / wsum : 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float w = __shfl_sync(0xffffffffu, wl, k);
+            if (k < parts) {
+                acc.x = fmaf(w, v[k].x, acc.x);
+                acc.y = fmaf(w, v[k].y, acc.y);
+                acc.z = fmaf(w, v[k].z, acc.z);
+                acc.w = fmaf(w, v[k].w, acc.w);
+            }
+        }
+        store_out(o + 4 * lane + 0, acc.x * iv);
+        store_out(o + 4 * lane + 1, acc.y * iv);
+        store_out(o + 4 * lane + 2, acc.z * iv);
+        store_out(o + 4 * lane + 3, acc.w * iv);
+        if (lse_out && lane == 0) lse_out[row] = (M == -INFINITY || !(wsum > 0.f)) ? -INFINITY : M + logf(wsum);
+        return;
+    }
     float M = -INFINITY;
     for (int k = lane; k < parts; k += 32) M = fmaxf(M, lses[(int64_t)k * rows + row]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     auto weight = [&](int k) { return M == -INFINITY ? 0.f : expf(lses[(int64_t)k * rows + row] - M); };
     float wsum = 0.f;
     for (int k = lane; k < parts; k += 32) wsum += weight(k);
     wsum = warp_sum(wsum);
     const float iv = wsum > 0.f ? 1.f / wsum : 0.f;
     const float wl = (parts <= 32 && lane < parts) ? weight(lane) : 0.f;
-    T *o = out + row * D;
     for (int d = lane; d < D; d += 32) {
         float acc = 0.f;
         for (int k = 0; k < parts; ++k) {
@@ -639,6 +681,7 @@ extern "C" int bkv_merge_attn_states(const void *outs, const float *lses, int32_
     if (parts < 1 || rows < 0 || head_dim < 1) return BKV_ERR_INVALID_ARG;
     if (rows == 0) return BKV_OK;
     if (!outs || !lses || !out) return BKV_ERR_INVALID_ARG;
+    if (head_dim == 128 && (!bkv::aligned(outs, 16) || !bkv::aligned(out, 16))) return BKV_ERR_INVALID_ARG;
     const int64_t blocks = (rows + 3) / 4;
     if (blocks > 0x7fffffff) return BKV_ERR_INVALID_ARG;
     const cudaError_t e =

@@ -17,6 +17,7 @@ import torch
 
 from . import bkv
 from .workloads import Workload
+from .workloads import cp_block_tables as wl_cp_tables
 
 PRIOR_FILL_TOKENS = 1 << 16  # tokens uploaded per prior-fill batch
 
@@ -30,18 +31,28 @@ def _t(a: np.ndarray, device, dtype=None):
 
 class DeviceWorkload:
     def __init__(self, w: Workload, device="cuda", background: str = "nan", fill_prior: bool = True,
-                 sliding_window: int = 0):
+                 sliding_window: int = 0, cp_world: int = 1, cp_rank: int = 0, cp_interleave: int = 1):
         self.w = w
         self.window = int(sliding_window)   # decode's default sliding window (0: full attention)
+        # decode context parallelism: this object is rank cp_rank of cp_world, holding only its
+        # share of every request's tokens in a cache of its own (block_size == kernel block size)
+        self.cp = (int(cp_world), int(cp_rank), int(cp_interleave))
+        if self.cp[0] > 1 and w.block_size != w.kernel_block_size:
+            raise ValueError("context-parallel staging needs block_size == kernel_block_size")
         self.device = torch.device(device)
         dev = self.device
         self.tdtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-        kshape = (w.total_kernel_blocks, w.kernel_block_size, w.num_kv_heads, w.head_dim)
+        if self.cp[0] > 1:
+            table, total = wl_cp_tables(w, self.cp[0])[self.cp[1]]
+        else:
+            table, total = w.block_table, w.total_kernel_blocks
+        kshape = (total, w.kernel_block_size, w.num_kv_heads, w.head_dim)
         fill = float("nan") if background == "nan" else 0.0
         self.k_cache = torch.full(kshape, fill, dtype=self.tdtype, device=dev)
         self.v_cache = torch.full(kshape, fill, dtype=self.tdtype, device=dev)
-        self.mgr_table = _t(w.block_table, dev)
-        self.kernel_table = torch.empty((w.num_rows, w.width * w.blocks_per_kv_block), dtype=torch.int32, device=dev)
+        self.mgr_table = _t(table, dev)
+        self.kernel_table = torch.empty((w.num_rows, table.shape[1] * w.blocks_per_kv_block), dtype=torch.int32,
+                                        device=dev)
         bkv.bkv_map_to_kernel_blocks(self.mgr_table, w.block_size, w.kernel_block_size, self.kernel_table)
         self.context_lens = _t(w.context_lens, dev)
         self.max_context_len = int(w.context_lens.max()) if w.num_rows else 0
@@ -56,6 +67,7 @@ class DeviceWorkload:
         if w.has_decode:
             self.q = _t(w.q(), dev, self.tdtype if w.dtype == "bf16" else None)
             self.out = torch.empty_like(self.q)
+            self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=dev)
             self.workspace = bkv.alloc_workspace(w.num_rows, w.q_len, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                                  w.kernel_block_size, self.max_context_len, device=dev)
         if fill_prior:
@@ -89,8 +101,7 @@ class DeviceWorkload:
         cast = self.tdtype if w.dtype == "bf16" else None
         kt, vt = _t(k, dev, cast), _t(v, dev, cast)
         slots = torch.empty(len(pos), dtype=torch.int64, device=dev)
-        bkv.bkv_compute_slot_mapping(self.kernel_table, _t(req, dev), _t(pos, dev), w.kernel_block_size, slots,
-                                     err_count=self.err_count)
+        self._slots(self.kernel_table, _t(req, dev), _t(pos, dev), slots)
         bkv.bkv_cache_write(kt, vt, slots, self.k_cache, self.v_cache, err_count=self.err_count)
 
     # -- the hot path ---------------------------------------------------------
@@ -99,11 +110,18 @@ class DeviceWorkload:
         bkv.bkv_map_to_kernel_blocks(self.mgr_table, w.block_size, w.kernel_block_size, self.kernel_table,
                                      stream=stream)
 
+    def _slots(self, table, req, pos, slots, num_tokens=None, stream=None):
+        w = self.w
+        if self.cp[0] > 1:
+            bkv.bkv_compute_slot_mapping_cp(table, req, pos, w.kernel_block_size, slots, *self.cp,
+                                            num_tokens=num_tokens, err_count=self.err_count, stream=stream)
+        else:
+            bkv.bkv_compute_slot_mapping(table, req, pos, w.kernel_block_size, slots, num_tokens=num_tokens,
+                                         err_count=self.err_count, stream=stream)
+
     def write_step(self, stream=None):
         w = self.w
-        bkv.bkv_compute_slot_mapping(self.kernel_table, self.req_indices, self.positions, w.kernel_block_size,
-                                     self.slot_mapping, num_tokens=w.num_tokens, err_count=self.err_count,
-                                     stream=stream)
+        self._slots(self.kernel_table, self.req_indices, self.positions, self.slot_mapping, w.num_tokens, stream)
         bkv.bkv_cache_write(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
                             num_tokens=w.num_tokens, err_count=self.err_count, stream=stream)
 
@@ -111,6 +129,11 @@ class DeviceWorkload:
         out = self.out if out is None else out
         sliding_window = self.window if sliding_window is None else sliding_window
         table = self.kernel_table if table is None else table
+        if self.cp[0] > 1:
+            bkv.bkv_paged_decode_cp(self.q, self.k_cache, self.v_cache, table, self.context_lens,
+                                    self.max_context_len, out, self.lse, self.workspace, *self.cp, mask_mode=mask_mode,
+                                    err_count=self.err_count, stream=stream)
+            return out
         bkv.bkv_paged_decode(self.q, self.k_cache, self.v_cache, table, self.context_lens, self.max_context_len,
                              out, self.workspace, mask_mode=mask_mode, err_count=self.err_count, stream=stream,
                              sliding_window=sliding_window)
@@ -132,11 +155,16 @@ class DeviceWorkload:
     # -- byte accounting (algorithmic, token granularity) ---------------------
     def decode_kv_bytes(self) -> int:
         """K and V bytes the decode must read: cache_len rows per request and KV head (with a
-        sliding window W, only the rows from the first query's window start, L - q_len - W + 1)."""
+        sliding window W, only the rows from the first query's window start, L - q_len - W + 1; with
+        context parallelism, only the rows this rank holds)."""
         w = self.w
         L = w.context_lens.astype(np.int64)
         if self.window > 0:
             L = L - np.maximum(0, L - w.q_len - self.window + 1)
+        if self.cp[0] > 1:
+            W, k, inter = self.cp
+            cyc = inter * W
+            L = (L // cyc) * inter + np.clip(L % cyc - k * inter, 0, inter)
         return int(L.sum()) * 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
 
     def write_bytes(self) -> int:
