@@ -17,6 +17,9 @@ Functions and the passages they follow (page titles and sections):
   Batching with Block KV", Cache Masking (mask_cache, mask_active).
 * :func:`decode_bucket` -- "Decode Context-Length Bucketing", Design /
   Per-step bucket selection (used to report bytes only).
+* :func:`paged_attention_ragged` -- the decode's attention over a mixed
+  step with per-request query counts ("Padding and Batching with Block KV",
+  Batching with Block KV; reading R15 of the C source).
 * :func:`compute_slot_mapping_cp`, :func:`paged_decode_cp`,
   :func:`merge_attn_states` -- "ブロック表" 設計動機 (DCP / PCP interleave:
   a rank writes real slots only for the tokens it owns); the ownership,
@@ -83,6 +86,9 @@ def _load():
             lib.orc_paged_decode_cp_request.argtypes = [i32, vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32,
                                                         i32, i64, dbl, ctypes.c_int, i32, i32, i32, i32,
                                                         ctypes.c_int, vp, vp]
+            lib.orc_paged_attention_ragged.restype = i64
+            lib.orc_paged_attention_ragged.argtypes = [vp, vp, vp, vp, vp, i64, i32, vp, i32, i64, i32, i32, i32, i32,
+                                                       i64, dbl, ctypes.c_int, ctypes.c_int, vp]
             lib.orc_merge_attn_states.restype = ctypes.c_int
             lib.orc_merge_attn_states.argtypes = [vp, vp, i32, i64, i32, vp, vp]
             lib.orc_decode_bucket.restype = i64
@@ -258,6 +264,33 @@ def paged_decode_cp(q, k_cache, v_cache, block_table, context_lens, cp_world=1, 
         err += e
     del keep
     return out, lse, int(err)
+
+
+def paged_attention_ragged(q, query_start_loc, k_cache, v_cache, block_table, context_lens, scale=None,
+                           mask_mode=0):
+    """fp64 attention of a mixed step (reading R15): q packed (num_tokens, H_q, D), request r's tokens at
+    [query_start_loc[r], query_start_loc[r+1]) ending at position context_lens[r] - 1.  Returns (out, errors)."""
+    qa = np.ascontiguousarray(q)
+    kc = np.ascontiguousarray(k_cache)
+    vc = np.ascontiguousarray(v_cache)
+    if not (qa.dtype == kc.dtype == vc.dtype):
+        raise TypeError("mixed dtypes")
+    dt = _dtype_code(kc)
+    qsl = _c(query_start_loc, np.int32)
+    bt = _c(block_table, np.int32)
+    cl = _c(context_lens, np.int32)
+    nt, hq, d = qa.shape
+    tb, bs, hkv, d2 = kc.shape
+    if d2 != d or len(qsl) != len(cl) + 1:
+        raise ValueError("shape mismatch")
+    sc = (1.0 / np.sqrt(d)) if scale is None else float(scale)
+    out = np.zeros((nt, hq, d), np.float64)
+    err = _load().orc_paged_attention_ragged(_ptr(qa), _ptr(qsl), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                                             bt.shape[1], _ptr(cl), len(cl), nt, hq, hkv, d, bs, tb, sc,
+                                             int(mask_mode), dt, _ptr(out))
+    if err < 0:
+        raise ValueError("invalid paged_attention_ragged arguments")
+    return out, int(err)
 
 
 def merge_attn_states(outs, lses):

@@ -46,6 +46,13 @@
  *       row) outputs 0.
  *   R10 a key whose block-table entry is <= 0 is masked out, not read.
  *   R12 a position past the table width gives slot -1 and counts an error.
+ *   R15 a mixed (ragged) step: request r has q_len_r = query_start_loc[r+1]
+ *       - query_start_loc[r] query tokens, packed token-major in q and out
+ *       ([num_tokens][H_q][D]); token i of request r sits at position
+ *       L_r - q_len_r + i ([P1 Batching with Block KV]: a request's tokens
+ *       are consecutive positions ending at its cache length, as in the
+ *       multi-token decode example) and sees keys as R7 with that position;
+ *       the decode is the case of one q_len for every request.
  *   R13 sliding window W > 0 ([P4 Block-table head-trim vs. SWA tail-trim;
  *       [P3] Layer-specific cache specification: an SWA layer keeps only
  *       the recent tokens within the window): query t at position p_t =
@@ -453,6 +460,110 @@ int64_t orc_paged_decode_cp_request(int32_t r, const void *q, const void *k_cach
     free(readable);
     free(gpos);
     free(s);
+    return errors;
+}
+
+/*
+ * O4 over a mixed step (R15): every request with its own number of query
+ * tokens, packed token-major.  The visible keys, the scores and the softmax
+ * are those of O4 for each token at its own position.  Returns the number of
+ * bad table entries met (once per request and block), or -1.
+ */
+int64_t orc_paged_attention_ragged(const void *q, const int32_t *query_start_loc,
+                                   const void *k_cache, const void *v_cache,
+                                   const int32_t *block_table, int64_t bt_stride,
+                                   int32_t bt_cols, const int32_t *context_lens,
+                                   int32_t num_reqs, int64_t num_tokens, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   int64_t total_blocks, double scale, int mask_mode,
+                                   int dtype, double *out)
+{
+    if (orc_elem_bytes(dtype) == 0 || num_reqs < 0 || num_tokens < 0 || num_q_heads <= 0 ||
+        num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || bt_cols < 0 || bt_stride < bt_cols ||
+        (mask_mode != 0 && mask_mode != 1))
+        return -1;
+    const int64_t D = head_dim;
+    const int64_t G = num_q_heads / num_kv_heads;
+    for (int64_t i = 0; i < num_tokens * num_q_heads * D; ++i)
+        out[i] = 0.0;
+    int64_t errors = 0;
+    for (int32_t r = 0; r < num_reqs; ++r) {
+        const int64_t t0 = query_start_loc[r], t1 = query_start_loc[r + 1];
+        if (t0 < 0 || t1 < t0 || t1 > num_tokens)
+            return -1;
+        const int64_t ql = t1 - t0;
+        const int64_t L = context_lens[r] > 0 ? context_lens[r] : 0;
+        if (ql == 0 || L == 0)
+            continue;
+        /* which keys may be read: j < L with a real block */
+        unsigned char *readable = (unsigned char *)malloc((size_t)L);
+        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        if (!readable || !s) {
+            free(readable);
+            free(s);
+            return -1;
+        }
+        for (int64_t j = 0; j < L; ++j) {
+            readable[j] = 0;
+            int64_t lb = j / block_size;
+            if (lb >= bt_cols) {
+                if (j % block_size == 0)
+                    errors += 1;
+                continue;
+            }
+            int64_t b = block_table[(int64_t)r * bt_stride + lb];
+            if (b <= 0)
+                continue;
+            if (b >= total_blocks) {
+                if (j % block_size == 0)
+                    errors += 1;
+                continue;
+            }
+            readable[j] = 1;
+        }
+        for (int64_t i = 0; i < ql; ++i) {
+            const int64_t p = L - ql + i; /* this token's position */
+            const int64_t last_visible = (mask_mode == 0) ? p : L - 1;
+            for (int64_t h = 0; h < num_q_heads; ++h) {
+                const int64_t g = h / G;
+                const int64_t qoff = ((t0 + i) * num_q_heads + h) * D;
+                double *o = out + qoff;
+                double m = -INFINITY;
+                int any = 0;
+                for (int64_t j = 0; j < L && j <= last_visible; ++j) {
+                    if (!readable[j])
+                        continue;
+                    int64_t b = block_table[(int64_t)r * bt_stride + j / block_size];
+                    int64_t krow = ((b * block_size + j % block_size) * num_kv_heads + g) * D;
+                    double dot = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        dot += orc_load(q, qoff + d, dtype) * orc_load(k_cache, krow + d, dtype);
+                    s[j] = scale * dot;
+                    if (!any || s[j] > m)
+                        m = s[j];
+                    any = 1;
+                }
+                if (!any)
+                    continue;
+                double denom = 0.0;
+                for (int64_t j = 0; j < L && j <= last_visible; ++j) {
+                    if (!readable[j])
+                        continue;
+                    int64_t b = block_table[(int64_t)r * bt_stride + j / block_size];
+                    int64_t vrow = ((b * block_size + j % block_size) * num_kv_heads + g) * D;
+                    double w = exp(s[j] - m);
+                    denom += w;
+                    for (int64_t d = 0; d < D; ++d)
+                        o[d] += w * orc_load(v_cache, vrow + d, dtype);
+                }
+                for (int64_t d = 0; d < D; ++d)
+                    o[d] /= denom;
+            }
+        }
+        free(readable);
+        free(s);
+    }
     return errors;
 }
 

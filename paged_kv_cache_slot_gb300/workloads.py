@@ -154,6 +154,16 @@ class Workload:
         x = rng.standard_normal((self.num_rows, self.q_len, self.num_q_heads, self.head_dim), dtype=np.float32)
         return self.cast(x * np.float32(self.qk_scale))
 
+    def query_start_loc(self) -> np.ndarray:
+        """int32 (num_rows + 1,): request r's query tokens are [qsl[r], qsl[r+1]) of the packed step."""
+        return np.concatenate([[0], np.cumsum(self.new_tokens)]).astype(np.int32)
+
+    def q_tokens(self) -> np.ndarray:
+        """Packed queries of this step's tokens (num_tokens, H_q, D), one draw per token."""
+        rng = np.random.default_rng([self.seed, 5])
+        x = rng.standard_normal((self.num_tokens, self.num_q_heads, self.head_dim), dtype=np.float32)
+        return self.cast(x * np.float32(self.qk_scale))
+
     # ---- token lists ----
     def step_tokens(self):
         """This step's tokens: req_indices (int32), positions (int64), both max_num_tokens long.
