@@ -232,6 +232,42 @@ int bkv_paged_decode_merge(const void *q, const void *k_cache, const void *v_cac
                            bkv_stream_t stream);
 
 /*
+ * bkv_paged_attention_ragged
+ *   Paged attention over a mixed (ragged) step: every request with its own
+ *   number of query tokens -- decode tokens, speculative drafts, chunked
+ *   prefill -- in one packed batch ("Padding and Batching with Block KV",
+ *   Batching with Block KV: a request's new tokens are consecutive
+ *   positions ending at its cache length; Cache Masking for mask_active).
+ *   Request r's query tokens are rows [query_start_loc[r],
+ *   query_start_loc[r+1]) of q and out; with q_len_r their count and L =
+ *   context_lens[r] (INCLUDING those tokens), token i sits at position
+ *   L - q_len_r + i and sees key j iff j < L, j <= its position
+ *   (BKV_MASK_CAUSAL) and its block entry is a real block, exactly as
+ *   bkv_paged_decode does for one q_len; out row = softmax-weighted V, 0 if
+ *   it sees no key.
+ *   q, out    [num_tokens, num_q_heads, head_dim] of `dtype` (token-major).
+ *   query_start_loc int32 [num_reqs + 1], non-decreasing, last <= num_tokens.
+ *   max_query_len / max_context_len  host bounds on q_len_r / context_lens
+ *             (size the grid).  A request with more query tokens than
+ *             max_query_len (or a malformed query_start_loc) is skipped, its
+ *             rows left as they were, and counted; a longer context is
+ *             clamped to max_context_len and counted.
+ *   Other arguments as bkv_paged_decode.  No workspace: bf16 with head_dim
+ *   128 and at most 128 query heads per KV head runs a tcgen05 kernel with
+ *   128-row query tiles; anything else a CUDA-core kernel.
+ *   INVALID_ARG: bad sizes or mask_mode, null pointers, grid too large.
+ *   UNSUPPORTED: dtype not BKV_BF16 / BKV_F32, head_dim > 256 or odd.
+ */
+int bkv_paged_attention_ragged(const void *q, const int32_t *query_start_loc, const void *k_cache,
+                               const void *v_cache, const int32_t *block_table, int64_t bt_stride,
+                               int32_t bt_cols, const int32_t *context_lens, int32_t max_context_len,
+                               int32_t max_query_len, int32_t num_reqs, int64_t num_tokens,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int64_t total_blocks, float softmax_scale,
+                               int mask_mode, int dtype, void *out, int32_t *err_count,
+                               bkv_stream_t stream);
+
+/*
  * bkv_compute_slot_mapping_cp
  *   bkv_compute_slot_mapping under decode context parallelism ("ブロック表"
  *   設計動機: with DCP the slot kernel writes the real slot only for the

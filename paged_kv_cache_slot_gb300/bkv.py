@@ -64,6 +64,9 @@ def load() -> ctypes.CDLL:
         lib.bkv_paged_decode_cp.restype = cint
         lib.bkv_paged_decode_cp.argtypes = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i32, i64, f32,
                                             cint, i32, i32, i32, cint, vp, vp, vp, sz, vp, vp]
+        lib.bkv_paged_attention_ragged.restype = cint
+        lib.bkv_paged_attention_ragged.argtypes = [vp, vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i64, i32, i32,
+                                                   i32, i32, i64, f32, cint, cint, vp, vp, vp]
         lib.bkv_merge_attn_states.restype = cint
         lib.bkv_merge_attn_states.argtypes = [vp, vp, i32, i64, i32, cint, vp, vp, vp]
         lib.bkv_map_to_kernel_blocks.restype = cint
@@ -262,6 +265,33 @@ def bkv_paged_decode_cp(q, k_cache, v_cache, block_table, context_lens, max_cont
         _dev(out, "out"), _opt(lse, "lse", torch.float32), ws_ptr, ws_bytes, _opt(err_count, "err_count", torch.int32),
         _stream(stream)))
     return out, lse
+
+
+def bkv_paged_attention_ragged(q, query_start_loc, k_cache, v_cache, block_table, context_lens, max_context_len,
+                               max_query_len, out, softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None,
+                               stream=None):
+    """Attention over a mixed step: q / out packed (num_tokens, H_q, D), request r's tokens at
+    [query_start_loc[r], query_start_loc[r+1]) (see include/bkv.h)."""
+    if q.dim() != 3 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("q/out must be (num_tokens, H_q, D); caches (total_blocks, bs, H_kv, D)")
+    nt, hq, d = q.shape
+    tb, bs, hkv, d2 = k_cache.shape
+    nr = query_start_loc.numel() - 1
+    if d2 != d or nr < 0 or context_lens.numel() < nr:
+        raise ValueError("head_dim / query_start_loc / context_lens mismatch")
+    if block_table.dim() != 2 or block_table.shape[0] < nr or block_table.stride(1) != 1:
+        raise ValueError("block_table must be (>= num_reqs, cols) with unit column stride")
+    dt = _kv_dtype(q)
+    for t, nm in ((k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{nm} dtype differs from q")
+    _check("bkv_paged_attention_ragged", load().bkv_paged_attention_ragged(
+        _dev(q, "q"), _dev(query_start_loc, "query_start_loc", torch.int32), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(block_table, "block_table", torch.int32, contiguous=False),
+        block_table.stride(0), block_table.shape[1], _dev(context_lens, "context_lens", torch.int32),
+        int(max_context_len), int(max_query_len), nr, nt, hq, hkv, d, bs, tb, float(softmax_scale), int(mask_mode),
+        dt, _dev(out, "out"), _opt(err_count, "err_count", torch.int32), _stream(stream)))
+    return out
 
 
 def bkv_merge_attn_states(outs, lses, out, lse_out=None, stream=None):
