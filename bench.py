@@ -466,6 +466,98 @@ def run_bkv(args):
     print(json.dumps(line), flush=True)
 
 
+def run_ragged(args):
+    """--attention ragged: paged attention over the mixed ragged_step batch (48 decode tokens and 16
+    prefill chunks of 64..1024 tokens over prior contexts of 0..2048, H_q 32, H_kv 8, D 128, kernel
+    bs 16, bf16), one bkv_paged_attention_ragged call per step, CUDA graph, L2 flushed before each
+    step.  Prefill dominates, so the roofline is the tensor one: algorithmic FLOPs = 4 * D per visible
+    (query head, key) pair."""
+    import torch
+
+    from paged_kv_cache_slot_gb300 import bkv
+    from paged_kv_cache_slot_gb300 import workloads as wl
+    from paged_kv_cache_slot_gb300.build import build
+    from paged_kv_cache_slot_gb300.staging import DeviceWorkload
+
+    dist = _dist()
+    rank = dist.get_rank() if dist else 0
+    world = dist.get_world_size() if dist else 1
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if rank == 0:
+        build()
+    if dist:
+        dist.barrier()
+    bkv.load()
+    w = wl.make("ragged_step")
+    dev = f"cuda:{local}"
+    dw = DeviceWorkload(w, device=dev)
+    dw.write_step()
+    q = torch.from_numpy(w.q_tokens()).view(torch.bfloat16).to(dev)
+    out = torch.empty_like(q)
+    qsl = torch.from_numpy(w.query_start_loc()).to(dev)
+    mq = int(w.new_tokens.max())
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+
+    def step():
+        bkv.bkv_paged_attention_ragged(q, qsl, dw.k_cache, dw.v_cache, dw.kernel_table, dw.context_lens,
+                                       dw.max_context_len, mq, out, err_count=err, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    torch.cuda.synchronize()
+    body = step
+    if not args.eager:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        body = g.replay
+    if dist:
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        times = _time_steps(torch, body, args.steps, flush, stream)
+    ms = sum(times) / len(times)
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    assert int(err.item()) == 0
+    if rank != 0:
+        return
+    L = w.context_lens.astype(np.int64)
+    n = w.new_tokens.astype(np.int64)
+    # token i of request r sees L - n + i + 1 keys: sum over i = n (L - n) + n (n + 1) / 2
+    pairs = int((n * (L - n) + n * (n + 1) // 2).sum()) * w.num_q_heads
+    flops = 4 * w.head_dim * pairs
+    kv_bytes = int(L[n > 0].sum()) * 2 * w.num_kv_heads * w.head_dim * 2
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        peaks = json.load(f)
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": "mixed-step paged attention TFLOP/s (ragged_step)", "value": world * achieved, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"ragged_step: {w.num_tokens} query tokens of 64 requests (48 x 1, 16 x 64..1024), "
+                               "prior 0..2048, H_q 32, H_kv 8, D 128, bs 16, bf16, causal",
+                   "attended_pairs": pairs, "flops_per_step": flops, "kv_bytes_once": kv_bytes,
+                   "l2": "flushed before every timed step (write 2x L2, read it back)",
+                   "cuda_graph": not args.eager},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "bkv_paged_attention_ragged (tcgen05 prefill kernel)",
+                     "peak_kind": "measured bf16 dense (burst)",
+                     "kv_GBps_once": kv_bytes / (ms / 1e3) / 1e9},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -479,6 +571,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD,
                     help="seeded workload to time (default: the Llama-3-8B-shaped decode batch)")
     ap.add_argument("--sliding-window", type=int, default=0, help="decode with this sliding window (0: none)")
+    ap.add_argument("--attention", default="decode", choices=["decode", "ragged"],
+                    help="decode: the headline decode step; ragged: attention over the mixed ragged_step batch")
     ap.add_argument("--cp-world", type=int, default=1,
                     help="time rank 0 of a decode-context-parallel split over this many ranks (1: none)")
     ap.add_argument("--cp-interleave", type=int, default=1, help="context-parallel interleave size")
@@ -486,7 +580,7 @@ def main():
     if args.impl == "reference":
         run_reference(args)
     else:
-        run_bkv(args)
+        run_ragged(args) if args.attention == "ragged" else run_bkv(args)
     d = _dist()
     if d:
         d.destroy_process_group()

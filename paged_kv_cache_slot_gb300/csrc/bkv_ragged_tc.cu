@@ -18,9 +18,14 @@
 //   K-major from the TMA tiles) into one of two TMEM buffers; the softmax
 //   reads its row in 32-column chunks (max pass, then exponentials), keeps
 //   the running max and sum, and writes P (bf16, K-major, 128-byte swizzle).
+//   The running max is a lazy reference: it moves only when a tile's max
+//   passes it by more than 8 (log2 units), so weights stay below 2^8 and O
+//   is rescaled only on those tiles; a tile every key of which is visible
+//   to all rows of a warp skips the per-key mask tests.
 // * O += P V (N = head_dim, V read MN-major straight from the TMA tile)
-//   accumulates in TMEM across the unit's key tiles; when a row's max rises
-//   the softmax rescales its O row in TMEM (only warps with such a row do).
+//   accumulates in TMEM across the unit's key tiles; when a row's reference
+//   max moves the softmax rescales its O row in TMEM (only warps with such a
+//   row do).
 // * Keys are gathered through the block table with one TMA load per block
 //   segment and head_dim half; null and out-of-range entries are not loaded,
 //   positions past the causal bound of the tile's last token are not loaded,
@@ -78,6 +83,31 @@ struct Unit {
 };
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+constexpr float kSlack = 8.f;   // lazy-rescale slack of the running max (log2 units)
+
+// Max and sum of 32 values as trees (depth 5, not a 32-long chain).
+__device__ __forceinline__ float tree_max32(const float (&v)[32]) {
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] = fmaxf(t[2 * i], t[2 * i + 1]);
+    return t[0];
+}
+
+__device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = v[2 * i] + v[2 * i + 1];
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] = t[2 * i] + t[2 * i + 1];
+    return t[0];
+}
 
 // Unit u of the launch (pre[] in shared memory holds the units before each
 // request; T tokens per tile).
@@ -211,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = a.G;
     const int nseg = kTile / seg_rows;
     const int seg_shift = 31 - __clz(seg_rows);
+    const uint32_t all_seg = nseg >= 32 ? 0xffffffffu : ((1u << nseg) - 1u);   // every segment loaded
 
     if (warp == 0 || warp == kWarpV) {
         // ================= TMA producers (warp 0: Q and K, last warp: V) =================
@@ -384,23 +415,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t mword = mask_words[j & 7];
                 const int32_t k0 = kt * kTile;
-                // key k of the tile counts for this row: its segment loaded, k0 + k < L, k0 + k <= lastv
-                auto seen = [&](int k) {
-                    return valid && ((mword >> (k >> seg_shift)) & 1u) && k0 + k < x.L && k0 + k <= lastv;
-                };
-                float mt = -INFINITY;
+                // This row sees keys k < lim of the tile (cache end and causal bound),
+                // and only those of loaded segments; invalid rows see none.
+                int32_t lim = min(x.L, lastv + 1) - k0;
+                lim = valid ? max(0, min(kTile, lim)) : 0;
+                const bool segs = mword == all_seg;   // no null entry in the tile
+                auto seen = [&](int k) { return k < lim && (segs || ((mword >> (k >> seg_shift)) & 1u)); };
+                // Every key of the tile visible to every row of this warp (the common
+                // case inside a long prefix): no per-key tests.
+                const bool full = __all_sync(0xffffffffu, lim == kTile) && segs;
+                // pass 1: the tile max of the raw scores (the scale is positive), as a tree
+                float mraw = -INFINITY;
                 if (warp_valid) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float sv[32];
                         tmem_ld32(tmem + lane_base + 128u * b + 32u * c, sv);
+                        if (!full) {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            if (seen(32 * c + k)) mt = fmaxf(mt, sv[k] * a.scale_log2);
+                            for (int k = 0; k < 32; ++k) sv[k] = seen(32 * c + k) ? sv[k] : -INFINITY;
+                        }
+                        mraw = fmaxf(mraw, tree_max32(sv));
                     }
                 }
-                const float mn = fmaxf(m, mt);
-                const float corr = (mn == -INFINITY) ? 1.f : fast_exp2(m - mn);
+                const float mt = mraw * a.scale_log2;
+                // Lazy rescale: the reference max m moves (and O, l are rescaled) only
+                // when the tile max passes it by more than kSlack, so weights stay
+                // below 2^kSlack and most tiles leave O alone.
+                const bool bump = mt > m + kSlack;
+                const float mn = bump ? mt : m;
+                const float corr = bump ? fast_exp2(m - mn) : 1.f;
                 // the previous tile's P.V must be done before P and O are touched
                 if (kt > 0) {
                     if (!mbar_wait_warp(bar_ofull, (uint32_t)((j - 1) & 1), abort_flag)) {
@@ -420,20 +464,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (warp_valid) {
+                    // pass 2: weights 2^(s * scale - mn) (0 where masked), their sum, P in bf16
+                    const float nb = -mn;
                     float psum = 0.f;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float sv[32];
                         tmem_ld32(tmem + lane_base + 128u * b + 32u * c, sv);
+                        if (full) {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) sv[k] = fast_exp2(fmaf(sv[k], a.scale_log2, nb));
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                // computed for every key, then selected: no branch per key
+                                const float e = fast_exp2(fmaf(sv[k], a.scale_log2, nb));
+                                sv[k] = seen(32 * c + k) ? e : 0.f;
+                            }
+                        }
                         uint32_t pk[16];
 #pragma unroll
                         for (int k = 0; k < 32; k += 2) {
-                            const float p0 = seen(32 * c + k) ? fast_exp2(sv[k] * a.scale_log2 - mn) : 0.f;
-                            const float p1 = seen(32 * c + k + 1) ? fast_exp2(sv[k + 1] * a.scale_log2 - mn) : 0.f;
-                            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                            psum += __low2float(pb) + __high2float(pb);
+                            const __nv_bfloat162 pb = __floats2bfloat162_rn(sv[k], sv[k + 1]);
                             pk[k >> 1] = *reinterpret_cast<const uint32_t *>(&pb);
                         }
+                        psum += tree_sum32(sv);
                         // keys 32c .. 32c + 31: half c / 2, 16-byte chunks 4 (c % 2) .. + 3
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4)
