@@ -24,6 +24,11 @@ Functions and the passages they follow (page titles and sections):
   :func:`merge_attn_states` -- "ブロック表" 設計動機 (DCP / PCP interleave:
   a rank writes real slots only for the tokens it owns); the ownership,
   local-position and merge readings are R14 of the C source.
+* :func:`e4m3_encode`, :func:`e4m3_decode`, :func:`cache_write_fp8`,
+  :func:`paged_decode_fp8` -- the FP8 (E4M3) KV cache: "Padding and Batching
+  with Block KV", Block ID 0 vs. Sentinel -1 names a non-FP8 pathway, nothing
+  more; the format and per-tensor scale convention are reading R16 of the C
+  source.
 
 Every function is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_*.py`` against worked values printed on the pages, brute
@@ -44,6 +49,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 DT_BF16 = 0
 DT_F32 = 1
+DT_E4M3 = 2
 
 _lib = None
 _lock = threading.Lock()
@@ -91,6 +97,17 @@ def _load():
                                                        i64, dbl, ctypes.c_int, ctypes.c_int, vp]
             lib.orc_merge_attn_states.restype = ctypes.c_int
             lib.orc_merge_attn_states.argtypes = [vp, vp, i32, i64, i32, vp, vp]
+            lib.orc_e4m3_decode.restype = dbl
+            lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_encode_array.restype = None
+            lib.orc_e4m3_encode_array.argtypes = [vp, i64, vp]
+            lib.orc_cache_write_fp8.restype = i64
+            lib.orc_cache_write_fp8.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int,
+                                                ctypes.c_float, ctypes.c_float]
+            lib.orc_paged_decode_fp8_request.restype = i64
+            lib.orc_paged_decode_fp8_request.argtypes = [i32, vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32,
+                                                         i32, i64, dbl, dbl, dbl, ctypes.c_int, i32, ctypes.c_int,
+                                                         vp]
             lib.orc_decode_bucket.restype = i64
             lib.orc_decode_bucket.argtypes = [vp, i64, i64, vp, i64, i64]
             _lib = lib
@@ -305,6 +322,84 @@ def merge_attn_states(outs, lses):
     if _load().orc_merge_attn_states(_ptr(o), _ptr(l), parts, rows, d, _ptr(out), _ptr(lse)) != 0:
         raise ValueError("invalid merge arguments")
     return out, lse
+
+
+def e4m3_decode(codes):
+    """float64 values of E4M3 codes (uint8 array; NaN for 0x7F / 0xFF), reading R16."""
+    c = np.asarray(codes, np.uint8)
+    lib = _load()
+    table = np.array([lib.orc_e4m3_decode(i) for i in range(256)], np.float64)
+    return table[c]
+
+
+def e4m3_encode(x):
+    """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating at 448, NaN -> 0x7F (R16)."""
+    xa = np.ascontiguousarray(np.asarray(x, np.float32))
+    out = np.empty(xa.shape, np.uint8)
+    _load().orc_e4m3_encode_array(_ptr(xa), xa.size, _ptr(out))
+    return out
+
+
+def cache_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, num_tokens=None,
+                    inplace=False):
+    """Scatter bf16 (uint16 bits) / float32 rows into E4M3 caches (uint8, (total_blocks, bs, H_kv, D)), each
+    element stored as the code of float32(x) / float32(scale) (reading R16).  Returns (k_cache, v_cache,
+    errors)."""
+    if inplace:
+        if not (k_cache.flags.c_contiguous and v_cache.flags.c_contiguous):
+            raise ValueError("in-place cache_write_fp8 needs C-contiguous caches")
+        kc, vc = k_cache, v_cache
+    else:
+        kc = np.array(k_cache, copy=True, order="C")
+        vc = np.array(v_cache, copy=True, order="C")
+    if kc.dtype != np.uint8 or vc.dtype != np.uint8:
+        raise TypeError("FP8 caches are uint8 codes")
+    kn = np.ascontiguousarray(k_new)
+    vn = np.ascontiguousarray(v_new)
+    if kn.dtype != vn.dtype:
+        raise TypeError("mixed dtypes")
+    dt = _dtype_code(kn)
+    sl = _c(slot_mapping, np.int64)
+    n = kn.shape[0] if num_tokens is None else int(num_tokens)
+    tb, bs, hkv, d = kc.shape
+    err = _load().orc_cache_write_fp8(_ptr(kn), _ptr(vn), n, hkv * d, _ptr(sl), _ptr(kc), _ptr(vc), tb, bs, hkv,
+                                      d, dt, float(k_scale), float(v_scale))
+    if err == -2:
+        raise ValueError("duplicate non-negative slot ids")
+    if err < 0:
+        raise ValueError("invalid cache_write_fp8 arguments")
+    return kc, vc, int(err)
+
+
+def paged_decode_fp8(q, k_cache, v_cache, block_table, context_lens, k_scale, v_scale, scale=None, mask_mode=0,
+                     sliding_window=0, rows=None):
+    """fp64 decode over E4M3 caches (uint8 codes; key value = code value * k_scale, value = * v_scale,
+    reading R16); q is bf16 bits (uint16) or float32.  ``rows`` limits the work to those requests (the others
+    stay 0).  Returns (out, errors)."""
+    qa = np.ascontiguousarray(q)
+    kc = np.ascontiguousarray(k_cache)
+    vc = np.ascontiguousarray(v_cache)
+    if kc.dtype != np.uint8 or vc.dtype != np.uint8:
+        raise TypeError("FP8 caches are uint8 codes")
+    dt = _dtype_code(qa)
+    bt = _c(block_table, np.int32)
+    cl = _c(context_lens, np.int32)
+    nr, ql, hq, d = qa.shape
+    tb, bs, hkv, d2 = kc.shape
+    if d2 != d:
+        raise ValueError("head_dim mismatch")
+    sc = (1.0 / np.sqrt(d)) if scale is None else float(scale)
+    out = np.zeros((nr, ql, hq, d), np.float64)
+    err = 0
+    lib = _load()
+    for r in (range(nr) if rows is None else rows):
+        e = lib.orc_paged_decode_fp8_request(int(r), _ptr(qa), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                                             bt.shape[1], _ptr(cl), nr, ql, hq, hkv, d, bs, tb, sc, float(k_scale),
+                                             float(v_scale), int(mask_mode), int(sliding_window), dt, _ptr(out))
+        if e < 0:
+            raise ValueError("invalid paged_decode_fp8 arguments")
+        err += e
+    return out, int(err)
 
 
 def decode_bucket(num_computed, num_speculative_tokens, buckets, max_model_len):

@@ -74,6 +74,16 @@
  *       visible keys (-inf if none); merging the ranks' (out, lse) by
  *       out = sum_k exp(lse_k - LSE) out_k, LSE = log sum_k exp(lse_k), is
  *       the attention over all keys.
+ *   R16 FP8 KV cache ([P1 Block ID 0 vs. Sentinel -1] names a non-FP8
+ *       pathway, so FP8 caches exist; nothing else about them is printed):
+ *       cache elements are OCP FP8 E4M3 ("fn": bias 7, no infinities, codes
+ *       0x7F / 0xFF are NaN, largest finite 448).  One scale per tensor,
+ *       k_scale for K and v_scale for V: a new element x is stored as the
+ *       code nearest to the fp32 quotient x / scale (IEEE division in
+ *       binary32), ties to the even code, magnitudes above 448 (and
+ *       infinities) saturated to 448, NaN to NaN; a stored code c stands for
+ *       the value e4m3(c) * scale.  Attention over an FP8 cache is O4 on
+ *       those values.
  */
 #include <math.h>
 #include <stdint.h>
@@ -82,6 +92,7 @@
 
 #define ORC_DT_BF16 0
 #define ORC_DT_F32 1
+#define ORC_DT_E4M3 2   /* cache elements only (R16) */
 
 /* ------------------------------------------------------------------ */
 /* element access                                                      */
@@ -102,6 +113,81 @@ static double orc_load(const void *base, int64_t idx, int dtype)
 static int orc_elem_bytes(int dtype)
 {
     return dtype == ORC_DT_BF16 ? 2 : (dtype == ORC_DT_F32 ? 4 : 0);
+}
+
+/* ------------------------------------------------------------------ */
+/* FP8 E4M3 (R16)                                                      */
+/* ------------------------------------------------------------------ */
+
+/*
+ * The value of code c: sign bit 7, exponent field e = bits 6..3 (bias 7),
+ * mantissa m = bits 2..0.  e = 0 is subnormal, m/8 * 2^-6; otherwise
+ * (1 + m/8) * 2^(e-7).  e = 15 with m = 7 is NaN (there is no infinity).
+ */
+double orc_e4m3_decode(uint8_t c)
+{
+    const int sign = c >> 7;
+    const int e = (c >> 3) & 15;
+    const int m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/*
+ * The code of the binary32 value x: NaN -> 0x7F; |x| >= 448 (infinities
+ * included) -> the largest finite magnitude, 0x7E, with x's sign;
+ * otherwise the finite code whose value is nearest to |x|, the even code on
+ * a tie (codes 0x00..0x7E increase with their value, so a binary search
+ * finds the two neighbours), with x's sign (so -0 and negative values that
+ * round to 0 give 0x80).
+ */
+uint8_t orc_e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    /* largest code lo with value(lo) <= a (value(0) = 0 <= a) */
+    int lo = 0, hi = 0x7E;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (orc_e4m3_decode((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    int c = lo;
+    if (lo < 0x7E) {
+        const double below = a - orc_e4m3_decode((uint8_t)lo);
+        const double above = orc_e4m3_decode((uint8_t)(lo + 1)) - a;
+        if (above < below || (above == below && ((lo + 1) % 2 == 0)))
+            c = lo + 1;
+    }
+    return (uint8_t)(sign | c);
+}
+
+/* Encode n binary32 values (a helper for the tests). */
+void orc_e4m3_encode_array(const float *x, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_encode(x[i]);
+}
+
+/* One cache element as a double: bf16 / fp32 exactly, an E4M3 code as its
+ * value times the tensor's scale (R16; the product is exact in binary64). */
+static double orc_load_kv(const void *base, int64_t idx, int dtype, double scale)
+{
+    if (dtype == ORC_DT_E4M3)
+        return orc_e4m3_decode(((const uint8_t *)base)[idx]) * scale;
+    return orc_load(base, idx, dtype);
 }
 
 /* ------------------------------------------------------------------ */
@@ -309,6 +395,62 @@ int64_t orc_cache_write(const void *k_new, const void *v_new,
     return errors;
 }
 
+/*
+ * O3 for an FP8 cache (R16): the same rows are written, each element of a
+ * new K row as orc_e4m3_encode((float)x / k_scale) and of a V row with
+ * v_scale, the quotient taken in binary32 (x is bf16 or fp32, widened
+ * exactly).  Same return values as orc_cache_write.
+ */
+int64_t orc_cache_write_fp8(const void *k_new, const void *v_new,
+                            int64_t num_tokens, int64_t new_token_stride,
+                            const int64_t *slot_mapping, uint8_t *k_cache,
+                            uint8_t *v_cache, int64_t total_blocks, int32_t block_size,
+                            int32_t num_kv_heads, int32_t head_dim, int src_dtype,
+                            float k_scale, float v_scale)
+{
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (orc_elem_bytes(src_dtype) == 0 || num_tokens < 0 || total_blocks < 0 ||
+        block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        new_token_stride < row || !(k_scale > 0.0f) || !(v_scale > 0.0f))
+        return -1;
+    int64_t capacity = total_blocks * block_size;
+    unsigned char *seen = (unsigned char *)calloc((size_t)(capacity > 0 ? capacity : 1), 1);
+    if (!seen)
+        return -1;
+    int64_t errors = 0;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0)
+            continue;
+        if (s >= capacity) {
+            errors += 1;
+            continue;
+        }
+        if (seen[s]) {
+            free(seen);
+            return -2;
+        }
+        seen[s] = 1;
+    }
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0 || s >= capacity)
+            continue;
+        int64_t dst = s * row;   /* block s / bs, offset s % bs */
+        int64_t src = i * new_token_stride;
+        for (int64_t e = 0; e < row; ++e) {
+            float k = (float)orc_load(k_new, src + e, src_dtype);
+            float v = (float)orc_load(v_new, src + e, src_dtype);
+            float kq = k / k_scale;
+            float vq = v / v_scale;
+            k_cache[dst + e] = orc_e4m3_encode(kq);
+            v_cache[dst + e] = orc_e4m3_encode(vq);
+        }
+    }
+    free(seen);
+    return errors;
+}
+
 /* ------------------------------------------------------------------ */
 /* O4: GQA paged decode attention (one request)                        */
 /* ------------------------------------------------------------------ */
@@ -340,17 +482,23 @@ int64_t orc_cache_write(const void *k_new, const void *v_new,
  * positions, masks and windows are global; j below is a local key index and
  * g its global position.
  */
-int64_t orc_paged_decode_cp_request(int32_t r, const void *q, const void *k_cache,
-                                    const void *v_cache, const int32_t *block_table,
-                                    int64_t bt_stride, int32_t bt_cols,
-                                    const int32_t *context_lens, int32_t num_reqs,
-                                    int32_t q_len, int32_t num_q_heads,
-                                    int32_t num_kv_heads, int32_t head_dim,
-                                    int32_t block_size, int64_t total_blocks,
-                                    double scale, int mask_mode, int32_t sliding_window,
-                                    int32_t cp_world, int32_t cp_rank, int32_t cp_interleave,
-                                    int dtype, double *out, double *lse)
+/* The decode of one request with the query type dtype and the cache
+ * element type kv_dtype (dtype itself, or ORC_DT_E4M3 with the tensors'
+ * scales, R16). */
+static int64_t orc_decode_core(int32_t r, const void *q, const void *k_cache,
+                               const void *v_cache, const int32_t *block_table,
+                               int64_t bt_stride, int32_t bt_cols,
+                               const int32_t *context_lens, int32_t num_reqs,
+                               int32_t q_len, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int64_t total_blocks,
+                               double scale, int mask_mode, int32_t sliding_window,
+                               int32_t cp_world, int32_t cp_rank, int32_t cp_interleave,
+                               int dtype, int kv_dtype, double k_scale, double v_scale,
+                               double *out, double *lse)
 {
+    if (kv_dtype != dtype && kv_dtype != ORC_DT_E4M3)
+        return -1;
     if (orc_elem_bytes(dtype) == 0 || r < 0 || r >= num_reqs || q_len <= 0 ||
         num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_q_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 ||
@@ -431,7 +579,7 @@ int64_t orc_paged_decode_cp_request(int32_t r, const void *q, const void *k_cach
                 int64_t krow = ((b * block_size + j % block_size) * num_kv_heads + g) * D;
                 double dot = 0.0;
                 for (int64_t d = 0; d < D; ++d)
-                    dot += orc_load(q, qoff + d, dtype) * orc_load(k_cache, krow + d, dtype);
+                    dot += orc_load(q, qoff + d, dtype) * orc_load_kv(k_cache, krow + d, kv_dtype, k_scale);
                 s[j] = scale * dot;
                 if (!any || s[j] > m)
                     m = s[j];
@@ -449,7 +597,7 @@ int64_t orc_paged_decode_cp_request(int32_t r, const void *q, const void *k_cach
                 double w = exp(s[j] - m);
                 denom += w;
                 for (int64_t d = 0; d < D; ++d)
-                    o[d] += w * orc_load(v_cache, vrow + d, dtype);
+                    o[d] += w * orc_load_kv(v_cache, vrow + d, kv_dtype, v_scale);
             }
             for (int64_t d = 0; d < D; ++d)
                 o[d] /= denom;
@@ -461,6 +609,48 @@ int64_t orc_paged_decode_cp_request(int32_t r, const void *q, const void *k_cach
     free(gpos);
     free(s);
     return errors;
+}
+
+int64_t orc_paged_decode_cp_request(int32_t r, const void *q, const void *k_cache,
+                                    const void *v_cache, const int32_t *block_table,
+                                    int64_t bt_stride, int32_t bt_cols,
+                                    const int32_t *context_lens, int32_t num_reqs,
+                                    int32_t q_len, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int64_t total_blocks,
+                                    double scale, int mask_mode, int32_t sliding_window,
+                                    int32_t cp_world, int32_t cp_rank, int32_t cp_interleave,
+                                    int dtype, double *out, double *lse)
+{
+    return orc_decode_core(r, q, k_cache, v_cache, block_table, bt_stride, bt_cols,
+                           context_lens, num_reqs, q_len, num_q_heads, num_kv_heads,
+                           head_dim, block_size, total_blocks, scale, mask_mode,
+                           sliding_window, cp_world, cp_rank, cp_interleave, dtype,
+                           dtype, 1.0, 1.0, out, lse);
+}
+
+/*
+ * O4 over an FP8 cache (R16), one request: the keys and values are the
+ * codes' values times k_scale / v_scale; q and out as orc_paged_decode_request.
+ */
+int64_t orc_paged_decode_fp8_request(int32_t r, const void *q, const uint8_t *k_cache,
+                                     const uint8_t *v_cache, const int32_t *block_table,
+                                     int64_t bt_stride, int32_t bt_cols,
+                                     const int32_t *context_lens, int32_t num_reqs,
+                                     int32_t q_len, int32_t num_q_heads,
+                                     int32_t num_kv_heads, int32_t head_dim,
+                                     int32_t block_size, int64_t total_blocks,
+                                     double scale, double k_scale, double v_scale,
+                                     int mask_mode, int32_t sliding_window,
+                                     int dtype, double *out)
+{
+    if (!(k_scale > 0.0) || !(v_scale > 0.0))
+        return -1;
+    return orc_decode_core(r, q, k_cache, v_cache, block_table, bt_stride, bt_cols,
+                           context_lens, num_reqs, q_len, num_q_heads, num_kv_heads,
+                           head_dim, block_size, total_blocks, scale, mask_mode,
+                           sliding_window, 1, 0, 1, dtype, ORC_DT_E4M3, k_scale,
+                           v_scale, out, NULL);
 }
 
 /*

@@ -3,10 +3,11 @@ own slot mapping and cache write.  TEST INFRASTRUCTURE, like the rest of
 this package; it calls only the oracle and the seeded input generators."""
 import numpy as np
 
-from . import cache_write, compute_slot_mapping, compute_slot_mapping_cp, map_to_kernel_blocks
+from . import cache_write, cache_write_fp8, compute_slot_mapping, compute_slot_mapping_cp, map_to_kernel_blocks
 from paged_kv_cache_slot_gb300 import workloads as wl
 
 BF16_NAN = np.uint16(0x7FC0)
+E4M3_NAN = np.uint8(0x7F)
 
 
 def nan_cache(w: wl.Workload, total_blocks=None, block_size=None, sparse=False):
@@ -73,3 +74,26 @@ def fill_oracle_cache_cp(w: wl.Workload, world: int, interleave: int, tables, ro
             assert err == 0
         out.append((kc, vc))
     return out
+
+
+def fill_oracle_cache_fp8(w: wl.Workload, k_scale: float, v_scale: float, rows=None, table=None):
+    """E4M3 caches (uint8 codes, unwritten bytes the NaN code 0x7F) holding every
+    token of ``rows``, written through the oracle's slot mapping and FP8 cache
+    write (reading R16).  Returns (k_cache, v_cache, kernel_table)."""
+    table = kernel_table(w) if table is None else table
+    shape = (w.total_kernel_blocks, w.kernel_block_size, w.num_kv_heads, w.head_dim)
+    kc = np.full(shape, E4M3_NAN, np.uint8)
+    vc = np.full(shape, E4M3_NAN, np.uint8)
+    rows = range(w.num_rows) if rows is None else rows
+    for r in rows:
+        L = int(w.context_lens[r])
+        if L == 0:
+            continue
+        k, v = w.kv_rows(r, 0, L)
+        req = np.full(L, r, np.int32)
+        pos = np.arange(L, dtype=np.int64)
+        slots, err = compute_slot_mapping(table, req, pos, w.kernel_block_size)
+        assert err == 0
+        kc, vc, err = cache_write_fp8(k, v, slots, kc, vc, k_scale, v_scale, inplace=True)
+        assert err == 0
+    return kc, vc, table
