@@ -49,6 +49,11 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "paged_decode_llama3_decode.txt
 DECODE_SOURCES = ["bkv_decode.cu", "bkv_decode_tc.cu", "bkv_decode.cuh"]
 
 
+# per-tensor scales of the FP8 runs: the Llama-shaped K/V draws (sd 1/sqrt(128)) span about +-0.4,
+# well inside 448 * scale
+FP8_SCALES = (2.0 ** -9, 1e-3)
+
+
 def _dist():
     if int(os.environ.get("WORLD_SIZE", "1")) > 1:
         import torch.distributed as dist
@@ -67,8 +72,11 @@ def _peaks():
     return 6800.0, "fallback"
 
 
-def _describe(w, window, cp=(1, 0, 1)):
+def _describe(w, window, cp=(1, 0, 1), fp8=None):
     """The workload's name and sizes, as the JSON line's config.workload."""
+    if fp8 is not None:
+        return (_describe(w, window, cp) + f", E4M3 KV cache (k_scale {fp8[0]:g}, v_scale {fp8[1]:g}; 1 byte per "
+                "element, widened to bf16 on chip)")
     if cp[0] > 1:
         return (_describe(w, window) + f", decode-context-parallel rank {cp[1]} of {cp[0]} (interleave {cp[2]}): "
                 f"its own share of every request's keys")
@@ -289,9 +297,10 @@ def run_bkv(args):
 
     w = wl.make(args.workload)
     cp = (args.cp_world, 0, args.cp_interleave)
+    fp8 = FP8_SCALES if args.kv_dtype == "fp8" else None
     dw = DeviceWorkload(w, device=f"cuda:{local}", sliding_window=args.sliding_window, cp_world=cp[0],
-                        cp_rank=cp[1], cp_interleave=cp[2])
-    headline = args.workload == WORKLOAD and args.sliding_window == 0 and cp[0] == 1
+                        cp_rank=cp[1], cp_interleave=cp[2], kv_fp8=fp8)
+    headline = args.workload == WORKLOAD and args.sliding_window == 0 and cp[0] == 1 and fp8 is None
     stream = torch.cuda.Stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=f"cuda:{local}")
@@ -435,8 +444,8 @@ def run_bkv(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": _describe(w, args.sliding_window, cp),
+        "vs_baseline": None, "dtype": "bf16" if fp8 is None else "e4m3 cache, bf16 MMA", "data": "synthetic",
+        "config": {"workload": _describe(w, args.sliding_window, cp, fp8),
                    "kv_bytes_per_step": kv_bytes, "l2": "flushed before every timed step (write 2x L2, read it back)",
                    "parallelism": f"replicas x{world}", "step": "expand + slot map + write + decode + merge",
                    "cuda_graph": bool(graphs)},
@@ -461,7 +470,7 @@ def run_bkv(args):
         line["secondary"] = secondary
     if cp_merge:
         line["cp_merge_states"] = cp_merge
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and fp8 is None:
         line["cpu_baseline"] = _cpu_baseline(args.cpu_budget, args.workload, args.sliding_window)
     print(json.dumps(line), flush=True)
 
@@ -573,6 +582,8 @@ def main():
     ap.add_argument("--sliding-window", type=int, default=0, help="decode with this sliding window (0: none)")
     ap.add_argument("--attention", default="decode", choices=["decode", "ragged"],
                     help="decode: the headline decode step; ragged: attention over the mixed ragged_step batch")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="cache element type: bf16, or E4M3 codes with per-tensor scales (bkv_*_fp8 calls)")
     ap.add_argument("--cp-world", type=int, default=1,
                     help="time rank 0 of a decode-context-parallel split over this many ranks (1: none)")
     ap.add_argument("--cp-interleave", type=int, default=1, help="context-parallel interleave size")

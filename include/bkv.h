@@ -1,7 +1,9 @@
 /*
  * bkv.h -- C ABI of libbkv.so, the GB300 (sm_103a) paged (block) KV cache
  * hot path: slot mapping, manager-to-kernel block expansion, the KV cache
- * scatter, and GQA paged decode attention with a split-KV merge.
+ * scatter (bf16 / fp32, or quantised to FP8), GQA paged decode attention
+ * with a split-KV merge, mixed-step attention, and the context-parallel
+ * slot filter and merge.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -230,6 +232,74 @@ int bkv_paged_decode_merge(const void *q, const void *k_cache, const void *v_cac
                            float softmax_scale, int mask_mode, int32_t sliding_window, int dtype,
                            void *out, void *workspace, size_t workspace_bytes, int32_t *err_count,
                            bkv_stream_t stream);
+
+/*
+ * bkv_cache_write_fp8
+ *   bkv_cache_write into an FP8 cache.  The pages name a non-FP8 pathway
+ *   ("Padding and Batching with Block KV", Block ID 0 vs. Sentinel -1) and
+ *   print nothing about the format or its scaling; this library's reading:
+ *   cache elements are OCP FP8 E4M3 codes (one byte: sign, 4 exponent bits
+ *   of bias 7, 3 mantissa bits; no infinity; 0x7F / 0xFF are NaN; largest
+ *   finite 448) with one scale per tensor.  Element x of k_new[i] is stored
+ *   as the code nearest to x / k_scale, the quotient taken in IEEE binary32,
+ *   ties to the even code, magnitudes above 448 (and infinities) saturated
+ *   to +-448, NaN stored as NaN; V likewise with v_scale.  Rows, slots, -1
+ *   padding and error counting are bkv_cache_write's.
+ *
+ *   k_new, v_new  [num_tokens, new_token_stride] of src_dtype (BKV_BF16 /
+ *                 BKV_F32), the first num_kv_heads * head_dim of each row.
+ *   k_cache, v_cache  uint8 [total_blocks, block_size, num_kv_heads, head_dim].
+ *   INVALID_ARG: as bkv_cache_write, or k_scale / v_scale not a positive
+ *   finite number.  UNSUPPORTED: src_dtype not BKV_BF16 / BKV_F32.
+ */
+int bkv_cache_write_fp8(const void *k_new, const void *v_new, int64_t num_tokens,
+                        int64_t new_token_stride, const int64_t *slot_mapping, uint8_t *k_cache,
+                        uint8_t *v_cache, int64_t total_blocks, int32_t block_size,
+                        int32_t num_kv_heads, int32_t head_dim, int src_dtype, float k_scale,
+                        float v_scale, int32_t *err_count, bkv_stream_t stream);
+
+/*
+ * bkv_paged_decode_fp8, bkv_paged_decode_fp8_partition, bkv_paged_decode_fp8_merge
+ *   bkv_paged_decode (and its two phases) over FP8 caches written by
+ *   bkv_cache_write_fp8: a key element with code c stands for the value
+ *   e4m3(c) * k_scale and a value element for e4m3(c) * v_scale; the
+ *   operation, masks, sliding window, null entries, error counting and
+ *   workspace are exactly bkv_paged_decode's ("Padding and Batching with
+ *   Block KV", Cache Masking; the FP8 format is the reading stated at
+ *   bkv_cache_write_fp8).  `dtype` is the type of q and out (BKV_BF16 /
+ *   BKV_F32); k_cache, v_cache are uint8 [total_blocks, block_size,
+ *   num_kv_heads, head_dim].  A cache byte at a masked position is never
+ *   used (NaN codes there change nothing).  bf16 q with head_dim 128 and at
+ *   most 16 query rows per KV head runs the tensor-core kernel, which widens
+ *   the codes to bf16 exactly on chip; anything else the CUDA-core kernel.
+ *   Errors: as bkv_paged_decode, plus INVALID_ARG for a scale that is not a
+ *   positive finite number.
+ */
+int bkv_paged_decode_fp8(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                         const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
+                         const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs,
+                         int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int64_t total_blocks, float softmax_scale, float k_scale,
+                         float v_scale, int mask_mode, int32_t sliding_window, int dtype, void *out,
+                         void *workspace, size_t workspace_bytes, int32_t *err_count,
+                         bkv_stream_t stream);
+int bkv_paged_decode_fp8_partition(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                   const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
+                                   const int32_t *context_lens, int32_t max_context_len,
+                                   int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   int64_t total_blocks, float softmax_scale, float k_scale,
+                                   float v_scale, int mask_mode, int32_t sliding_window, int dtype,
+                                   void *out, void *workspace, size_t workspace_bytes,
+                                   int32_t *err_count, bkv_stream_t stream);
+int bkv_paged_decode_fp8_merge(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                               const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
+                               const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs,
+                               int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int64_t total_blocks,
+                               float softmax_scale, float k_scale, float v_scale, int mask_mode,
+                               int32_t sliding_window, int dtype, void *out, void *workspace,
+                               size_t workspace_bytes, int32_t *err_count, bkv_stream_t stream);
 
 /*
  * bkv_paged_attention_ragged

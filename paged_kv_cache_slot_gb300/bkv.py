@@ -80,6 +80,13 @@ def load() -> ctypes.CDLL:
         for fn in ("bkv_paged_decode", "bkv_paged_decode_partition", "bkv_paged_decode_merge"):
             getattr(lib, fn).restype = cint
             getattr(lib, fn).argtypes = dec
+        lib.bkv_cache_write_fp8.restype = cint
+        lib.bkv_cache_write_fp8.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i32, i32, i32, cint, f32, f32, vp, vp]
+        dec8 = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i32, i64, f32, f32, f32, cint, i32, cint,
+                vp, vp, sz, vp, vp]
+        for fn in ("bkv_paged_decode_fp8", "bkv_paged_decode_fp8_partition", "bkv_paged_decode_fp8_merge"):
+            getattr(lib, fn).restype = cint
+            getattr(lib, fn).argtypes = dec8
         _lib = lib
         return lib
 
@@ -179,6 +186,31 @@ def bkv_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens=Non
         hkv, d, dt, _opt(err_count, "err_count", torch.int32), _stream(stream)))
 
 
+def bkv_cache_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, num_tokens=None,
+                        err_count=None, stream=None):
+    """Quantise k_new/v_new rows (num_tokens, H_kv, D; bf16 or fp32) into uint8 E4M3 caches at slot_mapping
+    with per-tensor scales (see include/bkv.h)."""
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("caches must be (total_blocks, block_size, H_kv, D) and equal in shape")
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("FP8 caches are uint8 tensors of E4M3 codes")
+    tb, bs, hkv, d = k_cache.shape
+    if k_new.dim() != 3 or tuple(k_new.shape[1:]) != (hkv, d) or k_new.shape != v_new.shape:
+        raise ValueError("k_new/v_new must be (num_tokens, H_kv, D) matching the cache")
+    if k_new.stride(2) != 1 or k_new.stride(1) != d or k_new.stride() != v_new.stride():
+        raise ValueError("k_new/v_new rows must be dense (a row stride is allowed)")
+    if k_new.dtype != v_new.dtype:
+        raise TypeError("mixed dtypes")
+    dt = _kv_dtype(k_new)
+    n = k_new.shape[0] if num_tokens is None else int(num_tokens)
+    if n > k_new.shape[0] or n > slot_mapping.numel():
+        raise ValueError("num_tokens exceeds k_new / slot_mapping")
+    _check("bkv_cache_write_fp8", load().bkv_cache_write_fp8(
+        _dev(k_new, "k_new", contiguous=False), _dev(v_new, "v_new", contiguous=False), n, k_new.stride(0),
+        _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), tb, bs,
+        hkv, d, dt, float(k_scale), float(v_scale), _opt(err_count, "err_count", torch.int32), _stream(stream)))
+
+
 def bkv_paged_decode_workspace_size(num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
                                     max_context_len) -> int:
     return int(load().bkv_paged_decode_workspace_size(int(num_reqs), int(q_len), int(num_q_heads),
@@ -210,7 +242,7 @@ def bkv_paged_decode_merge(q, k_cache, v_cache, block_table, context_lens, max_c
 
 
 def _decode(fn, q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace, softmax_scale,
-            mask_mode, sliding_window, err_count, stream):
+            mask_mode, sliding_window, err_count, stream, scales=None):
     if q.dim() != 4 or out.shape != q.shape or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
         raise ValueError("q/out must be (num_reqs, q_len, H_q, D); caches (total_blocks, bs, H_kv, D)")
     nr, ql, hq, d = q.shape
@@ -220,9 +252,10 @@ def _decode(fn, q, k_cache, v_cache, block_table, context_lens, max_context_len,
     if block_table.dim() != 2 or block_table.shape[0] < nr or block_table.stride(1) != 1:
         raise ValueError("block_table must be (>= num_reqs, cols) with unit column stride")
     dt = _kv_dtype(q)
-    for t, nm in ((k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
-        if t.dtype != q.dtype:
-            raise TypeError(f"{nm} dtype differs from q")
+    cache_dtype = q.dtype if scales is None else torch.uint8
+    for t, nm, want in ((k_cache, "k_cache", cache_dtype), (v_cache, "v_cache", cache_dtype), (out, "out", q.dtype)):
+        if t.dtype != want:
+            raise TypeError(f"{nm} must be {want}, got {t.dtype}")
     if workspace is not None and workspace.dtype != torch.uint8:
         raise TypeError("workspace must be a uint8 tensor")
     ws_ptr = None if workspace is None else _dev(workspace, "workspace")
@@ -231,9 +264,36 @@ def _decode(fn, q, k_cache, v_cache, block_table, context_lens, max_context_len,
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_table, "block_table", torch.int32, contiguous=False), block_table.stride(0),
         block_table.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), nr, ql, hq, hkv,
-        d, bs, tb, float(softmax_scale), int(mask_mode), int(sliding_window), dt, _dev(out, "out"), ws_ptr, ws_bytes,
+        d, bs, tb, float(softmax_scale), *(() if scales is None else (float(scales[0]), float(scales[1]))),
+        int(mask_mode), int(sliding_window), dt, _dev(out, "out"), ws_ptr, ws_bytes,
         _opt(err_count, "err_count", torch.int32), _stream(stream)))
     return out
+
+
+def bkv_paged_decode_fp8(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace, k_scale,
+                         v_scale, softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None,
+                         sliding_window=0):
+    """bkv_paged_decode over uint8 E4M3 caches with per-tensor scales (see include/bkv.h)."""
+    return _decode("bkv_paged_decode_fp8", q, k_cache, v_cache, block_table, context_lens, max_context_len, out,
+                   workspace, softmax_scale, mask_mode, sliding_window, err_count, stream, scales=(k_scale, v_scale))
+
+
+def bkv_paged_decode_fp8_partition(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
+                                   k_scale, v_scale, softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None,
+                                   stream=None, sliding_window=0):
+    """Phase 1 of bkv_paged_decode_fp8 (see include/bkv.h)."""
+    return _decode("bkv_paged_decode_fp8_partition", q, k_cache, v_cache, block_table, context_lens,
+                   max_context_len, out, workspace, softmax_scale, mask_mode, sliding_window, err_count, stream,
+                   scales=(k_scale, v_scale))
+
+
+def bkv_paged_decode_fp8_merge(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
+                               k_scale, v_scale, softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None,
+                               stream=None, sliding_window=0):
+    """Phase 2 of bkv_paged_decode_fp8 (see include/bkv.h)."""
+    return _decode("bkv_paged_decode_fp8_merge", q, k_cache, v_cache, block_table, context_lens, max_context_len,
+                   out, workspace, softmax_scale, mask_mode, sliding_window, err_count, stream,
+                   scales=(k_scale, v_scale))
 
 
 def bkv_paged_decode_cp(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, lse, workspace,

@@ -10,6 +10,9 @@
 // vectors, all loads of a round issued before its stores.  HBM-bound: the
 // algorithmic traffic is 2 * row bytes read + 2 * row bytes written + 8 bytes
 // of slot id per token.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
 #include "bkv_internal.cuh"
 
 namespace bkv {
@@ -85,7 +88,116 @@ __global__ void __launch_bounds__(kCwWarps * 32) cache_write_elem_kernel(
     }
 }
 
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) cache write.  The pages name a non-FP8 pathway and nothing more
+// ("Padding and Batching with Block KV", Block ID 0 vs. Sentinel -1); this
+// library's reading: each element x of a new row is stored as the E4M3 code
+// of the binary32 quotient x / scale (IEEE division), rounded to nearest even
+// with saturation to +-448 and NaN kept NaN, one scale for K and one for V.
+// One warp per token as above; each lane turns 16 source elements into one
+// 16-byte store.  HBM-bound: row * (2 * src bytes + 2) + 8 bytes per token.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float src_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float src_f(float x) { return x; }
+
+// Two elements to two E4M3 codes (the first in the low byte).
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b, float scale) {
+    const __nv_fp8x2_storage_t c =
+        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, scale), __fdiv_rn(b, scale)), __NV_SATFINITE, __NV_E4M3);
+    return (uint32_t)c;
+}
+
+// Sixteen consecutive source elements at p (16-byte aligned) as codes.
+template <typename E>
+__device__ __forceinline__ uint4 quant16(const E *p, float scale) {
+    constexpr int kVec = 16 / sizeof(E);   // elements per 16-byte load
+    E x[16];
+#pragma unroll
+    for (int u = 0; u < 16 / kVec; ++u) *reinterpret_cast<uint4 *>(x + u * kVec) = __ldg(reinterpret_cast<const uint4 *>(p) + u);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        w[q] = e4m3x2(src_f(x[4 * q]), src_f(x[4 * q + 1]), scale) |
+               (e4m3x2(src_f(x[4 * q + 2]), src_f(x[4 * q + 3]), scale) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// kVec16: the row and the source stride are multiples of 16 elements and the
+// bases 16-byte aligned; otherwise one element per lane and step.
+template <typename E, bool kVec16>
+__global__ void __launch_bounds__(kCwWarps * 32) cache_write_fp8_kernel(
+    const E *__restrict__ k_new, const E *__restrict__ v_new, int64_t num_tokens, int64_t src_stride,
+    const int64_t *__restrict__ slot_mapping, uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+    int64_t capacity, int64_t row, float k_scale, float v_scale, int32_t *err_count) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (int64_t)blockIdx.x * kCwWarps + (threadIdx.x >> 5);
+    const int64_t wstep = (int64_t)gridDim.x * kCwWarps;
+    for (int64_t i = warp0; i < num_tokens; i += wstep) {
+        const int64_t s = __ldg(slot_mapping + i);
+        if (s < 0) continue;
+        if (s >= capacity) {
+            if (lane == 0 && err_count) atomicAdd(err_count, 1);
+            continue;
+        }
+        const E *ks = k_new + i * src_stride;
+        const E *vs = v_new + i * src_stride;
+        uint8_t *kd = k_cache + s * row;
+        uint8_t *vd = v_cache + s * row;
+        if constexpr (kVec16) {
+            for (int64_t e = (int64_t)lane * 16; e < row; e += 32 * 16) {
+                const uint4 kq = quant16(ks + e, k_scale);
+                const uint4 vq = quant16(vs + e, v_scale);
+                *reinterpret_cast<uint4 *>(kd + e) = kq;
+                *reinterpret_cast<uint4 *>(vd + e) = vq;
+            }
+        } else {
+            for (int64_t e = lane; e < row; e += 32) {
+                kd[e] = (uint8_t)e4m3x2(src_f(ks[e]), 0.f, k_scale);
+                vd[e] = (uint8_t)e4m3x2(src_f(vs[e]), 0.f, v_scale);
+            }
+        }
+    }
+}
+
 }  // namespace bkv
+
+extern "C" int bkv_cache_write_fp8(const void *k_new, const void *v_new, int64_t num_tokens,
+                                   int64_t new_token_stride, const int64_t *slot_mapping, uint8_t *k_cache,
+                                   uint8_t *v_cache, int64_t total_blocks, int32_t block_size, int32_t num_kv_heads,
+                                   int32_t head_dim, int src_dtype, float k_scale, float v_scale,
+                                   int32_t *err_count, bkv_stream_t stream) {
+    if (src_dtype != BKV_BF16 && src_dtype != BKV_F32) return BKV_ERR_UNSUPPORTED;
+    if (num_tokens < 0 || total_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return BKV_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale)) return BKV_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (new_token_stride < row) return BKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return BKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return BKV_ERR_INVALID_ARG;
+    const int64_t capacity = total_blocks * block_size;
+    const int threads = bkv::kCwWarps * 32;
+    const unsigned grid = bkv::grid_for(num_tokens, bkv::kCwWarps, 16);
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool vec16 = row % 16 == 0 && new_token_stride % 16 == 0 && bkv::aligned(k_new, 16) &&
+                       bkv::aligned(v_new, 16) && bkv::aligned(k_cache, 16) && bkv::aligned(v_cache, 16);
+    cudaError_t e;
+    if (src_dtype == BKV_BF16) {
+        auto kern = vec16 ? bkv::cache_write_fp8_kernel<__nv_bfloat16, true>
+                          : bkv::cache_write_fp8_kernel<__nv_bfloat16, false>;
+        e = bkv::launch_pdl(kern, grid, threads, 0, st, (const __nv_bfloat16 *)k_new, (const __nv_bfloat16 *)v_new,
+                            num_tokens, new_token_stride, slot_mapping, k_cache, v_cache, capacity, row, k_scale,
+                            v_scale, err_count);
+    } else {
+        auto kern = vec16 ? bkv::cache_write_fp8_kernel<float, true> : bkv::cache_write_fp8_kernel<float, false>;
+        e = bkv::launch_pdl(kern, grid, threads, 0, st, (const float *)k_new, (const float *)v_new, num_tokens,
+                            new_token_stride, slot_mapping, k_cache, v_cache, capacity, row, k_scale, v_scale,
+                            err_count);
+    }
+    if (e != cudaSuccess) bkv::set_cuda_error(e);
+    return bkv::launch_status();
+}
 
 extern "C" int bkv_cache_write(const void *k_new, const void *v_new, int64_t num_tokens, int64_t new_token_stride,
                                const int64_t *slot_mapping, void *k_cache, void *v_cache, int64_t total_blocks,

@@ -17,6 +17,7 @@
 // log-sum-exp weights.  Partition boundaries depend only on logical
 // positions, so the result is independent of where blocks sit in memory.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "bkv_decode.cuh"
@@ -28,6 +29,8 @@ static constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_f(float x) { return x; }
+// an E4M3 cache code as its (unscaled) value, exactly
+__device__ __forceinline__ float to_f(__nv_fp8_e4m3 x) { return static_cast<float>(x); }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 __device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
 
@@ -55,7 +58,7 @@ __device__ __forceinline__ int32_t clamped_len(const DecodeArgs &a, int r, bool 
 // products reduce with warp shuffles, each warp keeps its own online softmax
 // and the four are combined through shared memory at the end.
 // ---------------------------------------------------------------------------
-template <typename T, int DPL, int QR>
+template <typename T, typename KV, int DPL, int QR>
 __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a) {
     constexpr int NW = 4;
     pdl_wait();
@@ -77,8 +80,8 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
     const int nrows = min(QR, a.nq - i0);
 
     const T *Q = static_cast<const T *>(a.q);
-    const T *K = static_cast<const T *>(a.k);
-    const T *V = static_cast<const T *>(a.v);
+    const KV *K = static_cast<const KV *>(a.k);
+    const KV *V = static_cast<const KV *>(a.v);
 
     float q[QR][DPL];
     int32_t lastv[QR], firstv[QR];
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
             for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
             const float wl = (M == -INFINITY || lane >= nch) ? 0.f : exp2f(ml.x - M);
             const float lsum = warp_sum(wl * ml.y);
-            const float iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : 1.f / lsum;
+            const float iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : a.v_scale / lsum;
             put_lse(M, lsum);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
             lsum = fmaf(wgt, ml.y, lsum);
         }
         lsum = warp_sum(lsum);
-        const float iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : 1.f / lsum;
+        const float iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : a.v_scale / lsum;
         put_lse(M, lsum);
         __syncwarp();
         if ((a.D & 3) == 0) {
@@ -401,20 +404,20 @@ bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int3
     return true;
 }
 
-template <typename T, int DPL>
+template <typename T, typename KV, int DPL>
 static void launch_generic(const DecodeArgs &a, cudaStream_t st) {
     constexpr int QR = 8;
     dim3 grid(a.n_chunks * a.num_reqs * a.H_kv, ceil_div(a.nq, QR));
-    const cudaError_t e = launch_pdl(decode_generic_kernel<T, DPL, QR>, grid, dim3(128), 0, st, a);
+    const cudaError_t e = launch_pdl(decode_generic_kernel<T, KV, DPL, QR>, grid, dim3(128), 0, st, a);
     if (e != cudaSuccess) set_cuda_error(e);
 }
 
-template <typename T>
+template <typename T, typename KV>
 static void launch_generic_dpl(const DecodeArgs &a, cudaStream_t st) {
-    if (a.D <= 32) launch_generic<T, 1>(a, st);
-    else if (a.D <= 64) launch_generic<T, 2>(a, st);
-    else if (a.D <= 128) launch_generic<T, 4>(a, st);
-    else launch_generic<T, 8>(a, st);
+    if (a.D <= 32) launch_generic<T, KV, 1>(a, st);
+    else if (a.D <= 64) launch_generic<T, KV, 2>(a, st);
+    else if (a.D <= 128) launch_generic<T, KV, 4>(a, st);
+    else launch_generic<T, KV, 8>(a, st);
 }
 
 }  // namespace bkv
@@ -447,8 +450,10 @@ static int decode_setup(const void *q, const void *k_cache, const void *v_cache,
                         int32_t block_size, int64_t total_blocks, float softmax_scale, int mask_mode, int dtype,
                         int32_t sliding_window, int32_t cp_world, int32_t cp_rank, int32_t cp_interleave,
                         void *out, float *lse, void *workspace, size_t workspace_bytes, int32_t *err_count,
-                        DecodeCall *c) {
+                        DecodeCall *c, int kv_fp8 = 0, float k_scale = 1.f, float v_scale = 1.f) {
     if (dtype != BKV_BF16 && dtype != BKV_F32) return BKV_ERR_UNSUPPORTED;
+    if (kv_fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale)))
+        return BKV_ERR_INVALID_ARG;
     if (sliding_window < 0) return BKV_ERR_INVALID_ARG;
     if (cp_world < 1 || cp_rank < 0 || cp_rank >= cp_world || cp_interleave < 1) return BKV_ERR_INVALID_ARG;
     if (cp_world > 1 && sliding_window > 0) return BKV_ERR_UNSUPPORTED;
@@ -479,7 +484,10 @@ static int decode_setup(const void *q, const void *k_cache, const void *v_cache,
     a.D = head_dim;
     a.bs = block_size;
     a.total_blocks = total_blocks;
-    a.scale_log2 = softmax_scale * kLog2e;
+    // an FP8 key is its code's value times k_scale: the factor joins the score scale
+    a.scale_log2 = kv_fp8 ? softmax_scale * kLog2e * k_scale : softmax_scale * kLog2e;
+    a.kv_fp8 = kv_fp8;
+    a.v_scale = kv_fp8 ? v_scale : 1.f;
     a.mask_mode = mask_mode;
     a.window = sliding_window;
     a.cp_world = cp_world;
@@ -515,8 +523,14 @@ static int decode_setup(const void *q, const void *k_cache, const void *v_cache,
 
 static int decode_partition(DecodeCall &c, cudaStream_t st) {
     if (c.tc) return launch_decode_tc(c.a, c.t, st);
-    if (c.a.dtype == BKV_BF16) launch_generic_dpl<__nv_bfloat16>(c.a, st);
-    else launch_generic_dpl<float>(c.a, st);
+    if (c.a.kv_fp8) {
+        if (c.a.dtype == BKV_BF16) launch_generic_dpl<__nv_bfloat16, __nv_fp8_e4m3>(c.a, st);
+        else launch_generic_dpl<float, __nv_fp8_e4m3>(c.a, st);
+    } else if (c.a.dtype == BKV_BF16) {
+        launch_generic_dpl<__nv_bfloat16, __nv_bfloat16>(c.a, st);
+    } else {
+        launch_generic_dpl<float, float>(c.a, st);
+    }
     return launch_status();
 }
 
@@ -566,6 +580,41 @@ extern "C" int bkv_paged_decode_partition(BKV_DECODE_PARAMS) {
 extern "C" int bkv_paged_decode_merge(BKV_DECODE_PARAMS) {
     bkv::DecodeCall c;
     const int rc = BKV_DECODE_SETUP(c);
+    if (rc != BKV_OK) return rc;
+    return bkv::decode_merge(c, (cudaStream_t)stream);
+}
+
+#define BKV_DECODE_FP8_PARAMS                                                                                     \
+    const void *q, const uint8_t *k_cache, const uint8_t *v_cache, const int32_t *block_table, int64_t bt_stride, \
+        int32_t bt_cols, const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs, int32_t q_len,  \
+        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t total_blocks,   \
+        float softmax_scale, float k_scale, float v_scale, int mask_mode, int32_t sliding_window, int dtype,     \
+        void *out, void *workspace, size_t workspace_bytes, int32_t *err_count, bkv_stream_t stream
+#define BKV_DECODE_FP8_SETUP(c)                                                                                   \
+    bkv::decode_setup(q, k_cache, v_cache, block_table, bt_stride, bt_cols, context_lens, max_context_len,       \
+                      num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, total_blocks, softmax_scale, \
+                      mask_mode, dtype, sliding_window, 1, 0, 1, out, nullptr, workspace, workspace_bytes,      \
+                      err_count, &(c), 1, k_scale, v_scale)
+
+extern "C" int bkv_paged_decode_fp8(BKV_DECODE_FP8_PARAMS) {
+    bkv::DecodeCall c;
+    int rc = BKV_DECODE_FP8_SETUP(c);
+    if (rc != BKV_OK) return rc;
+    rc = bkv::decode_partition(c, (cudaStream_t)stream);
+    if (rc != BKV_OK) return rc;
+    return bkv::decode_merge(c, (cudaStream_t)stream);
+}
+
+extern "C" int bkv_paged_decode_fp8_partition(BKV_DECODE_FP8_PARAMS) {
+    bkv::DecodeCall c;
+    const int rc = BKV_DECODE_FP8_SETUP(c);
+    if (rc != BKV_OK) return rc;
+    return bkv::decode_partition(c, (cudaStream_t)stream);
+}
+
+extern "C" int bkv_paged_decode_fp8_merge(BKV_DECODE_FP8_PARAMS) {
+    bkv::DecodeCall c;
+    const int rc = BKV_DECODE_FP8_SETUP(c);
     if (rc != BKV_OK) return rc;
     return bkv::decode_merge(c, (cudaStream_t)stream);
 }

@@ -24,7 +24,9 @@ struct DecodeArgs {
     int32_t window;    // sliding window W (> 0): query t sees keys j >= L - q_len + t - W + 1; 0: none
     int32_t cp_world, cp_rank, cp_inter;   // decode context parallelism: this rank's share of the keys
     float *lse;        // optional [num_reqs, q_len, H_q] natural-log sum of exp of the scaled scores
-    int dtype;         // BKV_BF16 or BKV_F32 (q, caches and out share it)
+    int dtype;         // BKV_BF16 or BKV_F32: q and out (and the caches unless kv_fp8)
+    int kv_fp8;        // caches hold E4M3 codes: a key is code * k_scale (folded into scale_log2)
+    float v_scale;     // and a value code * v_scale (applied by the merge); 1 otherwise
     int32_t chunk;     // tokens per split-KV partition (multiple of the tile and of bs)
     int32_t n_chunks;  // partitions per request at max_ctx
     int32_t G;         // query heads per KV head

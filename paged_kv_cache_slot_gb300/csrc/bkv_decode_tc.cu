@@ -51,6 +51,8 @@
 //   TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -71,41 +73,54 @@ constexpr int kN = 16;                // query rows per MMA (padded)
 #ifndef BKV_V_STAGES
 #define BKV_V_STAGES 3
 #endif
-constexpr int kKStages = BKV_K_STAGES;
-constexpr int kVStages = BKV_V_STAGES;
-static_assert(kKStages >= 2 && kKStages <= 3, "the 8-entry mask ring assumes at most 3 K slots");
+static_assert(BKV_K_STAGES >= 2 && BKV_K_STAGES <= 3, "the 8-entry mask ring assumes at most 3 K slots");
 constexpr int kHalfBytes = kTile * 128;          // 128 rows x 64 bf16 (128 B): one head_dim half
 constexpr int kTileBytes = 2 * kHalfBytes;       // K or V tile: 32 KB
+constexpr int kT8Bytes = kTile * 128;            // an FP8 K or V tile as loaded: 128 rows x 128 codes, 16 KB
 constexpr int kQBytes = 2 * kN * 128;            // 16 rows x 128 B x 2 halves: 4 KB
 constexpr int kPBytes = 2 * kN * 128;            // 16 rows x 128 positions (2 x 64) bf16: 4 KB
-constexpr int kThreads = 352;                    // K producer, MMA, two softmax warpgroups, V producer
-constexpr int kWarpV = kThreads / 32 - 1;        // the V producer's warp
+constexpr int kWarpV = 10;                       // the V producer's warp
 constexpr int kTmemCols = 64;                    // S x2 (16 cols each) + O x2
 constexpr int kTimeoutErr = 1 << 24;
 constexpr int kMaxReqs = 2048;                   // requests the in-kernel tile prefix handles
 constexpr int kWinBlocks = 128;                  // table entries a producer caches per window
 
-// Shared-memory layout (offsets from a 1024-aligned base).
-constexpr int kOffK = 0;                                  // kKStages K slots
-constexpr int kOffV = kOffK + kKStages * kTileBytes;      // kVStages V slots
-constexpr int kOffQ = kOffV + kVStages * kTileBytes;
-constexpr int kOffP = kOffQ + 2 * kQBytes;
-constexpr int kOffMask = kOffP + 2 * kPBytes;             // 8 words: loaded segments per tile (ring)
-constexpr int kOffRedMax = kOffMask + 64;                 // [warpgroup][2][16 rows][4 warps] floats
-constexpr int kOffRedSum = kOffRedMax + 4 * kN * 4 * 4;   // [warpgroup][16 rows][4 warps] floats
-constexpr int kOffBar = kOffRedSum + 2 * kN * 4 * 4;      // barriers (8 B each)
-constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 8;
-constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kOffPre = kOffAbort + 4;                    // [kMaxReqs + 1] tile prefix per request
-constexpr int kOffEnt = (kOffPre + (kMaxReqs + 1) * 4 + 15) / 16 * 16;   // [producer][2][kWinBlocks] entries
-// [kMaxReqs] last-tile fill of each request minus one: with the tile count it
-// gives the clamped length without a global read, len = (tiles - 1) * 128 + fill
-constexpr int kOffLrem = kOffEnt + 4 * kWinBlocks * 4;
-constexpr int kSmemUsed = kOffLrem + kMaxReqs;
-constexpr int kSmemBytes = kSmemUsed + 1024;              // slack for 1024 alignment
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
-static_assert(kOffEnt % 16 == 0, "entry buffers must stay aligned");
+// Shared-memory layout and role counts (offsets from a 1024-aligned base).
+// kF8: FP8 caches.  The producers load E4M3 tiles into their own 2-slot rings
+// and a converter warpgroup (warps 11..14) widens every tile to bf16 (exactly:
+// each E4M3 value is a bf16 value) into 2-slot bf16 rings the MMAs read.
+template <bool kF8>
+struct Cfg {
+    static constexpr int kThreads = kF8 ? 480 : 352;   // + the converter warpgroup
+    static constexpr int kKStages = kF8 ? 2 : BKV_K_STAGES;
+    static constexpr int kVStages = kF8 ? 2 : BKV_V_STAGES;
+    static constexpr int k8Stages = kF8 ? 2 : 0;       // FP8 slots per ring
+    static constexpr int kOffK = 0;                                  // kKStages K slots
+    static constexpr int kOffV = kOffK + kKStages * kTileBytes;      // kVStages V slots
+    static constexpr int kOffK8 = kOffV + kVStages * kTileBytes;     // k8Stages FP8 K slots
+    static constexpr int kOffV8 = kOffK8 + k8Stages * kT8Bytes;      // k8Stages FP8 V slots
+    static constexpr int kOffQ = kOffV8 + k8Stages * kT8Bytes;
+    static constexpr int kOffP = kOffQ + 2 * kQBytes;
+    static constexpr int kOffMask = kOffP + 2 * kPBytes;             // 8 words: loaded segments per tile (ring)
+    static constexpr int kOffRedMax = kOffMask + 64;                 // [warpgroup][2][16 rows][4 warps] floats
+    static constexpr int kOffRedSum = kOffRedMax + 4 * kN * 4 * 4;   // [warpgroup][16 rows][4 warps] floats
+    static constexpr int kOffBar = kOffRedSum + 2 * kN * 4 * 4;      // barriers (8 B each)
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 8 + 4 * k8Stages;
+    static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+    static constexpr int kOffAbort = kOffTmemSlot + 4;
+    static constexpr int kOffPre = kOffAbort + 4;                    // [kMaxReqs + 1] tile prefix per request
+    static constexpr int kOffEnt = (kOffPre + (kMaxReqs + 1) * 4 + 15) / 16 * 16;   // [producer][2][kWinBlocks]
+    // [kMaxReqs] last-tile fill of each request minus one: with the tile count it
+    // gives the clamped length without a global read, len = (tiles - 1) * 128 + fill
+    static constexpr int kOffLrem = kOffEnt + 4 * kWinBlocks * 4;
+    static constexpr int kSmemUsed = kOffLrem + kMaxReqs;
+    static constexpr int kSmemBytes = kSmemUsed + 1024;              // slack for 1024 alignment
+    static constexpr int kLensPerThread = (kMaxReqs + kThreads - 1) / kThreads;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
+    static_assert(kOffEnt % 16 == 0, "entry buffers must stay aligned");
+    static_assert(kOffK8 % 1024 == 0 && kOffV8 % 1024 == 0 && kOffQ % 1024 == 0, "swizzled tiles need 1 KB alignment");
+    static_assert(kWarpV == (kF8 ? 10 : kThreads / 32 - 1), "warp roles");
+};
 
 // The first NQ accumulator columns of this thread's TMEM lane.
 template <int NQ>
@@ -128,9 +143,11 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NQ]) {
 // length above the host bound is clamped to it and counted once (CTA 0).
 // The caller orders the V-ring stores before the TMA writes (proxy fence +
 // barrier).
-constexpr int kLensPerThread = (kMaxReqs + kThreads - 1) / kThreads;
-
+template <bool kF8>
 __device__ void schedule_loads(const DecodeArgs &a, int32_t *pre, uint8_t *lrem, uint8_t *smem) {
+    using C = Cfg<kF8>;
+    constexpr int kThreads = C::kThreads;
+    constexpr int kLensPerThread = C::kLensPerThread;
     const int n = a.num_reqs;
     int32_t lens[kLensPerThread];
 #pragma unroll
@@ -150,8 +167,8 @@ __device__ void schedule_loads(const DecodeArgs &a, int32_t *pre, uint8_t *lrem,
         }
     }
     const uint4 z = make_uint4(0, 0, 0, 0);
-    uint4 *v = reinterpret_cast<uint4 *>(smem + kOffV);
-    for (int i = threadIdx.x; i < kVStages * kTileBytes / 16; i += kThreads) v[i] = z;
+    uint4 *v = reinterpret_cast<uint4 *>(smem + C::kOffV);
+    for (int i = threadIdx.x; i < C::kVStages * kTileBytes / 16; i += kThreads) v[i] = z;
 #pragma unroll
     for (int i = 0; i < kLensPerThread; ++i) {
         const int r = threadIdx.x + i * kThreads;
@@ -169,8 +186,9 @@ __device__ void schedule_loads(const DecodeArgs &a, int32_t *pre, uint8_t *lrem,
 }
 
 // Exclusive prefix sum of the tile counts in place, pre[n] = total, over all
-// threads of the CTA (tot: 12 ints of scratch); CTA 0 also stores it in the
+// threads of the CTA (tot: one int per warp plus one of scratch); CTA 0 also stores it in the
 // workspace for the merge.  Starts and ends with a __syncthreads.
+template <int kThreads>
 __device__ void scan_prefix(const DecodeArgs &a, int32_t *pre, int32_t *tot) {
     constexpr int kWarps = kThreads / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -333,26 +351,62 @@ __device__ __forceinline__ bool reduced_writer(int lane) {
     return (lane & ((1 << (5 - k)) - 1)) == 0;
 }
 
+// Two E4M3 codes (low byte first) as two bf16 values in one word, exactly:
+// every E4M3 value, NaN included, is a half and a bf16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+// Row r of an E4M3 tile as TMA leaves it (128-byte rows, 16-byte chunk c of
+// row r at chunk c ^ (r & 7)) into row r of a bf16 tile in the MMA layout
+// (two head_dim halves of 128-byte rows, the same chunk swizzle): code chunk
+// c (head_dim 16c .. 16c + 15) becomes bf16 chunks 2(c & 3), 2(c & 3) + 1 of
+// half c / 4.  Conflict-free when consecutive lanes take consecutive rows.
+__device__ __forceinline__ void widen_row_e4m3(const uint8_t *src_tile, uint8_t *dst_tile, int r) {
+    const uint8_t *src = src_tile + r * 128;
+    const int sw = r & 7;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(src + ((c ^ sw) << 4));
+        const uint4 lo = make_uint4(e4m3x2_to_bf16x2(w.x & 0xFFFFu), e4m3x2_to_bf16x2(w.x >> 16),
+                                    e4m3x2_to_bf16x2(w.y & 0xFFFFu), e4m3x2_to_bf16x2(w.y >> 16));
+        const uint4 hi = make_uint4(e4m3x2_to_bf16x2(w.z & 0xFFFFu), e4m3x2_to_bf16x2(w.z >> 16),
+                                    e4m3x2_to_bf16x2(w.w & 0xFFFFu), e4m3x2_to_bf16x2(w.w >> 16));
+        uint8_t *dst = dst_tile + (c >> 2) * kHalfBytes + r * 128;
+        const int c2 = 2 * (c & 3);
+        *reinterpret_cast<uint4 *>(dst + ((c2 ^ sw) << 4)) = lo;
+        *reinterpret_cast<uint4 *>(dst + (((c2 + 1) ^ sw) << 4)) = hi;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int NQ, bool kCP>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NQ, bool kCP, bool kF8>
+__global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a, int seg_rows) {
+    using C = Cfg<kF8>;
+    constexpr int kThreads = C::kThreads;
+    constexpr int kKStages = C::kKStages;
+    constexpr int kVStages = C::kVStages;
+    constexpr int k8Stages = C::k8Stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    uint32_t *mask_words = reinterpret_cast<uint32_t *>(smem + kOffMask);
-    float *red_max = reinterpret_cast<float *>(smem + kOffRedMax);
-    float *red_sum = reinterpret_cast<float *>(smem + kOffRedSum);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemSlot);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
-    int32_t *pre = reinterpret_cast<int32_t *>(smem + kOffPre);
-    const uint32_t bar0 = sbase + kOffBar;
+    uint32_t *mask_words = reinterpret_cast<uint32_t *>(smem + C::kOffMask);
+    float *red_max = reinterpret_cast<float *>(smem + C::kOffRedMax);
+    float *red_sum = reinterpret_cast<float *>(smem + C::kOffRedSum);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffTmemSlot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffAbort);
+    int32_t *pre = reinterpret_cast<int32_t *>(smem + C::kOffPre);
+    const uint32_t bar0 = sbase + C::kOffBar;
     // K and V tiles have separate rings (same slot numbering): a K slot is
     // released as soon as the S MMA that reads it completes.
     constexpr int kB = 2 * kKStages + 2 * kVStages;   // first barrier after the rings
@@ -368,20 +422,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_group = [&](int k) { return bar0 + 8u * (kB + 10 + k); };   // four warps of warpgroup k
     // "loaded segments" word of tile j: mask_words[j & 7], published with bar_mask(j & 7)
     auto bar_mask = [&](int m) { return bar0 + 8u * (kB + 12 + m); };
-    const uint32_t sm_k = sbase + kOffK;
-    const uint32_t sm_v = sbase + kOffV;
-    const uint32_t sm_q = sbase + kOffQ;
-    const uint32_t sm_p = sbase + kOffP;
+    // FP8 rings (kF8): producer -> converter
+    auto bar_k8full = [&](int s) { return bar0 + 8u * (kB + 20 + s); };
+    auto bar_k8empty = [&](int s) { return bar0 + 8u * (kB + 20 + k8Stages + s); };
+    auto bar_v8full = [&](int s) { return bar0 + 8u * (kB + 20 + 2 * k8Stages + s); };
+    auto bar_v8empty = [&](int s) { return bar0 + 8u * (kB + 20 + 3 * k8Stages + s); };
+    const uint32_t sm_k = sbase + C::kOffK;
+    const uint32_t sm_v = sbase + C::kOffV;
+    const uint32_t sm_q = sbase + C::kOffQ;
+    const uint32_t sm_p = sbase + C::kOffP;
 
     // ---- set-up (no global memory): barriers, zeroed Q / P buffers, TMEM ----
     if (threadIdx.x == 0) {
+        // with FP8 caches the bf16 K / V slots are filled by the four converter warps
+        const uint32_t fill_count = kF8 ? 4u : 1u;
         for (int s = 0; s < kKStages; ++s) {
-            mbar_init(bar_kfull(s), 1);
+            mbar_init(bar_kfull(s), fill_count);
             mbar_init(bar_kempty(s), 1);
         }
         for (int s = 0; s < kVStages; ++s) {
-            mbar_init(bar_vfull(s), 1);
+            mbar_init(bar_vfull(s), fill_count);
             mbar_init(bar_vempty(s), 1);
+        }
+        for (int s = 0; s < k8Stages; ++s) {
+            mbar_init(bar_k8full(s), 1);
+            mbar_init(bar_k8empty(s), 4);
+            mbar_init(bar_v8full(s), 1);
+            mbar_init(bar_v8empty(s), 4);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_qfull(b), 1);
@@ -404,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
         // Q rows past the group and P start at zero
         const uint4 z = make_uint4(0, 0, 0, 0);
-        uint4 *qp = reinterpret_cast<uint4 *>(smem + kOffQ);
+        uint4 *qp = reinterpret_cast<uint4 *>(smem + C::kOffQ);
         for (int i = threadIdx.x; i < (2 * kQBytes + 2 * kPBytes) / 16; i += kThreads) qp[i] = z;
     }
     if (warp == 1) {
@@ -419,11 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     pdl_wait();                // global memory is read from here on
     pdl_trigger();
-    uint8_t *lrem = smem + kOffLrem;
-    schedule_loads(a, pre, lrem, smem);
+    uint8_t *lrem = smem + C::kOffLrem;
+    schedule_loads<kF8>(a, pre, lrem, smem);
     fence_proxy_async();       // the zeroed V ring before any TMA write to it
     // red_max is free until the softmax starts: scratch for the scan
-    scan_prefix(a, pre, reinterpret_cast<int32_t *>(red_max));
+    scan_prefix<kThreads>(a, pre, reinterpret_cast<int32_t *>(red_max));
     const uint32_t tmem = *tmem_slot;
 
     const int G = a.G;
@@ -439,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // table lookup sits between a slot becoming free and its refill.  An
         // entry past the table width is parked as INT32_MIN.
         const bool is_v = warp == kWarpV;
-        int32_t *ent_buf = reinterpret_cast<int32_t *>(smem + kOffEnt) + (is_v ? 2 * kWinBlocks : 0);
+        int32_t *ent_buf = reinterpret_cast<int32_t *>(smem + C::kOffEnt) + (is_v ? 2 * kWinBlocks : 0);
         const int win_tiles = max(1, ((kWinBlocks - 1) * a.bs) / kTile);
         struct Win {
             Unit u;
@@ -517,10 +584,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             for (int jt = cur.t0; jt < cur.t1; ++jt, ++j) {
-                const int nst = is_v ? kVStages : kKStages;
+                // FP8 caches: the tile goes to the producer's FP8 ring, which the
+                // converter warpgroup drains
+                const int nst = kF8 ? k8Stages : (is_v ? kVStages : kKStages);
                 const int s = (int)(j % nst);
-                const uint32_t bar_e = is_v ? bar_vempty(s) : bar_kempty(s);
-                const uint32_t bar_f = is_v ? bar_vfull(s) : bar_kfull(s);
+                const uint32_t bar_e = kF8 ? (is_v ? bar_v8empty(s) : bar_k8empty(s))
+                                           : (is_v ? bar_vempty(s) : bar_kempty(s));
+                const uint32_t bar_f = kF8 ? (is_v ? bar_v8full(s) : bar_k8full(s))
+                                           : (is_v ? bar_vfull(s) : bar_kfull(s));
                 if (!mbar_wait_warp(bar_e, (uint32_t)((j / nst) & 1) ^ 1u, abort_flag)) break;
                 const int32_t ts = x.start + jt * kTile;
                 // lane i handles block segment i of the tile
@@ -546,20 +617,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the S MMA of tile j - kKStages completed, which is issued only after
                     // the softmax released tile j - kKStages - 2, so it is never more than
                     // kKStages + 2 <= 5 tiles ahead of the reader and phases cannot alias.
+                    // (FP8: only after the converter released the FP8 slot of tile j - 2,
+                    // which it converts after its own read of every earlier word and
+                    // only once the S MMA of tile j - 4 completed: 4 tiles ahead at most.)
                     if (!is_v) {
                         mask_words[j & 7] = ballot;
                         mbar_arrive(bar_mask((int)(j & 7)));
                     }
-                    const uint32_t bytes = (uint32_t)__popc(ballot) * (uint32_t)seg_rows * 128u * 2u;
+                    const uint32_t bytes = (uint32_t)__popc(ballot) * (uint32_t)seg_rows * 128u * (kF8 ? 1u : 2u);
                     mbar_arrive_expect_tx(bar_f, bytes);
                 }
                 __syncwarp();
                 if (load) {
-                    const uint32_t dst = (is_v ? sm_v : sm_k) + s * kTileBytes + lane * seg_rows * 128;
                     const CUtensorMap *map = is_v ? &tmV : &tmK;
                     const int z = (int)row0;
-                    tma_load_3d(dst, map, bar_f, 0, x.g, z);
-                    tma_load_3d(dst + kHalfBytes, map, bar_f, 64, x.g, z);
+                    if constexpr (kF8) {
+                        // one box of seg_rows rows x 128 codes (the whole head_dim)
+                        const uint32_t dst = sbase + (is_v ? C::kOffV8 : C::kOffK8) + s * kT8Bytes +
+                                             lane * seg_rows * 128;
+                        tma_load_3d(dst, map, bar_f, 0, x.g, z);
+                    } else {
+                        const uint32_t dst = (is_v ? sm_v : sm_k) + s * kTileBytes + lane * seg_rows * 128;
+                        tma_load_3d(dst, map, bar_f, 0, x.g, z);
+                        tma_load_3d(dst + kHalfBytes, map, bar_f, 64, x.g, z);
+                    }
                 }
                 __syncwarp();
             }
@@ -645,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && pending >= 0) issue_pv(pending, pending_stage);
         }
         __syncwarp();
-    } else {
+    } else if (warp < kWarpV) {
         // ================= softmax + output (two warpgroups of 128 threads) =================
         // Warpgroup k takes the tiles with (tile sequence number & 1) == k,
         // i.e. the S / P / O buffers of parity k, and writes partial slot
@@ -725,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 float corr[NQ];
-                uint8_t *pgen = smem + kOffP + b * kPBytes + p_row_off;
+                uint8_t *pgen = smem + C::kOffP + b * kPBytes + p_row_off;
 #pragma unroll
                 for (int n = 0; n < NQ; ++n) {
                     const float4 t4 = *reinterpret_cast<const float4 *>(rm + n * 4);
@@ -739,16 +820,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<__nv_bfloat16 *>(pgen + n * 128 + ((p_chunk ^ (n & 7)) << 4)) = pbv;
                 }
                 // V rows that were loaded but lie past the end must be zero for P.V
-                // (after the V tile has landed)
-                const bool zero_row = loaded && pos >= x.cend;
+                // (after the V tile has landed; with FP8 caches the converter writes
+                // zeros for every row it does not convert)
+                const bool zero_row = !kF8 && loaded && pos >= x.cend;
                 if (__any_sync(0xffffffffu, zero_row) &&
                     !mbar_wait_warp(bar_vfull(sv_slot), (uint32_t)((j / kVStages) & 1), abort_flag)) {
                     ok = false;
                     break;
                 }
                 if (zero_row) {
-                    uint4 *vrow0 = reinterpret_cast<uint4 *>(smem + kOffV + sv_slot * kTileBytes + row * 128);
-                    uint4 *vrow1 = reinterpret_cast<uint4 *>(smem + kOffV + sv_slot * kTileBytes + kHalfBytes + row * 128);
+                    uint4 *vrow0 = reinterpret_cast<uint4 *>(smem + C::kOffV + sv_slot * kTileBytes + row * 128);
+                    uint4 *vrow1 =
+                        reinterpret_cast<uint4 *>(smem + C::kOffV + sv_slot * kTileBytes + kHalfBytes + row * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         vrow0[c] = make_uint4(0, 0, 0, 0);
@@ -800,6 +883,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if constexpr (kF8) {
+        if (warp > kWarpV) {
+            // ================= converter (FP8 caches; warps 11..14: one tile row per thread) =================
+            // Walks the tiles in sequence: widens tile j's E4M3 K rows into bf16 K slot j % 2
+            // once the S MMA of tile j - 2 has released it, then its V rows likewise after the
+            // P.V MMA of tile j - 2.  Rows outside the tile's loaded, in-range positions are
+            // not converted: K rows there are masked by the softmax, V rows are written as
+            // zeros (P is 0 there, and 0 * anything stale must not be NaN).
+            const int crow = 32 * (warp & 3) + lane;   // warps 11..14 cover rows 96.., 0.., 32.., 64..
+            int64_t j = 0;
+            bool ok = true;
+            StreamK sk;
+            sk.init(a, pre, lrem);
+            Unit x;
+            while (ok && sk.next(a, x)) {
+                for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
+                    const int s8 = (int)(j % k8Stages);
+                    const uint32_t p8 = (uint32_t)((j / k8Stages) & 1);
+                    const int sk_ = (int)(j % kKStages);
+                    const int sv = (int)(j % kVStages);
+                    if (!mbar_wait_warp(bar_k8full(s8), p8, abort_flag) ||
+                        !mbar_wait_warp(bar_kempty(sk_), (uint32_t)((j / kKStages) & 1) ^ 1u, abort_flag) ||
+                        !mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t mword = mask_words[j & 7];
+                    const int32_t pos = x.start + jt * kTile + crow;
+                    const bool valid = ((mword >> (crow >> seg_shift)) & 1u) && pos < x.cend;
+                    if (valid)
+                        widen_row_e4m3(smem + C::kOffK8 + s8 * kT8Bytes, smem + C::kOffK + sk_ * kTileBytes, crow);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(bar_kfull(sk_));
+                        mbar_arrive(bar_k8empty(s8));
+                    }
+                    if (!mbar_wait_warp(bar_v8full(s8), p8, abort_flag) ||
+                        !mbar_wait_warp(bar_vempty(sv), (uint32_t)((j / kVStages) & 1) ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *vdst = smem + C::kOffV + sv * kTileBytes;
+                    if (valid) {
+                        widen_row_e4m3(smem + C::kOffV8 + s8 * kT8Bytes, vdst, crow);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            *reinterpret_cast<uint4 *>(vdst + crow * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(vdst + kHalfBytes + crow * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(bar_vfull(sv));
+                        mbar_arrive(bar_v8empty(s8));
+                    }
+                }
+            }
+        }
+    }
+
     // ---- teardown ----
     tc_fence_before();
     __syncthreads();
@@ -828,14 +974,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 static bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
-                      uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+                      uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                      CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
     const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+    return fn(m, type, 3, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -843,6 +990,7 @@ static bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1
 }  // namespace tc
 
 bool prepare_decode_tc(const DecodeArgs &a, TcLaunch *t) {
+    if (a.kv_fp8 && a.cp_world > 1) return false;   // FP8 caches are decoded without context parallelism
     if (a.dtype != BKV_BF16 || a.D != tc::kD || a.nq > tc::kN || a.nq <= 0) return false;
     if (a.bs < 8 || !((tc::kTile % a.bs == 0) || (a.bs % tc::kTile == 0))) return false;
     if (a.G > 256 || a.q_len > 256 || a.H_kv > 65535 || a.num_reqs > tc::kMaxReqs || !a.sk_pre) return false;
@@ -855,6 +1003,16 @@ bool prepare_decode_tc(const DecodeArgs &a, TcLaunch *t) {
     using namespace tc;
     t->seg_rows = a.bs < kTile ? a.bs : kTile;
     const uint64_t rows = (uint64_t)a.total_blocks * (uint64_t)a.bs;
+    if (a.kv_fp8) {
+        // E4M3 codes: one box of 128 codes (the whole head_dim, 128 bytes) per row
+        const uint64_t row_stride = (uint64_t)a.H_kv * kD;
+        const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        if (!encode_3d(&t->mk, a.k, kD, a.H_kv, rows, kD, row_stride, 128, 1, t->seg_rows, u8) ||
+            !encode_3d(&t->mv, a.v, kD, a.H_kv, rows, kD, row_stride, 128, 1, t->seg_rows, u8))
+            return false;
+        return encode_3d(&t->mq, a.q, kD, a.H_q, (uint64_t)a.num_reqs * a.q_len, kD * 2, (uint64_t)a.H_q * kD * 2,
+                         64, a.G, a.q_len);
+    }
     const uint64_t row_stride = (uint64_t)a.H_kv * kD * 2;
     return encode_3d(&t->mk, a.k, kD, a.H_kv, rows, kD * 2, row_stride, 64, 1, t->seg_rows) &&
            encode_3d(&t->mv, a.v, kD, a.H_kv, rows, kD * 2, row_stride, 64, 1, t->seg_rows) &&
@@ -862,30 +1020,40 @@ bool prepare_decode_tc(const DecodeArgs &a, TcLaunch *t) {
                      a.G, a.q_len);
 }
 
-int launch_decode_tc(const DecodeArgs &a, const TcLaunch &t, cudaStream_t st) {
+template <bool kF8>
+static int launch_variant(const DecodeArgs &a, const TcLaunch &t, cudaStream_t st) {
     using namespace tc;
+    using C = Cfg<kF8>;
     // the grid is the stream-K CTA count the workspace was laid out for
     const int64_t grid = a.sk_grid;
     // the softmax handles only the query rows that exist (4, 8 or 16 columns);
     // context parallelism (global-position masks) has its own instances
-    const bool cp = a.cp_world > 1;
-    auto kern = cp ? (a.nq <= 4 ? decode_tc_kernel<4, true>
-                                : (a.nq <= 8 ? decode_tc_kernel<8, true> : decode_tc_kernel<16, true>))
-                   : (a.nq <= 4 ? decode_tc_kernel<4, false>
-                                : (a.nq <= 8 ? decode_tc_kernel<8, false> : decode_tc_kernel<16, false>));
-    const int slot = (a.nq <= 4 ? 0 : (a.nq <= 8 ? 1 : 2)) + (cp ? 3 : 0);
-    static bool attr_set[64][6] = {};
+    const bool cp = !kF8 && a.cp_world > 1;
+    auto plain = a.nq <= 4 ? decode_tc_kernel<4, false, kF8>
+                           : (a.nq <= 8 ? decode_tc_kernel<8, false, kF8> : decode_tc_kernel<16, false, kF8>);
+    auto kern = plain;
+    if constexpr (!kF8) {
+        if (cp)
+            kern = a.nq <= 4 ? decode_tc_kernel<4, true, false>
+                             : (a.nq <= 8 ? decode_tc_kernel<8, true, false> : decode_tc_kernel<16, true, false>);
+    }
+    const int slot = (a.nq <= 4 ? 0 : (a.nq <= 8 ? 1 : 2)) + (cp ? 3 : 0) + (kF8 ? 6 : 0);
+    static bool attr_set[64][9] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev][slot]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
             return launch_status();
         attr_set[dev][slot] = true;
     }
-    const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, t.mk, t.mv, t.mq, a,
-                                     t.seg_rows);
+    const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(C::kThreads), C::kSmemBytes, st, t.mk, t.mv,
+                                     t.mq, a, t.seg_rows);
     if (e != cudaSuccess) set_cuda_error(e);
     return launch_status();
+}
+
+int launch_decode_tc(const DecodeArgs &a, const TcLaunch &t, cudaStream_t st) {
+    return a.kv_fp8 ? launch_variant<true>(a, t, st) : launch_variant<false>(a, t, st);
 }
 
 }  // namespace bkv

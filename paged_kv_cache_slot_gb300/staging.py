@@ -31,9 +31,14 @@ def _t(a: np.ndarray, device, dtype=None):
 
 class DeviceWorkload:
     def __init__(self, w: Workload, device="cuda", background: str = "nan", fill_prior: bool = True,
-                 sliding_window: int = 0, cp_world: int = 1, cp_rank: int = 0, cp_interleave: int = 1):
+                 sliding_window: int = 0, cp_world: int = 1, cp_rank: int = 0, cp_interleave: int = 1,
+                 kv_fp8=None):
         self.w = w
         self.window = int(sliding_window)   # decode's default sliding window (0: full attention)
+        # FP8 (E4M3) caches: (k_scale, v_scale); new rows are quantised by the cache write
+        self.fp8 = None if kv_fp8 is None else (float(kv_fp8[0]), float(kv_fp8[1]))
+        if self.fp8 is not None and int(cp_world) > 1:
+            raise ValueError("FP8 caches are not combined with context parallelism here")
         # decode context parallelism: this object is rank cp_rank of cp_world, holding only its
         # share of every request's tokens in a cache of its own (block_size == kernel block size)
         self.cp = (int(cp_world), int(cp_rank), int(cp_interleave))
@@ -47,9 +52,14 @@ class DeviceWorkload:
         else:
             table, total = w.block_table, w.total_kernel_blocks
         kshape = (total, w.kernel_block_size, w.num_kv_heads, w.head_dim)
-        fill = float("nan") if background == "nan" else 0.0
-        self.k_cache = torch.full(kshape, fill, dtype=self.tdtype, device=dev)
-        self.v_cache = torch.full(kshape, fill, dtype=self.tdtype, device=dev)
+        if self.fp8 is not None:
+            code = 0x7F if background == "nan" else 0   # 0x7F: the E4M3 NaN code
+            self.k_cache = torch.full(kshape, code, dtype=torch.uint8, device=dev)
+            self.v_cache = torch.full(kshape, code, dtype=torch.uint8, device=dev)
+        else:
+            fill = float("nan") if background == "nan" else 0.0
+            self.k_cache = torch.full(kshape, fill, dtype=self.tdtype, device=dev)
+            self.v_cache = torch.full(kshape, fill, dtype=self.tdtype, device=dev)
         self.mgr_table = _t(table, dev)
         self.kernel_table = torch.empty((w.num_rows, table.shape[1] * w.blocks_per_kv_block), dtype=torch.int32,
                                         device=dev)
@@ -102,7 +112,15 @@ class DeviceWorkload:
         kt, vt = _t(k, dev, cast), _t(v, dev, cast)
         slots = torch.empty(len(pos), dtype=torch.int64, device=dev)
         self._slots(self.kernel_table, _t(req, dev), _t(pos, dev), slots)
-        bkv.bkv_cache_write(kt, vt, slots, self.k_cache, self.v_cache, err_count=self.err_count)
+        self._write(kt, vt, slots)
+
+    def _write(self, k, v, slots, num_tokens=None, stream=None):
+        if self.fp8 is not None:
+            bkv.bkv_cache_write_fp8(k, v, slots, self.k_cache, self.v_cache, *self.fp8, num_tokens=num_tokens,
+                                    err_count=self.err_count, stream=stream)
+        else:
+            bkv.bkv_cache_write(k, v, slots, self.k_cache, self.v_cache, num_tokens=num_tokens,
+                                err_count=self.err_count, stream=stream)
 
     # -- the hot path ---------------------------------------------------------
     def expand_blocks(self, stream=None):
@@ -122,8 +140,7 @@ class DeviceWorkload:
     def write_step(self, stream=None):
         w = self.w
         self._slots(self.kernel_table, self.req_indices, self.positions, self.slot_mapping, w.num_tokens, stream)
-        bkv.bkv_cache_write(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
-                            num_tokens=w.num_tokens, err_count=self.err_count, stream=stream)
+        self._write(self.k_new, self.v_new, self.slot_mapping, w.num_tokens, stream)
 
     def decode(self, stream=None, out=None, table=None, mask_mode=bkv.BKV_MASK_CAUSAL, sliding_window=None):
         out = self.out if out is None else out
@@ -134,6 +151,11 @@ class DeviceWorkload:
                                     self.max_context_len, out, self.lse, self.workspace, *self.cp, mask_mode=mask_mode,
                                     err_count=self.err_count, stream=stream)
             return out
+        if self.fp8 is not None:
+            bkv.bkv_paged_decode_fp8(self.q, self.k_cache, self.v_cache, table, self.context_lens,
+                                     self.max_context_len, out, self.workspace, *self.fp8, mask_mode=mask_mode,
+                                     err_count=self.err_count, stream=stream, sliding_window=sliding_window)
+            return out
         bkv.bkv_paged_decode(self.q, self.k_cache, self.v_cache, table, self.context_lens, self.max_context_len,
                              out, self.workspace, mask_mode=mask_mode, err_count=self.err_count, stream=stream,
                              sliding_window=sliding_window)
@@ -141,6 +163,12 @@ class DeviceWorkload:
 
     def decode_partition(self, stream=None):
         """Phase 1 of the decode alone (the partition kernel), for timing."""
+        if self.fp8 is not None:
+            bkv.bkv_paged_decode_fp8_partition(self.q, self.k_cache, self.v_cache, self.kernel_table,
+                                               self.context_lens, self.max_context_len, self.out, self.workspace,
+                                               *self.fp8, err_count=self.err_count, stream=stream,
+                                               sliding_window=self.window)
+            return
         bkv.bkv_paged_decode_partition(self.q, self.k_cache, self.v_cache, self.kernel_table, self.context_lens,
                                        self.max_context_len, self.out, self.workspace, err_count=self.err_count,
                                        stream=stream, sliding_window=self.window)
@@ -165,9 +193,12 @@ class DeviceWorkload:
             W, k, inter = self.cp
             cyc = inter * W
             L = (L // cyc) * inter + np.clip(L % cyc - k * inter, 0, inter)
-        return int(L.sum()) * 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+        return int(L.sum()) * 2 * w.num_kv_heads * w.head_dim * self.cache_elem_bytes()
+
+    def cache_elem_bytes(self) -> int:
+        return 1 if self.fp8 is not None else self.w.elem_bytes
 
     def write_bytes(self) -> int:
         """Cache-write traffic: new K/V rows read + written, plus the slot ids."""
         w = self.w
-        return w.num_tokens * (4 * w.num_kv_heads * w.head_dim * w.elem_bytes + 8)
+        return w.num_tokens * (2 * w.num_kv_heads * w.head_dim * (w.elem_bytes + self.cache_elem_bytes()) + 8)

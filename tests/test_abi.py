@@ -112,3 +112,35 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(bkv, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         bkv.load()
+
+
+def test_fp8_entry_points_reject_bad_arguments(lib):
+    w = lib.bkv_cache_write_fp8
+    # src_dtype, scale <= 0, scale inf / nan, stride too small, null pointers, empty
+    assert w(NULL, NULL, 1, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 7, 1.0, 1.0, NULL, NULL) == bkv.BKV_ERR_UNSUPPORTED
+    assert w(NULL, NULL, 1, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 0, 0.0, 1.0, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
+    assert w(NULL, NULL, 1, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 0, 1.0, float("inf"), NULL, NULL) == \
+        bkv.BKV_ERR_INVALID_ARG
+    assert w(NULL, NULL, 1, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 0, float("nan"), 1.0, NULL, NULL) == \
+        bkv.BKV_ERR_INVALID_ARG
+    assert w(NULL, NULL, 1, 1023, NULL, NULL, NULL, 4, 16, 8, 128, 0, 1.0, 1.0, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
+    assert w(NULL, NULL, 1, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 0, 1.0, 1.0, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
+    assert w(NULL, NULL, 0, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 0, 1.0, 1.0, NULL, NULL) == bkv.BKV_OK
+    base = dict(q=NULL, k=NULL, v=NULL, bt=NULL, bt_stride=4, bt_cols=4, ctx=NULL, max_ctx=16, num_reqs=2, q_len=1,
+                hq=32, hkv=8, d=128, bs=16, tb=8, scale=0.0, ks=1.0, vs=1.0, mask=0, window=0, dtype=0, out=NULL,
+                ws=NULL, wsb=0, err=NULL, stream=NULL)
+    for fn in ("bkv_paged_decode_fp8", "bkv_paged_decode_fp8_partition", "bkv_paged_decode_fp8_merge"):
+        f = getattr(lib, fn)
+
+        def call(**kw):
+            a = dict(base, **kw)
+            return f(*a.values())
+
+        assert call(dtype=5) == bkv.BKV_ERR_UNSUPPORTED
+        assert call(d=512) == bkv.BKV_ERR_UNSUPPORTED
+        assert call(ks=0.0) == bkv.BKV_ERR_INVALID_ARG
+        assert call(vs=-1.0) == bkv.BKV_ERR_INVALID_ARG
+        assert call(vs=float("inf")) == bkv.BKV_ERR_INVALID_ARG
+        assert call(mask=2) == bkv.BKV_ERR_INVALID_ARG
+        assert call(hq=30) == bkv.BKV_ERR_INVALID_ARG
+        assert call() == bkv.BKV_ERR_INVALID_ARG            # null pointers / no workspace
