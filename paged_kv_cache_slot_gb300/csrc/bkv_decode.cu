@@ -400,7 +400,12 @@ bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int3
     const int64_t slots = slots_generic > slots_sk ? slots_generic : slots_sk;
     const int64_t prows = slots * nq;
     const int64_t o_bytes = ceil_div<int64_t>(prows * head_dim * 4, 256) * 256;
-    plan->ws_bytes = plan->header_bytes + (size_t)(o_bytes + prows * 2 * 4);
+    const int64_t part_bytes = ceil_div<int64_t>(o_bytes + prows * 2 * 4, 256) * 256;
+    // the FP8 tensor-core path's split queries: two E4M3 parts and a scale per row
+    const int64_t qrows = (int64_t)num_reqs * q_len * num_q_heads;
+    const int64_t q8_bytes = head_dim == 128 ? qrows * (2 * 128 + 4) : 0;
+    plan->q8_offset = plan->header_bytes + (size_t)part_bytes;
+    plan->ws_bytes = plan->q8_offset + (size_t)q8_bytes;
     return true;
 }
 
@@ -508,6 +513,9 @@ static int decode_setup(const void *q, const void *k_cache, const void *v_cache,
         a.ws_ml = reinterpret_cast<float *>(base + ceil_div<int64_t>(slots * plan.nq * head_dim * 4, 256) * 256);
     };
     const int64_t units = (int64_t)num_reqs * num_kv_heads;
+    a.q8 = head_dim == 128 ? static_cast<uint8_t *>(workspace) + plan.q8_offset : nullptr;
+    a.qexp = head_dim == 128 ? reinterpret_cast<float *>(a.q8 + (size_t)2 * num_reqs * q_len * num_q_heads * 128)
+                             : nullptr;
     a.parts = 2;
     a.sk_pre = static_cast<int32_t *>(workspace);
     a.sk_grid = plan.sk_grid;
@@ -522,7 +530,13 @@ static int decode_setup(const void *q, const void *k_cache, const void *v_cache,
 }
 
 static int decode_partition(DecodeCall &c, cudaStream_t st) {
-    if (c.tc) return launch_decode_tc(c.a, c.t, st);
+    if (c.tc) {
+        if (c.a.kv_fp8) {
+            const int rc = launch_q_split_e4m3(c.a, st);
+            if (rc != BKV_OK) return rc;
+        }
+        return launch_decode_tc(c.a, c.t, st);
+    }
     if (c.a.kv_fp8) {
         if (c.a.dtype == BKV_BF16) launch_generic_dpl<__nv_bfloat16, __nv_fp8_e4m3>(c.a, st);
         else launch_generic_dpl<float, __nv_fp8_e4m3>(c.a, st);

@@ -27,6 +27,8 @@ struct DecodeArgs {
     int dtype;         // BKV_BF16 or BKV_F32: q and out (and the caches unless kv_fp8)
     int kv_fp8;        // caches hold E4M3 codes: a key is code * k_scale (folded into scale_log2)
     float v_scale;     // and a value code * v_scale (applied by the merge); 1 otherwise
+    uint8_t *q8;       // FP8 tensor-core path: q split into two E4M3 parts [2][num_reqs * q_len][H_q][128]
+    float *qexp;       // and the power of two each query row was divided by first [num_reqs * q_len][H_q]
     int32_t chunk;     // tokens per split-KV partition (multiple of the tile and of bs)
     int32_t n_chunks;  // partitions per request at max_ctx
     int32_t G;         // query heads per KV head
@@ -88,6 +90,7 @@ struct DecodePlan {
     int32_t nq;
     int32_t sk_grid;
     size_t header_bytes;
+    size_t q8_offset;  // workspace offset of the FP8 path's split queries (head_dim 128 only)
     size_t ws_bytes;
 };
 
@@ -104,5 +107,7 @@ struct TcLaunch {
 };
 bool prepare_decode_tc(const DecodeArgs &a, TcLaunch *t);
 int launch_decode_tc(const DecodeArgs &a, const TcLaunch &t, cudaStream_t stream);
+// FP8 caches: the split of q into two E4M3 parts the tensor-core kernel reads.
+int launch_q_split_e4m3(const DecodeArgs &a, cudaStream_t stream);
 
 }  // namespace bkv

@@ -74,6 +74,15 @@ constexpr int kN = 16;                // query rows per MMA (padded)
 #define BKV_V_STAGES 3
 #endif
 static_assert(BKV_K_STAGES >= 2 && BKV_K_STAGES <= 3, "the 8-entry mask ring assumes at most 3 K slots");
+// FP8 caches: slots of the E4M3 K ring (read by the MMAs as loaded) and of
+// the E4M3 V ring (widened to f16 by the softmax warpgroups)
+#ifndef BKV_F8_K_STAGES
+#define BKV_F8_K_STAGES 4
+#endif
+#ifndef BKV_F8_STAGES
+#define BKV_F8_STAGES 4
+#endif
+static_assert(BKV_F8_K_STAGES >= 2 && BKV_F8_K_STAGES <= 5, "the 8-entry mask ring assumes at most 5 K slots");
 constexpr int kHalfBytes = kTile * 128;          // 128 rows x 64 bf16 (128 B): one head_dim half
 constexpr int kTileBytes = 2 * kHalfBytes;       // K or V tile: 32 KB
 constexpr int kT8Bytes = kTile * 128;            // an FP8 K or V tile as loaded: 128 rows x 128 codes, 16 KB
@@ -86,26 +95,27 @@ constexpr int kMaxReqs = 2048;                   // requests the in-kernel tile 
 constexpr int kWinBlocks = 128;                  // table entries a producer caches per window
 
 // Shared-memory layout and role counts (offsets from a 1024-aligned base).
-// kF8: FP8 caches.  The producers load E4M3 tiles into their own 2-slot rings
-// and a converter warpgroup (warps 11..14) widens every tile to bf16 (exactly:
-// each E4M3 value is a bf16 value) into 2-slot bf16 rings the MMAs read.
+// kF8: FP8 caches.  S = K Q^T runs on E4M3 operands (kind::f8f6f4): K tiles
+// straight from TMA, q as two E4M3 parts prepared by q_split_e4m3_kernel.
+// P V runs on f16 operands: each softmax warpgroup widens its tiles' E4M3 V
+// rows to f16 (exactly) into its own V slot and writes P as f16.
 template <bool kF8>
 struct Cfg {
-    static constexpr int kThreads = kF8 ? 480 : 352;   // + the converter warpgroup
-    static constexpr int kKStages = kF8 ? 2 : BKV_K_STAGES;
-    static constexpr int kVStages = kF8 ? 2 : BKV_V_STAGES;
-    static constexpr int k8Stages = kF8 ? 2 : 0;       // FP8 slots per ring
+    static constexpr int kThreads = 352;                 // K producer, MMA, two softmax warpgroups, V producer
+    static constexpr int kKStages = kF8 ? BKV_F8_K_STAGES : BKV_K_STAGES;
+    static constexpr int kVStages = kF8 ? 2 : BKV_V_STAGES;   // FP8: one f16 V slot per softmax warpgroup
+    static constexpr int k8Stages = kF8 ? BKV_F8_STAGES : 0;  // E4M3 V slots
+    static constexpr int kKSlot = kF8 ? kT8Bytes : kTileBytes;
     static constexpr int kOffK = 0;                                  // kKStages K slots
-    static constexpr int kOffV = kOffK + kKStages * kTileBytes;      // kVStages V slots
-    static constexpr int kOffK8 = kOffV + kVStages * kTileBytes;     // k8Stages FP8 K slots
-    static constexpr int kOffV8 = kOffK8 + k8Stages * kT8Bytes;      // k8Stages FP8 V slots
+    static constexpr int kOffV = kOffK + kKStages * kKSlot;          // kVStages V slots
+    static constexpr int kOffV8 = kOffV + kVStages * kTileBytes;     // k8Stages E4M3 V slots
     static constexpr int kOffQ = kOffV8 + k8Stages * kT8Bytes;
     static constexpr int kOffP = kOffQ + 2 * kQBytes;
     static constexpr int kOffMask = kOffP + 2 * kPBytes;             // 8 words: loaded segments per tile (ring)
     static constexpr int kOffRedMax = kOffMask + 64;                 // [warpgroup][2][16 rows][4 warps] floats
     static constexpr int kOffRedSum = kOffRedMax + 4 * kN * 4 * 4;   // [warpgroup][16 rows][4 warps] floats
     static constexpr int kOffBar = kOffRedSum + 2 * kN * 4 * 4;      // barriers (8 B each)
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 8 + 4 * k8Stages;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 8 + 2 * k8Stages;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffPre = kOffAbort + 4;                    // [kMaxReqs + 1] tile prefix per request
@@ -118,8 +128,9 @@ struct Cfg {
     static constexpr int kLensPerThread = (kMaxReqs + kThreads - 1) / kThreads;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
     static_assert(kOffEnt % 16 == 0, "entry buffers must stay aligned");
-    static_assert(kOffK8 % 1024 == 0 && kOffV8 % 1024 == 0 && kOffQ % 1024 == 0, "swizzled tiles need 1 KB alignment");
-    static_assert(kWarpV == (kF8 ? 10 : kThreads / 32 - 1), "warp roles");
+    static_assert(kOffV % 1024 == 0 && kOffV8 % 1024 == 0 && kOffQ % 1024 == 0, "swizzled tiles need 1 KB alignment");
+    static_assert(kWarpV == kThreads / 32 - 1, "warp roles");
+    static_assert(!kF8 || kVStages == 2, "FP8: each softmax warpgroup widens its tiles' V into its own slot");
 };
 
 // The first NQ accumulator columns of this thread's TMEM lane.
@@ -351,34 +362,74 @@ __device__ __forceinline__ bool reduced_writer(int lane) {
     return (lane & ((1 << (5 - k)) - 1)) == 0;
 }
 
-// Two E4M3 codes (low byte first) as two bf16 values in one word, exactly:
-// every E4M3 value, NaN included, is a half and a bf16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-    return *reinterpret_cast<const uint32_t *>(&b);
+// E4M3 codes to f16 for the MMAs.  Two ways, both exact:
+// * BKV_F8_HWCVT: the hardware conversion (one instruction per two codes),
+//   giving the codes' values;
+// * otherwise byte-parallel integer operations on four codes at a time,
+//   giving the values times 2^-8: with a code's exponent field e (4 bits) and
+//   mantissa m (3 bits), the f16 with sign bit 15, exponent field e and
+//   mantissa m << 7 is 2^(e-15) (1 + m/8) for e > 0 and the subnormal
+//   m 2^-17 for e = 0, i.e. the E4M3 value 2^(e-7) (1 + m/8), resp. m 2^-9,
+//   times 2^-8.  Its high byte is sign | (e m) >> 1 and its low byte
+//   (m & 1) << 7; the NaN codes (magnitude 0x7F) also set high-byte bit 6,
+//   which makes an f16 NaN.
+// kF8Unscale is the factor the scores and the output take back (exactly).
+#ifndef BKV_F8_HWCVT
+#define BKV_F8_HWCVT 1
+#endif
+constexpr float kF8Unscale = BKV_F8_HWCVT ? 1.f : 256.f;
+
+// Four codes (byte k = code k) -> four f16 in two words (codes 0, 1 in a; 2, 3 in b).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &a, uint32_t &b) {
+#if BKV_F8_HWCVT
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+    a = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+    b = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+#else
+    const uint32_t mag = w & 0x7F7F7F7Fu;
+    const uint32_t nan7 = (mag + 0x01010101u) & 0x80808080u;          // 0x80 in the bytes with mag 0x7F
+    const uint32_t hb = (((mag | nan7) >> 1) & 0x7F7F7F7Fu) | (w & 0x80808080u);
+    const uint32_t lb = (w << 7) & 0x80808080u;
+    a = __byte_perm(lb, hb, 0x5140);   // [lb0 hb0 lb1 hb1]
+    b = __byte_perm(lb, hb, 0x7362);   // [lb2 hb2 lb3 hb3]
+#endif
 }
 
 // Row r of an E4M3 tile as TMA leaves it (128-byte rows, 16-byte chunk c of
-// row r at chunk c ^ (r & 7)) into row r of a bf16 tile in the MMA layout
+// row r at chunk c ^ (r & 7)) into row r of an f16 tile in the MMA layout
 // (two head_dim halves of 128-byte rows, the same chunk swizzle): code chunk
-// c (head_dim 16c .. 16c + 15) becomes bf16 chunks 2(c & 3), 2(c & 3) + 1 of
+// c (head_dim 16c .. 16c + 15) becomes f16 chunks 2(c & 3), 2(c & 3) + 1 of
 // half c / 4.  Conflict-free when consecutive lanes take consecutive rows.
-__device__ __forceinline__ void widen_row_e4m3(const uint8_t *src_tile, uint8_t *dst_tile, int r) {
+__device__ __forceinline__ void widen_row_e4m3(const uint8_t *__restrict__ src_tile, uint8_t *__restrict__ dst_tile,
+                                               int r) {
     const uint8_t *src = src_tile + r * 128;
     const int sw = r & 7;
+    // all eight loads first: the stores could otherwise not pass the next load
+    uint4 w[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) w[c] = *reinterpret_cast<const uint4 *>(src + ((c ^ sw) << 4));
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(src + ((c ^ sw) << 4));
-        const uint4 lo = make_uint4(e4m3x2_to_bf16x2(w.x & 0xFFFFu), e4m3x2_to_bf16x2(w.x >> 16),
-                                    e4m3x2_to_bf16x2(w.y & 0xFFFFu), e4m3x2_to_bf16x2(w.y >> 16));
-        const uint4 hi = make_uint4(e4m3x2_to_bf16x2(w.z & 0xFFFFu), e4m3x2_to_bf16x2(w.z >> 16),
-                                    e4m3x2_to_bf16x2(w.w & 0xFFFFu), e4m3x2_to_bf16x2(w.w >> 16));
+        uint4 lo, hi;
+        e4m3x4_to_f16x4(w[c].x, lo.x, lo.y);
+        e4m3x4_to_f16x4(w[c].y, lo.z, lo.w);
+        e4m3x4_to_f16x4(w[c].z, hi.x, hi.y);
+        e4m3x4_to_f16x4(w[c].w, hi.z, hi.w);
         uint8_t *dst = dst_tile + (c >> 2) * kHalfBytes + r * 128;
         const int c2 = 2 * (c & 3);
         *reinterpret_cast<uint4 *>(dst + ((c2 ^ sw) << 4)) = lo;
         *reinterpret_cast<uint4 *>(dst + (((c2 + 1) ^ sw) << 4)) = hi;
+    }
+}
+
+// Row r of a widened tile as zeros (a row no load wrote: P is 0 there, and
+// 0 times stale bits must not be NaN).
+__device__ __forceinline__ void zero_row_f16(uint8_t *dst_tile, int r) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        *reinterpret_cast<uint4 *>(dst_tile + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(dst_tile + kHalfBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -422,11 +473,9 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
     auto bar_group = [&](int k) { return bar0 + 8u * (kB + 10 + k); };   // four warps of warpgroup k
     // "loaded segments" word of tile j: mask_words[j & 7], published with bar_mask(j & 7)
     auto bar_mask = [&](int m) { return bar0 + 8u * (kB + 12 + m); };
-    // FP8 rings (kF8): producer -> converter
-    auto bar_k8full = [&](int s) { return bar0 + 8u * (kB + 20 + s); };
-    auto bar_k8empty = [&](int s) { return bar0 + 8u * (kB + 20 + k8Stages + s); };
-    auto bar_v8full = [&](int s) { return bar0 + 8u * (kB + 20 + 2 * k8Stages + s); };
-    auto bar_v8empty = [&](int s) { return bar0 + 8u * (kB + 20 + 3 * k8Stages + s); };
+    // E4M3 V ring (kF8): V producer -> the softmax warpgroup that widens the tile
+    auto bar_v8full = [&](int s) { return bar0 + 8u * (kB + 20 + s); };
+    auto bar_v8empty = [&](int s) { return bar0 + 8u * (kB + 20 + k8Stages + s); };
     const uint32_t sm_k = sbase + C::kOffK;
     const uint32_t sm_v = sbase + C::kOffV;
     const uint32_t sm_q = sbase + C::kOffQ;
@@ -434,19 +483,16 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
 
     // ---- set-up (no global memory): barriers, zeroed Q / P buffers, TMEM ----
     if (threadIdx.x == 0) {
-        // with FP8 caches the bf16 K / V slots are filled by the four converter warps
-        const uint32_t fill_count = kF8 ? 4u : 1u;
         for (int s = 0; s < kKStages; ++s) {
-            mbar_init(bar_kfull(s), fill_count);
+            mbar_init(bar_kfull(s), 1);
             mbar_init(bar_kempty(s), 1);
         }
+        // with FP8 caches the f16 V slots are filled by the four warps of a softmax warpgroup
         for (int s = 0; s < kVStages; ++s) {
-            mbar_init(bar_vfull(s), fill_count);
+            mbar_init(bar_vfull(s), kF8 ? 4u : 1u);
             mbar_init(bar_vempty(s), 1);
         }
         for (int s = 0; s < k8Stages; ++s) {
-            mbar_init(bar_k8full(s), 1);
-            mbar_init(bar_k8empty(s), 4);
             mbar_init(bar_v8full(s), 1);
             mbar_init(bar_v8empty(s), 4);
         }
@@ -579,19 +625,25 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(bar_qfull(qb), 2u * 128u * (uint32_t)nq);
                     const uint32_t dq = sm_q + qb * kQBytes;
-                    tma_load_3d(dq, &tmQ, bar_qfull(qb), 0, x.g * G, x.r * a.q_len);
-                    tma_load_3d(dq + kN * 128, &tmQ, bar_qfull(qb), 64, x.g * G, x.r * a.q_len);
+                    if constexpr (kF8) {
+                        // the two E4M3 parts of the rows, 128 codes each: part p of token row
+                        // t is row p * num_reqs * q_len + t of the split map
+                        const int rows = a.num_reqs * a.q_len;
+                        tma_load_3d(dq, &tmQ, bar_qfull(qb), 0, x.g * G, x.r * a.q_len);
+                        tma_load_3d(dq + kN * 128, &tmQ, bar_qfull(qb), 0, x.g * G, rows + x.r * a.q_len);
+                    } else {
+                        tma_load_3d(dq, &tmQ, bar_qfull(qb), 0, x.g * G, x.r * a.q_len);
+                        tma_load_3d(dq + kN * 128, &tmQ, bar_qfull(qb), 64, x.g * G, x.r * a.q_len);
+                    }
                 }
             }
             for (int jt = cur.t0; jt < cur.t1; ++jt, ++j) {
-                // FP8 caches: the tile goes to the producer's FP8 ring, which the
-                // converter warpgroup drains
-                const int nst = kF8 ? k8Stages : (is_v ? kVStages : kKStages);
+                // FP8 caches: V tiles go to the E4M3 V ring, which the softmax
+                // warpgroups drain; K tiles go to the K ring the MMAs read
+                const int nst = (kF8 && is_v) ? k8Stages : (is_v ? kVStages : kKStages);
                 const int s = (int)(j % nst);
-                const uint32_t bar_e = kF8 ? (is_v ? bar_v8empty(s) : bar_k8empty(s))
-                                           : (is_v ? bar_vempty(s) : bar_kempty(s));
-                const uint32_t bar_f = kF8 ? (is_v ? bar_v8full(s) : bar_k8full(s))
-                                           : (is_v ? bar_vfull(s) : bar_kfull(s));
+                const uint32_t bar_e = (kF8 && is_v) ? bar_v8empty(s) : (is_v ? bar_vempty(s) : bar_kempty(s));
+                const uint32_t bar_f = (kF8 && is_v) ? bar_v8full(s) : (is_v ? bar_vfull(s) : bar_kfull(s));
                 if (!mbar_wait_warp(bar_e, (uint32_t)((j / nst) & 1) ^ 1u, abort_flag)) break;
                 const int32_t ts = x.start + jt * kTile;
                 // lane i handles block segment i of the tile
@@ -617,9 +669,6 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     // the S MMA of tile j - kKStages completed, which is issued only after
                     // the softmax released tile j - kKStages - 2, so it is never more than
                     // kKStages + 2 <= 5 tiles ahead of the reader and phases cannot alias.
-                    // (FP8: only after the converter released the FP8 slot of tile j - 2,
-                    // which it converts after its own read of every earlier word and
-                    // only once the S MMA of tile j - 4 completed: 4 tiles ahead at most.)
                     if (!is_v) {
                         mask_words[j & 7] = ballot;
                         mbar_arrive(bar_mask((int)(j & 7)));
@@ -633,7 +682,7 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     const int z = (int)row0;
                     if constexpr (kF8) {
                         // one box of seg_rows rows x 128 codes (the whole head_dim)
-                        const uint32_t dst = sbase + (is_v ? C::kOffV8 : C::kOffK8) + s * kT8Bytes +
+                        const uint32_t dst = sbase + (is_v ? C::kOffV8 : C::kOffK) + s * kT8Bytes +
                                              lane * seg_rows * 128;
                         tma_load_3d(dst, map, bar_f, 0, x.g, z);
                     } else {
@@ -659,8 +708,10 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
     } else if (warp == 1) {
         // ================= MMA issuer (one thread) =================
         if (lane == 0) {
-            constexpr uint32_t kIdescS = idesc_bf16(128, kN, 0, 0);   // K (K-major) x Q (K-major)
-            constexpr uint32_t kIdescO = idesc_bf16(128, kN, 1, 0);   // V^T (MN-major) x P (K-major)
+            // K (K-major) x Q (K-major); V^T (MN-major) x P (K-major).  FP8 caches: S on E4M3
+            // operands (the descriptor's E4M3 type codes are 0, as f16's), P V on f16 operands
+            constexpr uint32_t kIdescS = kF8 ? idesc_f16(128, kN, 0, 0) : idesc_bf16(128, kN, 0, 0);
+            constexpr uint32_t kIdescO = kF8 ? idesc_f16(128, kN, 1, 0) : idesc_bf16(128, kN, 1, 0);
             int64_t j = 0;
             int us = 0;
             int64_t pending = -1;        // tile whose P.V MMA is still to be issued
@@ -701,15 +752,29 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t k_base = sm_k + s * kTileBytes;
                     const uint32_t q_base = sm_q + qb * kQBytes;
                     const uint32_t d_tmem = tmem + 16u * (uint32_t)(j & 1);
+                    if constexpr (kF8) {
+                        // S^T = K (E4M3, 128-code rows) . (Q_1 + Q_2)^T: two parts of four
+                        // 32-code steps, accumulated in one TMEM tile
+                        const uint32_t k_base = sm_k + s * kT8Bytes;
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint32_t half = (uint32_t)(kk >> 2) * kHalfBytes;
-                        const uint64_t adesc = sdesc(k_base + half + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bdesc = sdesc(q_base + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
-                        mma_bf16(d_tmem, adesc, bdesc, kIdescS, kk > 0);
+                        for (int part = 0; part < 2; ++part)
+#pragma unroll
+                            for (int kk = 0; kk < kD / 32; ++kk) {
+                                const uint64_t adesc = sdesc(k_base + kk * 32, 16, 1024);
+                                const uint64_t bdesc = sdesc(q_base + part * (kN * 128) + kk * 32, 16, 1024);
+                                mma_f8(d_tmem, adesc, bdesc, kIdescS, (part | kk) > 0);
+                            }
+                    } else {
+                        const uint32_t k_base = sm_k + s * kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint32_t half = (uint32_t)(kk >> 2) * kHalfBytes;
+                            const uint64_t adesc = sdesc(k_base + half + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bdesc = sdesc(q_base + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+                            mma_bf16(d_tmem, adesc, bdesc, kIdescS, kk > 0);
+                        }
                     }
                     mma_commit(bar_sfull((int)(j & 1)));
                     mma_commit(bar_kempty(s));
@@ -732,6 +797,10 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         // i.e. the S / P / O buffers of parity k, and writes partial slot
         // 2 (CTA + stream) + k of every unit.
         const int wg = (warp - 2) >> 2;
+        // FP8 caches: query row i entered the S MMA divided by qexp[i] (a power of two),
+        // taken back per column below; the values may enter the P.V MMA as 2^-8 times
+        // theirs (kF8Unscale), taken back at the partial output
+        const float s_scale = a.scale_log2;
         const int row = 32 * (warp & 3) + lane;          // TMEM lane: position in tile / head_dim row
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const int wq = warp & 3;
@@ -768,12 +837,16 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 Lg = c > a.max_ctx ? a.max_ctx : c;
             }
             int32_t lastv[NQ], firstv[NQ];
+            float cs[NQ];   // score scale of each query column
 #pragma unroll
             for (int n = 0; n < NQ; ++n) {
                 o[n] = 0.f;
                 lsum[n] = 0.f;
                 mrun[n] = -INFINITY;
                 const int t = n / G;
+                cs[n] = s_scale;
+                if (kF8 && n < nq)
+                    cs[n] = s_scale * __ldg(a.qexp + ((int64_t)x.r * a.q_len + t) * a.H_q + x.g * G + (n - t * G));
                 lastv[n] = (n < nq) ? (a.mask_mode == 0 ? Lg - a.q_len + t : Lg - 1) : -1;
                 firstv[n] = a.window > 0 ? Lg - a.q_len + t - a.window + 1 : INT32_MIN;
             }
@@ -782,6 +855,29 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 const int sv_slot = (int)(j % kVStages);
                 const int b = wg;
                 const uint32_t par = (uint32_t)((j >> 1) & 1);
+                if constexpr (kF8) {
+                    // widen this tile's E4M3 V rows into this warpgroup's V slot (j % 2 == wg;
+                    // its previous P.V, two tiles back, completed before that tile's O update),
+                    // zeros where nothing was loaded or past the end
+                    const int s8 = (int)(j % k8Stages);
+                    if (!mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag) ||
+                        !mbar_wait_warp(bar_v8full(s8), (uint32_t)((j / k8Stages) & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int32_t vpos = x.start + jt * kTile + row;
+                    uint8_t *vdst = smem + C::kOffV + sv_slot * kTileBytes;
+                    if (((mask_words[j & 7] >> (row >> seg_shift)) & 1u) && vpos < x.cend)
+                        widen_row_e4m3(smem + C::kOffV8 + s8 * kT8Bytes, vdst, row);
+                    else
+                        zero_row_f16(vdst, row);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(bar_vfull(sv_slot));
+                        mbar_arrive(bar_v8empty(s8));
+                    }
+                }
                 if (!mbar_wait_warp(bar_sfull(b), par, abort_flag) ||
                     !mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag)) {
                     ok = false;
@@ -796,7 +892,7 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 const int32_t gpos = kCP ? cp_global32(a, pos) : pos;
 #pragma unroll
                 for (int n = 0; n < NQ; ++n)
-                    sv[n] = (inrange && gpos <= lastv[n] && gpos >= firstv[n]) ? sv[n] * a.scale_log2 : -INFINITY;
+                    sv[n] = (inrange && gpos <= lastv[n] && gpos >= firstv[n]) ? sv[n] * cs[n] : -INFINITY;
                 // tile max per query row across the warpgroup's 128 threads
                 const float wmax = warp_reduce_rows<true, NQ>(sv, lane);
                 float *rm = red_max + (wg * 2 + (int)par) * (kN * 4);
@@ -815,9 +911,16 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     corr[n] = (mn == -INFINITY) ? 1.f : fast_exp2(mrun[n] - mn);
                     mrun[n] = mn;
                     const float p = (sv[n] == -INFINITY) ? 0.f : fast_exp2(sv[n] - mn);
-                    const __nv_bfloat16 pbv = __float2bfloat16_rn(p);
-                    lsum[n] = fmaf(lsum[n], corr[n], __bfloat162float(pbv));
-                    *reinterpret_cast<__nv_bfloat16 *>(pgen + n * 128 + ((p_chunk ^ (n & 7)) << 4)) = pbv;
+                    // P as the MMA's operand type; the sum takes the rounded weights
+                    if constexpr (kF8) {
+                        const __half pv = __float2half_rn(p);
+                        lsum[n] = fmaf(lsum[n], corr[n], __half2float(pv));
+                        *reinterpret_cast<__half *>(pgen + n * 128 + ((p_chunk ^ (n & 7)) << 4)) = pv;
+                    } else {
+                        const __nv_bfloat16 pbv = __float2bfloat16_rn(p);
+                        lsum[n] = fmaf(lsum[n], corr[n], __bfloat162float(pbv));
+                        *reinterpret_cast<__nv_bfloat16 *>(pgen + n * 128 + ((p_chunk ^ (n & 7)) << 4)) = pbv;
+                    }
                 }
                 // V rows that were loaded but lie past the end must be zero for P.V
                 // (after the V tile has landed; with FP8 caches the converter writes
@@ -865,7 +968,7 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 const int64_t prow0 = (2 * ((int64_t)blockIdx.x + x.s) + wg) * nq;
 #pragma unroll
                 for (int n = 0; n < NQ; ++n)
-                    if (n < nq) a.ws_o[(prow0 + n) * kD + row] = o[n];
+                    if (n < nq) a.ws_o[(prow0 + n) * kD + row] = kF8 ? o[n] * kF8Unscale : o[n];
                 if (row < nq) {
                     const float4 t4 = *reinterpret_cast<const float4 *>(my_red_sum + row * 4);
                     float m_row = -INFINITY;
@@ -883,69 +986,6 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         }
     }
 
-    if constexpr (kF8) {
-        if (warp > kWarpV) {
-            // ================= converter (FP8 caches; warps 11..14: one tile row per thread) =================
-            // Walks the tiles in sequence: widens tile j's E4M3 K rows into bf16 K slot j % 2
-            // once the S MMA of tile j - 2 has released it, then its V rows likewise after the
-            // P.V MMA of tile j - 2.  Rows outside the tile's loaded, in-range positions are
-            // not converted: K rows there are masked by the softmax, V rows are written as
-            // zeros (P is 0 there, and 0 * anything stale must not be NaN).
-            const int crow = 32 * (warp & 3) + lane;   // warps 11..14 cover rows 96.., 0.., 32.., 64..
-            int64_t j = 0;
-            bool ok = true;
-            StreamK sk;
-            sk.init(a, pre, lrem);
-            Unit x;
-            while (ok && sk.next(a, x)) {
-                for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
-                    const int s8 = (int)(j % k8Stages);
-                    const uint32_t p8 = (uint32_t)((j / k8Stages) & 1);
-                    const int sk_ = (int)(j % kKStages);
-                    const int sv = (int)(j % kVStages);
-                    if (!mbar_wait_warp(bar_k8full(s8), p8, abort_flag) ||
-                        !mbar_wait_warp(bar_kempty(sk_), (uint32_t)((j / kKStages) & 1) ^ 1u, abort_flag) ||
-                        !mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t mword = mask_words[j & 7];
-                    const int32_t pos = x.start + jt * kTile + crow;
-                    const bool valid = ((mword >> (crow >> seg_shift)) & 1u) && pos < x.cend;
-                    if (valid)
-                        widen_row_e4m3(smem + C::kOffK8 + s8 * kT8Bytes, smem + C::kOffK + sk_ * kTileBytes, crow);
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(bar_kfull(sk_));
-                        mbar_arrive(bar_k8empty(s8));
-                    }
-                    if (!mbar_wait_warp(bar_v8full(s8), p8, abort_flag) ||
-                        !mbar_wait_warp(bar_vempty(sv), (uint32_t)((j / kVStages) & 1) ^ 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *vdst = smem + C::kOffV + sv * kTileBytes;
-                    if (valid) {
-                        widen_row_e4m3(smem + C::kOffV8 + s8 * kT8Bytes, vdst, crow);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            *reinterpret_cast<uint4 *>(vdst + crow * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                            *reinterpret_cast<uint4 *>(vdst + kHalfBytes + crow * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                        }
-                    }
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(bar_vfull(sv));
-                        mbar_arrive(bar_v8empty(s8));
-                    }
-                }
-            }
-        }
-    }
-
     // ---- teardown ----
     tc_fence_before();
     __syncthreads();
@@ -954,6 +994,47 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
+}
+
+// ---------------------------------------------------------------------------
+// FP8 caches: the queries as two E4M3 parts for the S MMA
+// ---------------------------------------------------------------------------
+// Row i of q (one query token and head, 128 bf16 values) with absolute maximum
+// m is scaled by 2^-e, e = floor(log2 m) - 7, so that its largest element
+// lies in [128, 256); each scaled element x is written as hi = E4M3(x) (round
+// to nearest) and lo = E4M3(x - hi).  x has at most 8 significant bits, so
+// x - hi is a multiple of ulp(x) / 128 of at most 8 of them: hi + lo = x
+// exactly when |x| >= 2^-2 (the step of E4M3 subnormals is 2^-9), and
+// otherwise within 2^-10, i.e. 2^-17 of the row's largest element.
+// qexp[i] = 2^e restores the scale of the row's scores.  One warp per row.
+__global__ void __launch_bounds__(256) q_split_e4m3_kernel(const __nv_bfloat16 *__restrict__ q, int64_t rows,
+                                                           uint8_t *__restrict__ q8, float *__restrict__ qexp) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const uint2 raw = *reinterpret_cast<const uint2 *>(q + row * kD + 4 * lane);
+    const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+    const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+    const float x[4] = {x01.x, x01.y, x23.x, x23.y};
+    float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int e = (m > 0.f && m <= 3.402823466e38f) ? ilogbf(m) - 7 : 0;
+    uint32_t hi = 0, lo = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float xs = ldexpf(x[i], -e);
+        const __nv_fp8_storage_t h = __nv_cvt_float_to_fp8(xs, __NV_SATFINITE, __NV_E4M3);
+        const float hf = __half2float(__half(__nv_cvt_fp8_to_halfraw(h, __NV_E4M3)));
+        const __nv_fp8_storage_t l = __nv_cvt_float_to_fp8(xs - hf, __NV_SATFINITE, __NV_E4M3);
+        hi |= (uint32_t)h << (8 * i);
+        lo |= (uint32_t)l << (8 * i);
+    }
+    *reinterpret_cast<uint32_t *>(q8 + row * kD + 4 * lane) = hi;
+    *reinterpret_cast<uint32_t *>(q8 + (rows + row) * kD + 4 * lane) = lo;
+    if (lane == 0) qexp[row] = ldexpf(1.f, e);
 }
 
 // ---------------------------------------------------------------------------
@@ -1004,14 +1085,16 @@ bool prepare_decode_tc(const DecodeArgs &a, TcLaunch *t) {
     t->seg_rows = a.bs < kTile ? a.bs : kTile;
     const uint64_t rows = (uint64_t)a.total_blocks * (uint64_t)a.bs;
     if (a.kv_fp8) {
-        // E4M3 codes: one box of 128 codes (the whole head_dim, 128 bytes) per row
+        // E4M3 codes: one box of 128 codes (the whole head_dim, 128 bytes) per row;
+        // the split queries (two parts stacked along the token rows) likewise
+        if (!a.q8 || !aligned(a.q8, 16)) return false;
         const uint64_t row_stride = (uint64_t)a.H_kv * kD;
         const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
         if (!encode_3d(&t->mk, a.k, kD, a.H_kv, rows, kD, row_stride, 128, 1, t->seg_rows, u8) ||
             !encode_3d(&t->mv, a.v, kD, a.H_kv, rows, kD, row_stride, 128, 1, t->seg_rows, u8))
             return false;
-        return encode_3d(&t->mq, a.q, kD, a.H_q, (uint64_t)a.num_reqs * a.q_len, kD * 2, (uint64_t)a.H_q * kD * 2,
-                         64, a.G, a.q_len);
+        return encode_3d(&t->mq, a.q8, kD, a.H_q, 2 * (uint64_t)a.num_reqs * a.q_len, kD, (uint64_t)a.H_q * kD, 128,
+                         a.G, a.q_len, u8);
     }
     const uint64_t row_stride = (uint64_t)a.H_kv * kD * 2;
     return encode_3d(&t->mk, a.k, kD, a.H_kv, rows, kD * 2, row_stride, 64, 1, t->seg_rows) &&
@@ -1048,6 +1131,17 @@ static int launch_variant(const DecodeArgs &a, const TcLaunch &t, cudaStream_t s
     }
     const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(C::kThreads), C::kSmemBytes, st, t.mk, t.mv,
                                      t.mq, a, t.seg_rows);
+    if (e != cudaSuccess) set_cuda_error(e);
+    return launch_status();
+}
+
+int launch_q_split_e4m3(const DecodeArgs &a, cudaStream_t st) {
+    const int64_t rows = (int64_t)a.num_reqs * a.q_len * a.H_q;
+    const int64_t blocks = (rows + 7) / 8;
+    if (blocks <= 0) return BKV_OK;
+    if (blocks > 0x7fffffff) return BKV_ERR_INVALID_ARG;
+    const cudaError_t e = launch_pdl(tc::q_split_e4m3_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                                     static_cast<const __nv_bfloat16 *>(a.q), rows, a.q8, a.qexp);
     if (e != cudaSuccess) set_cuda_error(e);
     return launch_status();
 }
