@@ -76,7 +76,7 @@ def _describe(w, window, cp=(1, 0, 1), fp8=None):
     """The workload's name and sizes, as the JSON line's config.workload."""
     if fp8 is not None:
         return (_describe(w, window, cp) + f", E4M3 KV cache (k_scale {fp8[0]:g}, v_scale {fp8[1]:g}; 1 byte per "
-                "element, widened to bf16 on chip)")
+                "element, K used as loaded by E4M3 tensor cores, V widened to f16 on chip)")
     if cp[0] > 1:
         return (_describe(w, window) + f", decode-context-parallel rank {cp[1]} of {cp[0]} (interleave {cp[2]}): "
                 f"its own share of every request's keys")

@@ -270,8 +270,12 @@ int bkv_cache_write_fp8(const void *k_new, const void *v_new, int64_t num_tokens
  *   BKV_F32); k_cache, v_cache are uint8 [total_blocks, block_size,
  *   num_kv_heads, head_dim].  A cache byte at a masked position is never
  *   used (NaN codes there change nothing).  bf16 q with head_dim 128 and at
- *   most 16 query rows per KV head runs the tensor-core kernel, which widens
- *   the codes to bf16 exactly on chip; anything else the CUDA-core kernel.
+ *   most 16 query rows per KV head runs the tensor-core kernel: q . k on
+ *   E4M3 tensor cores with each query row split into two E4M3 parts (exact
+ *   for elements down to 2^-10 of the row's largest, within 2^-17 of it
+ *   below), P . v on f16 with the value codes widened exactly; anything else
+ *   runs the CUDA-core kernel on the exact code values.  The workspace
+ *   (bkv_paged_decode_workspace_size) includes the split queries.
  *   Errors: as bkv_paged_decode, plus INVALID_ARG for a scale that is not a
  *   positive finite number.
  */

@@ -1,5 +1,6 @@
 // bkv_decode_tc.cu -- tensor-core (tcgen05 + TMA) partition kernel of the
-// paged decode, bf16, head_dim 128, up to 16 query rows per KV head.
+// paged decode, bf16 queries, bf16 or FP8 (E4M3) caches, head_dim 128, up to
+// 16 query rows per KV head.
 //
 // Operation ("Padding and Batching with Block KV", Cache Masking; Special
 // Block and Slot Values): for a run of consecutive 128-position tiles of one
@@ -49,6 +50,16 @@
 // * Every wait is bounded: after ~2 s a wait gives up, the CTA records an
 //   error in *err_count (+ 1 << 24), lets copies in flight land, frees its
 //   TMEM and exits.
+// * FP8 caches (the reading of the cache format is stated in bkv.h): tiles
+//   are 128 rows x 128 E4M3 codes (16 KB, one box per block segment).  S^T =
+//   K . Q^T runs as kind::f8f6f4 on the codes straight from TMA, with q split
+//   beforehand (q_split_e4m3_kernel) into two E4M3 parts whose sum is the
+//   query row divided by a power of two, so the products are exact; the
+//   softmax multiplies each column back.  P V runs on f16: the softmax
+//   warpgroup that owns a tile widens its E4M3 V rows to f16 (exact) into its
+//   own V slot before it reads S, and writes P as f16.  Widening every K and
+//   V element on chip was measured slower (the conversions, not the bytes,
+//   bound the kernel), which is why K is never widened.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -378,6 +389,7 @@ __device__ __forceinline__ bool reduced_writer(int lane) {
 #define BKV_F8_HWCVT 1
 #endif
 constexpr float kF8Unscale = BKV_F8_HWCVT ? 1.f : 256.f;
+
 
 // Four codes (byte k = code k) -> four f16 in two words (codes 0, 1 in a; 2, 3 in b).
 __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &a, uint32_t &b) {
@@ -855,16 +867,15 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 const int sv_slot = (int)(j % kVStages);
                 const int b = wg;
                 const uint32_t par = (uint32_t)((j >> 1) & 1);
-                if constexpr (kF8) {
-                    // widen this tile's E4M3 V rows into this warpgroup's V slot (j % 2 == wg;
-                    // its previous P.V, two tiles back, completed before that tile's O update),
-                    // zeros where nothing was loaded or past the end
+                // FP8: widen this tile's E4M3 V rows into this warpgroup's V slot (j % 2 == wg;
+                // its previous P.V, two tiles back, completed before that tile's O update),
+                // zeros where nothing was loaded or past the end.  Done before the wait for S
+                // (measured faster than after writing P).
+                auto widen_v = [&]() -> bool {
                     const int s8 = (int)(j % k8Stages);
                     if (!mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag) ||
-                        !mbar_wait_warp(bar_v8full(s8), (uint32_t)((j / k8Stages) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                        !mbar_wait_warp(bar_v8full(s8), (uint32_t)((j / k8Stages) & 1), abort_flag))
+                        return false;
                     const int32_t vpos = x.start + jt * kTile + row;
                     uint8_t *vdst = smem + C::kOffV + sv_slot * kTileBytes;
                     if (((mask_words[j & 7] >> (row >> seg_shift)) & 1u) && vpos < x.cend)
@@ -877,6 +888,11 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                         mbar_arrive(bar_vfull(sv_slot));
                         mbar_arrive(bar_v8empty(s8));
                     }
+                    return true;
+                };
+                if (kF8 && !widen_v()) {
+                    ok = false;
+                    break;
                 }
                 if (!mbar_wait_warp(bar_sfull(b), par, abort_flag) ||
                     !mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag)) {
