@@ -135,6 +135,33 @@ int bkv_cache_write(const void *k_new, const void *v_new, int64_t num_tokens,
                     int32_t head_dim, int dtype, int32_t *err_count, bkv_stream_t stream);
 
 /*
+ * bkv_slot_mapping_cache_write
+ *   bkv_compute_slot_mapping followed by bkv_cache_write, as one kernel
+ *   ("Padding and Batching with Block KV", The Core Formula; Slot ID -1:
+ *   Padding Tokens; Block Structure): the step's slots are computed and its
+ *   new K/V rows scattered to them in one pass.  The results are exactly
+ *   those of the two calls in sequence with the same arguments: the same
+ *   slot_mapping[0, max_num_tokens) (-1 past num_tokens), the same cache
+ *   bytes, and the same *err_count increments (a bad request index,
+ *   position or table width, and a slot past total_blocks * block_size,
+ *   each counted once).  `block_size` is both the table's and the cache's
+ *   block size (use the kernel table of bkv_map_to_kernel_blocks for
+ *   hybrid block sizes).
+ *
+ *   Arguments as bkv_compute_slot_mapping (block_table .. slot_mapping) and
+ *   bkv_cache_write (k_new .. dtype); the rows of tokens i < num_tokens are
+ *   read.  INVALID_ARG / UNSUPPORTED: the union of the two calls' checks.
+ */
+int bkv_slot_mapping_cache_write(const int32_t *block_table, int32_t num_reqs, int64_t bt_stride,
+                                 int32_t bt_cols, const int32_t *req_indices,
+                                 const int64_t *positions, int64_t num_tokens,
+                                 int64_t max_num_tokens, int64_t *slot_mapping, const void *k_new,
+                                 const void *v_new, int64_t new_token_stride, void *k_cache,
+                                 void *v_cache, int64_t total_blocks, int32_t block_size,
+                                 int32_t num_kv_heads, int32_t head_dim, int dtype,
+                                 int32_t *err_count, bkv_stream_t stream);
+
+/*
  * bkv_paged_decode_workspace_size
  *   Bytes of device workspace bkv_paged_decode needs for these sizes on the
  *   CURRENT device (the split of long contexts into partitions depends on

@@ -14,6 +14,7 @@
 #include <cuda_fp8.h>
 
 #include "bkv_internal.cuh"
+#include "bkv_slot.cuh"
 
 namespace bkv {
 
@@ -81,6 +82,116 @@ __global__ void __launch_bounds__(kCwWarps * 32) cache_write_elem_kernel(
             if (lane == 0 && err_count) atomicAdd(err_count, 1);
             continue;
         }
+        for (int64_t e = lane; e < row; e += 32) {
+            k_cache[s * row + e] = k_new[i * src_stride + e];
+            v_cache[s * row + e] = v_new[i * src_stride + e];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Slot mapping and cache write in one pass (the composition of
+// slot_mapping_kernel and the cache-write kernels above, with the same
+// results: the same slot_mapping array, cache bytes and error counts).  One
+// warp per token i < max_num_tokens: the lanes read the token's request and
+// position, and a real token's source rows are loaded while its table entry
+// is (they do not depend on the slot), so a step's slot computation and copy
+// cost one chain of memory round trips instead of two dependent launches.
+// Lane 0 writes slot_mapping[i] (-1 for the padded tail and padded requests).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kCwWarps * 32) slot_write_vec16_kernel(
+    const int32_t *__restrict__ block_table, int32_t num_reqs, int64_t bt_stride, int32_t bt_cols,
+    const int32_t *__restrict__ req_indices, const int64_t *__restrict__ positions, int64_t num_tokens,
+    int64_t max_num_tokens, int32_t block_size, int64_t *__restrict__ slot_mapping, const char *__restrict__ k_new,
+    const char *__restrict__ v_new, int64_t src_stride_bytes, char *__restrict__ k_cache, char *__restrict__ v_cache,
+    int64_t capacity, int64_t row_bytes, int32_t *err_count) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (int64_t)blockIdx.x * kCwWarps + (threadIdx.x >> 5);
+    const int64_t wstep = (int64_t)gridDim.x * kCwWarps;
+    for (int64_t i = warp0; i < max_num_tokens; i += wstep) {
+        int32_t r = -1;
+        int64_t p = 0;
+        if (i < num_tokens) {
+            r = __ldg(req_indices + i);
+            p = __ldg(positions + i);
+        }
+        if (r < 0) {   // padded tail or padded request
+            if (lane == 0) slot_mapping[i] = -1;
+            continue;
+        }
+        const char *ks = k_new + i * src_stride_bytes;
+        const char *vs = v_new + i * src_stride_bytes;
+        // the first round of the row (up to 32 x 16 x kCwUnroll bytes) in flight with the table read
+        uint4 kr[kCwUnroll], vr[kCwUnroll];
+#pragma unroll
+        for (int u = 0; u < kCwUnroll; ++u) {
+            const int64_t off = (int64_t)lane * 16 + (int64_t)u * 32 * 16;
+            if (off < row_bytes) {
+                kr[u] = __ldg(reinterpret_cast<const uint4 *>(ks + off));
+                vr[u] = __ldg(reinterpret_cast<const uint4 *>(vs + off));
+            }
+        }
+        bool bad;
+        const int64_t s = slot_of(block_table, num_reqs, bt_stride, bt_cols, r, p, block_size, 1, 0, 1, &bad);
+        if (lane == 0) {
+            slot_mapping[i] = s;
+            if ((bad || s >= capacity) && err_count) atomicAdd(err_count, 1);
+        }
+        if (s < 0 || s >= capacity) continue;
+        char *kd = k_cache + s * row_bytes;
+        char *vd = v_cache + s * row_bytes;
+        for (int64_t base = (int64_t)lane * 16;; ) {
+#pragma unroll
+            for (int u = 0; u < kCwUnroll; ++u) {
+                const int64_t off = base + (int64_t)u * 32 * 16;
+                if (off < row_bytes) {
+                    *reinterpret_cast<uint4 *>(kd + off) = kr[u];
+                    *reinterpret_cast<uint4 *>(vd + off) = vr[u];
+                }
+            }
+            base += 32 * 16 * kCwUnroll;
+            if (base >= row_bytes) break;
+#pragma unroll
+            for (int u = 0; u < kCwUnroll; ++u) {
+                const int64_t off = base + (int64_t)u * 32 * 16;
+                if (off < row_bytes) {
+                    kr[u] = __ldg(reinterpret_cast<const uint4 *>(ks + off));
+                    vr[u] = __ldg(reinterpret_cast<const uint4 *>(vs + off));
+                }
+            }
+        }
+    }
+}
+
+// Element path of the fused pass, for rows or strides that are not 16-byte multiples.
+template <typename E>
+__global__ void __launch_bounds__(kCwWarps * 32) slot_write_elem_kernel(
+    const int32_t *__restrict__ block_table, int32_t num_reqs, int64_t bt_stride, int32_t bt_cols,
+    const int32_t *__restrict__ req_indices, const int64_t *__restrict__ positions, int64_t num_tokens,
+    int64_t max_num_tokens, int32_t block_size, int64_t *__restrict__ slot_mapping, const E *__restrict__ k_new,
+    const E *__restrict__ v_new, int64_t src_stride, E *__restrict__ k_cache, E *__restrict__ v_cache,
+    int64_t capacity, int64_t row, int32_t *err_count) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (int64_t)blockIdx.x * kCwWarps + (threadIdx.x >> 5);
+    const int64_t wstep = (int64_t)gridDim.x * kCwWarps;
+    for (int64_t i = warp0; i < max_num_tokens; i += wstep) {
+        const int32_t r = i < num_tokens ? __ldg(req_indices + i) : -1;
+        if (r < 0) {
+            if (lane == 0) slot_mapping[i] = -1;
+            continue;
+        }
+        bool bad;
+        const int64_t s = slot_of(block_table, num_reqs, bt_stride, bt_cols, r, __ldg(positions + i), block_size,
+                                  1, 0, 1, &bad);
+        if (lane == 0) {
+            slot_mapping[i] = s;
+            if ((bad || s >= capacity) && err_count) atomicAdd(err_count, 1);
+        }
+        if (s < 0 || s >= capacity) continue;
         for (int64_t e = lane; e < row; e += 32) {
             k_cache[s * row + e] = k_new[i * src_stride + e];
             v_cache[s * row + e] = v_new[i * src_stride + e];
@@ -230,6 +341,52 @@ extern "C" int bkv_cache_write(const void *k_new, const void *v_new, int64_t num
         e = bkv::launch_pdl(bkv::cache_write_elem_kernel<uint32_t>, grid, threads, 0, st, (const uint32_t *)k_new,
                             (const uint32_t *)v_new, num_tokens, new_token_stride, slot_mapping, (uint32_t *)k_cache,
                             (uint32_t *)v_cache, capacity, row, err_count);
+    }
+    if (e != cudaSuccess) bkv::set_cuda_error(e);
+    return bkv::launch_status();
+}
+
+extern "C" int bkv_slot_mapping_cache_write(const int32_t *block_table, int32_t num_reqs, int64_t bt_stride,
+                                            int32_t bt_cols, const int32_t *req_indices, const int64_t *positions,
+                                            int64_t num_tokens, int64_t max_num_tokens, int64_t *slot_mapping,
+                                            const void *k_new, const void *v_new, int64_t new_token_stride,
+                                            void *k_cache, void *v_cache, int64_t total_blocks, int32_t block_size,
+                                            int32_t num_kv_heads, int32_t head_dim, int dtype, int32_t *err_count,
+                                            bkv_stream_t stream) {
+    if (dtype != BKV_BF16 && dtype != BKV_F32) return BKV_ERR_UNSUPPORTED;
+    if (block_size <= 0 || num_tokens < 0 || max_num_tokens < num_tokens || num_reqs < 0 || bt_cols < 0 ||
+        bt_stride < bt_cols || total_blocks < 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return BKV_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (new_token_stride < row) return BKV_ERR_INVALID_ARG;
+    if (max_num_tokens == 0) return BKV_OK;
+    if (!slot_mapping) return BKV_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!req_indices || !positions || !k_new || !v_new || !k_cache || !v_cache))
+        return BKV_ERR_INVALID_ARG;
+    if (num_tokens > 0 && num_reqs > 0 && bt_cols > 0 && !block_table) return BKV_ERR_INVALID_ARG;
+    const int64_t eb = dtype == BKV_BF16 ? 2 : 4;
+    const int64_t capacity = total_blocks * block_size;
+    const int threads = bkv::kCwWarps * 32;
+    const unsigned grid = bkv::grid_for(max_num_tokens, bkv::kCwWarps, 16);
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool vec16 = (row * eb) % 16 == 0 && (new_token_stride * eb) % 16 == 0 && bkv::aligned(k_new, 16) &&
+                       bkv::aligned(v_new, 16) && bkv::aligned(k_cache, 16) && bkv::aligned(v_cache, 16);
+    cudaError_t e;
+    if (vec16) {
+        e = bkv::launch_pdl(bkv::slot_write_vec16_kernel, grid, threads, 0, st, block_table, num_reqs, bt_stride,
+                            bt_cols, req_indices, positions, num_tokens, max_num_tokens, block_size, slot_mapping,
+                            (const char *)k_new, (const char *)v_new, new_token_stride * eb, (char *)k_cache,
+                            (char *)v_cache, capacity, row * eb, err_count);
+    } else if (eb == 2) {
+        e = bkv::launch_pdl(bkv::slot_write_elem_kernel<uint16_t>, grid, threads, 0, st, block_table, num_reqs,
+                            bt_stride, bt_cols, req_indices, positions, num_tokens, max_num_tokens, block_size,
+                            slot_mapping, (const uint16_t *)k_new, (const uint16_t *)v_new, new_token_stride,
+                            (uint16_t *)k_cache, (uint16_t *)v_cache, capacity, row, err_count);
+    } else {
+        e = bkv::launch_pdl(bkv::slot_write_elem_kernel<uint32_t>, grid, threads, 0, st, block_table, num_reqs,
+                            bt_stride, bt_cols, req_indices, positions, num_tokens, max_num_tokens, block_size,
+                            slot_mapping, (const uint32_t *)k_new, (const uint32_t *)v_new, new_token_stride,
+                            (uint32_t *)k_cache, (uint32_t *)v_cache, capacity, row, err_count);
     }
     if (e != cudaSuccess) bkv::set_cuda_error(e);
     return bkv::launch_status();

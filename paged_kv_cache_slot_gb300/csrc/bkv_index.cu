@@ -4,17 +4,14 @@
 // element, 64-bit index arithmetic, no shared memory.  Their cost is launch
 // latency plus a few bytes per token; the block table they read stays in L2.
 #include "bkv_internal.cuh"
+#include "bkv_slot.cuh"
 
 namespace bkv {
 
-// slot = block_table[r][p / bs] * bs + p % bs, with -1 for padding, null or
-// sentinel entries and bad indices ("Padding and Batching with Block KV",
-// The Core Formula; Special Block and Slot Values; "ブロック表" 設計動機 for the
-// padded tail).  Under decode context parallelism ("ブロック表" 設計動機: a
-// rank writes real slots only for the tokens it owns, PAD for the rest)
-// position p belongs to rank (p / inter) % world and is stored there at the
-// local position (p / (inter * world)) * inter + p % inter, which the rank's
-// table indexes; world = 1 is the plain formula.
+// slot_mapping[i] for i < max_num_tokens: the slot formula of bkv_slot.cuh
+// for real tokens, -1 for the padded tail i >= num_tokens ("ブロック表" 設計動機)
+// and for padded requests (r < 0; "Padding and Batching with Block KV", Slot
+// ID -1: Padding Tokens).
 __global__ void __launch_bounds__(256) slot_mapping_kernel(
     const int32_t *__restrict__ block_table, int32_t num_reqs, int64_t bt_stride, int32_t bt_cols,
     const int32_t *__restrict__ req_indices, const int64_t *__restrict__ positions, int64_t num_tokens,
@@ -27,24 +24,10 @@ __global__ void __launch_bounds__(256) slot_mapping_kernel(
         int64_t slot = -1;
         if (i < num_tokens) {
             const int32_t r = req_indices[i];
-            int64_t p = positions[i];
             if (r >= 0) {
-                bool bad = (r >= num_reqs) || (p < 0);
-                bool mine = true;
-                if (!bad && cp_world > 1) {
-                    const int64_t run = p / cp_inter;
-                    mine = run % cp_world == cp_rank;
-                    p = run / cp_world * cp_inter + (p - run * cp_inter);   // local position
-                }
-                if (!bad && mine) {
-                    const int64_t lb = p / block_size;
-                    if (lb >= bt_cols) {
-                        bad = true;
-                    } else {
-                        const int64_t b = __ldg(block_table + (int64_t)r * bt_stride + lb);
-                        if (b > 0) slot = b * block_size + (p - lb * block_size);
-                    }
-                }
+                bool bad;
+                slot = slot_of(block_table, num_reqs, bt_stride, bt_cols, r, positions[i], block_size, cp_world,
+                               cp_rank, cp_inter, &bad);
                 if (bad && err_count) atomicAdd(err_count, 1);
             }
         }

@@ -7,8 +7,9 @@ written them.  Caches start as NaN so that any read of a position that was
 never written shows up in the output.
 
 ``DeviceWorkload.step()`` is one pass of the hot path over one batch:
-block expansion (manager -> kernel ids), slot mapping of this step's tokens,
-the K/V scatter and the paged decode (partition + merge kernels).
+block expansion (manager -> kernel ids), slot mapping of this step's tokens
+and the K/V scatter (one fused kernel, or the two calls), and the paged
+decode (partition + merge kernels).
 """
 from __future__ import annotations
 
@@ -32,8 +33,11 @@ def _t(a: np.ndarray, device, dtype=None):
 class DeviceWorkload:
     def __init__(self, w: Workload, device="cuda", background: str = "nan", fill_prior: bool = True,
                  sliding_window: int = 0, cp_world: int = 1, cp_rank: int = 0, cp_interleave: int = 1,
-                 kv_fp8=None):
+                 kv_fp8=None, fused_write: bool = True):
         self.w = w
+        # the step's slot mapping + cache write as one bkv_slot_mapping_cache_write call (bf16 / fp32
+        # caches without context parallelism), else the two calls
+        self.fused_write = bool(fused_write)
         self.window = int(sliding_window)   # decode's default sliding window (0: full attention)
         # FP8 (E4M3) caches: (k_scale, v_scale); new rows are quantised by the cache write
         self.fp8 = None if kv_fp8 is None else (float(kv_fp8[0]), float(kv_fp8[1]))
@@ -137,8 +141,16 @@ class DeviceWorkload:
             bkv.bkv_compute_slot_mapping(table, req, pos, w.kernel_block_size, slots, num_tokens=num_tokens,
                                          err_count=self.err_count, stream=stream)
 
-    def write_step(self, stream=None):
+    def write_step(self, stream=None, fused=None):
+        """Slot mapping + cache write of this step's tokens: one fused call where it applies (``fused``
+        None: the object's default), else the two calls."""
         w = self.w
+        fused = self.fused_write if fused is None else fused
+        if fused and self.cp[0] == 1 and self.fp8 is None:
+            bkv.bkv_slot_mapping_cache_write(self.kernel_table, self.req_indices, self.positions, self.slot_mapping,
+                                             self.k_new, self.v_new, self.k_cache, self.v_cache, num_tokens=w.num_tokens,
+                                             err_count=self.err_count, stream=stream)
+            return
         self._slots(self.kernel_table, self.req_indices, self.positions, self.slot_mapping, w.num_tokens, stream)
         self._write(self.k_new, self.v_new, self.slot_mapping, w.num_tokens, stream)
 

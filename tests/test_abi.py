@@ -33,7 +33,7 @@ def _declared():
 def test_header_declares_the_entry_points():
     names = _declared()
     for n in ("bkv_compute_slot_mapping", "bkv_map_to_kernel_blocks", "bkv_cache_write", "bkv_paged_decode",
-              "bkv_paged_decode_workspace_size"):
+              "bkv_paged_decode_workspace_size", "bkv_slot_mapping_cache_write"):
         assert n in names
 
 
@@ -80,6 +80,25 @@ def test_cache_write_rejects_bad_arguments(lib):
     assert f(NULL, NULL, 1, 1024, NULL, NULL, NULL, 4, 0, 8, 128, 0, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
     assert f(NULL, NULL, 1, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 0, NULL, NULL) == bkv.BKV_ERR_INVALID_ARG
     assert f(NULL, NULL, 0, 1024, NULL, NULL, NULL, 4, 16, 8, 128, 0, NULL, NULL) == bkv.BKV_OK
+
+
+def test_fused_slot_write_rejects_bad_arguments(lib):
+    f = lib.bkv_slot_mapping_cache_write
+
+    def call(**kw):
+        a = dict(bt=NULL, nr=1, st=4, cols=4, req=NULL, pos=NULL, n=1, mx=1, slots=NULL, kn=NULL, vn=NULL, sst=1024,
+                 kc=NULL, vc=NULL, tb=4, bs=16, h=8, d=128, dt=0)
+        a.update(kw)
+        return f(*a.values(), NULL, NULL)
+
+    assert call(dt=7) == bkv.BKV_ERR_UNSUPPORTED
+    assert call(bs=0) == bkv.BKV_ERR_INVALID_ARG
+    assert call(n=5, mx=4) == bkv.BKV_ERR_INVALID_ARG          # max_num_tokens < num_tokens
+    assert call(st=2) == bkv.BKV_ERR_INVALID_ARG               # bt_stride < bt_cols
+    assert call(sst=1023) == bkv.BKV_ERR_INVALID_ARG           # source stride < H_kv * D
+    assert call(h=0) == bkv.BKV_ERR_INVALID_ARG
+    assert call() == bkv.BKV_ERR_INVALID_ARG                   # null pointers
+    assert call(n=0, mx=0) == bkv.BKV_OK                       # nothing to do launches nothing
 
 
 def test_paged_decode_rejects_bad_arguments(lib):

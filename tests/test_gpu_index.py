@@ -119,10 +119,11 @@ def _host_bits(t):
     return x.view(torch.int16).numpy() if x.dtype == torch.bfloat16 else x.view(torch.int32).numpy()
 
 
-def test_cache_write_ragged_step_bit_exact():
+@pytest.mark.parametrize("fused", [False, True])
+def test_cache_write_ragged_step_bit_exact(fused):
     w = wl.make("ragged_step")
     dw = DeviceWorkload(w, fill_prior=False)
-    dw.write_step()
+    dw.write_step(fused=fused)
     torch.cuda.synchronize()
     req, pos = w.step_tokens()
     slots, _ = oracle.compute_slot_mapping(w.block_table, req, pos, w.block_size, w.num_tokens, w.max_num_tokens)
