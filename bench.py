@@ -63,6 +63,17 @@ def _dist():
     return None
 
 
+def max_over_ranks(values, dist, device="cpu"):
+    """Each value's maximum over the ranks of the job (the values themselves at one rank): a step
+    time is that of the slowest replica."""
+    if not dist:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -401,10 +412,7 @@ def run_bkv(args):
     dms = sum(dec_ms) / len(dec_ms)
     ems = sum(e2e_ms) / len(e2e_ms)
     pms = sum(part_ms) / len(part_ms)
-    if dist:
-        t = torch.tensor([ms, dms, ems, pms], dtype=torch.float64, device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, dms, ems, pms = t.tolist()
+    ms, dms, ems, pms = max_over_ranks([ms, dms, ems, pms], dist, f"cuda:{local}")
 
     # context parallelism: the merge of cp_world ranks' (out, lse) that follows their exchange
     cp_merge = None
@@ -567,10 +575,7 @@ def run_ragged(args):
     with ClockSampler(local) as clk:
         times = _time_steps(torch, body, args.steps, flush, stream)
     ms = sum(times) / len(times)
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
+    ms, = max_over_ranks([ms], dist, dev)
     assert int(err.item()) == 0
     if rank != 0:
         return

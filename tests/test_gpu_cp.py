@@ -198,3 +198,34 @@ def test_merge_attn_states_matches_oracle(dtype):
     gl = lse.cpu().numpy().astype(np.float64)
     assert np.abs(gl[fin] - want_lse[fin]).max() <= 1e-5
     assert np.isneginf(gl[~fin]).all() and (got[5] == 0).all()
+
+
+def test_dcp_merge_across_ranks_single_process_nccl(tmp_path):
+    """The process-group exchange on the GPU (NCCL), in a one-rank group (each GPU box here has one GPU;
+    the two-rank exchange runs on gloo in test_dist_gloo.py): gathering a rank's state and merging it
+    equals the merge kernel on that state directly, bitwise."""
+    import torch.distributed as dist
+    from paged_kv_cache_slot_gb300.dcp import merge_across_ranks
+
+    w = _custom(1, 32, 8, 128, 64, (700, 1, 2300, 129), "bf16")
+    tables = wl.cp_block_tables(w, 2)
+    kc, vc, tab = _rank_caches(w, 2, 16, tables)[0]
+    qt, ctx = _dev(w.q(), w), _dev(w.context_lens)
+    mx = int(w.context_lens.max())
+    ws = bkv.alloc_workspace(w.num_rows, 1, 32, 8, 128, 64, mx)
+    out = torch.empty_like(qt)
+    lse = torch.empty((w.num_rows, 1, 32), dtype=torch.float32, device="cuda")
+    bkv.bkv_paged_decode_cp(qt, kc, vc, tab, ctx, mx, out, lse, ws, 2, 0, 16)
+    want = torch.empty_like(qt)
+    want_lse = torch.empty_like(lse)
+    bkv.bkv_merge_attn_states(out.unsqueeze(0), lse.unsqueeze(0), want, want_lse)
+    dist.init_process_group("nccl", init_method=f"file://{tmp_path / 'store'}", rank=0, world_size=1)
+    try:
+        got = torch.empty_like(qt)
+        got_lse = torch.empty_like(lse)
+        merge_across_ranks(out, lse, got, got_lse)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    assert torch.equal(got_lse, want_lse)
