@@ -609,6 +609,77 @@ def run_ragged(args):
     print(json.dumps(line), flush=True)
 
 
+def run_write(args):
+    """--part write: the other half of the metric alone, slot mapping + K/V cache write of the ragged
+    mixed step (ragged_step: 9691 tokens of 64 requests, 48 x 1 + 16 x 64..1024, kernel bs 16, H_kv 8,
+    D 128, bf16) as one bkv_slot_mapping_cache_write call per step, CUDA graph, L2 flushed before each
+    step.  HBM-bound: algorithmic bytes = per token the K and V rows read and written plus its request
+    index, position and slot (DeviceWorkload.write_bytes)."""
+    import torch
+
+    from paged_kv_cache_slot_gb300 import bkv
+    from paged_kv_cache_slot_gb300 import workloads as wl
+    from paged_kv_cache_slot_gb300.build import build
+    from paged_kv_cache_slot_gb300.staging import DeviceWorkload
+
+    dist = _dist()
+    rank = dist.get_rank() if dist else 0
+    world = dist.get_world_size() if dist else 1
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if rank == 0:
+        build()
+    if dist:
+        dist.barrier()
+    bkv.load()
+    dev = f"cuda:{local}"
+    w = wl.make("ragged_step")
+    dw = DeviceWorkload(w, device=dev, fill_prior=False)
+    stream = torch.cuda.Stream()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+
+    def step():
+        dw.write_step(stream=stream, fused=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    torch.cuda.synchronize()
+    body = step
+    if not args.eager:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        body = g.replay
+    if dist:
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        times = _time_steps(torch, body, args.steps, flush, stream)
+    ms, = max_over_ranks([sum(times) / len(times)], dist, dev)
+    assert int(dw.err_count.item()) == 0
+    if rank != 0:
+        return
+    peak, peak_kind = _peaks()
+    nbytes = dw.write_bytes() + w.num_tokens * 12      # + request index and position read per token
+    achieved = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": "slot-map+cache-write tokens/s (ragged_step)", "value": world * w.num_tokens / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"ragged_step: {w.num_tokens} tokens of 64 requests (48 x 1, 16 x 64..1024), prior "
+                               "0..2048, kernel bs 16, H_kv 8, D 128, bf16",
+                   "bytes_per_step": nbytes, "l2": "flushed before every timed step (write 2x L2, read it back)",
+                   "cuda_graph": not args.eager},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "bkv_slot_mapping_cache_write (slot_write_vec16_kernel)",
+                     "peak_kind": f"{peak_kind} copy bandwidth"},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -629,11 +700,16 @@ def main():
     ap.add_argument("--cp-world", type=int, default=1,
                     help="time rank 0 of a decode-context-parallel split over this many ranks (1: none)")
     ap.add_argument("--cp-interleave", type=int, default=1, help="context-parallel interleave size")
+    ap.add_argument("--part", default="step", choices=["step", "write"],
+                    help="step: the whole path (default); write: slot mapping + cache write of the ragged step alone")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
     else:
-        run_ragged(args) if args.attention == "ragged" else run_bkv(args)
+        if args.part == "write":
+            run_write(args)
+        else:
+            run_ragged(args) if args.attention == "ragged" else run_bkv(args)
     d = _dist()
     if d:
         d.destroy_process_group()
