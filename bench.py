@@ -36,6 +36,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -141,8 +142,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv") if os.path.isdir(
-            os.path.join(ROOT, "gpurun_out")) else f"/tmp/bkv_clocks_{os.getpid()}.csv"
+        # the raw samples: BKV_CLOCKS_CSV if set (a path to keep them), else a temporary file
+        self.path = os.environ.get("BKV_CLOCKS_CSV") or os.path.join(
+            tempfile.gettempdir(), f"bkv_clocks_{os.getpid()}_{index}.csv")
 
     def __enter__(self):
         try:
