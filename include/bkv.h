@@ -43,7 +43,7 @@ typedef struct CUstream_st *bkv_stream_t; /* same object as cudaStream_t */
 enum {
     BKV_OK = 0,
     BKV_ERR_INVALID_ARG = 1, /* a scalar argument or null pointer is invalid */
-    BKV_ERR_UNSUPPORTED = 2, /* dtype / head_dim / shape this build does not handle */
+    BKV_ERR_UNSUPPORTED = 2, /* dtype / head_dim / shape this library does not handle */
     BKV_ERR_CUDA = 3         /* a CUDA launch failed; see bkv_last_cuda_error() */
 };
 

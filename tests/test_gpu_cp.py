@@ -201,9 +201,9 @@ def test_merge_attn_states_matches_oracle(dtype):
 
 
 def test_dcp_merge_across_ranks_single_process_nccl(tmp_path):
-    """The process-group exchange on the GPU (NCCL), in a one-rank group (each GPU box here has one GPU;
-    the two-rank exchange runs on gloo in test_dist_gloo.py): gathering a rank's state and merging it
-    equals the merge kernel on that state directly, bitwise."""
+    """The process-group exchange on the GPU (NCCL), in a one-rank group (two ranks need two GPUs, as
+    their collectives wait on one another; the two-rank exchange runs on gloo in test_dist_gloo.py):
+    gathering a rank's state and merging it equals the merge kernel on that state directly, bitwise."""
     import torch.distributed as dist
     from paged_kv_cache_slot_gb300.dcp import merge_across_ranks
 
