@@ -481,7 +481,12 @@ def run_bkv(args):
     if rank != 0:
         return
     peak, peak_kind = _peaks()
-    kstep = 4 if (cp[0] == 1 and fp8 is None) else 5
+    # library kernels per timed body: block expansion; the write (one fused kernel, or slot mapping + write
+    # under context parallelism); the decode (partition + merge, after the query split with FP8 caches)
+    kwrite = 1 if cp[0] == 1 else 2
+    kdec = 3 if fp8 is not None else 2
+    kpart = kdec if cp[0] > 1 else kdec - 1
+    kstep = 1 + kwrite + kdec
     achieved = kv_bytes / (pms / 1e3) / 1e9
     value = world * kv_bytes / (ms / 1e3) / 1e9
     clocks = clk.summary()
@@ -492,13 +497,12 @@ def run_bkv(args):
         "config": {"workload": _describe(w, args.sliding_window, cp, fp8),
                    "kv_bytes_per_step": kv_bytes, "l2": "flushed before every timed step (write 2x L2, read it back)",
                    "parallelism": f"replicas x{world}",
-                   "step": ("expand + fused slot map & write + decode + merge" if kstep == 4
+                   "step": ("expand + fused slot map & write + decode + merge" if kwrite == 1
                             else "expand + slot map + write + decode + merge"),
                    "cuda_graph": bool(graphs)},
-        # library kernels in the timed region, per step: step (k) + decode alone (2) + partition alone (1)
-        # + end-to-end step (k), plus the eager pass of the step (k) when graphs are used; k = 4 (expand,
-        # fused slot map + write, partition, merge) or 5 when the write takes two calls
-        "gpu_launches": args.steps * (2 * kstep + 2 + 1) + (args.steps * kstep if graphs else 0),
+        # library kernels in the timed region: per step the step, the decode alone, the partition alone and
+        # the end-to-end step, plus the eager pass of the step when graphs are used
+        "gpu_launches": args.steps * (2 * kstep + kdec + kpart) + (args.steps * kstep if graphs else 0),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic() if headline else None,
                      "kernel": ("decode partition kernel (bkv_paged_decode_partition, CUDA events around it)"

@@ -286,6 +286,29 @@ int bkv_cache_write_fp8(const void *k_new, const void *v_new, int64_t num_tokens
                         float v_scale, int32_t *err_count, bkv_stream_t stream);
 
 /*
+ * bkv_slot_mapping_cache_write_fp8
+ *   bkv_compute_slot_mapping followed by bkv_cache_write_fp8, as one kernel
+ *   (the quantising write of bkv_cache_write_fp8, the slots of
+ *   bkv_compute_slot_mapping): the same slot_mapping[0, max_num_tokens), the
+ *   same cache bytes and the same *err_count increments as the two calls in
+ *   sequence, as bkv_slot_mapping_cache_write is for bf16 / fp32 caches.
+ *
+ *   Arguments as bkv_slot_mapping_cache_write, with src_dtype the type of
+ *   k_new / v_new (BKV_BF16 / BKV_F32), uint8 caches of E4M3 codes, and the
+ *   per-tensor k_scale / v_scale of bkv_cache_write_fp8.
+ *   INVALID_ARG / UNSUPPORTED: the union of the two calls' checks.
+ */
+int bkv_slot_mapping_cache_write_fp8(const int32_t *block_table, int32_t num_reqs, int64_t bt_stride,
+                                     int32_t bt_cols, const int32_t *req_indices,
+                                     const int64_t *positions, int64_t num_tokens,
+                                     int64_t max_num_tokens, int64_t *slot_mapping,
+                                     const void *k_new, const void *v_new,
+                                     int64_t new_token_stride, uint8_t *k_cache, uint8_t *v_cache,
+                                     int64_t total_blocks, int32_t block_size, int32_t num_kv_heads,
+                                     int32_t head_dim, int src_dtype, float k_scale, float v_scale,
+                                     int32_t *err_count, bkv_stream_t stream);
+
+/*
  * bkv_paged_decode_fp8, bkv_paged_decode_fp8_partition, bkv_paged_decode_fp8_merge
  *   bkv_paged_decode (and its two phases) over FP8 caches written by
  *   bkv_cache_write_fp8: a key element with code c stands for the value

@@ -73,6 +73,9 @@ def load() -> ctypes.CDLL:
         lib.bkv_map_to_kernel_blocks.argtypes = [vp, i32, i64, i32, i32, i32, vp, i64, vp]
         lib.bkv_cache_write.restype = cint
         lib.bkv_cache_write.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i32, i32, i32, cint, vp, vp]
+        lib.bkv_slot_mapping_cache_write_fp8.restype = cint
+        lib.bkv_slot_mapping_cache_write_fp8.argtypes = [vp, i32, i64, i32, vp, vp, i64, i64, vp, vp, vp, i64, vp,
+                                                         vp, i64, i32, i32, i32, cint, f32, f32, vp, vp]
         lib.bkv_slot_mapping_cache_write.restype = cint
         lib.bkv_slot_mapping_cache_write.argtypes = [vp, i32, i64, i32, vp, vp, i64, i64, vp, vp, vp, i64, vp, vp,
                                                      i64, i32, i32, i32, cint, vp, vp]
@@ -208,6 +211,38 @@ def bkv_slot_mapping_cache_write(block_table, req_indices, positions, slot_mappi
         _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_new, "k_new", contiguous=False),
         _dev(v_new, "v_new", contiguous=False), k_new.stride(0), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         tb, bs, hkv, d, dt, _opt(err_count, "err_count", torch.int32), _stream(stream)))
+    return slot_mapping
+
+
+def bkv_slot_mapping_cache_write_fp8(block_table, req_indices, positions, slot_mapping, k_new, v_new, k_cache,
+                                     v_cache, k_scale, v_scale, num_tokens=None, err_count=None, stream=None):
+    """bkv_compute_slot_mapping then bkv_cache_write_fp8 in one kernel, with the same results: k_new / v_new
+    (num_tokens, H_kv, D) bf16 or fp32 quantised into uint8 E4M3 caches (see include/bkv.h)."""
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be 2-D with unit column stride")
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("caches must be (total_blocks, block_size, H_kv, D) and equal in shape")
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("FP8 caches are uint8 tensors of E4M3 codes")
+    tb, bs, hkv, d = k_cache.shape
+    if k_new.dim() != 3 or tuple(k_new.shape[1:]) != (hkv, d) or k_new.shape != v_new.shape:
+        raise ValueError("k_new/v_new must be (num_tokens, H_kv, D) matching the cache")
+    if k_new.stride(2) != 1 or k_new.stride(1) != d or k_new.stride() != v_new.stride():
+        raise ValueError("k_new/v_new rows must be dense (a row stride is allowed)")
+    if k_new.dtype != v_new.dtype:
+        raise TypeError("mixed dtypes")
+    dt = _kv_dtype(k_new)
+    n = positions.numel() if num_tokens is None else int(num_tokens)
+    if n > positions.numel() or n > req_indices.numel() or n > slot_mapping.numel() or n > k_new.shape[0]:
+        raise ValueError("num_tokens exceeds positions / req_indices / slot_mapping / k_new")
+    _check("bkv_slot_mapping_cache_write_fp8", load().bkv_slot_mapping_cache_write_fp8(
+        _dev(block_table, "block_table", torch.int32, contiguous=False), block_table.shape[0],
+        block_table.stride(0), block_table.shape[1], _dev(req_indices, "req_indices", torch.int32),
+        _dev(positions, "positions", torch.int64), n, slot_mapping.numel(),
+        _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_new, "k_new", contiguous=False),
+        _dev(v_new, "v_new", contiguous=False), k_new.stride(0), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        tb, bs, hkv, d, dt, float(k_scale), float(v_scale), _opt(err_count, "err_count", torch.int32),
+        _stream(stream)))
     return slot_mapping
 
 

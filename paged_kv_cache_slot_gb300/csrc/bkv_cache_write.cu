@@ -233,8 +233,30 @@ __device__ __forceinline__ uint4 quant16(const E *p, float scale) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// kVec16: the row and the source stride are multiples of 16 elements and the
-// bases 16-byte aligned; otherwise one element per lane and step.
+// One token's K and V rows (`row` source elements each) quantised into their
+// cache rows by the 32 lanes of a warp.  kVec16: the row and the source
+// stride are multiples of 16 elements and the bases 16-byte aligned, each
+// lane turning 16 elements into one 16-byte store; otherwise one element per
+// lane and step.
+template <typename E, bool kVec16>
+__device__ __forceinline__ void quant_rows(const E *ks, const E *vs, uint8_t *kd, uint8_t *vd, int64_t row,
+                                           float k_scale, float v_scale, int lane) {
+    if constexpr (kVec16) {
+        for (int64_t e = (int64_t)lane * 16; e < row; e += 32 * 16) {
+            const uint4 kq = quant16(ks + e, k_scale);
+            const uint4 vq = quant16(vs + e, v_scale);
+            *reinterpret_cast<uint4 *>(kd + e) = kq;
+            *reinterpret_cast<uint4 *>(vd + e) = vq;
+        }
+    } else {
+        for (int64_t e = lane; e < row; e += 32) {
+            kd[e] = (uint8_t)e4m3x2(src_f(ks[e]), 0.f, k_scale);
+            vd[e] = (uint8_t)e4m3x2(src_f(vs[e]), 0.f, v_scale);
+        }
+    }
+}
+
+// The quantising cache write: warps over tokens, slots read from slot_mapping.
 template <typename E, bool kVec16>
 __global__ void __launch_bounds__(kCwWarps * 32) cache_write_fp8_kernel(
     const E *__restrict__ k_new, const E *__restrict__ v_new, int64_t num_tokens, int64_t src_stride,
@@ -252,23 +274,43 @@ __global__ void __launch_bounds__(kCwWarps * 32) cache_write_fp8_kernel(
             if (lane == 0 && err_count) atomicAdd(err_count, 1);
             continue;
         }
-        const E *ks = k_new + i * src_stride;
-        const E *vs = v_new + i * src_stride;
-        uint8_t *kd = k_cache + s * row;
-        uint8_t *vd = v_cache + s * row;
-        if constexpr (kVec16) {
-            for (int64_t e = (int64_t)lane * 16; e < row; e += 32 * 16) {
-                const uint4 kq = quant16(ks + e, k_scale);
-                const uint4 vq = quant16(vs + e, v_scale);
-                *reinterpret_cast<uint4 *>(kd + e) = kq;
-                *reinterpret_cast<uint4 *>(vd + e) = vq;
-            }
-        } else {
-            for (int64_t e = lane; e < row; e += 32) {
-                kd[e] = (uint8_t)e4m3x2(src_f(ks[e]), 0.f, k_scale);
-                vd[e] = (uint8_t)e4m3x2(src_f(vs[e]), 0.f, v_scale);
-            }
+        quant_rows<E, kVec16>(k_new + i * src_stride, v_new + i * src_stride, k_cache + s * row, v_cache + s * row,
+                              row, k_scale, v_scale, lane);
+    }
+}
+
+// Slot mapping and the quantising write in one pass: the composition of
+// slot_mapping_kernel and cache_write_fp8_kernel, with the same slots, cache
+// bytes and error counts.  One warp per token i < max_num_tokens; lane 0
+// writes slot_mapping[i] (-1 for the padded tail and padded requests).
+template <typename E, bool kVec16>
+__global__ void __launch_bounds__(kCwWarps * 32) slot_write_fp8_kernel(
+    const int32_t *__restrict__ block_table, int32_t num_reqs, int64_t bt_stride, int32_t bt_cols,
+    const int32_t *__restrict__ req_indices, const int64_t *__restrict__ positions, int64_t num_tokens,
+    int64_t max_num_tokens, int32_t block_size, int64_t *__restrict__ slot_mapping, const E *__restrict__ k_new,
+    const E *__restrict__ v_new, int64_t src_stride, uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+    int64_t capacity, int64_t row, float k_scale, float v_scale, int32_t *err_count) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (int64_t)blockIdx.x * kCwWarps + (threadIdx.x >> 5);
+    const int64_t wstep = (int64_t)gridDim.x * kCwWarps;
+    for (int64_t i = warp0; i < max_num_tokens; i += wstep) {
+        const int32_t r = i < num_tokens ? __ldg(req_indices + i) : -1;
+        if (r < 0) {
+            if (lane == 0) slot_mapping[i] = -1;
+            continue;
         }
+        bool bad;
+        const int64_t s = slot_of(block_table, num_reqs, bt_stride, bt_cols, r, __ldg(positions + i), block_size,
+                                  1, 0, 1, &bad);
+        if (lane == 0) {
+            slot_mapping[i] = s;
+            if ((bad || s >= capacity) && err_count) atomicAdd(err_count, 1);
+        }
+        if (s < 0 || s >= capacity) continue;
+        quant_rows<E, kVec16>(k_new + i * src_stride, v_new + i * src_stride, k_cache + s * row, v_cache + s * row,
+                              row, k_scale, v_scale, lane);
     }
 }
 
@@ -387,6 +429,51 @@ extern "C" int bkv_slot_mapping_cache_write(const int32_t *block_table, int32_t 
                             bt_stride, bt_cols, req_indices, positions, num_tokens, max_num_tokens, block_size,
                             slot_mapping, (const uint32_t *)k_new, (const uint32_t *)v_new, new_token_stride,
                             (uint32_t *)k_cache, (uint32_t *)v_cache, capacity, row, err_count);
+    }
+    if (e != cudaSuccess) bkv::set_cuda_error(e);
+    return bkv::launch_status();
+}
+
+extern "C" int bkv_slot_mapping_cache_write_fp8(const int32_t *block_table, int32_t num_reqs, int64_t bt_stride,
+                                                int32_t bt_cols, const int32_t *req_indices, const int64_t *positions,
+                                                int64_t num_tokens, int64_t max_num_tokens, int64_t *slot_mapping,
+                                                const void *k_new, const void *v_new, int64_t new_token_stride,
+                                                uint8_t *k_cache, uint8_t *v_cache, int64_t total_blocks,
+                                                int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                                int src_dtype, float k_scale, float v_scale, int32_t *err_count,
+                                                bkv_stream_t stream) {
+    if (src_dtype != BKV_BF16 && src_dtype != BKV_F32) return BKV_ERR_UNSUPPORTED;
+    if (block_size <= 0 || num_tokens < 0 || max_num_tokens < num_tokens || num_reqs < 0 || bt_cols < 0 ||
+        bt_stride < bt_cols || total_blocks < 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return BKV_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale)) return BKV_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (new_token_stride < row) return BKV_ERR_INVALID_ARG;
+    if (max_num_tokens == 0) return BKV_OK;
+    if (!slot_mapping) return BKV_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!req_indices || !positions || !k_new || !v_new || !k_cache || !v_cache))
+        return BKV_ERR_INVALID_ARG;
+    if (num_tokens > 0 && num_reqs > 0 && bt_cols > 0 && !block_table) return BKV_ERR_INVALID_ARG;
+    const int64_t capacity = total_blocks * block_size;
+    const int threads = bkv::kCwWarps * 32;
+    const unsigned grid = bkv::grid_for(max_num_tokens, bkv::kCwWarps, 16);
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool vec16 = row % 16 == 0 && new_token_stride % 16 == 0 && bkv::aligned(k_new, 16) &&
+                       bkv::aligned(v_new, 16) && bkv::aligned(k_cache, 16) && bkv::aligned(v_cache, 16);
+    cudaError_t e;
+    if (src_dtype == BKV_BF16) {
+        auto kern = vec16 ? bkv::slot_write_fp8_kernel<__nv_bfloat16, true>
+                          : bkv::slot_write_fp8_kernel<__nv_bfloat16, false>;
+        e = bkv::launch_pdl(kern, grid, threads, 0, st, block_table, num_reqs, bt_stride, bt_cols, req_indices,
+                            positions, num_tokens, max_num_tokens, block_size, slot_mapping,
+                            (const __nv_bfloat16 *)k_new, (const __nv_bfloat16 *)v_new, new_token_stride, k_cache,
+                            v_cache, capacity, row, k_scale, v_scale, err_count);
+    } else {
+        auto kern = vec16 ? bkv::slot_write_fp8_kernel<float, true> : bkv::slot_write_fp8_kernel<float, false>;
+        e = bkv::launch_pdl(kern, grid, threads, 0, st, block_table, num_reqs, bt_stride, bt_cols, req_indices,
+                            positions, num_tokens, max_num_tokens, block_size, slot_mapping, (const float *)k_new,
+                            (const float *)v_new, new_token_stride, k_cache, v_cache, capacity, row, k_scale, v_scale,
+                            err_count);
     }
     if (e != cudaSuccess) bkv::set_cuda_error(e);
     return bkv::launch_status();

@@ -35,8 +35,8 @@ class DeviceWorkload:
                  sliding_window: int = 0, cp_world: int = 1, cp_rank: int = 0, cp_interleave: int = 1,
                  kv_fp8=None, fused_write: bool = True):
         self.w = w
-        # the step's slot mapping + cache write as one bkv_slot_mapping_cache_write call (bf16 / fp32
-        # caches without context parallelism), else the two calls
+        # the step's slot mapping + cache write as one bkv_slot_mapping_cache_write(_fp8) call (without
+        # context parallelism), else the two calls
         self.fused_write = bool(fused_write)
         self.window = int(sliding_window)   # decode's default sliding window (0: full attention)
         # FP8 (E4M3) caches: (k_scale, v_scale); new rows are quantised by the cache write
@@ -146,10 +146,15 @@ class DeviceWorkload:
         None: the object's default), else the two calls."""
         w = self.w
         fused = self.fused_write if fused is None else fused
-        if fused and self.cp[0] == 1 and self.fp8 is None:
-            bkv.bkv_slot_mapping_cache_write(self.kernel_table, self.req_indices, self.positions, self.slot_mapping,
-                                             self.k_new, self.v_new, self.k_cache, self.v_cache, num_tokens=w.num_tokens,
-                                             err_count=self.err_count, stream=stream)
+        if fused and self.cp[0] == 1:
+            args = (self.kernel_table, self.req_indices, self.positions, self.slot_mapping, self.k_new, self.v_new,
+                    self.k_cache, self.v_cache)
+            if self.fp8 is not None:
+                bkv.bkv_slot_mapping_cache_write_fp8(*args, *self.fp8, num_tokens=w.num_tokens,
+                                                     err_count=self.err_count, stream=stream)
+            else:
+                bkv.bkv_slot_mapping_cache_write(*args, num_tokens=w.num_tokens, err_count=self.err_count,
+                                                 stream=stream)
             return
         self._slots(self.kernel_table, self.req_indices, self.positions, self.slot_mapping, w.num_tokens, stream)
         self._write(self.k_new, self.v_new, self.slot_mapping, w.num_tokens, stream)

@@ -33,7 +33,7 @@ def _declared():
 def test_header_declares_the_entry_points():
     names = _declared()
     for n in ("bkv_compute_slot_mapping", "bkv_map_to_kernel_blocks", "bkv_cache_write", "bkv_paged_decode",
-              "bkv_paged_decode_workspace_size", "bkv_slot_mapping_cache_write"):
+              "bkv_paged_decode_workspace_size", "bkv_slot_mapping_cache_write", "bkv_slot_mapping_cache_write_fp8"):
         assert n in names
 
 
@@ -99,6 +99,24 @@ def test_fused_slot_write_rejects_bad_arguments(lib):
     assert call(h=0) == bkv.BKV_ERR_INVALID_ARG
     assert call() == bkv.BKV_ERR_INVALID_ARG                   # null pointers
     assert call(n=0, mx=0) == bkv.BKV_OK                       # nothing to do launches nothing
+
+
+def test_fused_slot_write_fp8_rejects_bad_arguments(lib):
+    f = lib.bkv_slot_mapping_cache_write_fp8
+
+    def call(**kw):
+        a = dict(bt=NULL, nr=1, st=4, cols=4, req=NULL, pos=NULL, n=1, mx=1, slots=NULL, kn=NULL, vn=NULL, sst=1024,
+                 kc=NULL, vc=NULL, tb=4, bs=16, h=8, d=128, dt=0, ks=1.0, vs=1.0)
+        a.update(kw)
+        return f(*a.values(), NULL, NULL)
+
+    assert call(dt=7) == bkv.BKV_ERR_UNSUPPORTED
+    assert call(ks=0.0) == bkv.BKV_ERR_INVALID_ARG                  # scales must be positive and finite
+    assert call(vs=float("inf")) == bkv.BKV_ERR_INVALID_ARG
+    assert call(n=5, mx=4) == bkv.BKV_ERR_INVALID_ARG
+    assert call(sst=1023) == bkv.BKV_ERR_INVALID_ARG
+    assert call() == bkv.BKV_ERR_INVALID_ARG
+    assert call(n=0, mx=0) == bkv.BKV_OK
 
 
 def test_paged_decode_rejects_bad_arguments(lib):

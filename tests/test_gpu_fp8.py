@@ -115,6 +115,63 @@ def test_cache_write_fp8_strided_source_and_num_tokens():
     assert (vc.cpu().numpy() == want_v).all()
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(8, 128), (2, 12)])            # 16-byte path, element path
+def test_fused_slot_write_fp8_matches_oracle_and_two_calls(dtype, shape):
+    """bkv_slot_mapping_cache_write_fp8: slots, E4M3 cache bytes and the error count equal the oracle's
+    slot mapping followed by its quantising write, and the library's two calls, with padded requests, a
+    padded tail, null entries, bad request indices and positions, a block id past the cache, and
+    saturating, subnormal and NaN inputs."""
+    hkv, d = shape
+    rng = np.random.default_rng(23)
+    nr, cols, bs, tb = 11, 6, 16, 70
+    table = rng.permutation(np.arange(1, nr * cols + 10))[: nr * cols].astype(np.int32).reshape(nr, cols)
+    table[rng.random(table.shape) < 0.1] = 0                      # null entries; some ids >= tb: counted
+    pairs = rng.permutation(nr * cols * bs)[:250]
+    req = (pairs // (cols * bs)).astype(np.int32)
+    pos = (pairs % (cols * bs)).astype(np.int64)
+    req[::13] = -1
+    req[5] = nr + 2
+    pos[7] = -3
+    pos[9] = cols * bs + 5
+    n, mx = 230, 260
+    cast = wl.f32_to_bf16_bits if dtype == "bf16" else (lambda x: x.astype(np.float32))
+    x = rng.standard_normal((2, len(req), hkv, d)).astype(np.float32) * np.float32(0.05)
+    x[:, :15] *= np.float32(1e4)
+    x[:, 15:30] *= np.float32(1e-4)
+    x[0, 31, 0, 0] = np.nan
+    k, v = cast(x[0]), cast(x[1])
+    want_s, serr = oracle.compute_slot_mapping(table, req, pos, bs, n, mx)
+    kc0 = np.full((tb, bs, hkv, d), NAN8, np.uint8)
+    want_k, want_v, werr = oracle.cache_write_fp8(k, v, want_s, kc0, kc0, K_SCALE, V_SCALE, num_tokens=n)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    kt = torch.from_numpy(k).cuda().view(tdt) if dtype == "bf16" else torch.from_numpy(k).cuda()
+    vt = torch.from_numpy(v).cuda().view(tdt) if dtype == "bf16" else torch.from_numpy(v).cuda()
+    tab, rq, ps = torch.from_numpy(table).cuda(), torch.from_numpy(req).cuda(), torch.from_numpy(pos).cuda()
+    results = []
+    for fused in (True, False):
+        kc = torch.full((tb, bs, hkv, d), NAN8, dtype=torch.uint8, device="cuda")
+        vc = torch.full_like(kc, NAN8)
+        slots = torch.full((mx,), 777, dtype=torch.int64, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            bkv.bkv_slot_mapping_cache_write_fp8(tab, rq, ps, slots, kt, vt, kc, vc, K_SCALE, V_SCALE, num_tokens=n,
+                                                 err_count=err)
+        else:
+            bkv.bkv_compute_slot_mapping(tab, rq, ps, bs, slots, num_tokens=n, err_count=err)
+            bkv.bkv_cache_write_fp8(kt, vt, slots, kc, vc, K_SCALE, V_SCALE, num_tokens=n, err_count=err)
+        torch.cuda.synchronize()
+        results.append((slots.cpu().numpy(), kc.cpu().numpy(), vc.cpu().numpy(), int(err.item())))
+    (s1, k1, v1, e1), (s2, k2, v2, e2) = results
+    assert np.array_equal(s1, want_s) and np.array_equal(s2, want_s)
+    assert e1 == e2 == serr + werr > 0
+    assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
+    for got, want in ((k1, want_k), (v1, want_v)):
+        nan_w = (want & 0x7F) == 0x7F
+        assert (((got & 0x7F) == 0x7F) == nan_w).all()
+        assert (got[~nan_w] == want[~nan_w]).all()
+
+
 # ---------------------------------------------------------------------------
 # decode
 # ---------------------------------------------------------------------------
