@@ -1,0 +1,58 @@
+"""Host-side logic of bench.py that needs no GPU: the clock-sample summary
+(median SM clock and the throttle reasons seen) and the gate that reports the
+committed ncu traffic only while the decode sources are the profiled ones."""
+import os
+
+import bench
+
+
+def _sampler(tmp_path, lines):
+    path = tmp_path / "clocks.csv"
+    path.write_text("".join(l + "\n" for l in lines))
+    s = bench.ClockSampler(0)
+    s.path = str(path)
+    s.proc = object()          # a sampler that ran
+    return s
+
+
+def test_clock_summary_median_and_reasons(tmp_path):
+    rows = ["0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 1980, 2070, 1300.1, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "garbage line"]
+    got = _sampler(tmp_path, rows).summary()
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+
+
+def test_clock_summary_reports_thermal_and_hw_slowdown(tmp_path):
+    rows = ["0, 1500, 2070, 1390, 0x48, Active, Not Active, Active, Not Active"]
+    got = _sampler(tmp_path, rows).summary()
+    assert got["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"] and got["sm_mhz"] == 1500.0
+
+
+def test_clock_summary_without_samples(tmp_path):
+    assert _sampler(tmp_path, []).summary() is None
+    s = bench.ClockSampler(0)
+    s.proc = None              # nvidia-smi could not be started
+    assert s.summary() is None
+
+
+def test_profiled_traffic_follows_the_decode_sources(tmp_path, monkeypatch):
+    # the committed summary carries the hash of the current decode sources
+    assert bench._profiled_traffic() is not None
+    fake = tmp_path / "profile.txt"
+    fake.write_text("decode_source_sha256: 0000000000000000\ntraffic_bytes_per_launch: 123\n")
+    monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(fake))
+    assert bench._profiled_traffic() is None            # stale: another source version
+    fake.write_text(f"decode_source_sha256: {bench._decode_source_sha()}\ntraffic_bytes_per_launch: 123\n")
+    assert bench._profiled_traffic() == 123
+    monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(tmp_path / "missing.txt"))
+    assert bench._profiled_traffic() is None
+
+
+def test_peaks_come_from_the_measured_file_when_present():
+    peak, kind = bench._peaks()
+    if os.path.exists(os.path.join(bench.ROOT, "MEASURED_PEAKS.json")):
+        assert kind == "measured" and peak > 1000
+    else:
+        assert kind == "fallback"
