@@ -2,12 +2,12 @@
 
 One step = one pass of the whole path over one batch of the Llama-3-8B-shaped
 decode workload (32 requests, contexts uniform in [512, 4096], H_q 32,
-H_kv 8, head_dim 128, block_size 64, bf16): manager->kernel block expansion,
-slot mapping of the step's tokens and the K/V cache scatter (one fused
-kernel), and the paged decode (partition + merge kernels).  Inputs are seeded, synthetic and
-resident in HBM; the caches were filled beforehand through the same
-library.  L2 is flushed (a write of 2x the L2 size) before every timed step,
-outside the timed interval.
+H_kv 8, head_dim 128, block_size 64, bf16): manager->kernel block
+expansion, slot mapping of the step's tokens and the K/V cache scatter (one
+fused kernel), and the paged decode (partition + merge kernels).  Inputs
+are seeded, synthetic and resident in HBM; the caches were filled
+beforehand through the same library.  L2 is flushed (a write of 2x the L2
+size, read back) before every timed step, outside the timed interval.
 
 value  = decode KV bytes needed per step (cache_len rows x K,V x H_kv x D x 2B)
          / device time of the step (CUDA events), aggregated over ranks.
@@ -16,13 +16,18 @@ e2e    = the same bytes / time of a step that also copies the step's inputs
 roofline.achieved = the same bytes / device time of the decode partition
          kernel alone (the dominant kernel; bkv_paged_decode_partition);
          decode_ms is the whole decode call (partition + merge).
+secondary = slot mapping + cache write of the ragged mixed step (tokens/s).
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bkv|reference]
-                  [--workload NAME] [--sliding-window W]
---workload / --sliding-window time another seeded workload (long_context,
-hybrid_spec, ...) or a sliding-window decode on the same harness; the
-default is the headline configuration above.
+                  [--workload NAME] [--sliding-window W] [--kv-dtype bf16|fp8]
+                  [--cp-world W [--cp-interleave I]] [--attention decode|ragged]
+                  [--part step|write] [--eager] [--no-cpu-baseline] [--no-secondary]
+--workload / --sliding-window / --kv-dtype / --cp-world time another seeded
+workload, a sliding-window decode, FP8 caches or one decode-context-parallel
+rank on the same harness; --attention ragged times the mixed-step attention
+(tensor roofline); --part write times slot mapping + cache write of the
+ragged step alone.  The default is the headline configuration above.
 Under torchrun every rank runs an independent replica (the path has no
 exchange step); rank 0 prints one JSON line.
 """
