@@ -173,16 +173,8 @@ def bkv_map_to_kernel_blocks(mgr_table, block_size, kernel_block_size, kernel_ta
 
 def bkv_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens=None, err_count=None, stream=None):
     """Scatter k_new/v_new rows (num_tokens, H_kv, D) into the caches at slot_mapping (see include/bkv.h)."""
-    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
-        raise ValueError("caches must be (total_blocks, block_size, H_kv, D) and equal in shape")
+    dt = _check_kv_rows(k_new, v_new, k_cache, v_cache)
     tb, bs, hkv, d = k_cache.shape
-    if k_new.dim() != 3 or tuple(k_new.shape[1:]) != (hkv, d) or k_new.shape != v_new.shape:
-        raise ValueError("k_new/v_new must be (num_tokens, H_kv, D) matching the cache")
-    if k_new.stride(2) != 1 or k_new.stride(1) != d or k_new.stride() != v_new.stride():
-        raise ValueError("k_new/v_new rows must be dense (a row stride is allowed)")
-    dt = _kv_dtype(k_cache)
-    if k_new.dtype != k_cache.dtype or v_new.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
-        raise TypeError("mixed dtypes")
     n = k_new.shape[0] if num_tokens is None else int(num_tokens)
     if n > k_new.shape[0] or n > slot_mapping.numel():
         raise ValueError("num_tokens exceeds k_new / slot_mapping")
@@ -198,9 +190,8 @@ def bkv_slot_mapping_cache_write(block_table, req_indices, positions, slot_mappi
     block size is the table's (see include/bkv.h)."""
     if block_table.dim() != 2 or block_table.stride(1) != 1:
         raise ValueError("block_table must be 2-D with unit column stride")
-    _check_kv_rows(k_new, v_new, k_cache, v_cache)
+    dt = _check_kv_rows(k_new, v_new, k_cache, v_cache)
     tb, bs, hkv, d = k_cache.shape
-    dt = _kv_dtype(k_cache)
     n = positions.numel() if num_tokens is None else int(num_tokens)
     if n > positions.numel() or n > req_indices.numel() or n > slot_mapping.numel() or n > k_new.shape[0]:
         raise ValueError("num_tokens exceeds positions / req_indices / slot_mapping / k_new")
@@ -220,18 +211,8 @@ def bkv_slot_mapping_cache_write_fp8(block_table, req_indices, positions, slot_m
     (num_tokens, H_kv, D) bf16 or fp32 quantised into uint8 E4M3 caches (see include/bkv.h)."""
     if block_table.dim() != 2 or block_table.stride(1) != 1:
         raise ValueError("block_table must be 2-D with unit column stride")
-    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
-        raise ValueError("caches must be (total_blocks, block_size, H_kv, D) and equal in shape")
-    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
-        raise TypeError("FP8 caches are uint8 tensors of E4M3 codes")
+    dt = _check_kv_rows(k_new, v_new, k_cache, v_cache, fp8=True)
     tb, bs, hkv, d = k_cache.shape
-    if k_new.dim() != 3 or tuple(k_new.shape[1:]) != (hkv, d) or k_new.shape != v_new.shape:
-        raise ValueError("k_new/v_new must be (num_tokens, H_kv, D) matching the cache")
-    if k_new.stride(2) != 1 or k_new.stride(1) != d or k_new.stride() != v_new.stride():
-        raise ValueError("k_new/v_new rows must be dense (a row stride is allowed)")
-    if k_new.dtype != v_new.dtype:
-        raise TypeError("mixed dtypes")
-    dt = _kv_dtype(k_new)
     n = positions.numel() if num_tokens is None else int(num_tokens)
     if n > positions.numel() or n > req_indices.numel() or n > slot_mapping.numel() or n > k_new.shape[0]:
         raise ValueError("num_tokens exceeds positions / req_indices / slot_mapping / k_new")
@@ -246,7 +227,11 @@ def bkv_slot_mapping_cache_write_fp8(block_table, req_indices, positions, slot_m
     return slot_mapping
 
 
-def _check_kv_rows(k_new, v_new, k_cache, v_cache):
+def _check_kv_rows(k_new, v_new, k_cache, v_cache, fp8=False):
+    """Shape, layout and dtype checks shared by the cache writes; returns the dtype code of the rows.
+
+    Caches (total_blocks, block_size, H_kv, D), equal in shape: bf16 / fp32 like the rows, or uint8 E4M3
+    codes when ``fp8``.  Rows (num_tokens, H_kv, D), dense within a row (a row stride is allowed)."""
     if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
         raise ValueError("caches must be (total_blocks, block_size, H_kv, D) and equal in shape")
     _, _, hkv, d = k_cache.shape
@@ -254,26 +239,23 @@ def _check_kv_rows(k_new, v_new, k_cache, v_cache):
         raise ValueError("k_new/v_new must be (num_tokens, H_kv, D) matching the cache")
     if k_new.stride(2) != 1 or k_new.stride(1) != d or k_new.stride() != v_new.stride():
         raise ValueError("k_new/v_new rows must be dense (a row stride is allowed)")
+    if fp8:
+        if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+            raise TypeError("FP8 caches are uint8 tensors of E4M3 codes")
+        if k_new.dtype != v_new.dtype:
+            raise TypeError("mixed dtypes")
+        return _kv_dtype(k_new)
     if k_new.dtype != k_cache.dtype or v_new.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
         raise TypeError("mixed dtypes")
+    return _kv_dtype(k_cache)
 
 
 def bkv_cache_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, num_tokens=None,
                         err_count=None, stream=None):
     """Quantise k_new/v_new rows (num_tokens, H_kv, D; bf16 or fp32) into uint8 E4M3 caches at slot_mapping
     with per-tensor scales (see include/bkv.h)."""
-    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
-        raise ValueError("caches must be (total_blocks, block_size, H_kv, D) and equal in shape")
-    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
-        raise TypeError("FP8 caches are uint8 tensors of E4M3 codes")
+    dt = _check_kv_rows(k_new, v_new, k_cache, v_cache, fp8=True)
     tb, bs, hkv, d = k_cache.shape
-    if k_new.dim() != 3 or tuple(k_new.shape[1:]) != (hkv, d) or k_new.shape != v_new.shape:
-        raise ValueError("k_new/v_new must be (num_tokens, H_kv, D) matching the cache")
-    if k_new.stride(2) != 1 or k_new.stride(1) != d or k_new.stride() != v_new.stride():
-        raise ValueError("k_new/v_new rows must be dense (a row stride is allowed)")
-    if k_new.dtype != v_new.dtype:
-        raise TypeError("mixed dtypes")
-    dt = _kv_dtype(k_new)
     n = k_new.shape[0] if num_tokens is None else int(num_tokens)
     if n > k_new.shape[0] or n > slot_mapping.numel():
         raise ValueError("num_tokens exceeds k_new / slot_mapping")
