@@ -69,3 +69,71 @@ def test_binding_refuses_host_tensors():
         bkv.bkv_cache_write(_rows(3), _rows(3), slots, _cache(), _cache())
     with pytest.raises(TypeError, match="CUDA tensor"):
         bkv.bkv_slot_mapping_cache_write(table, req, pos, slots, _rows(3), _rows(3), _cache(), _cache())
+
+
+class _FakeLib:
+    """Records the arguments each entry point is called with."""
+
+    def __init__(self):
+        self.calls = {}
+
+    def __getattr__(self, name):
+        def f(*args):
+            self.calls[name] = args
+            return 0
+        return f
+
+
+@pytest.fixture
+def fake(monkeypatch):
+    lib = _FakeLib()
+    monkeypatch.setattr(bkv, "load", lambda: lib)
+    ptrs = {}
+    monkeypatch.setattr(bkv, "_dev", lambda t, name, dtype=None, contiguous=True: ptrs.setdefault(name, len(ptrs) + 1))
+    monkeypatch.setattr(bkv, "_stream", lambda s: 999)
+    lib.ptrs = ptrs
+    return lib
+
+
+def test_cache_write_marshalling(fake):
+    fused = torch.zeros(5, 3, 8, 128, dtype=torch.float32)
+    k, v = fused[:, 1], fused[:, 2]                                   # row stride 3 * 8 * 128
+    bkv.bkv_cache_write(k, v, torch.zeros(5, dtype=torch.int64), _cache(dtype=torch.float32),
+                        _cache(dtype=torch.float32), num_tokens=4)
+    p = fake.ptrs
+    assert fake.calls["bkv_cache_write"] == (p["k_new"], p["v_new"], 4, 3 * 8 * 128, p["slot_mapping"], p["k_cache"],
+                                             p["v_cache"], 3, 16, 8, 128, bkv.BKV_F32, None, 999)
+
+
+def test_cache_write_fp8_marshalling(fake):
+    u8 = torch.uint8
+    bkv.bkv_cache_write_fp8(_rows(), _rows(), torch.zeros(5, dtype=torch.int64), _cache(dtype=u8), _cache(dtype=u8),
+                            0.5, 0.25)
+    p = fake.ptrs
+    assert fake.calls["bkv_cache_write_fp8"] == (p["k_new"], p["v_new"], 5, 8 * 128, p["slot_mapping"],
+                                                 p["k_cache"], p["v_cache"], 3, 16, 8, 128, bkv.BKV_BF16, 0.5, 0.25,
+                                                 None, 999)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_fused_write_marshalling(fake, fp8):
+    wide = torch.ones(4, 10, dtype=torch.int32)
+    table = wide[:, 2:8]                                              # row stride 10, 6 columns
+    req = torch.zeros(7, dtype=torch.int32)
+    pos = torch.zeros(7, dtype=torch.int64)
+    slots = torch.zeros(9, dtype=torch.int64)
+    cdt = torch.uint8 if fp8 else torch.bfloat16
+    if fp8:
+        bkv.bkv_slot_mapping_cache_write_fp8(table, req, pos, slots, _rows(7), _rows(7), _cache(dtype=cdt),
+                                             _cache(dtype=cdt), 2.0, 3.0, num_tokens=6)
+        name, tail = "bkv_slot_mapping_cache_write_fp8", (2.0, 3.0, None, 999)
+    else:
+        bkv.bkv_slot_mapping_cache_write(table, req, pos, slots, _rows(7), _rows(7), _cache(dtype=cdt),
+                                         _cache(dtype=cdt), num_tokens=6)
+        name, tail = "bkv_slot_mapping_cache_write", (None, 999)
+    p = fake.ptrs
+    assert fake.calls[name] == (p["block_table"], 4, 10, 6, p["req_indices"], p["positions"], 6, 9, p["slot_mapping"],
+                                p["k_new"], p["v_new"], 8 * 128, p["k_cache"], p["v_cache"], 3, 16, 8, 128,
+                                bkv.BKV_BF16) + tail
+    with pytest.raises(ValueError):                                    # more tokens than rows
+        bkv.bkv_slot_mapping_cache_write(table, req, pos, slots, _rows(3), _rows(3), _cache(), _cache())
