@@ -60,7 +60,7 @@ const char *bkv_status_string(int status);
 /* Text of the last CUDA error seen by this library in this thread ("" if none). */
 const char *bkv_last_cuda_error(void);
 
-/* Library version, e.g. "bkv 0.1.0 sm_103a". */
+/* Library version, e.g. "bkv 0.2.0 sm_103a". */
 const char *bkv_version(void);
 
 /*
