@@ -1,7 +1,6 @@
 """CPU checks of the C ABI: libbkv.so builds, loads, exports every entry point
 include/bkv.h declares, and rejects bad arguments on the host (before any
 CUDA call) with the documented status codes."""
-import ctypes
 import os
 import re
 

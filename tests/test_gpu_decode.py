@@ -7,7 +7,6 @@ configuration states.  Caches start as NaN everywhere, so a read of any
 position that was never written (block 0, slack blocks, the tail of a
 request's last block) poisons the output and fails the comparison.
 """
-import dataclasses
 
 import numpy as np
 import pytest

@@ -24,7 +24,7 @@ import torch
 
 import oracle
 from paged_kv_cache_slot_gb300 import workloads as wl
-from oracle.cases import BF16_NAN, fill_oracle_cache, nan_cache
+from oracle.cases import BF16_NAN, fill_oracle_cache
 
 F64 = torch.float64
 
