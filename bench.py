@@ -201,44 +201,82 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _oracle_pass(oracle, rows, q, kc, vc, table, ctx, window, threads):
+    """The oracle's decode of ``rows`` (longest first), one request per call, on ``threads`` host threads
+    (the C oracle runs with the interpreter lock released, so the calls run in parallel)."""
+    if threads <= 1:
+        for r in rows:
+            oracle.paged_decode_request(r, q, kc, vc, table, ctx, sliding_window=window)
+        return
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda r: oracle.paged_decode_request(r, q, kc, vc, table, ctx, sliding_window=window), rows))
+
+
 def _cpu_baseline(budget_s: float, workload: str = WORKLOAD, window: int = 0):
-    """The oracle, as it stands, on a bounded sample of the workload: every
-    request decoded (single thread, fp64), each repeated ``reps`` times so that
-    the timed CPU work comes to about ``budget_s``; ``reps`` is calibrated on
-    the longest request."""
+    """The oracle, as it stands, on the whole workload: every request decoded (fp64), timed once over all
+    host cores (threads over requests, longest first) and once on a single thread, each pass repeated
+    until about ``budget_s`` / 2 of CPU work.  The all-cores figure is the baseline; the single-thread
+    one is reported beside it."""
     import oracle
     from oracle.cases import fill_oracle_cache
     from paged_kv_cache_slot_gb300 import workloads as wl
 
     w = wl.make(workload)
     q = w.q()
-    order = [int(r) for r in np.argsort(w.context_lens)[::-1]]      # fixed order, longest first
+    kc, vc, table = fill_oracle_cache(w)
+    rows = [int(r) for r in np.argsort(w.context_lens, kind="stable")[::-1] if w.context_lens[r] > 0]
     per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
     Ls = w.context_lens.astype(np.int64)
     eff = Ls - (np.maximum(0, Ls - w.q_len - window + 1) if window > 0 else 0)   # rows each request reads
-    total_ctx = int(eff.sum())
-    done_bytes, done_t, reps = 0, 0.0, None
-    for r in order:
-        kc, vc, table = fill_oracle_cache(w, rows=[r])
-        if reps is None:
-            t0 = time.perf_counter()
-            oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens, sliding_window=window)
-            t_row = time.perf_counter() - t0
-            pass_est = t_row * total_ctx / max(int(eff[r]), 1)
-            reps = max(1, math.ceil(budget_s / max(pass_est, 1e-6)))
+    pass_bytes = int(eff.sum()) * per_tok
+    cores = os.cpu_count() or 1
+
+    def timed(threads):
+        t0 = time.perf_counter()
+        _oracle_pass(oracle, rows, q, kc, vc, table, w.context_lens, window, threads)
+        first = time.perf_counter() - t0
+        reps = max(1, math.ceil((budget_s / 2) / max(first, 1e-6)) - 1)
         t0 = time.perf_counter()
         for _ in range(reps):
-            oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens, sliding_window=window)
-        done_t += time.perf_counter() - t0
-        done_bytes += reps * int(eff[r]) * per_tok
-        del kc, vc
-    return {"value": done_bytes / done_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"all {w.num_rows} requests of {workload} x {reps} repeats decoded by the fp64 C oracle "
-                      f"({done_bytes / 1e6:.1f} MB of K/V, {done_t:.1f} s, single thread)"}
+            _oracle_pass(oracle, rows, q, kc, vc, table, w.context_lens, window, threads)
+        dt = time.perf_counter() - t0
+        return pass_bytes * reps / dt / 1e9, reps, dt
+
+    v_all, reps_all, t_all = timed(cores)
+    v_one, reps_one, t_one = timed(1)
+    model = cpu_model()
+    return {"value": v_all, "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu_model": model,
+            "sample": f"all {len(rows)} requests of {workload} ({pass_bytes / 1e6:.1f} MB of K/V per pass) decoded by "
+                      f"the fp64 C oracle, {reps_all} passes in {t_all:.1f} s on {cores} threads (requests in "
+                      f"parallel, longest first)",
+            "single_thread": {"value": v_one, "unit": "GB/s", "cores": 1,
+                              "sample": f"{reps_one} passes in {t_one:.1f} s on one thread"}}
 
 
 def run_reference(args):
-    """--impl reference: the oracle timed on the host cores, same metric and config."""
+    """--impl reference: the oracle, as it stands, on the host cores, with this arm's metric and config:
+    each step is the whole headline step of the Llama-shaped batch -- block expansion, slot mapping and
+    cache write of the step's 32 tokens, and the decode of all 32 requests (threads over requests on
+    every core) -- over caches the oracle filled beforehand."""
     dist = _dist()
     rank = dist.get_rank() if dist else 0
     if rank != 0:
@@ -249,15 +287,22 @@ def run_reference(args):
 
     w = wl.make(WORKLOAD)
     q = w.q()
+    w_prior = wl.make(WORKLOAD)
+    w_prior.new_tokens = np.zeros_like(w_prior.new_tokens)      # the caches before this step: prior tokens only
+    kc, vc, _ = fill_oracle_cache(w_prior)
+    req, pos = w.step_tokens()
+    kn, vn = w.step_kv()
     per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
-    rows = [int(np.argsort(w.context_lens)[len(w.context_lens) // 2])]  # the median-length request
-    kc, vc, table = fill_oracle_cache(w, rows=rows)
-    step_bytes = sum(int(w.context_lens[r]) for r in rows) * per_tok
+    step_bytes = int(w.context_lens.astype(np.int64).sum()) * per_tok
+    rows = [int(r) for r in np.argsort(w.context_lens, kind="stable")[::-1]]
+    cores = os.cpu_count() or 1
 
     def one_step():
         t0 = time.perf_counter()
-        for r in rows:
-            oracle.paged_decode_request(r, q, kc, vc, table, w.context_lens)
+        table = oracle.map_to_kernel_blocks(w.block_table, w.block_size, w.kernel_block_size)
+        slots, _ = oracle.compute_slot_mapping(table, req, pos, w.kernel_block_size, w.num_tokens, w.max_num_tokens)
+        oracle.cache_write(kn, vn, slots, kc, vc, num_tokens=w.num_tokens, inplace=True)
+        _oracle_pass(oracle, rows, q, kc, vc, table, w.context_lens, 0, cores)
         return time.perf_counter() - t0
 
     for _ in range(args.warmup):
@@ -265,15 +310,39 @@ def run_reference(args):
     times = [one_step() for _ in range(args.steps)]
     ms = 1e3 * sum(times) / len(times)
     value = step_bytes / (ms / 1e3) / 1e9
+    sample = (f"the whole step per timed step: block expansion, slot mapping + cache write of 32 tokens and the "
+              f"decode of all 32 requests ({step_bytes / 1e6:.1f} MB of K/V) by the fp64 C oracle on {cores} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "llama3_decode: 32 req, ctx U[512,4096]+1, H_q 32, H_kv 8, D 128, bs 64, bf16",
-                       "sample": f"request {rows[0]} ({int(w.context_lens[rows[0]])} positions) per step"},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"one median-length request ({step_bytes / 1e6:.1f} MB K/V) per step"},
+            "config": {"workload": _describe(w, 0), "sample": "every request of the workload, every step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def bucket_report(w):
+    """The long-context decode's K/V bytes three ways ("Decode Context-Length Bucketing", Problem: a
+    request that reads its full max_model_len row of the block table moves far more than its context;
+    Design / Per-step bucket selection: needed_seq = max(num_computed) + 1 + num_speculative_tokens and
+    the bucket is the smallest configured length >= needed_seq, max_model_len last): what the decode
+    reads (each request's cache_len rows), the full rows, and the chosen bucket's rows for every
+    request of the batch."""
+    per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+    spec = w.q_len - 1
+    needed = int(w.prior_lens[: w.num_real].max()) + 1 + spec
+    mml = int(w.extra["max_model_len"])
+    cands = sorted(int(b) for b in w.extra["buckets"]) + [mml]
+    bucket = next((b for b in cands if b >= needed), -1)
+    read = int(w.context_lens[: w.num_real].astype(np.int64).sum()) * per_tok
+    full = w.num_real * mml * per_tok
+    bucketed = w.num_real * bucket * per_tok if bucket > 0 else None
+    return {"workload": w.name, "needed_seq": needed, "buckets": cands, "bucket": bucket,
+            "kv_bytes_read": read, "full_row_bytes": full, "bucketed_bytes": bucketed,
+            "full_row_over_read": full / read, "bucketed_over_read": (bucketed / read) if bucketed else None,
+            "source": "Decode Context-Length Bucketing: Problem (~32x DMA amplification of full-row reads, "
+                      "Trn2/Trn3) and Design / Per-step bucket selection"}
 
 
 def torch_int64():
@@ -483,6 +552,17 @@ def run_bkv(args):
                      "cuda_graph": not args.eager}
         del rdw
 
+    # the other workloads, read variants and the mixed-step attention, each timed on its own
+    extra, ragged = None, None
+    if rank == 0 and headline and not args.no_extra:
+        extra = []
+        for name, window, use_fp8, cpx in EXTRA_DECODE_LEGS:
+            leg = decode_leg(torch, f"cuda:{local}", flush, stream, args.steps, name, window,
+                             FP8_SCALES if use_fp8 else None, cpx, args.eager)
+            leg.update({"sliding_window": window, "kv_cache": "e4m3" if use_fp8 else "bf16", "cp_world": cpx[0]})
+            extra.append(leg)
+        ragged = ragged_leg(torch, f"cuda:{local}", flush, stream, args.steps, args.eager)
+
     if rank != 0:
         return
     peak, peak_kind = _peaks()
@@ -524,6 +604,12 @@ def run_bkv(args):
     }
     if secondary:
         line["secondary"] = secondary
+    if headline:
+        line["config4_bytes"] = bucket_report(wl.make("long_context"))
+    if extra:
+        line["other_workloads"] = extra
+    if ragged:
+        line["ragged_attention"] = ragged
     if cp_merge:
         line["cp_merge_states"] = cp_merge
     if not args.no_cpu_baseline and fp8 is None:
@@ -531,18 +617,64 @@ def run_bkv(args):
     print(json.dumps(line), flush=True)
 
 
+def ragged_leg(torch, dev, flush, stream, steps, eager=False, loud=False):
+    """Paged attention over the mixed ragged_step batch (48 decode tokens and 16 prefill chunks of 64..1024
+    tokens over prior contexts of 0..2048, H_q 32, H_kv 8, D 128, kernel bs 16, bf16), one
+    bkv_paged_attention_ragged call per step, CUDA graph, L2 flushed before each step.  Prefill dominates,
+    so the roofline is the tensor one: algorithmic FLOPs = 4 * D per visible (query head, key) pair."""
+    from paged_kv_cache_slot_gb300 import bkv
+    from paged_kv_cache_slot_gb300 import workloads as wl
+    from paged_kv_cache_slot_gb300.staging import DeviceWorkload
+
+    w = wl.make("ragged_step", loud=loud)
+    dw = DeviceWorkload(w, device=dev)
+    dw.write_step()
+    q = torch.from_numpy(w.q_tokens()).view(torch.bfloat16).to(dev)
+    out = torch.empty_like(q)
+    qsl = torch.from_numpy(w.query_start_loc()).to(dev)
+    mq = int(w.new_tokens.max())
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        bkv.bkv_paged_attention_ragged(q, qsl, dw.k_cache, dw.v_cache, dw.kernel_table, dw.context_lens,
+                                       dw.max_context_len, mq, out, err_count=err, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    body = step
+    if not eager:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        body = g.replay
+    times = _time_steps(torch, body, steps, flush, stream)
+    ms = sum(times) / len(times)
+    assert int(err.item()) == 0
+    L = w.context_lens.astype(np.int64)
+    n = w.new_tokens.astype(np.int64)
+    # token i of request r sees L - n + i + 1 keys: sum over i = n (L - n) + n (n + 1) / 2
+    pairs = int((n * (L - n) + n * (n + 1) // 2).sum()) * w.num_q_heads
+    flops = 4 * w.head_dim * pairs
+    kv_bytes = int(L[n > 0].sum()) * 2 * w.num_kv_heads * w.head_dim * 2
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        peak = float(json.load(f)["bf16_tflops"])
+    achieved = flops / (ms / 1e3) / 1e12
+    return {"workload": f"ragged_step: {w.num_tokens} query tokens of 64 requests (48 x 1, 16 x 64..1024), prior "
+                        "0..2048, H_q 32, H_kv 8, D 128, bs 16, bf16, causal",
+            "ms_per_step": ms, "attended_pairs": pairs, "flops_per_step": flops, "kv_bytes_once": kv_bytes,
+            "TFLOPs": achieved, "peak_TFLOPs": peak, "frac": achieved / peak,
+            "peak_kind": "measured bf16 dense (burst)", "kv_GBps_once": kv_bytes / (ms / 1e3) / 1e9,
+            "kernel": "bkv_paged_attention_ragged (tcgen05 prefill kernel)", "cuda_graph": not eager}
+
+
 def run_ragged(args):
-    """--attention ragged: paged attention over the mixed ragged_step batch (48 decode tokens and 16
-    prefill chunks of 64..1024 tokens over prior contexts of 0..2048, H_q 32, H_kv 8, D 128, kernel
-    bs 16, bf16), one bkv_paged_attention_ragged call per step, CUDA graph, L2 flushed before each
-    step.  Prefill dominates, so the roofline is the tensor one: algorithmic FLOPs = 4 * D per visible
-    (query head, key) pair."""
+    """--attention ragged: the ragged leg alone, as its own JSON line (tensor roofline)."""
     import torch
 
     from paged_kv_cache_slot_gb300 import bkv
-    from paged_kv_cache_slot_gb300 import workloads as wl
     from paged_kv_cache_slot_gb300.build import build
-    from paged_kv_cache_slot_gb300.staging import DeviceWorkload
 
     dist = _dist()
     rank = dist.get_rank() if dist else 0
@@ -554,70 +686,94 @@ def run_ragged(args):
     if dist:
         dist.barrier()
     bkv.load()
-    w = wl.make("ragged_step")
     dev = f"cuda:{local}"
-    dw = DeviceWorkload(w, device=dev)
-    dw.write_step()
-    q = torch.from_numpy(w.q_tokens()).view(torch.bfloat16).to(dev)
-    out = torch.empty_like(q)
-    qsl = torch.from_numpy(w.query_start_loc()).to(dev)
-    mq = int(w.new_tokens.max())
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
-
-    def step():
-        bkv.bkv_paged_attention_ragged(q, qsl, dw.k_cache, dw.v_cache, dw.kernel_table, dw.context_lens,
-                                       dw.max_context_len, mq, out, err_count=err, stream=stream)
-
-    with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            step()
-    torch.cuda.synchronize()
-    body = step
-    if not args.eager:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step()
-        body = g.replay
     if dist:
         dist.barrier()
     with ClockSampler(local) as clk:
-        times = _time_steps(torch, body, args.steps, flush, stream)
-    ms = sum(times) / len(times)
-    ms, = max_over_ranks([ms], dist, dev)
-    assert int(err.item()) == 0
+        leg = ragged_leg(torch, dev, flush, stream, args.steps, args.eager)
+    ms, = max_over_ranks([leg["ms_per_step"]], dist, dev)
     if rank != 0:
         return
-    L = w.context_lens.astype(np.int64)
-    n = w.new_tokens.astype(np.int64)
-    # token i of request r sees L - n + i + 1 keys: sum over i = n (L - n) + n (n + 1) / 2
-    pairs = int((n * (L - n) + n * (n + 1) // 2).sum()) * w.num_q_heads
-    flops = 4 * w.head_dim * pairs
-    kv_bytes = int(L[n > 0].sum()) * 2 * w.num_kv_heads * w.head_dim * 2
-    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-        peaks = json.load(f)
-    peak = float(peaks["bf16_tflops"])
-    achieved = flops / (ms / 1e3) / 1e12
+    achieved = leg["flops_per_step"] / (ms / 1e3) / 1e12
     line = {
         "metric": "mixed-step paged attention TFLOP/s (ragged_step)", "value": world * achieved, "unit": "TFLOP/s",
-        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+        "n_gpus": world, "steps": args.steps, "warmup": 3, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"ragged_step: {w.num_tokens} query tokens of 64 requests (48 x 1, 16 x 64..1024), "
-                               "prior 0..2048, H_q 32, H_kv 8, D 128, bs 16, bf16, causal",
-                   "attended_pairs": pairs, "flops_per_step": flops, "kv_bytes_once": kv_bytes,
+        "config": {"workload": leg["workload"], "attended_pairs": leg["attended_pairs"],
+                   "flops_per_step": leg["flops_per_step"], "kv_bytes_once": leg["kv_bytes_once"],
                    "l2": "flushed before every timed step (write 2x L2, read it back)",
-                   "cuda_graph": not args.eager},
+                   "cuda_graph": leg["cuda_graph"]},
         "gpu_launches": args.steps,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "kernel": "bkv_paged_attention_ragged (tcgen05 prefill kernel)",
-                     "peak_kind": "measured bf16 dense (burst)",
-                     "kv_GBps_once": kv_bytes / (ms / 1e3) / 1e9},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": leg["peak_TFLOPs"], "unit": "TFLOP/s",
+                     "frac": achieved / leg["peak_TFLOPs"], "traffic": None, "kernel": leg["kernel"],
+                     "peak_kind": leg["peak_kind"], "kv_GBps_once": leg["kv_GBps_once"]},
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
+
+
+def decode_leg(torch, dev, flush, stream, steps, name, window=0, fp8=None, cp=(1, 0, 1), eager=False):
+    """Device times of one workload's decode, outside the headline's timed region: the partition kernel
+    alone and the whole decode call (partition + merge), each a CUDA graph replayed after an L2 flush;
+    the caches hold device-drawn values (timing does not depend on them)."""
+    from paged_kv_cache_slot_gb300 import workloads as wl
+    from paged_kv_cache_slot_gb300.staging import DeviceWorkload
+
+    w = wl.make(name)
+    dw = DeviceWorkload(w, device=dev, sliding_window=window, kv_fp8=fp8, cp_world=cp[0], cp_rank=cp[1],
+                        cp_interleave=cp[2], prior_values="device")
+    dw.write_step()
+    kv = dw.decode_kv_bytes()
+
+    def dec():
+        dw.decode(stream=stream)
+
+    def part():
+        dw.decode_partition(stream=stream) if cp[0] == 1 else dw.decode(stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dec()
+            part()
+    torch.cuda.synchronize()
+    bodies = {"decode": dec, "partition": part}
+    if not eager:
+        for k, fn in list(bodies.items()):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            bodies[k] = g.replay
+    dms = statistics.mean(_time_steps(torch, bodies["decode"], steps, flush, stream))
+    pms = statistics.mean(_time_steps(torch, bodies["partition"], steps, flush, stream))
+    assert int(dw.err_count.item()) == 0
+    peak, _ = _peaks()
+    out = {"workload": _describe(w, window, cp, fp8), "kv_bytes": kv, "partition_us": 1e3 * pms,
+           "decode_call_us": 1e3 * dms, "partition_GBps": kv / (pms / 1e3) / 1e9,
+           "decode_call_GBps": kv / (dms / 1e3) / 1e9}
+    out["partition_frac"] = out["partition_GBps"] / peak
+    out["decode_call_frac"] = out["decode_call_GBps"] / peak
+    del dw
+    torch.cuda.empty_cache()
+    return out
+
+
+# the other workloads and read variants timed beside the headline: (name, sliding window, FP8 cache,
+# context-parallel (world, rank, interleave))
+EXTRA_DECODE_LEGS = [
+    ("long_context", 0, False, (1, 0, 1)),
+    ("hybrid_spec", 0, False, (1, 0, 1)),
+    ("llama3_decode", 1024, False, (1, 0, 1)),
+    ("long_context", 4096, False, (1, 0, 1)),
+    ("hybrid_spec", 512, False, (1, 0, 1)),
+    ("llama3_decode", 0, True, (1, 0, 1)),
+    ("long_context", 0, True, (1, 0, 1)),
+    ("hybrid_spec", 0, True, (1, 0, 1)),
+    ("llama3_decode", 0, False, (2, 0, 1)),
+    ("llama3_decode", 0, False, (4, 0, 1)),
+]
 
 
 def run_write(args):
@@ -700,6 +856,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads, read variants and mixed-step attention timed beside the headline")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA graphs")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="seeded workload to time (default: the Llama-3-8B-shaped decode batch)")

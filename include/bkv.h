@@ -60,7 +60,7 @@ const char *bkv_status_string(int status);
 /* Text of the last CUDA error seen by this library in this thread ("" if none). */
 const char *bkv_last_cuda_error(void);
 
-/* Library version, e.g. "bkv 0.2.0 sm_103a". */
+/* Library version, e.g. "bkv 0.3.0 sm_103a". */
 const char *bkv_version(void);
 
 /*
@@ -102,7 +102,8 @@ int bkv_compute_slot_mapping(const int32_t *block_table, int32_t num_reqs, int64
  *     m = mgr_table[r * mgr_stride + j]
  *   so that the kernel view (total_blocks * bpk, kernel_block_size, H, D) of
  *   a cache is the same memory as the manager view.  Columns at or past
- *   mgr_cols * bpk are not written.  m * bpk + t must fit in int32.
+ *   mgr_cols * bpk are not written.  An id m * bpk + t above INT32_MAX
+ *   cannot be held by the int32 table and is written as -1 (no block).
  *
  *   INVALID_ARG: kernel_block_size <= 0, block_size % kernel_block_size != 0,
  *   kernel_stride < mgr_cols * bpk, mgr_stride < mgr_cols, null pointers.
@@ -184,8 +185,7 @@ size_t bkv_paged_decode_workspace_size(int32_t num_reqs, int32_t q_len, int32_t 
  *   For request r with L = context_lens[r] (cache length INCLUDING this
  *   step's q_len tokens), query token t < q_len, query head h, G =
  *   num_q_heads / num_kv_heads:
- *     key j is visible iff j < L, j <= L - q_len + t (BKV_MASK_CAUSAL only),
- *     j >= L - q_len + t - sliding_window + 1 (sliding_window > 0 only)
+ *     key j is visible iff j < L, j <= L - q_len + t (BKV_MASK_CAUSAL only)
  *     and b = block_table[r * bt_stride + j / block_size] > 0;
  *     out[r][t][h] = softmax_j(softmax_scale * q[r][t][h] . K[b][j % block_size][h / G])
  *                    . V[b][j % block_size][h / G]
@@ -199,24 +199,18 @@ size_t bkv_paged_decode_workspace_size(int32_t num_reqs, int32_t q_len, int32_t 
  *   block_table int32 [num_reqs, bt_stride], bt_cols columns valid.
  *   context_lens int32 [num_reqs].
  *   max_context_len  host-side upper bound on context_lens (sizes the grid);
- *             a larger context_lens[r] is clamped to it and counted as an error.
+ *             a larger context_lens[r] is clamped to it and counted once per
+ *             such request in *err_count.
  *   softmax_scale    <= 0 selects 1 / sqrt(head_dim).
- *   sliding_window   W > 0: a sliding-window attention layer ("KV Caching
- *             with vLLM", Layer-specific cache specification: an SWA layer
- *             keeps only the recent tokens within the window; "Decode
- *             Context-Length Bucketing", Block-table head-trim vs. SWA
- *             tail-trim): query t sees only the last W positions up to its
- *             own, and only the blocks that overlap some query's window are
- *             read, so the entries of older blocks may already be null (-1)
- *             and their memory reused.  The table keeps logical block
- *             numbering (entry j covers positions [j * block_size, ...)), so
- *             no position offset is passed.  0: full attention.
  *   workspace        device scratch of workspace_bytes >=
  *                    bkv_paged_decode_workspace_size(...); may be null when
- *                    that size is 0.  Used only while the call's kernels run.
- *   Ids >= total_blocks and positions past bt_cols are masked and counted.
+ *                    that size is 0.  Used only while the call's kernels run;
+ *                    its contents on entry do not matter.
+ *   Bad table entries among those a request needs (an id >= total_blocks,
+ *   or a block past bt_cols) are masked like null entries and each counts
+ *   num_kv_heads times in *err_count (once per KV head that would read it).
  *   INVALID_ARG: num_q_heads % num_kv_heads != 0, non-positive sizes, bad
- *   mask_mode, negative sliding_window, workspace too small, null pointers.
+ *   mask_mode, workspace too small, null pointers.
  *   UNSUPPORTED: dtype not BKV_BF16 / BKV_F32, head_dim > 256 or odd.
  */
 int bkv_paged_decode(const void *q, const void *k_cache, const void *v_cache,
@@ -224,24 +218,51 @@ int bkv_paged_decode(const void *q, const void *k_cache, const void *v_cache,
                      const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs,
                      int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                      int32_t block_size, int64_t total_blocks, float softmax_scale, int mask_mode,
-                     int32_t sliding_window, int dtype, void *out, void *workspace,
-                     size_t workspace_bytes, int32_t *err_count, bkv_stream_t stream);
+                     int dtype, void *out, void *workspace, size_t workspace_bytes,
+                     int32_t *err_count, bkv_stream_t stream);
+
+/*
+ * bkv_paged_decode_swa
+ *   bkv_paged_decode for a sliding-window attention layer ("KV Caching with
+ *   vLLM", Layer-specific cache specification: an SWA layer keeps only the
+ *   recent tokens within the window; "Decode Context-Length Bucketing",
+ *   Block-table head-trim vs. SWA tail-trim).  The same arguments with
+ *   `sliding_window` inserted after `mask_mode`:
+ *     sliding_window W > 0: key j is visible to query t only if also
+ *             j >= L - q_len + t - W + 1 (the last W positions up to its
+ *             own), and only the blocks that overlap some query's window
+ *             are read, so the entries of older blocks may already be null
+ *             (-1) and their memory reused.  The table keeps logical block
+ *             numbering (entry j covers positions [j * block_size, ...)), so
+ *             no position offset is passed.  Bad entries are counted only
+ *             among the blocks that are read.
+ *     W = 0: exactly bkv_paged_decode.
+ *   INVALID_ARG: as bkv_paged_decode, or sliding_window < 0.
+ */
+int bkv_paged_decode_swa(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
+                         const int32_t *context_lens, int32_t max_context_len, int32_t num_reqs,
+                         int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int64_t total_blocks, float softmax_scale, int mask_mode,
+                         int32_t sliding_window, int dtype, void *out, void *workspace,
+                         size_t workspace_bytes, int32_t *err_count, bkv_stream_t stream);
 
 /*
  * bkv_paged_decode_partition, bkv_paged_decode_merge
- *   The two phases of bkv_paged_decode, with exactly its arguments and
- *   checks: the partition phase reads the cache and writes every split-KV
- *   partial (o, max, sum of weights) into `workspace`; the merge phase,
- *   enqueued later with the same arguments and the same workspace contents,
- *   combines them into `out`.  The operation is the one bkv_paged_decode
- *   defines ("Padding and Batching with Block KV", Cache Masking); the pages
- *   prescribe no split, so the split itself and its exact log-sum-exp merge
- *   of partial softmaxes belong to this library (no counterpart on the
- *   pages).  bkv_paged_decode is exactly partition followed by merge, so the
- *   two-call form gives bit-identical results.  Between the calls the caller
- *   may run other work on the stream; the workspace layout is private to
- *   this library version, so it must reach the merge unchanged.
- *   Errors: as bkv_paged_decode; each call validates its arguments again.
+ *   The two phases of bkv_paged_decode_swa (sliding_window 0: of
+ *   bkv_paged_decode), with exactly its arguments and checks: the partition
+ *   phase reads the cache and writes every split-KV partial (o, max, sum of
+ *   weights) into `workspace`; the merge phase, enqueued later with the same
+ *   arguments and the same workspace contents, combines them into `out`.
+ *   The operation is the one bkv_paged_decode defines ("Padding and Batching
+ *   with Block KV", Cache Masking); the pages prescribe no split, so the
+ *   split itself and its exact log-sum-exp merge of partial softmaxes belong
+ *   to this library (no counterpart on the pages).  bkv_paged_decode_swa is
+ *   exactly partition followed by merge, so the two-call form gives
+ *   bit-identical results.  Between the calls the caller may run other work
+ *   on the stream; the workspace layout is private to this library version,
+ *   so it must reach the merge unchanged.
+ *   Errors: as bkv_paged_decode_swa; each call validates its arguments again.
  */
 int bkv_paged_decode_partition(const void *q, const void *k_cache, const void *v_cache,
                                const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
@@ -310,11 +331,11 @@ int bkv_slot_mapping_cache_write_fp8(const int32_t *block_table, int32_t num_req
 
 /*
  * bkv_paged_decode_fp8, bkv_paged_decode_fp8_partition, bkv_paged_decode_fp8_merge
- *   bkv_paged_decode (and its two phases) over FP8 caches written by
+ *   bkv_paged_decode_swa (and its two phases) over FP8 caches written by
  *   bkv_cache_write_fp8: a key element with code c stands for the value
  *   e4m3(c) * k_scale and a value element for e4m3(c) * v_scale; the
  *   operation, masks, sliding window, null entries, error counting and
- *   workspace are exactly bkv_paged_decode's ("Padding and Batching with
+ *   workspace are exactly bkv_paged_decode_swa's ("Padding and Batching with
  *   Block KV", Cache Masking; the FP8 format is the reading stated at
  *   bkv_cache_write_fp8).  `dtype` is the type of q and out (BKV_BF16 /
  *   BKV_F32); k_cache, v_cache are uint8 [total_blocks, block_size,
@@ -326,8 +347,8 @@ int bkv_slot_mapping_cache_write_fp8(const int32_t *block_table, int32_t num_req
  *   below), P . v on f16 with the value codes widened exactly; anything else
  *   runs the CUDA-core kernel on the exact code values.  The workspace
  *   (bkv_paged_decode_workspace_size) includes the split queries.
- *   Errors: as bkv_paged_decode, plus INVALID_ARG for a scale that is not a
- *   positive finite number.
+ *   Errors: as bkv_paged_decode_swa, plus INVALID_ARG for a scale that is
+ *   not a positive finite number.
  */
 int bkv_paged_decode_fp8(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
                          const int32_t *block_table, int64_t bt_stride, int32_t bt_cols,
@@ -479,12 +500,17 @@ int bkv_merge_attn_states(const void *outs, const float *lses, int32_t parts, in
  *   BKV_ERR_UNSUPPORTED before anything is enqueued (use bkv_paged_decode
  *   with your own workspace for those).
  *
- *   The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.  All calls share the one array and leave the
- *   last call's partial results in it (nothing in it has to start at zero):
- *   calls whose kernels overlap on the GPU (on different streams without
- *   ordering between them) race on it and give undefined results.
+ *   The array's device address is looked up (cudaGetSymbolAddress, with
+ *   the call's device current) on every call made outside stream capture,
+ *   so a device reset between calls does no harm.  A call made while its
+ *   stream is being captured uses the address the last call outside
+ *   capture found on that device: make one call on each device before
+ *   capturing (a first call under capture returns BKV_ERR_CUDA), and do not
+ *   reset the device between that call and the replays.  All calls share
+ *   the one array and leave the last call's partial results in it (nothing
+ *   in it has to start at zero): calls whose kernels overlap on the GPU (on
+ *   different streams without ordering between them) race on it and give
+ *   undefined results.
  */
 #define BKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 

@@ -84,6 +84,9 @@
  *       infinities) saturated to 448, NaN to NaN; a stored code c stands for
  *       the value e4m3(c) * scale.  Attention over an FP8 cache is O4 on
  *       those values.
+ *   R17 an expanded kernel block id m*bpk + t above INT32_MAX cannot be
+ *       held by the int32 kernel table: it is written as -1 (no block),
+ *       the same outcome as an entry <= 0 under R2.
  */
 #include <math.h>
 #include <stdint.h>
@@ -305,6 +308,9 @@ int64_t orc_compute_slot_mapping_cp(const int32_t *block_table, int32_t num_reqs
  * same bytes as the manager view: kernel block m*bpk + t holds tokens
  * [t*kbs, (t+1)*kbs) of manager block m.
  *
+ * R17: a kernel id m*bpk + t that does not fit in the int32 table names
+ * no block; it is written as -1, like an id <= 0 (R2).
+ *
  * Returns 0, or 1 for invalid arguments.  Columns of the output past
  * mgr_cols * bpk are left as they were.
  */
@@ -325,6 +331,8 @@ int orc_map_to_kernel_blocks(const int32_t *mgr_table, int32_t rows,
             int64_t m = mgr_table[(int64_t)r * mgr_stride + j];
             for (int64_t t = 0; t < bpk; ++t) {
                 int64_t out = (m > 0) ? m * bpk + t : -1;
+                if (out > INT32_MAX)
+                    out = -1;
                 kernel_table[(int64_t)r * kernel_stride + j * bpk + t] = (int32_t)out;
             }
         }

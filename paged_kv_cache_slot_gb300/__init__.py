@@ -4,4 +4,4 @@
 expansion, KV cache scatter, GQA paged decode); ``workloads`` draws the seeded
 synthetic inputs; ``build`` compiles the CUDA sources for sm_103a.
 """
-__version__ = "0.1.0"
+__version__ = "0.3.0"

@@ -83,9 +83,14 @@ def load() -> ctypes.CDLL:
         lib.bkv_paged_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         dec = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i32, i64, f32, cint, i32, cint, vp, vp, sz,
                vp, vp]
-        for fn in ("bkv_paged_decode", "bkv_paged_decode_partition", "bkv_paged_decode_merge"):
+        for fn in ("bkv_paged_decode_swa", "bkv_paged_decode_partition", "bkv_paged_decode_merge"):
             getattr(lib, fn).restype = cint
             getattr(lib, fn).argtypes = dec
+        # the boundary's own form: no sliding_window argument
+        lib.bkv_paged_decode.restype = cint
+        lib.bkv_paged_decode.argtypes = dec[:17] + dec[18:]
+        lib.bkv_paged_decode_noalloc.restype = cint
+        lib.bkv_paged_decode_noalloc.argtypes = dec[:17] + [cint, vp, vp, vp]
         lib.bkv_cache_write_fp8.restype = cint
         lib.bkv_cache_write_fp8.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i32, i32, i32, cint, f32, f32, vp, vp]
         dec8 = [vp, vp, vp, vp, i64, i32, vp, i32, i32, i32, i32, i32, i32, i32, i64, f32, f32, f32, cint, i32, cint,
@@ -273,10 +278,26 @@ def bkv_paged_decode_workspace_size(num_reqs, q_len, num_q_heads, num_kv_heads, 
 
 
 def bkv_paged_decode(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
-                     softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None, sliding_window=0):
+                     softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None):
     """GQA paged decode attention into ``out`` (num_reqs, q_len, H_q, D) (see include/bkv.h)."""
     return _decode("bkv_paged_decode", q, k_cache, v_cache, block_table, context_lens, max_context_len, out,
+                   workspace, softmax_scale, mask_mode, None, err_count, stream)
+
+
+def bkv_paged_decode_swa(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
+                         sliding_window, softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None):
+    """bkv_paged_decode of a sliding-window layer: query t sees the last ``sliding_window`` positions up to its
+    own (0: full attention) (see include/bkv.h)."""
+    return _decode("bkv_paged_decode_swa", q, k_cache, v_cache, block_table, context_lens, max_context_len, out,
                    workspace, softmax_scale, mask_mode, sliding_window, err_count, stream)
+
+
+def bkv_paged_decode_noalloc(q, k_cache, v_cache, block_table, context_lens, max_context_len, out,
+                             softmax_scale=0.0, mask_mode=BKV_MASK_CAUSAL, err_count=None, stream=None):
+    """bkv_paged_decode with its scratch in the library's fixed device array instead of a workspace (see
+    include/bkv.h)."""
+    return _decode("bkv_paged_decode_noalloc", q, k_cache, v_cache, block_table, context_lens, max_context_len, out,
+                   False, softmax_scale, mask_mode, None, err_count, stream)
 
 
 def bkv_paged_decode_partition(q, k_cache, v_cache, block_table, context_lens, max_context_len, out, workspace,
@@ -310,17 +331,20 @@ def _decode(fn, q, k_cache, v_cache, block_table, context_lens, max_context_len,
     for t, nm, want in ((k_cache, "k_cache", cache_dtype), (v_cache, "v_cache", cache_dtype), (out, "out", q.dtype)):
         if t.dtype != want:
             raise TypeError(f"{nm} must be {want}, got {t.dtype}")
-    if workspace is not None and workspace.dtype != torch.uint8:
+    # workspace: a uint8 tensor, None (a null pointer), or False (the entry point takes none)
+    if workspace is not None and workspace is not False and workspace.dtype != torch.uint8:
         raise TypeError("workspace must be a uint8 tensor")
-    ws_ptr = None if workspace is None else _dev(workspace, "workspace")
-    ws_bytes = 0 if workspace is None else workspace.numel()
+    ws = ()
+    if workspace is not False:
+        ws = (None, 0) if workspace is None else (_dev(workspace, "workspace"), workspace.numel())
+    window = () if sliding_window is None else (int(sliding_window),)
     _check(fn, getattr(load(), fn)(
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_table, "block_table", torch.int32, contiguous=False), block_table.stride(0),
         block_table.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), nr, ql, hq, hkv,
         d, bs, tb, float(softmax_scale), *(() if scales is None else (float(scales[0]), float(scales[1]))),
-        int(mask_mode), int(sliding_window), dt, _dev(out, "out"), ws_ptr, ws_bytes,
-        _opt(err_count, "err_count", torch.int32), _stream(stream)))
+        int(mask_mode), *window, dt, _dev(out, "out"), *ws, _opt(err_count, "err_count", torch.int32),
+        _stream(stream)))
     return out
 
 

@@ -40,4 +40,4 @@ extern "C" const char *bkv_status_string(int status) {
 
 extern "C" const char *bkv_last_cuda_error(void) { return bkv::g_last_error; }
 
-extern "C" const char *bkv_version(void) { return "bkv 0.2.0 sm_103a"; }
+extern "C" const char *bkv_version(void) { return "bkv 0.3.0 sm_103a"; }

@@ -120,21 +120,23 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
     }
 
     const int32_t j0 = max(start, jmin);   // a window implies cp_world == 1: local = global
+    // Bad entries among the blocks this partition needs (past the table width,
+    // or an id past the cache): counted once per (request, KV head) by the
+    // first query-row group.  Partitions hold whole blocks, so no block is
+    // counted twice; every needed block counts, whichever query sees it.
+    if (a.err && blockIdx.y == 0 && j0 < end) {
+        for (int32_t lb = j0 / a.bs + threadIdx.x; lb <= (end - 1) / a.bs; lb += blockDim.x) {
+            const bool bad = lb >= a.bt_cols || __ldg(a.bt + (int64_t)r * a.bt_stride + lb) >= a.total_blocks;
+            if (bad) atomicAdd(a.err, 1);
+        }
+    }
     for (int32_t j = j0 + warp; j < end && cp_global(a, j) <= jmax; j += NW) {
         const int64_t gj = cp_global(a, j);
         const int32_t lb = j / a.bs;
         const int32_t off = j - lb * a.bs;
-        const bool first = (j == j0) || (off == 0);  // count a bad entry once per CTA
-        if (lb >= a.bt_cols) {
-            if (first && lane == 0 && a.err) atomicAdd(a.err, 1);
-            continue;
-        }
+        if (lb >= a.bt_cols) continue;
         const int64_t b = __ldg(a.bt + (int64_t)r * a.bt_stride + lb);
-        if (b <= 0) continue;  // null block or sentinel: masked, never read
-        if (b >= a.total_blocks) {
-            if (first && lane == 0 && a.err) atomicAdd(a.err, 1);
-            continue;
-        }
+        if (b <= 0 || b >= a.total_blocks) continue;  // null, sentinel or bad: masked, never read
         const int64_t rowoff = ((b * a.bs + off) * a.H_kv + g) * a.D;
         float kv[DPL];
 #pragma unroll
@@ -575,13 +577,26 @@ static int decode_merge(DecodeCall &c, cudaStream_t st) {
                       mask_mode, dtype, sliding_window, 1, 0, 1, out, nullptr, workspace, workspace_bytes,      \
                       err_count, &(c))
 
-extern "C" int bkv_paged_decode(BKV_DECODE_PARAMS) {
+extern "C" int bkv_paged_decode_swa(BKV_DECODE_PARAMS) {
     bkv::DecodeCall c;
     int rc = BKV_DECODE_SETUP(c);
     if (rc != BKV_OK) return rc;
     rc = bkv::decode_partition(c, (cudaStream_t)stream);
     if (rc != BKV_OK) return rc;
     return bkv::decode_merge(c, (cudaStream_t)stream);
+}
+
+// The full-attention decode: bkv_paged_decode_swa without a window.
+extern "C" int bkv_paged_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                                int64_t bt_stride, int32_t bt_cols, const int32_t *context_lens,
+                                int32_t max_context_len, int32_t num_reqs, int32_t q_len, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t total_blocks,
+                                float softmax_scale, int mask_mode, int dtype, void *out, void *workspace,
+                                size_t workspace_bytes, int32_t *err_count, bkv_stream_t stream) {
+    return bkv_paged_decode_swa(q, k_cache, v_cache, block_table, bt_stride, bt_cols, context_lens, max_context_len,
+                                num_reqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, total_blocks,
+                                softmax_scale, mask_mode, 0, dtype, out, workspace, workspace_bytes, err_count,
+                                stream);
 }
 
 extern "C" int bkv_paged_decode_partition(BKV_DECODE_PARAMS) {

@@ -667,7 +667,10 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                         const int32_t lb = p0 / a.bs;
                         const int64_t e = ents[lb - lb_first];
                         if (e == INT32_MIN || e >= a.total_blocks) {
-                            if (!is_v && a.err) atomicAdd(a.err, 1);
+                            // a bad entry counts once per stream, at the first segment of
+                            // its block that is read: the block's first segment, or the
+                            // one holding the window's first key
+                            if (!is_v && a.err && (p0 - lb * a.bs < seg_rows || p0 <= wlo)) atomicAdd(a.err, 1);
                         } else if (e > 0) {
                             load = true;
                             row0 = e * a.bs + (p0 - (int64_t)lb * a.bs);

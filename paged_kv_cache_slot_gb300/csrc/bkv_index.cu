@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(256) slot_mapping_kernel(
     }
 }
 
-// Manager block m -> kernel blocks m * bpk + t ("ブロック表" 設計動機).
+// Manager block m -> kernel blocks m * bpk + t ("ブロック表" 設計動機); an id
+// the int32 table cannot hold (m * bpk + t > INT32_MAX) names no block: -1.
 __global__ void __launch_bounds__(256) kernel_blocks_kernel(
     const int32_t *__restrict__ mgr, int32_t rows, int64_t mgr_stride, int32_t mgr_cols, int32_t bpk,
     int32_t *__restrict__ out, int64_t out_stride) {
@@ -50,7 +51,8 @@ __global__ void __launch_bounds__(256) kernel_blocks_kernel(
         const int64_t j = c / bpk;
         const int64_t t = c - j * bpk;
         const int64_t m = __ldg(mgr + r * mgr_stride + j);
-        out[r * out_stride + c] = (m > 0) ? (int32_t)(m * bpk + t) : -1;
+        const int64_t id = m * bpk + t;
+        out[r * out_stride + c] = (m > 0 && id <= INT32_MAX) ? (int32_t)id : -1;
     }
 }
 

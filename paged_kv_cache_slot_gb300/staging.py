@@ -33,8 +33,14 @@ def _t(a: np.ndarray, device, dtype=None):
 class DeviceWorkload:
     def __init__(self, w: Workload, device="cuda", background: str = "nan", fill_prior: bool = True,
                  sliding_window: int = 0, cp_world: int = 1, cp_rank: int = 0, cp_interleave: int = 1,
-                 kv_fp8=None, fused_write: bool = True):
+                 kv_fp8=None, fused_write: bool = True, prior_values: str = "host"):
         self.w = w
+        # values of the prior tokens: "host" draws the workload's own (what the oracle sees); "device"
+        # draws N(0, 1) with the workload's scales on the GPU (seeded), for timing runs that compare
+        # nothing with the oracle and would otherwise spend their time generating values on the host
+        if prior_values not in ("host", "device"):
+            raise ValueError("prior_values must be 'host' or 'device'")
+        self.prior_values = prior_values
         # the step's slot mapping + cache write as one bkv_slot_mapping_cache_write(_fp8) call (without
         # context parallelism), else the two calls
         self.fused_write = bool(fused_write)
@@ -109,11 +115,18 @@ class DeviceWorkload:
     def _write_rows(self, rows):
         w, dev = self.w, self.device
         req, pos = w.prior_tokens(rows)
-        ks, vs = zip(*(w.kv_rows(r, 0, int(w.prior_lens[r])) for r in rows))
-        k = np.concatenate(ks)
-        v = np.concatenate(vs)
-        cast = self.tdtype if w.dtype == "bf16" else None
-        kt, vt = _t(k, dev, cast), _t(v, dev, cast)
+        if self.prior_values == "device":
+            g = torch.Generator(device=dev)
+            g.manual_seed(int(w.seed) * 1000003 + int(rows[0]))
+            shape = (len(pos), w.num_kv_heads, w.head_dim)
+            kt = (torch.randn(shape, generator=g, device=dev) * w.qk_scale).to(self.tdtype)
+            vt = (torch.randn(shape, generator=g, device=dev) * w.v_scale).to(self.tdtype)
+        else:
+            ks, vs = zip(*(w.kv_rows(r, 0, int(w.prior_lens[r])) for r in rows))
+            k = np.concatenate(ks)
+            v = np.concatenate(vs)
+            cast = self.tdtype if w.dtype == "bf16" else None
+            kt, vt = _t(k, dev, cast), _t(v, dev, cast)
         slots = torch.empty(len(pos), dtype=torch.int64, device=dev)
         self._slots(self.kernel_table, _t(req, dev), _t(pos, dev), slots)
         self._write(kt, vt, slots)
@@ -173,9 +186,13 @@ class DeviceWorkload:
                                      self.max_context_len, out, self.workspace, *self.fp8, mask_mode=mask_mode,
                                      err_count=self.err_count, stream=stream, sliding_window=sliding_window)
             return out
-        bkv.bkv_paged_decode(self.q, self.k_cache, self.v_cache, table, self.context_lens, self.max_context_len,
-                             out, self.workspace, mask_mode=mask_mode, err_count=self.err_count, stream=stream,
-                             sliding_window=sliding_window)
+        if sliding_window:
+            bkv.bkv_paged_decode_swa(self.q, self.k_cache, self.v_cache, table, self.context_lens,
+                                     self.max_context_len, out, self.workspace, sliding_window, mask_mode=mask_mode,
+                                     err_count=self.err_count, stream=stream)
+        else:
+            bkv.bkv_paged_decode(self.q, self.k_cache, self.v_cache, table, self.context_lens, self.max_context_len,
+                                 out, self.workspace, mask_mode=mask_mode, err_count=self.err_count, stream=stream)
         return out
 
     def decode_partition(self, stream=None):

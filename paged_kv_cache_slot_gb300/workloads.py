@@ -31,8 +31,13 @@ never handed out, as the pages' block pool reserves it); the pool holds the
 needed blocks plus 25% slack.  Unused table entries are -1.  K, V and Q are
 N(0, 1) scaled by 1/sqrt(head_dim) for the bf16 workloads (unscaled for
 ``tiny``); ``sharp=True`` leaves Q and K unscaled so attention weights are far
-from uniform.  K/V rows of request r are drawn in chunks of 1024 positions
-from ``default_rng([seed, 7, r, chunk])`` so that any position range can be
+from uniform; ``loud=True`` draws Q and K with variance 2 (scores of standard
+deviation 2 at the 1/sqrt(head_dim) softmax scale, so a few dozen to a few
+hundred keys, spread over the whole context, carry most of the weight) and V
+unscaled, so that outputs are O(0.1 .. 1) and an absolute error bar of 1e-2
+separates a right answer from a wrong one at every context length.  K/V rows
+of request r are drawn in chunks of 1024 positions from
+``default_rng([seed, 7, r, chunk])`` so that any position range can be
 regenerated on its own.
 """
 from __future__ import annotations
@@ -244,10 +249,17 @@ def _ceil_div(a, b):
     return -(-np.asarray(a, dtype=np.int64) // b)
 
 
-def make(name: str, *, sharp: bool = False, tiny_reading: str = "record") -> Workload:
-    """Draw workload ``name`` with its fixed seed."""
+def _qk(s: float, sharp: bool, loud: bool) -> float:
+    """Scale of the drawn Q and K values: s (the recipe), 1 (sharp) or sqrt(2) (loud)."""
+    return math.sqrt(2.0) if loud else (1.0 if sharp else s)
+
+
+def make(name: str, *, sharp: bool = False, loud: bool = False, tiny_reading: str = "record") -> Workload:
+    """Draw workload ``name`` with its fixed seed (``sharp`` / ``loud``: the test variants above)."""
     if name not in WORKLOADS:
         raise KeyError(name)
+    if sharp and loud:
+        raise ValueError("sharp and loud are different variants")
     seed = SEEDS[name]
     rng = np.random.default_rng(seed)
 
@@ -276,7 +288,7 @@ def make(name: str, *, sharp: bool = False, tiny_reading: str = "record") -> Wor
         table, total = _assign_blocks(rng, _ceil_div(prior + new, bs), width)
         s = 1.0 / math.sqrt(d)
         return Workload(name, seed, "bf16", nr, nr, 1, 32, 8, d, bs, bs, prior, new, table, total,
-                        max_num_tokens=nr, qk_scale=1.0 if sharp else s, v_scale=s)
+                        max_num_tokens=nr, qk_scale=_qk(s, sharp, loud), v_scale=1.0 if loud else s)
 
     if name == "ragged_step":
         nr, bs, d = 64, 16, 128
@@ -290,7 +302,8 @@ def make(name: str, *, sharp: bool = False, tiny_reading: str = "record") -> Wor
         max_tokens = int(_ceil_div(n, 1024) * 1024)  # slot buffer sized for reuse, tail padded
         s = 1.0 / math.sqrt(d)
         return Workload(name, seed, "bf16", nr, nr, 0, 32, 8, d, bs, bs, prior, new, table, total,
-                        max_num_tokens=max_tokens, qk_scale=s, v_scale=s, has_decode=False)
+                        max_num_tokens=max_tokens, qk_scale=_qk(s, sharp, loud), v_scale=1.0 if loud else s,
+                        has_decode=False)
 
     if name == "long_context":
         nr, bs, d, max_model_len = 8, 64, 128, 131072
@@ -301,7 +314,7 @@ def make(name: str, *, sharp: bool = False, tiny_reading: str = "record") -> Wor
         table, total = _assign_blocks(rng, _ceil_div(prior + new, bs), width)
         s = 1.0 / math.sqrt(d)
         return Workload(name, seed, "bf16", nr, nr, 1, 64, 8, d, bs, bs, prior, new, table, total,
-                        max_num_tokens=nr, qk_scale=1.0 if sharp else s, v_scale=s,
+                        max_num_tokens=nr, qk_scale=_qk(s, sharp, loud), v_scale=1.0 if loud else s,
                         extra={"max_model_len": max_model_len, "buckets": [4096, 8192, 16384]})
 
     # hybrid_spec
@@ -315,4 +328,4 @@ def make(name: str, *, sharp: bool = False, tiny_reading: str = "record") -> Wor
     table, total = _assign_blocks(rng, _ceil_div(prior + new, mbs), width)
     s = 1.0 / math.sqrt(d)
     return Workload(name, seed, "bf16", nr, real, q_len, 32, 8, d, mbs, kbs, prior, new, table, total,
-                    max_num_tokens=nr * q_len, qk_scale=1.0 if sharp else s, v_scale=s)
+                    max_num_tokens=nr * q_len, qk_scale=_qk(s, sharp, loud), v_scale=1.0 if loud else s)

@@ -47,9 +47,18 @@ int main(void) {
 
     /* the decode rejects a too-small workspace before enqueuing anything */
     check(bkv_paged_decode((void *)16, (void *)16, (void *)16, (const int32_t *)16, 4, 4, (const int32_t *)16, 100,
-                           2, 1, 8, 2, 128, 16, 10, 0.f, BKV_MASK_CAUSAL, 0, BKV_BF16, (void *)16, (void *)16, 16,
+                           2, 1, 8, 2, 128, 16, 10, 0.f, BKV_MASK_CAUSAL, BKV_BF16, (void *)16, (void *)16, 16,
                            NULL, NULL) == BKV_ERR_INVALID_ARG,
           "decode rejects a workspace that is too small");
+    check(bkv_paged_decode((void *)16, (void *)16, (void *)16, (const int32_t *)16, 4, 4, (const int32_t *)16, 100,
+                           2, 1, 8, 2, 128, 16, 10, 0.f, BKV_MASK_CAUSAL, 7, (void *)16, (void *)16, 1 << 20,
+                           NULL, NULL) == BKV_ERR_UNSUPPORTED,
+          "decode rejects an unknown dtype");
+    /* the sliding-window form: a negative window is invalid */
+    check(bkv_paged_decode_swa((void *)16, (void *)16, (void *)16, (const int32_t *)16, 4, 4, (const int32_t *)16,
+                               100, 2, 1, 8, 2, 128, 16, 10, 0.f, BKV_MASK_CAUSAL, -1, BKV_BF16, (void *)16,
+                               (void *)16, 1 << 20, NULL, NULL) == BKV_ERR_INVALID_ARG,
+          "windowed decode rejects a negative window");
 
     if (failures) return 1;
     printf("ok\n");

@@ -47,6 +47,11 @@ def test_status_strings(lib):
     assert lib.bkv_version().startswith(b"bkv ")
 
 
+def test_package_version_is_the_library_version(lib):
+    import paged_kv_cache_slot_gb300 as pkg
+    assert lib.bkv_version().split()[1].decode() == pkg.__version__
+
+
 NULL = None
 
 
@@ -118,11 +123,16 @@ def test_fused_slot_write_fp8_rejects_bad_arguments(lib):
     assert call(n=0, mx=0) == bkv.BKV_OK
 
 
-def test_paged_decode_rejects_bad_arguments(lib):
-    f = lib.bkv_paged_decode
+@pytest.mark.parametrize("fn", ["bkv_paged_decode", "bkv_paged_decode_swa", "bkv_paged_decode_partition",
+                                "bkv_paged_decode_merge"])
+def test_paged_decode_rejects_bad_arguments(lib, fn):
+    f = getattr(lib, fn)
+    windowed = fn != "bkv_paged_decode"      # the survey's signature has no window argument
     base = dict(q=NULL, k=NULL, v=NULL, bt=NULL, bt_stride=4, bt_cols=4, ctx=NULL, max_ctx=16, num_reqs=2, q_len=1,
                 hq=32, hkv=8, d=128, bs=16, tb=8, scale=0.0, mask=0, window=0, dtype=0, out=NULL, ws=NULL, wsb=0,
                 err=NULL, stream=NULL)
+    if not windowed:
+        del base["window"]
 
     def call(**kw):
         a = dict(base, **kw)
@@ -131,11 +141,24 @@ def test_paged_decode_rejects_bad_arguments(lib):
     assert call(dtype=5) == bkv.BKV_ERR_UNSUPPORTED
     assert call(d=512) == bkv.BKV_ERR_UNSUPPORTED
     assert call(mask=2) == bkv.BKV_ERR_INVALID_ARG
-    assert call(window=-1) == bkv.BKV_ERR_INVALID_ARG
+    if windowed:
+        assert call(window=-1) == bkv.BKV_ERR_INVALID_ARG
     assert call(bt_stride=2) == bkv.BKV_ERR_INVALID_ARG
     assert call(hq=30) == bkv.BKV_ERR_INVALID_ARG          # 30 % 8 != 0
     assert call(num_reqs=0) == bkv.BKV_ERR_INVALID_ARG
     assert call() == bkv.BKV_ERR_INVALID_ARG                # null pointers / no workspace
+
+
+def test_paged_decode_has_the_survey_signature():
+    """bkv_paged_decode is declared with exactly the argument list of the boundary's statement (no
+    window: the sliding-window form is bkv_paged_decode_swa)."""
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "bkv.h")).read(), flags=re.S)
+    decl = re.search(r"int bkv_paged_decode\((.*?)\);", text, flags=re.S).group(1)
+    names = [a.strip().split()[-1].lstrip("*") for a in decl.split(",")]
+    assert names == ["q", "k_cache", "v_cache", "block_table", "bt_stride", "bt_cols", "context_lens",
+                     "max_context_len", "num_reqs", "q_len", "num_q_heads", "num_kv_heads", "head_dim",
+                     "block_size", "total_blocks", "softmax_scale", "mask_mode", "dtype", "out", "workspace",
+                     "workspace_bytes", "err_count", "stream"]
 
 
 def test_workspace_size_is_zero_for_invalid_sizes(lib):

@@ -38,8 +38,7 @@ def test_clock_summary_without_samples(tmp_path):
 
 
 def test_profiled_traffic_follows_the_decode_sources(tmp_path, monkeypatch):
-    # the committed summary carries the hash of the current decode sources
-    assert bench._profiled_traffic() is not None
+    # the traffic is reported only while the summary carries the hash of the current decode sources
     fake = tmp_path / "profile.txt"
     fake.write_text("decode_source_sha256: 0000000000000000\ntraffic_bytes_per_launch: 123\n")
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(fake))
@@ -56,3 +55,28 @@ def test_peaks_come_from_the_measured_file_when_present():
         assert kind == "measured" and peak > 1000
     else:
         assert kind == "fallback"
+
+
+def test_bucket_report_follows_the_oracle_and_the_page_formula():
+    """config4_bytes: needed_seq and the bucket as the oracle's decode_bucket gives them ("Decode
+    Context-Length Bucketing", Design / Per-step bucket selection), bytes at token granularity."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_slot_gb300 import workloads as wl
+
+    w = wl.make("long_context")
+    rep = bench.bucket_report(w)
+    mml = w.extra["max_model_len"]
+    want = oracle.decode_bucket(w.prior_lens, w.q_len - 1, w.extra["buckets"], mml)
+    assert rep["bucket"] == want
+    assert rep["needed_seq"] == int(w.prior_lens.max()) + 1 + (w.q_len - 1)
+    per_tok = 2 * w.num_kv_heads * w.head_dim * 2
+    assert rep["kv_bytes_read"] == int(w.context_lens.astype(np.int64).sum()) * per_tok
+    assert rep["full_row_bytes"] == 8 * 131072 * 4096
+    assert rep["bucketed_bytes"] == 8 * want * 4096
+    # a batch whose longest request needs more than the largest bucket falls back to max_model_len
+    w.prior_lens = np.array([100, 20000, 5, 7, 9, 11, 13, 15], np.int64)
+    rep = bench.bucket_report(w)
+    assert rep["bucket"] == oracle.decode_bucket(w.prior_lens, 0, w.extra["buckets"], mml) == mml
+    assert rep["full_row_over_read"] > rep["bucketed_over_read"] - 1e-12

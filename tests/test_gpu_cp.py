@@ -4,8 +4,9 @@ decode (out, lse) over caches written through the library's own CP slot
 mapping and cache write matches the oracle's rank; and the ranks merged by
 bkv_merge_attn_states match the UNSPLIT oracle attention.
 
-Tolerances: out as the decode (1e-2 bf16, 1e-5 fp32, max abs); lse (natural
-log) 4e-3 for bf16 (the kernel sums bf16-rounded weights, relative error up
+Tolerances: out as the decode (tests/_parity.py: per output row, max abs
+error <= 1e-2 of the row's largest oracle value for bf16, 1e-5 of it for
+fp32; rows that see nothing exactly 0); lse (natural log) 4e-3 for bf16 (the kernel sums bf16-rounded weights, relative error up
 to 2^-9 per weight) and 1e-5 for fp32.
 """
 import numpy as np
@@ -13,13 +14,13 @@ import pytest
 import torch
 
 import oracle
+from _parity import check_attention
 from oracle.cases import fill_oracle_cache, fill_oracle_cache_cp
 from paged_kv_cache_slot_gb300 import bkv
 from paged_kv_cache_slot_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"bf16": 1e-2, "f32": 1e-5}
 LSE_TOL = {"bf16": 4e-3, "f32": 1e-5}
 
 
@@ -136,8 +137,7 @@ def test_cp_ranks_match_oracle_and_merge_to_unsplit(case, world, inter):
                                                    world, rank, inter)
         got = out.float().cpu().numpy().astype(np.float64)
         gl = lse.cpu().numpy().astype(np.float64)
-        assert np.isfinite(got).all()
-        assert np.abs(got - want).max() <= TOL[dtype]
+        check_attention(got, want, dtype, f"rank {rank} of {world}")
         fin = np.isfinite(want_lse)
         assert (np.isfinite(gl) == fin).all()
         if fin.any():
@@ -152,7 +152,7 @@ def test_cp_ranks_match_oracle_and_merge_to_unsplit(case, world, inter):
     kc0, vc0, t0 = fill_oracle_cache(w)
     want, want_lse, _ = oracle.paged_decode_cp(q, kc0, vc0, t0, w.context_lens)
     got = merged.float().cpu().numpy().astype(np.float64)
-    assert np.abs(got - want).max() <= TOL[dtype]
+    check_attention(got, want, dtype, f"merged {world} ranks")
     assert (got[w.num_rows - 1] == 0).all()                  # the NULL row
     fin = np.isfinite(want_lse)
     gl = mlse.cpu().numpy().astype(np.float64)
@@ -193,7 +193,7 @@ def test_merge_attn_states_matches_oracle(dtype):
     bkv.bkv_merge_attn_states(o, torch.from_numpy(lses).cuda(), out, lse)
     torch.cuda.synchronize()
     got = out.float().cpu().numpy().astype(np.float64)
-    assert np.abs(got - want).max() <= TOL[dtype] * (1 if dtype == "f32" else 4)
+    check_attention(got, want, dtype, "merge")               # outputs up to ~4: the bar scales with them
     fin = np.isfinite(want_lse)
     gl = lse.cpu().numpy().astype(np.float64)
     assert np.abs(gl[fin] - want_lse[fin]).max() <= 1e-5

@@ -5,8 +5,10 @@ scale with ties to even and saturation at 448, value = code value * scale).
 * bkv_cache_write_fp8: every byte of both caches equals the oracle's, for
   bf16 and fp32 sources, 16-byte and element paths, a strided source,
   padding (-1) and out-of-range slots, NaN, saturating and subnormal inputs.
-* bkv_paged_decode_fp8: max abs error <= 1e-2 (bf16 q / out) or 1e-5 (fp32)
-  against the oracle on caches written by the library; unwritten cache bytes
+* bkv_paged_decode_fp8: per output row, max abs error <= 1e-2 (bf16 q / out)
+  or 1e-5 (fp32) of the row's largest oracle value (tests/_parity.py; at
+  least as tight as the absolute 1e-2 / 1e-5 for outputs up to 1), against
+  the oracle on caches written by the library; unwritten cache bytes
   hold the NaN code 0x7F, so any read of them poisons the output; both mask
   modes, sliding windows, null entries inside a range, NULL rows; partition
   + merge equals the one call bit for bit.
@@ -16,6 +18,7 @@ import pytest
 import torch
 
 import oracle
+from _parity import check_attention
 from oracle.cases import fill_oracle_cache_fp8
 from paged_kv_cache_slot_gb300 import bkv
 from paged_kv_cache_slot_gb300 import workloads as wl
@@ -23,7 +26,6 @@ from paged_kv_cache_slot_gb300.staging import DeviceWorkload
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"bf16": 1e-2, "f32": 1e-5}
 K_SCALE = 2.0 ** -9
 V_SCALE = 1e-3
 NAN8 = 0x7F
@@ -188,11 +190,7 @@ def _decode_check(w, mask_mode=0, window=0, scales=(K_SCALE, V_SCALE), label="")
     want, err = oracle.paged_decode_fp8(w.q(), kc, vc, table, w.context_lens, *scales, mask_mode=mask_mode,
                                         sliding_window=window)
     assert err == 0
-    worst = 0.0
-    for r in range(w.num_rows):
-        assert np.isfinite(got[r]).all(), f"{label} row {r}: non-finite"
-        worst = max(worst, float(np.abs(got[r] - want[r]).max()))
-    assert worst <= TOL[w.dtype], f"{label}: max abs err {worst:.3e}"
+    check_attention(got, want, w.dtype, label)
     return dw, got
 
 
@@ -242,15 +240,20 @@ def test_decode_fp8_partition_then_merge_equals_one_call():
     assert torch.equal(out2.view(torch.uint16), dw.out.view(torch.uint16))
 
 
-def test_decode_fp8_llama_shape_sampled_rows():
-    w = wl.make("llama3_decode")
-    rows = [int(np.argmin(w.context_lens)), int(np.argmax(w.context_lens)), 7]
-    dw = DeviceWorkload(w, kv_fp8=(K_SCALE, V_SCALE))
+@pytest.mark.parametrize("variant", ["literal", "loud"])
+def test_decode_fp8_llama_shape_all_rows(variant):
+    """Every request of the Llama-shaped batch: the literal draw (scales as the benchmark's) and the loud one
+    (K, V values up to ~7: scales 1/32, a few codes saturate), where outputs are O(0.1 .. 1)."""
+    loud = variant == "loud"
+    w = wl.make("llama3_decode", loud=loud)
+    scales = (1.0 / 32, 1.0 / 32) if loud else (K_SCALE, V_SCALE)
+    dw = DeviceWorkload(w, kv_fp8=scales)
     dw.write_step()
+    dw.workspace.fill_(0xFF)
     got = _f64(dw.decode())
     torch.cuda.synchronize()
     assert int(dw.err_count.item()) == 0
-    kc, vc, table = fill_oracle_cache_fp8(w, K_SCALE, V_SCALE, rows=rows)
-    want, _ = oracle.paged_decode_fp8(w.q(), kc, vc, table, w.context_lens, K_SCALE, V_SCALE, rows=rows)
-    for r in rows:
-        assert np.abs(got[r] - want[r]).max() <= TOL["bf16"], f"row {r}"
+    kc, vc, table = fill_oracle_cache_fp8(w, *scales)
+    want, err = oracle.paged_decode_fp8(w.q(), kc, vc, table, w.context_lens, *scales)
+    assert err == 0
+    check_attention(got, want, "bf16", f"fp8 llama/{variant}", min_magnitude=0.1 if loud else None)

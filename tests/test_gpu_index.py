@@ -103,6 +103,16 @@ def test_block_expansion_bit_exact(bs, kbs):
     assert (got[:, cols * bpk:] == 12345).all()
 
 
+@pytest.mark.parametrize("bpk", [2, 3, 16])
+def test_block_expansion_at_the_int32_edge_bit_exact(bpk):
+    top = (2**31 - 1 - (bpk - 1)) // bpk
+    mgr = np.array([[top, top + 1, 2**31 - 1, 7, -1, 0], [1, top - 1, top, top + 1, 2**31 - 2, 5]], np.int32)
+    want = oracle.map_to_kernel_blocks(mgr, 16 * bpk, 16)
+    kt = torch.full(want.shape, 12345, dtype=torch.int32, device=DEV)
+    bkv.bkv_map_to_kernel_blocks(_d(mgr), 16 * bpk, 16, kt)
+    assert np.array_equal(kt.cpu().numpy(), want)
+
+
 def test_block_expansion_hybrid_workload_and_error():
     w = wl.make("hybrid_spec")
     want = oracle.map_to_kernel_blocks(w.block_table, w.block_size, w.kernel_block_size)

@@ -142,6 +142,23 @@ def test_kernel_block_expansion_preserves_slots(bs, kbs):
     assert ((kt == -1) == np.repeat(mgr <= 0, bs // kbs, axis=1)).all()
 
 
+@pytest.mark.parametrize("bpk", [2, 3, 16])
+def test_kernel_block_expansion_at_the_int32_edge(bpk):
+    """R17: the table holds int32 ids, so an expanded id above 2^31 - 1 names no block (-1); the largest
+    manager id whose every kernel id fits expands normally (closed form m * bpk + t)."""
+    top = (2**31 - 1 - (bpk - 1)) // bpk          # largest m with m * bpk + bpk - 1 <= INT32_MAX
+    mgr = np.array([[top, top + 1, 2**31 - 1, 7]], np.int32)
+    kt = oracle.map_to_kernel_blocks(mgr, 16 * bpk, 16)
+    t = np.arange(bpk)
+    assert kt[0, :bpk].tolist() == (top * bpk + t).tolist()
+    assert max(kt[0, :bpk]) <= 2**31 - 1
+    straddle = [(top + 1) * bpk + x for x in t]     # some (or all) of these exceed INT32_MAX
+    assert kt[0, bpk:2 * bpk].tolist() == [v if v <= 2**31 - 1 else -1 for v in straddle]
+    assert (kt[0, bpk:2 * bpk] == -1).any()
+    assert (kt[0, 2 * bpk:3 * bpk] == -1).all()
+    assert kt[0, 3 * bpk:].tolist() == (7 * bpk + t).tolist()
+
+
 def test_kernel_block_expansion_rejects_indivisible():
     with pytest.raises(ValueError):
         oracle.map_to_kernel_blocks(np.ones((1, 2), np.int32), 32, 12)
