@@ -389,13 +389,17 @@ def run_bkv(args):
     if dist:
         dist.barrier()
     bkv.load()
+    if args.decode_kernel == "generic":
+        # the CUDA-core partition kernel on every shape (a comparison switch the library never sets)
+        bkv.load().bkv_testing_force_generic_decode(1)
 
     w = wl.make(args.workload)
     cp = (args.cp_world, 0, args.cp_interleave)
     fp8 = FP8_SCALES if args.kv_dtype == "fp8" else None
     dw = DeviceWorkload(w, device=f"cuda:{local}", sliding_window=args.sliding_window, cp_world=cp[0],
                         cp_rank=cp[1], cp_interleave=cp[2], kv_fp8=fp8)
-    headline = args.workload == WORKLOAD and args.sliding_window == 0 and cp[0] == 1 and fp8 is None
+    headline = (args.workload == WORKLOAD and args.sliding_window == 0 and cp[0] == 1 and fp8 is None
+                and args.decode_kernel == "auto")
     stream = torch.cuda.Stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=f"cuda:{local}")
@@ -591,7 +595,8 @@ def run_bkv(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic() if headline else None,
                      "kernel": ("decode partition kernel (bkv_paged_decode_partition, CUDA events around it)"
-                                if cp[0] == 1 else "context-parallel rank's decode call (partition + merge)"),
+                                if cp[0] == 1 else "context-parallel rank's decode call (partition + merge)")
+                               + (": the CUDA-core kernel, forced" if args.decode_kernel == "generic" else ""),
                      "decode_call_GBps": kv_bytes / (dms / 1e3) / 1e9,
                      "peak_kind": f"{peak_kind} copy bandwidth"},
         "decode_ms": dms,
@@ -869,6 +874,8 @@ def main():
     ap.add_argument("--cp-world", type=int, default=1,
                     help="time rank 0 of a decode-context-parallel split over this many ranks (1: none)")
     ap.add_argument("--cp-interleave", type=int, default=1, help="context-parallel interleave size")
+    ap.add_argument("--decode-kernel", default="auto", choices=["auto", "generic"],
+                    help="auto: the library's choice; generic: force the CUDA-core partition kernel (comparison)")
     ap.add_argument("--part", default="step", choices=["step", "write"],
                     help="step: the whole path (default); write: slot mapping + cache write of the ragged step alone")
     args = ap.parse_args()

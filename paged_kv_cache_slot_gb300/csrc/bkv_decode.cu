@@ -216,12 +216,15 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
 // ...: the lanes read the slots' (m, l) pairs in one round, turn them into
 // weights in the warp's own shared-memory strip, and then each lane sums
 // four head_dim elements over the slots with 16-byte loads.
+// The stream's slots follow from the context lengths alone (the stream-K
+// split of the tensor-core kernel), which the partition kernel does not
+// write: they are read and the slot range computed before the grid-
+// dependency wait, so that only the partials' loads follow it.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int max_slots) {
-    pdl_wait();
-    pdl_trigger();
     extern __shared__ float sw[];   // [4 warps][max_slots] weights
+    __shared__ int64_t red[2][4];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int64_t rg = blockIdx.x;            // stream: r * H_kv + g
@@ -231,15 +234,34 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
     // a stream's partial slots are contiguous
     int nch = 0;          // slots of this stream
     int64_t unit0 = 0;    // its first slot
-    if (a.sk_pre) {
-        // stream-K: stream s has Ts tiles starting at global tile S; CTA k of
-        // geff = min(sk_grid, TT) covers [k TT / geff, (k + 1) TT / geff) and
-        // writes slots 2 (k + s) and 2 (k + s) + 1 for its overlap with s
-        const int64_t Ts = a.sk_pre[r + 1] - a.sk_pre[r];   // tiles of the stream
-        const int64_t TT = (int64_t)a.H_kv * a.sk_pre[a.num_reqs];
+    if (a.stream_k) {
+        // tiles of all requests and of those before r, over the CTA
+        int64_t all = 0, before = 0;
+        for (int rr = threadIdx.x; rr < a.num_reqs; rr += blockDim.x) {
+            const int64_t t = sk_tiles(a, __ldg(a.ctx + rr));
+            all += t;
+            if (rr < r) before += t;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            all += __shfl_xor_sync(0xffffffffu, all, o);
+            before += __shfl_xor_sync(0xffffffffu, before, o);
+        }
+        if (lane == 0) {
+            red[0][warp] = all;
+            red[1][warp] = before;
+        }
+        __syncthreads();
+        all = red[0][0] + red[0][1] + red[0][2] + red[0][3];
+        before = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+        const int64_t Ts = sk_tiles(a, __ldg(a.ctx + r));   // tiles of the stream
+        const int64_t TT = (int64_t)a.H_kv * all;
         if (Ts > 0 && L > 0) {
-            const int64_t geff = TT < (int64_t)a.sk_grid ? TT : (int64_t)a.sk_grid;   // CTAs with tiles
-            const int64_t S = (int64_t)a.H_kv * a.sk_pre[r] + g * Ts;
+            // stream s has Ts tiles starting at global tile S; CTA k of geff =
+            // min(sk_grid, TT) covers [k TT / geff, (k + 1) TT / geff) and writes
+            // slots 2 (k + s) and 2 (k + s) + 1 for its overlap with s
+            const int64_t geff = TT < (int64_t)a.sk_grid ? TT : (int64_t)a.sk_grid;
+            const int64_t S = (int64_t)a.H_kv * before + g * Ts;
             const int64_t k0 = ((S + 1) * geff - 1) / TT;
             const int64_t k1 = ((S + Ts) * geff - 1) / TT;
             nch = (int)(2 * (k1 - k0 + 1));
@@ -249,6 +271,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
         nch = L > 0 ? (int)ceil_div<int32_t>(L, a.chunk) * a.parts : 0;
         unit0 = rg * a.n_chunks * a.parts;
     }
+    pdl_wait();
+    pdl_trigger();
     float *wts = sw + (size_t)warp * max_slots;
     for (int row = warp; row < a.nq; row += 4) {
         const int t = row / a.G;
@@ -396,7 +420,7 @@ bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int3
     plan->n_chunks = (int32_t)n_chunks;
     plan->nq = (int32_t)nq;
     plan->sk_grid = (int32_t)sms;
-    plan->header_bytes = (size_t)ceil_div<int64_t>(((int64_t)num_reqs + 1) * 4, 256) * 256;
+    plan->header_bytes = 256;
     const int64_t slots_generic = units * n_chunks;
     const int64_t slots_sk = 2 * (sms + units);
     const int64_t slots = slots_generic > slots_sk ? slots_generic : slots_sk;
@@ -438,6 +462,18 @@ extern "C" size_t bkv_paged_decode_workspace_size(int32_t num_reqs, int32_t q_le
         return 0;
     return p.ws_bytes;
 }
+
+namespace bkv {
+
+// Not part of the ABI (bkv.h does not declare it): a process-wide switch that
+// makes every later decode call run the CUDA-core kernel, so that the
+// tensor-core kernel can be timed against it on the same shapes.  The library
+// itself never sets it.
+static volatile int g_force_generic = 0;
+
+}  // namespace bkv
+
+extern "C" void bkv_testing_force_generic_decode(int on) { bkv::g_force_generic = on ? 1 : 0; }
 
 namespace bkv {
 
@@ -519,13 +555,13 @@ static int decode_setup(const void *q, const void *k_cache, const void *v_cache,
     a.qexp = head_dim == 128 ? reinterpret_cast<float *>(a.q8 + (size_t)2 * num_reqs * q_len * num_q_heads * 128)
                              : nullptr;
     a.parts = 2;
-    a.sk_pre = static_cast<int32_t *>(workspace);
+    a.stream_k = 1;
     a.sk_grid = plan.sk_grid;
     set_slots(2 * (plan.sk_grid + units));
-    c->tc = prepare_decode_tc(a, &c->t);
+    c->tc = !g_force_generic && prepare_decode_tc(a, &c->t);
     if (!c->tc) {
         a.parts = 1;
-        a.sk_pre = nullptr;
+        a.stream_k = 0;
         set_slots(units * plan.n_chunks);
     }
     return BKV_OK;
@@ -552,7 +588,7 @@ static int decode_partition(DecodeCall &c, cudaStream_t st) {
 
 static int decode_merge(DecodeCall &c, cudaStream_t st) {
     const DecodeArgs &a = c.a;
-    const int max_slots = a.sk_pre ? 2 * c.plan.sk_grid : c.plan.n_chunks * a.parts;
+    const int max_slots = a.stream_k ? 2 * c.plan.sk_grid : c.plan.n_chunks * a.parts;
     const size_t msmem = 4 * (size_t)max_slots * 4;
     const dim3 mgrid((unsigned)((int64_t)a.num_reqs * a.H_kv));
     const cudaError_t e =

@@ -34,7 +34,7 @@ struct DecodeArgs {
     int32_t G;         // query heads per KV head
     int32_t nq;        // query rows per KV head: q_len * G, row i = t * G + (h % G)
     int32_t parts;     // partials per unit (slots): 1 for the generic kernel, 2 for the tensor-core one
-    int32_t *sk_pre;   // tensor-core kernel: [num_reqs + 1] tiles-per-request prefix (written by its CTA 0)
+    int32_t stream_k;  // 1: the tensor-core kernel's stream-K partial slots; 0: the generic kernel's
     int32_t sk_grid;   // tensor-core kernel: CTAs of the stream-K split
     float *ws_o;       // [slots][nq][D] unnormalised partial outputs
     float *ws_ml;      // [slots][nq][2]  (running max in base 2, sum of weights)
@@ -43,11 +43,10 @@ struct DecodeArgs {
 };
 
 // Split of each request's context into partitions; identical for the
-// workspace query and the decode call.  The workspace holds, in order, the
-// stream-K header ([num_reqs + 1] int32, 256-byte padded) and the partials
-// of whichever kernel runs: the generic kernel's (request, KV head,
-// partition) slots or the tensor-core kernel's 2 (sk_grid + num_reqs * H_kv)
-// stream-K slots.
+// workspace query and the decode call.  The workspace holds, in order, a
+// 256-byte header (unused, kept for alignment) and the partials of whichever
+// kernel runs: the generic kernel's (request, KV head, partition) slots or
+// the tensor-core kernel's 2 (sk_grid + num_reqs * H_kv) stream-K slots.
 // Decode context parallelism ("ブロック表" 設計動機, DCP interleave): with
 // world size W, rank k and interleave I, global position p belongs to rank
 // (p / I) % W and is its local key (p / (I W)) I + p % I.  cp_local_len is
@@ -82,6 +81,17 @@ __host__ __device__ inline int32_t window_lo(const DecodeArgs &a, int32_t L) {
     if (a.window <= 0) return 0;
     const int64_t lo = (int64_t)L - a.q_len - a.window + 1;
     return lo > 0 ? (int32_t)lo : 0;
+}
+
+// Tiles of a request in the tensor-core kernel's stream-K schedule: its
+// keys' 128-position tiles from the one holding the first visible key.  The
+// partition kernel lays all streams' tiles end to end in this count, and the
+// merge recomputes each stream's slots from it.
+constexpr int kDecodeTile = 128;
+__host__ __device__ inline int32_t sk_tiles(const DecodeArgs &a, int32_t ctx_len) {
+    const int32_t Lg = ctx_len > a.max_ctx ? a.max_ctx : (ctx_len < 0 ? 0 : ctx_len);
+    const int32_t L = cp_local_len(a, Lg);
+    return (L + kDecodeTile - 1) / kDecodeTile - window_lo(a, Lg) / kDecodeTile;
 }
 
 struct DecodePlan {

@@ -20,8 +20,7 @@
 //   the overlap of CTA k and stream s with k + s increasing by at least one
 //   per step, so unit (k, s) writes partial slots 2 (k + s) and
 //   2 (k + s) + 1 (one per softmax warpgroup), and stream s's slots are the
-//   contiguous range the merge recomputes from the per-request tile prefix
-//   sums that CTA 0 leaves in the workspace.
+//   contiguous range the merge recomputes from the context lengths.
 // * Warp roles: warp 0 gathers K tiles (and Q), the last warp gathers V
 //   tiles, warp 1 issues tcgen05.mma from one thread and owns the TMEM
 //   allocation, and two warpgroups (warps 2..5 and 6..9) run the softmax and
@@ -74,7 +73,7 @@
 namespace bkv {
 namespace tc {
 
-constexpr int kTile = 128;            // positions per tile
+constexpr int kTile = kDecodeTile;    // positions per tile
 constexpr int kD = 128;               // head_dim handled
 constexpr int kN = 16;                // query rows per MMA (padded)
 // K and V tiles have separate rings of 32 KB slots
@@ -201,15 +200,15 @@ __device__ void schedule_loads(const DecodeArgs &a, int32_t *pre, uint8_t *lrem,
             // sliding window (never combined with it) drops the tiles wholly before
             // its first visible key
             const int32_t L = cp_local_len(a, Lg);
-            pre[r] = (L + kTile - 1) / kTile - window_lo(a, Lg) / kTile;
+            pre[r] = sk_tiles(a, lens[i]);
             lrem[r] = (uint8_t)((L - 1) & (kTile - 1));
         }
     }
 }
 
 // Exclusive prefix sum of the tile counts in place, pre[n] = total, over all
-// threads of the CTA (tot: one int per warp plus one of scratch); CTA 0 also stores it in the
-// workspace for the merge.  Starts and ends with a __syncthreads.
+// threads of the CTA (tot: one int per warp plus one of scratch).  Starts and
+// ends with a __syncthreads.
 template <int kThreads>
 __device__ void scan_prefix(const DecodeArgs &a, int32_t *pre, int32_t *tot) {
     constexpr int kWarps = kThreads / 32;
@@ -249,8 +248,6 @@ __device__ void scan_prefix(const DecodeArgs &a, int32_t *pre, int32_t *tot) {
     }
     if (threadIdx.x == 0) pre[n] = tot[kWarps];
     __syncthreads();
-    if (blockIdx.x == 0)
-        for (int r = threadIdx.x; r <= n; r += blockDim.x) a.sk_pre[r] = pre[r];
 }
 
 // One unit: tiles [lo, hi) of stream s = r * H_kv + g, counted from the
@@ -1093,7 +1090,7 @@ bool prepare_decode_tc(const DecodeArgs &a, TcLaunch *t) {
     if (a.kv_fp8 && a.cp_world > 1) return false;   // FP8 caches are decoded without context parallelism
     if (a.dtype != BKV_BF16 || a.D != tc::kD || a.nq > tc::kN || a.nq <= 0) return false;
     if (a.bs < 8 || !((tc::kTile % a.bs == 0) || (a.bs % tc::kTile == 0))) return false;
-    if (a.G > 256 || a.q_len > 256 || a.H_kv > 65535 || a.num_reqs > tc::kMaxReqs || !a.sk_pre) return false;
+    if (a.G > 256 || a.q_len > 256 || a.H_kv > 65535 || a.num_reqs > tc::kMaxReqs || !a.stream_k) return false;
     if ((int64_t)a.total_blocks * a.bs >= ((int64_t)1 << 31) || a.total_blocks <= 0) return false;
     if ((int64_t)a.num_reqs * a.q_len >= ((int64_t)1 << 31)) return false;
     // the tile prefix sums and the global tile numbers stay within int32

@@ -1,35 +1,48 @@
 // bkv_ragged_tc.cu -- tensor-core (tcgen05 + TMA) prefill kernel of the
-// mixed-step attention: bf16, head_dim 128, query tiles of 128 rows.
+// mixed-step attention: bf16, head_dim 128, query tiles of 128 rows, two
+// query tiles per unit of work.
 //
 // Operation ("Padding and Batching with Block KV", Batching with Block KV
 // and Cache Masking; see bkv_ragged.cu): each query token of a request
 // attends, at its own position, over the request's paged keys.
 //
 // Design (sm_103a):
-// * Work unit = (request r, KV head g, query tile qt): the T = 128 / G query
-//   tokens qt T, ... of r for the G query heads of g, 128 rows ordered
+// * Work unit = (request r, KV head g, pair p of query tiles): tile A is the
+//   request's query tile 2p and tile B tile 2p + 1 (absent when the request
+//   has an odd number of tiles; a decode token has one), each the T = 128 / G
+//   query tokens of the tile times the G query heads of g, 128 rows ordered
 //   (token, head) -- exactly the box a 3-D TMA load of q (head_dim, H_q,
-//   tokens) delivers.  Persistent CTAs (one per SM) take units round robin.
-// * Warp roles: warp 0 loads Q (per unit) and gathers K tiles, the last warp
-//   gathers V tiles (2-slot rings of 128 keys, 32 KB), warp 1 issues
-//   tcgen05.mma from one thread, warps 2..5 run the softmax, one query row
-//   (TMEM lane) per thread.
-// * S = Q K^T (M = 128 query rows, N = 128 keys, K = head_dim; both operands
-//   K-major from the TMA tiles) into one of two TMEM buffers; the softmax
-//   reads its row in 32-column chunks (max pass, then exponentials), keeps
-//   the running max and sum, and writes P (bf16, K-major, 128-byte swizzle).
-//   The running max is a lazy reference: it moves only when a tile's max
-//   passes it by more than 8 (log2 units), so weights stay below 2^8 and O
-//   is rescaled only on those tiles; a tile every key of which is visible
-//   to all rows of a warp skips the per-key mask tests.
-// * O += P V (N = head_dim, V read MN-major straight from the TMA tile)
-//   accumulates in TMEM across the unit's key tiles; when a row's reference
-//   max moves the softmax rescales its O row in TMEM (only warps with such a
-//   row do).
+//   tokens) delivers.  Both tiles read the same key tiles [0, nk), nk
+//   covering the causal bound of the unit's last token, so every K and V
+//   tile is loaded once for two MMAs.  Persistent CTAs (one per SM) take
+//   units round robin.
+// * Warp roles: warp 0 loads Q and gathers K tiles, the last warp gathers V
+//   tiles (2-slot rings of 32 KB), warp 1 issues tcgen05.mma from one thread
+//   and owns the tensor memory, warps 2..5 run the softmax of tile A and
+//   warps 6..9 that of tile B, one query row (TMEM lane) per thread.
+// * Tensor memory (512 columns): S_A, S_B (128 fp32 columns each) and the
+//   accumulators O_A, O_B (128 each).  A softmax writes its P (bf16, two per
+//   32-bit column) over the first 64 columns of its S, and P V takes P from
+//   tensor memory (tcgen05.mma with A in TMEM), so P never goes through
+//   shared memory.
+// * MMA order per key tile j: O_A += P_A(j-1) V(j-1); S_A(j) = Q_A K(j)^T;
+//   O_B += P_B(j-1) V(j-1); S_B(j) = Q_B K(j)^T.  While softmax A works on
+//   S_A(j) the tensor cores run O_B and S_B, and the other way round, so the
+//   two softmax warpgroups overlap each other and the MMAs.  The MMA that
+//   overwrites S_X's columns is issued after the one that reads P_X from
+//   them (one thread's tcgen05 MMAs run in issue order), and a commit after
+//   S_X(j) completes only once O_X(j-1) has, so when softmax X sees S_X(j)
+//   its O_X is settled and may be rescaled.
+// * Softmax: S read from TMEM in 32-column chunks (max pass, then
+//   exponentials); per-row key limit (cache end and causal bound) and a
+//   null-segment mask; a tile fully visible to every row of a warp skips the
+//   per-key tests.  The running max is a lazy reference that moves only when
+//   a tile's max passes it by more than 8 (log2 units), so O in TMEM is
+//   rescaled only on those tiles.
 // * Keys are gathered through the block table with one TMA load per block
 //   segment and head_dim half; null and out-of-range entries are not loaded,
-//   positions past the causal bound of the tile's last token are not loaded,
-//   and V rows loaded past the cache end are zeroed before P V.
+//   positions past the causal bound of the unit's last token are not loaded,
+//   and V rows loaded past the cache end are zeroed (by softmax A) before P V.
 // * Every wait is bounded (~2 s), after which the CTA records 1 << 24 in
 //   err_count, frees its TMEM and exits.
 #include <cuda.h>
@@ -51,20 +64,18 @@ constexpr int kD = 128;                      // head_dim handled
 constexpr int kStages = 2;                   // K ring and V ring depth
 constexpr int kHalfBytes = kTile * 128;      // 128 rows x 64 bf16: one head_dim (or key) half
 constexpr int kTileBytes = 2 * kHalfBytes;   // 32 KB
-constexpr int kThreads = 224;                // K producer, MMA, 4 softmax warps, V producer
+constexpr int kThreads = 352;                // K producer, MMA, 2 x 4 softmax warps, V producer
 constexpr int kWarpV = kThreads / 32 - 1;
-constexpr int kTmemCols = 512;               // S x2 (128 columns each) + O (128)
-constexpr uint32_t kColO = 256;
+constexpr int kTmemCols = 512;               // S_A, S_B, O_A, O_B (128 columns each)
 constexpr int kTimeoutErr = 1 << 24;
 constexpr int kMaxReqs = 2048;
 
-constexpr int kOffK = 0;
+constexpr int kOffQ = 0;                                 // Q_A, Q_B
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffQ = kOffV + kStages * kTileBytes;
-constexpr int kOffP = kOffQ + kTileBytes;
-constexpr int kOffMask = kOffP + kTileBytes;             // 8 words: loaded segments per tile (ring)
+constexpr int kOffMask = kOffV + kStages * kTileBytes;   // 8 words: loaded segments per tile (ring)
 constexpr int kOffBar = kOffMask + 64;
-constexpr int kNumBars = 4 * kStages + 2 + 2 + 1 + 1 + 8;
+constexpr int kNumBars = 4 * kStages + 2 + 8 + 8;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffPre = (kOffAbort + 4 + 15) / 16 * 16;  // [kMaxReqs + 1] units before request r
@@ -72,13 +83,17 @@ constexpr int kSmemUsed = kOffPre + (kMaxReqs + 1) * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;             // slack for 1024 alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
 
+__host__ __device__ constexpr uint32_t col_s(int x) { return 128u * (uint32_t)x; }         // S_A, S_B
+__host__ __device__ constexpr uint32_t col_o(int x) { return 256u + 128u * (uint32_t)x; }  // O_A, O_B
+
 // One unit of work and the facts every role derives from it.
 struct Unit {
     int r, g;
     int64_t t0;          // first packed token of the request
     int32_t ql, L;       // query tokens and cache length of the request
-    int32_t tok0, ntok;  // the tile's tokens: [tok0, tok0 + ntok) of the request
-    int32_t kend;        // keys [0, kend) may be visible to some row of the tile
+    int32_t tok0;        // tile A's first token (of the request); tile B starts T later
+    int32_t ntok[2];     // tokens of tile A and B (B: 0 when absent)
+    int32_t kend;        // keys [0, kend) may be visible to some row of the unit
     int32_t nk;          // key tiles
 };
 
@@ -109,6 +124,9 @@ __device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
     return t[0];
 }
 
+// Units of request r: H_kv KV heads times its pairs of query tiles.
+__device__ __forceinline__ int pairs_of(int32_t ql, int T) { return ceil_div_i(ceil_div_i(ql, T), 2); }
+
 // Unit u of the launch (pre[] in shared memory holds the units before each
 // request; T tokens per tile).
 __device__ __forceinline__ Unit unit_at(const RaggedArgs &a, const int32_t *pre, int64_t u, int T) {
@@ -124,14 +142,16 @@ __device__ __forceinline__ Unit unit_at(const RaggedArgs &a, const int32_t *pre,
     x.t0 = q.t0;
     x.ql = q.ql;
     x.L = q.L;
-    const int qtiles = ceil_div_i(q.ql, T);
+    const int np = pairs_of(q.ql, T);
     const int64_t v = u - pre[lo];
-    x.g = (int)(v / qtiles);
-    const int qt = (int)(v - (int64_t)x.g * qtiles);
-    x.tok0 = qt * T;
-    x.ntok = min(T, q.ql - x.tok0);
-    const int32_t plast = q.L - q.ql + x.tok0 + x.ntok - 1;   // position of the tile's last token
-    int32_t kend = a.mask_mode == 0 ? min(q.L, plast + 1) : q.L;
+    x.g = (int)(v / np);
+    const int p = (int)(v - (int64_t)x.g * np);
+    x.tok0 = 2 * p * T;
+    x.ntok[0] = min(T, q.ql - x.tok0);
+    x.ntok[1] = max(0, min(T, q.ql - x.tok0 - T));
+    const int32_t last = x.ntok[1] > 0 ? x.tok0 + T + x.ntok[1] - 1 : x.tok0 + x.ntok[0] - 1;
+    const int32_t plast = q.L - q.ql + last;   // position of the unit's last token
+    const int32_t kend = a.mask_mode == 0 ? min(q.L, plast + 1) : q.L;
     x.kend = kend > 0 ? kend : 0;
     x.nk = ceil_div_i(x.kend, kTile);
     return x;
@@ -157,14 +177,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_vempty = [&](int s) { return bar0 + 8u * (3 * kStages + s); };
     const uint32_t bar_qfull = bar0 + 8u * (4 * kStages);
     const uint32_t bar_qempty = bar0 + 8u * (4 * kStages + 1);
-    auto bar_sfull = [&](int b) { return bar0 + 8u * (4 * kStages + 2 + b); };
-    const uint32_t bar_pfull = bar0 + 8u * (4 * kStages + 4);
-    const uint32_t bar_ofull = bar0 + 8u * (4 * kStages + 5);
-    auto bar_mask = [&](int m) { return bar0 + 8u * (4 * kStages + 6 + m); };
+    // per query tile x (0: A, 1: B): S ready, P ready (4 warps), O ready, O read out (4 warps)
+    auto bar_sfull = [&](int x) { return bar0 + 8u * (4 * kStages + 2 + x); };
+    auto bar_pfull = [&](int x) { return bar0 + 8u * (4 * kStages + 4 + x); };
+    auto bar_ofull = [&](int x) { return bar0 + 8u * (4 * kStages + 6 + x); };
+    auto bar_oempty = [&](int x) { return bar0 + 8u * (4 * kStages + 8 + x); };
+    auto bar_mask = [&](int m) { return bar0 + 8u * (4 * kStages + 10 + m); };
+    const uint32_t sm_q = sbase + kOffQ;
     const uint32_t sm_k = sbase + kOffK;
     const uint32_t sm_v = sbase + kOffV;
-    const uint32_t sm_q = sbase + kOffQ;
-    const uint32_t sm_p = sbase + kOffP;
 
     // ---- set-up (no global memory) ----
     if (threadIdx.x == 0) {
@@ -176,10 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar_qfull, 1);
         mbar_init(bar_qempty, 1);
-        mbar_init(bar_sfull(0), 1);
-        mbar_init(bar_sfull(1), 1);
-        mbar_init(bar_pfull, 4);
-        mbar_init(bar_ofull, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar_sfull(x), 1);
+            mbar_init(bar_pfull(x), 4);
+            mbar_init(bar_ofull(x), 1);
+            mbar_init(bar_oempty(x), 4);
+        }
         for (int m = 0; m < 8; ++m) mbar_init(bar_mask(m), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -190,11 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmQ);
     }
     {
-        // V ring, Q and P start at zero: a row no TMA load or softmax writes must
-        // never hold uninitialised bits (NaN) that an MMA could read
+        // the V ring starts at zero: a row no TMA load writes must never hold
+        // uninitialised bits (NaN) that P V could read
         const uint4 z = make_uint4(0, 0, 0, 0);
         uint4 *v = reinterpret_cast<uint4 *>(smem + kOffV);
-        for (int i = threadIdx.x; i < (kStages + 2) * kTileBytes / 16; i += kThreads) v[i] = z;
+        for (int i = threadIdx.x; i < kStages * kTileBytes / 16; i += kThreads) v[i] = z;
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -208,10 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     pdl_wait();   // global memory is read from here on
     pdl_trigger();
-    // units per request (H_kv * query tiles), then their exclusive prefix sum
+    // units per request (H_kv * pairs of query tiles), then their exclusive prefix sum
     for (int r = threadIdx.x; r < a.num_reqs; r += kThreads) {
         const RaggedReq q = ragged_req(a, r);
-        pre[r] = q.ql > 0 ? a.H_kv * ceil_div_i(q.ql, T) : 0;
+        pre[r] = q.ql > 0 ? a.H_kv * pairs_of(q.ql, T) : 0;
         if (q.bad && blockIdx.x == 0 && a.err) atomicAdd(a.err, 1);
     }
     __syncthreads();
@@ -254,10 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!is_v) {
                 if (!mbar_wait_warp(bar_qempty, (uint32_t)(uq & 1) ^ 1u, abort_flag)) break;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(bar_qfull, 2u * 128u * (uint32_t)(G * T));
-                    const int tq = (int)(x.t0 + x.tok0);
-                    tma_load_3d(sm_q, &tmQ, bar_qfull, 0, x.g * G, tq);
-                    tma_load_3d(sm_q + kHalfBytes, &tmQ, bar_qfull, 64, x.g * G, tq);
+                    const bool has_b = x.ntok[1] > 0;
+                    mbar_arrive_expect_tx(bar_qfull, (has_b ? 2u : 1u) * (uint32_t)kTileBytes);
+                    for (int xb = 0; xb < (has_b ? 2 : 1); ++xb) {
+                        const int tq = (int)(x.t0 + x.tok0 + xb * T);
+                        const uint32_t dq = sm_q + xb * kTileBytes;
+                        tma_load_3d(dq, &tmQ, bar_qfull, 0, x.g * G, tq);
+                        tma_load_3d(dq + kHalfBytes, &tmQ, bar_qfull, 64, x.g * G, tq);
+                    }
                 }
             }
             // block entry of this lane's segment of key tile kt: the row to load, or -1
@@ -288,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool load = row_cur >= 0;
                 const uint32_t ballot = __ballot_sync(0xffffffffu, load);
                 if (lane == 0) {
-                    // the mask word ring is written at most a few tiles ahead of its reader
-                    // (two K slots, two S buffers), well inside its 8 entries
+                    // the mask word ring is written at most a few tiles ahead of its
+                    // readers (two K slots, one S per softmax), well inside its 8 entries
                     if (!is_v) {
                         mask_words[j & 7] = ballot;
                         mbar_arrive(bar_mask((int)(j & 7)));
@@ -317,87 +344,111 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= MMA issuer (one thread) =================
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0, 0);   // Q (K-major) x K (K-major)
-            constexpr uint32_t kIdescO = idesc_bf16(128, 128, 0, 1);   // P (K-major) x V (MN-major)
+            constexpr uint32_t kIdescO = idesc_bf16(128, 128, 0, 1);   // P (TMEM) x V (MN-major)
             int64_t j = 0;
             int uq = 0;
-            int64_t pend = -1;   // key tile whose P.V is still to be issued
-            bool pend_first = false;
+            int np[2] = {0, 0};   // P tiles of A / B consumed so far
+            int nu[2] = {0, 0};   // units of A / B started so far
             bool ok = true;
-            auto issue_pv = [&](int64_t jp, bool first) -> bool {
-                const int s = (int)(jp % kStages);
-                if (!mbar_wait(bar_pfull, (uint32_t)(jp & 1), abort_flag) ||
-                    !mbar_wait(bar_vfull(s), (uint32_t)((jp / kStages) & 1), abort_flag))
+            // O_X += P_X(tile) V(stage): the unit's first P V (first) overwrites O_X,
+            // so it waits until softmax X has read the previous unit's O_X out
+            auto issue_pv = [&](int xb, int stage, bool first) -> bool {
+                if (!mbar_wait(bar_pfull(xb), (uint32_t)(np[xb] & 1), abort_flag)) return false;
+                ++np[xb];
+                if (first && nu[xb] > 1 && !mbar_wait(bar_oempty(xb), (uint32_t)((nu[xb] - 2) & 1), abort_flag))
                     return false;
                 tc_fence_after();
-                const uint32_t v_base = sm_v + s * kTileBytes;
+                const uint32_t v_base = sm_v + stage * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint64_t adesc = sdesc(sm_p + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
                     const uint64_t bdesc = sdesc(v_base + kk * 2048, kHalfBytes, 1024);
-                    mma_bf16(tmem + kColO, adesc, bdesc, kIdescO, (first && kk == 0) ? 0u : 1u);
+                    mma_bf16_ts(tmem + col_o(xb), tmem + col_s(xb) + 8u * kk, bdesc, kIdescO,
+                                (first && kk == 0) ? 0u : 1u);
                 }
-                mma_commit(bar_ofull);
-                mma_commit(bar_vempty(s));
                 return true;
+            };
+            auto issue_s = [&](int xb, int stage) {
+                const uint32_t k_base = sm_k + stage * kTileBytes;
+                const uint32_t q_base = sm_q + xb * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                    mma_bf16(tmem + col_s(xb), sdesc(q_base + off, 16, 1024), sdesc(k_base + off, 16, 1024), kIdescS,
+                             kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar_sfull(xb));
             };
             for (int64_t u = blockIdx.x; ok && u < U; u += gridDim.x) {
                 const Unit x = unit_at(a, pre, u, T);
                 if (x.nk == 0) continue;
+                const bool has_b = x.ntok[1] > 0;
+                ++nu[0];
+                if (has_b) ++nu[1];
                 if (!mbar_wait(bar_qfull, (uint32_t)(uq & 1), abort_flag)) {
                     ok = false;
                     break;
                 }
-                for (int kt = 0; kt < x.nk; ++kt, ++j) {
+                for (int kt = 0; ok && kt <= x.nk; ++kt, ++j) {
+                    // P V of the previous key tile, then S of this one, tile A then B
+                    const int sp = (int)((j - 1) % kStages);
+                    if (kt > 0 && !mbar_wait(bar_vfull(sp), (uint32_t)(((j - 1) / kStages) & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     const int s = (int)(j % kStages);
-                    const int b = (int)(j & 1);
-                    if (!mbar_wait(bar_kfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
+                    if (kt < x.nk && !mbar_wait(bar_kfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t k_base = sm_k + s * kTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint32_t off = (uint32_t)(kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        mma_bf16(tmem + 128u * b, sdesc(sm_q + off, 16, 1024), sdesc(k_base + off, 16, 1024), kIdescS,
-                                 kk > 0 ? 1u : 0u);
+                    for (int xb = 0; xb < (has_b ? 2 : 1); ++xb) {
+                        if (kt > 0 && !issue_pv(xb, sp, kt == 1)) {
+                            ok = false;
+                            break;
+                        }
+                        if (kt == x.nk) mma_commit(bar_ofull(xb));
+                        if (kt < x.nk) issue_s(xb, s);
                     }
-                    mma_commit(bar_sfull(b));
-                    mma_commit(bar_kempty(s));
-                    if (kt == x.nk - 1) mma_commit(bar_qempty);
-                    if (pend >= 0 && !issue_pv(pend, pend_first)) {
-                        ok = false;
-                        break;
+                    if (!ok) break;
+                    if (kt > 0) mma_commit(bar_vempty(sp));
+                    if (kt < x.nk) {
+                        mma_commit(bar_kempty(s));
+                        if (kt == x.nk - 1) mma_commit(bar_qempty);
                     }
-                    pend = j;
-                    pend_first = kt == 0;
                 }
+                --j;   // the loop ran nk + 1 turns for nk key tiles
                 ++uq;
             }
-            if (ok && pend >= 0) issue_pv(pend, pend_first);
         }
         __syncwarp();
-    } else {
-        // ================= softmax (warps 2..5: one query row per thread) =================
+    } else if (warp < kWarpV) {
+        // ================= softmax (warps 2..5: tile A, 6..9: tile B; one query row per thread) =================
+        const int xb = (warp - 2) >> 2;                  // query tile of this warpgroup
         const int qw = warp & 3;                         // TMEM lane quarter this warp may access
         const int row = 32 * qw + lane;                  // query row of the tile: token row / G, head row % G
         const uint32_t lane_base = (uint32_t)(32 * qw) << 16;
         const int tt = row / G;
         const int hh = row - tt * G;
-        // this thread's bytes in P (K-major, 128-byte swizzle): row `row`, 16-byte chunk c of key half h
-        auto p_addr = [&](int h, int c) -> uint8_t * {
-            return smem + kOffP + h * kHalfBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
-        };
-        int64_t j = 0;
+        const uint32_t s_col = tmem + lane_base + col_s(xb);
+        const uint32_t o_col = tmem + lane_base + col_o(xb);
+        int64_t j = 0;       // key-tile sequence number in this CTA (the mask ring)
+        int ns = 0;          // S tiles of this query tile seen so far
+        int no = 0;          // units of this query tile finished so far
         bool ok = true;
         for (int64_t u = blockIdx.x; ok && u < U; u += gridDim.x) {
             const Unit x = unit_at(a, pre, u, T);
-            const bool valid = row < G * T && tt < x.ntok;
-            const int32_t pos = x.L - x.ql + x.tok0 + tt;           // this row's token position
+            const int ntok = x.ntok[xb];
+            if (ntok <= 0) {      // no tile B in this unit
+                j += x.nk;
+                continue;
+            }
+            const bool valid = row < G * T && tt < ntok;
+            const int32_t tok = x.tok0 + xb * T + tt;                    // this row's token (of the request)
+            const int32_t pos = x.L - x.ql + tok;                        // and its position
             const int32_t lastv = a.mask_mode == 0 ? pos : x.L - 1;
             const bool warp_valid = __any_sync(0xffffffffu, valid);
-            __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) +
-                                 ((x.t0 + x.tok0 + tt) * a.H_q + (int64_t)x.g * G + hh) * kD;
+            __nv_bfloat16 *out =
+                static_cast<__nv_bfloat16 *>(a.out) + ((x.t0 + tok) * a.H_q + (int64_t)x.g * G + hh) * kD;
             if (x.nk == 0) {
                 if (valid)
                     for (int d = 0; d < kD; d += 8) *reinterpret_cast<uint4 *>(out + d) = make_uint4(0, 0, 0, 0);
@@ -405,13 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float m = -INFINITY, l = 0.f;
             for (int kt = 0; kt < x.nk; ++kt, ++j) {
-                const int b = (int)(j & 1);
                 const int s = (int)(j % kStages);
-                if (!mbar_wait_warp(bar_sfull(b), (uint32_t)((j >> 1) & 1), abort_flag) ||
+                if (!mbar_wait_warp(bar_sfull(xb), (uint32_t)(ns & 1), abort_flag) ||
                     !mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag)) {
                     ok = false;
                     break;
                 }
+                ++ns;
                 tc_fence_after();
                 const uint32_t mword = mask_words[j & 7];
                 const int32_t k0 = kt * kTile;
@@ -427,10 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // pass 1: the tile max of the raw scores (the scale is positive), as a tree
                 float mraw = -INFINITY;
                 if (warp_valid) {
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         float sv[32];
-                        tmem_ld32(tmem + lane_base + 128u * b + 32u * c, sv);
+                        tmem_ld32(s_col + 32u * c, sv);
                         if (!full) {
 #pragma unroll
                             for (int k = 0; k < 32; ++k) sv[k] = seen(32 * c + k) ? sv[k] : -INFINITY;
@@ -445,94 +496,94 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool bump = mt > m + kSlack;
                 const float mn = bump ? mt : m;
                 const float corr = bump ? fast_exp2(m - mn) : 1.f;
-                // the previous tile's P.V must be done before P and O are touched
-                if (kt > 0) {
-                    if (!mbar_wait_warp(bar_ofull, (uint32_t)((j - 1) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (warp_valid && __any_sync(0xffffffffu, corr != 1.f)) {
+                // O_X(kt - 1) completed before S_X(kt) did: rescale it in place
+                if (kt > 0 && warp_valid && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        float ov[32];
+                        tmem_ld32(o_col + 32u * c, ov);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            float ov[32];
-                            tmem_ld32(tmem + lane_base + kColO + 32u * c, ov);
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) ov[k] *= corr;
-                            tmem_st32(tmem + lane_base + kColO + 32u * c, ov);
-                        }
+                        for (int k = 0; k < 32; ++k) ov[k] *= corr;
+                        tmem_st32(o_col + 32u * c, ov);
                     }
                 }
-                if (warp_valid) {
-                    // pass 2: weights 2^(s * scale - mn) (0 where masked), their sum, P in bf16
+                // pass 2: weights 2^(s * scale - mn) (0 where masked), their sum, and P
+                // (bf16) over the first 64 columns of S: chunk c's 8 packed columns
+                // [8c, 8c + 8) lie at or below the 16 columns [16c, 16c + 16) just read
+                float psum = 0.f;
+                {
                     const float nb = -mn;
-                    float psum = 0.f;
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        float sv[16];
+                        tmem_ld16(s_col + 16u * c, sv);
+                        if (!warp_valid) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float sv[32];
-                        tmem_ld32(tmem + lane_base + 128u * b + 32u * c, sv);
-                        if (full) {
+                            for (int k = 0; k < 16; ++k) sv[k] = 0.f;
+                        } else if (full) {
 #pragma unroll
-                            for (int k = 0; k < 32; ++k) sv[k] = fast_exp2(fmaf(sv[k], a.scale_log2, nb));
+                            for (int k = 0; k < 16; ++k) sv[k] = fast_exp2(fmaf(sv[k], a.scale_log2, nb));
                         } else {
 #pragma unroll
-                            for (int k = 0; k < 32; ++k) {
+                            for (int k = 0; k < 16; ++k) {
                                 // computed for every key, then selected: no branch per key
                                 const float e = fast_exp2(fmaf(sv[k], a.scale_log2, nb));
-                                sv[k] = seen(32 * c + k) ? e : 0.f;
+                                sv[k] = seen(16 * c + k) ? e : 0.f;
                             }
                         }
-                        uint32_t pk[16];
+                        uint32_t pk[8];
 #pragma unroll
-                        for (int k = 0; k < 32; k += 2) {
+                        for (int k = 0; k < 16; k += 2) {
                             const __nv_bfloat162 pb = __floats2bfloat162_rn(sv[k], sv[k + 1]);
                             pk[k >> 1] = *reinterpret_cast<const uint32_t *>(&pb);
+                            psum += sv[k] + sv[k + 1];
                         }
-                        psum += tree_sum32(sv);
-                        // keys 32c .. 32c + 31: half c / 2, 16-byte chunks 4 (c % 2) .. + 3
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            *reinterpret_cast<uint4 *>(p_addr(c >> 1, 4 * (c & 1) + q4)) =
-                                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                        tmem_st8(s_col + 8u * c, pk);
                     }
-                    l = fmaf(l, corr, psum);
-                    m = mn;
+                    tmem_st_wait();
                 }
+                l = fmaf(l, corr, psum);
+                m = mn;
                 // V rows loaded past the cache end (the last segment's tail) must be zero
-                // for P.V; any thread may clear any row once the V tile has landed
-                const bool zero_row = ((mword >> (row >> seg_shift)) & 1u) && k0 + row >= x.L;
-                if (__any_sync(0xffffffffu, zero_row)) {
-                    if (!mbar_wait_warp(bar_vfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    if (zero_row) {
-                        uint4 *v0 = reinterpret_cast<uint4 *>(smem + kOffV + s * kTileBytes + row * 128);
-                        uint4 *v1 = reinterpret_cast<uint4 *>(smem + kOffV + s * kTileBytes + kHalfBytes + row * 128);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            v0[c] = make_uint4(0, 0, 0, 0);
-                            v1[c] = make_uint4(0, 0, 0, 0);
+                // for P V; softmax A clears them once the V tile has landed (P V of tile
+                // B is issued after P V of tile A)
+                if (xb == 0) {
+                    const bool zero_row = ((mword >> (row >> seg_shift)) & 1u) && k0 + row >= x.L;
+                    if (__any_sync(0xffffffffu, zero_row)) {
+                        if (!mbar_wait_warp(bar_vfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
+                            ok = false;
+                            break;
                         }
+                        if (zero_row) {
+                            uint4 *v0 = reinterpret_cast<uint4 *>(smem + kOffV + s * kTileBytes + row * 128);
+                            uint4 *v1 =
+                                reinterpret_cast<uint4 *>(smem + kOffV + s * kTileBytes + kHalfBytes + row * 128);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                v0[c] = make_uint4(0, 0, 0, 0);
+                                v1[c] = make_uint4(0, 0, 0, 0);
+                            }
+                        }
+                        fence_proxy_async();
                     }
                 }
-                fence_proxy_async();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_pfull);
+                if (lane == 0) mbar_arrive(bar_pfull(xb));
             }
             if (!ok) break;
-            // the unit's last P.V, then this row's output
-            if (!mbar_wait_warp(bar_ofull, (uint32_t)((j - 1) & 1), abort_flag)) {
+            // the unit's last P V, then this row's output; O_X is free again after
+            if (!mbar_wait_warp(bar_ofull(xb), (uint32_t)(no & 1), abort_flag)) {
                 ok = false;
                 break;
             }
+            ++no;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 float ov[32];
-                tmem_ld32(tmem + lane_base + kColO + 32u * c, ov);
+                tmem_ld32(o_col + 32u * c, ov);
                 if (valid) {
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
@@ -548,6 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_oempty(xb));
         }
     }
 
