@@ -471,23 +471,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int32_t lim = min(x.L, lastv + 1) - k0;
                 lim = valid ? max(0, min(kTile, lim)) : 0;
                 const bool segs = mword == all_seg;   // no null entry in the tile
-                auto seen = [&](int k) { return k < lim && (segs || ((mword >> (k >> seg_shift)) & 1u)); };
+                // Visible keys [32c, 32c + 32) of the tile as a bit mask: below lim, and in
+                // a loaded segment (segments of seg_rows keys, one bit each in mword).
+                auto vis32 = [&](int c) -> uint32_t {
+                    const int lo = 32 * c;
+                    uint32_t v = lim >= lo + 32 ? 0xffffffffu : (lim > lo ? (1u << (lim - lo)) - 1u : 0u);
+                    if (!segs) {
+                        uint32_t sb;
+                        if (seg_rows >= 32) {
+                            sb = ((mword >> (lo >> seg_shift)) & 1u) ? 0xffffffffu : 0u;
+                        } else {
+                            const int per = 32 >> seg_shift;            // segments in the chunk: 2 or 4
+                            const uint32_t ones = (1u << seg_rows) - 1u;
+                            const uint32_t bits = mword >> (lo >> seg_shift);
+                            sb = 0u;
+                            for (int i = 0; i < per; ++i)
+                                if ((bits >> i) & 1u) sb |= ones << (i * seg_rows);
+                        }
+                        v &= sb;
+                    }
+                    return v;
+                };
                 // Every key of the tile visible to every row of this warp (the common
                 // case inside a long prefix): no per-key tests.
                 const bool full = __all_sync(0xffffffffu, lim == kTile) && segs;
+                // A warp with no valid row does no softmax work: its P rows feed O rows
+                // that are never stored, and the MMA keeps rows apart.
+                // V rows loaded past the cache end (the last segment's tail) must be zero
+                // for P V; softmax A clears them (every warp its 32 rows of the tile)
+                // once the V tile has landed; P V of tile B is issued after that of A.
+                auto zero_v_rows = [&]() -> bool {
+                    if (xb != 0) return true;
+                    const bool zero_row = ((mword >> (row >> seg_shift)) & 1u) && k0 + row >= x.L;
+                    if (!__any_sync(0xffffffffu, zero_row)) return true;
+                    if (!mbar_wait_warp(bar_vfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) return false;
+                    if (zero_row) {
+                        uint4 *v0 = reinterpret_cast<uint4 *>(smem + kOffV + s * kTileBytes + row * 128);
+                        uint4 *v1 = reinterpret_cast<uint4 *>(smem + kOffV + s * kTileBytes + kHalfBytes + row * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            v0[c] = make_uint4(0, 0, 0, 0);
+                            v1[c] = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    fence_proxy_async();
+                    return true;
+                };
+                if (!warp_valid) {
+                    if (!zero_v_rows()) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_pfull(xb));
+                    continue;
+                }
                 // pass 1: the tile max of the raw scores (the scale is positive), as a tree
                 float mraw = -INFINITY;
-                if (warp_valid) {
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        float sv[32];
-                        tmem_ld32(s_col + 32u * c, sv);
-                        if (!full) {
+                for (int c = 0; c < 4; ++c) {
+                    float sv[32];
+                    tmem_ld32(s_col + 32u * c, sv);
+                    if (!full) {
+                        const uint32_t vm = vis32(c);
 #pragma unroll
-                            for (int k = 0; k < 32; ++k) sv[k] = seen(32 * c + k) ? sv[k] : -INFINITY;
-                        }
-                        mraw = fmaxf(mraw, tree_max32(sv));
+                        for (int k = 0; k < 32; ++k) sv[k] = (vm & (1u << k)) ? sv[k] : -INFINITY;
                     }
+                    mraw = fmaxf(mraw, tree_max32(sv));
                 }
                 const float mt = mraw * a.scale_log2;
                 // Lazy rescale: the reference max m moves (and O, l are rescaled) only
@@ -497,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mn = bump ? mt : m;
                 const float corr = bump ? fast_exp2(m - mn) : 1.f;
                 // O_X(kt - 1) completed before S_X(kt) did: rescale it in place
-                if (kt > 0 && warp_valid && __any_sync(0xffffffffu, corr != 1.f)) {
+                if (kt > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         float ov[32];
@@ -513,22 +564,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float psum = 0.f;
                 {
                     const float nb = -mn;
+                    uint32_t vm = 0;
 #pragma unroll 1
                     for (int c = 0; c < 8; ++c) {
                         float sv[16];
                         tmem_ld16(s_col + 16u * c, sv);
-                        if (!warp_valid) {
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) sv[k] = 0.f;
-                        } else if (full) {
+                        if (full) {
 #pragma unroll
                             for (int k = 0; k < 16; ++k) sv[k] = fast_exp2(fmaf(sv[k], a.scale_log2, nb));
                         } else {
+                            if ((c & 1) == 0) vm = vis32(c >> 1);
+                            const uint32_t vh = (c & 1) ? (vm >> 16) : vm;
 #pragma unroll
                             for (int k = 0; k < 16; ++k) {
                                 // computed for every key, then selected: no branch per key
                                 const float e = fast_exp2(fmaf(sv[k], a.scale_log2, nb));
-                                sv[k] = seen(16 * c + k) ? e : 0.f;
+                                sv[k] = (vh & (1u << k)) ? e : 0.f;
                             }
                         }
                         uint32_t pk[8];
@@ -544,28 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l = fmaf(l, corr, psum);
                 m = mn;
-                // V rows loaded past the cache end (the last segment's tail) must be zero
-                // for P V; softmax A clears them once the V tile has landed (P V of tile
-                // B is issued after P V of tile A)
-                if (xb == 0) {
-                    const bool zero_row = ((mword >> (row >> seg_shift)) & 1u) && k0 + row >= x.L;
-                    if (__any_sync(0xffffffffu, zero_row)) {
-                        if (!mbar_wait_warp(bar_vfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        if (zero_row) {
-                            uint4 *v0 = reinterpret_cast<uint4 *>(smem + kOffV + s * kTileBytes + row * 128);
-                            uint4 *v1 =
-                                reinterpret_cast<uint4 *>(smem + kOffV + s * kTileBytes + kHalfBytes + row * 128);
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                v0[c] = make_uint4(0, 0, 0, 0);
-                                v1[c] = make_uint4(0, 0, 0, 0);
-                            }
-                        }
-                        fence_proxy_async();
-                    }
+                if (!zero_v_rows()) {
+                    ok = false;
+                    break;
                 }
                 tc_fence_before();
                 __syncwarp();
