@@ -14,17 +14,22 @@
 //   (token, head) -- exactly the box a 3-D TMA load of q (head_dim, H_q,
 //   tokens) delivers.  Both tiles read the same key tiles [0, nk), nk
 //   covering the causal bound of the unit's last token, so every K and V
-//   tile is loaded once for two MMAs.  Persistent CTAs (one per SM) take
-//   units round robin.
+//   tile is loaded once for two MMAs.  Persistent CTAs, one per SM.
 // * Warp roles: warp 0 loads Q and gathers K tiles, the last warp gathers V
 //   tiles (2-slot rings of 32 KB), warp 1 issues tcgen05.mma from one thread
-//   and owns the tensor memory, warps 2..5 run the softmax of tile A and
-//   warps 6..9 that of tile B, one query row (TMEM lane) per thread.
+//   and owns the tensor memory; sixteen softmax warps, four warpgroups: for
+//   each query tile one per half of every key tile (keys 0..63, 64..127),
+//   one query row (TMEM lane) per thread.  The two halves of a row exchange
+//   their partial tile max (and at the end their weight sums) through shared
+//   memory at a bounded two-warp barrier, so both take the same rescaling
+//   decision.
+// * Units are ranked by cost (key tiles, one or two query tiles) and dealt
+//   to the CTAs back and forth, largest first.
 // * Tensor memory (512 columns): S_A, S_B (128 fp32 columns each) and the
-//   accumulators O_A, O_B (128 each).  A softmax writes its P (bf16, two per
-//   32-bit column) over the first 64 columns of its S, and P V takes P from
-//   tensor memory (tcgen05.mma with A in TMEM), so P never goes through
-//   shared memory.
+//   accumulators O_A, O_B (128 each).  Each key half writes its P (bf16, two
+//   per 32-bit column) over the first 32 of its own 64 S columns, and P V
+//   takes P from tensor memory (tcgen05.mma with A in TMEM), so P never goes
+//   through shared memory.
 // * MMA order per key tile j: O_A += P_A(j-1) V(j-1); S_A(j) = Q_A K(j)^T;
 //   O_B += P_B(j-1) V(j-1); S_B(j) = Q_B K(j)^T.  While softmax A works on
 //   S_A(j) the tensor cores run O_B and S_B, and the other way round, so the
@@ -64,7 +69,7 @@ constexpr int kD = 128;                      // head_dim handled
 constexpr int kStages = 2;                   // K ring and V ring depth
 constexpr int kHalfBytes = kTile * 128;      // 128 rows x 64 bf16: one head_dim (or key) half
 constexpr int kTileBytes = 2 * kHalfBytes;   // 32 KB
-constexpr int kThreads = 352;                // K producer, MMA, 2 x 4 softmax warps, V producer
+constexpr int kThreads = 608;                // K producer, MMA, 4 x 4 softmax warps, V producer
 constexpr int kWarpV = kThreads / 32 - 1;
 constexpr int kTmemCols = 512;               // S_A, S_B, O_A, O_B (128 columns each)
 constexpr int kTimeoutErr = 1 << 24;
@@ -75,11 +80,23 @@ constexpr int kOffK = kOffQ + 2 * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
 constexpr int kOffMask = kOffV + kStages * kTileBytes;   // 8 words: loaded segments per tile (ring)
 constexpr int kOffBar = kOffMask + 64;
-constexpr int kNumBars = 4 * kStages + 2 + 8 + 8;
+constexpr int kNumBars = 4 * kStages + 2 + 8 + 8 + 8;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffPre = (kOffAbort + 4 + 15) / 16 * 16;  // [kMaxReqs + 1] units before request r
-constexpr int kSmemUsed = kOffPre + (kMaxReqs + 1) * 4;
+// the two key halves of a query tile exchange, per row, their partial tile max
+// ([tile][half][tile parity][row]) and at the end their partial row sums ([tile][half][row])
+constexpr int kOffXmax = (kOffPre + (kMaxReqs + 1) * 4 + 15) / 16 * 16;
+constexpr int kOffXsum = kOffXmax + 2 * 2 * 2 * kTile * 4;
+// the unit schedule: each unit's cost, a histogram of costs, this CTA's units
+constexpr int kSchedUnits = 4096;            // launches with more units are dealt round robin
+constexpr int kBuckets = 1024;
+constexpr int kMaxMine = 64;
+constexpr int kOffCost = kOffXsum + 2 * 2 * kTile * 4;
+constexpr int kOffHist = kOffCost + kSchedUnits * 2;
+constexpr int kOffMine = kOffHist + kBuckets * 4;
+constexpr int kOffNMine = kOffMine + kMaxMine * 4;
+constexpr int kSmemUsed = kOffNMine + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;             // slack for 1024 alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
 
@@ -183,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_ofull = [&](int x) { return bar0 + 8u * (4 * kStages + 6 + x); };
     auto bar_oempty = [&](int x) { return bar0 + 8u * (4 * kStages + 8 + x); };
     auto bar_mask = [&](int m) { return bar0 + 8u * (4 * kStages + 10 + m); };
+    // the two warps (one per key half) that share TMEM lane quarter qw of query tile x
+    auto bar_pair = [&](int x, int qw) { return bar0 + 8u * (4 * kStages + 18 + 4 * x + qw); };
     const uint32_t sm_q = sbase + kOffQ;
     const uint32_t sm_k = sbase + kOffK;
     const uint32_t sm_v = sbase + kOffV;
@@ -199,9 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_qempty, 1);
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar_sfull(x), 1);
-            mbar_init(bar_pfull(x), 4);
+            mbar_init(bar_pfull(x), 8);
             mbar_init(bar_ofull(x), 1);
-            mbar_init(bar_oempty(x), 4);
+            mbar_init(bar_oempty(x), 8);
+            for (int qw = 0; qw < 4; ++qw) mbar_init(bar_pair(x, qw), 2);
         }
         for (int m = 0; m < 8; ++m) mbar_init(bar_mask(m), 1);
         *abort_flag = 0;
@@ -266,12 +286,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seg_shift = 31 - __clz(seg_rows);
     const uint32_t all_seg = nseg >= 32 ? 0xffffffffu : ((1u << nseg) - 1u);   // every segment loaded
 
+    // ---- the unit schedule ----
+    // Units differ in cost (key tiles, one or two query tiles).  Every CTA ranks all units by
+    // cost, largest first (a counting sort over cost buckets, ties in unit order, so every CTA
+    // computes the same ranking), and takes the ranks it gets when they are dealt over the
+    // CTAs back and forth (0 .. grid-1, grid-1 .. 0, ...): the largest units are spread first
+    // and the per-CTA sums come out close.  Beyond kSchedUnits units, round robin.
+    const int64_t grid = gridDim.x;
+    const bool lpt = U > grid && U <= kSchedUnits && (U + grid - 1) / grid <= kMaxMine;
+    int32_t *mine = reinterpret_cast<int32_t *>(smem + kOffMine);
+    if (lpt) {
+        uint16_t *cost = reinterpret_cast<uint16_t *>(smem + kOffCost);
+        int32_t *hist = reinterpret_cast<int32_t *>(smem + kOffHist);
+        for (int b = threadIdx.x; b < kBuckets; b += kThreads) hist[b] = 0;
+        __syncthreads();
+        for (int u = threadIdx.x; u < U; u += kThreads) {
+            const Unit x = unit_at(a, pre, u, T);
+            const int c = min(x.nk * (x.ntok[1] > 0 ? 3 : 2), kBuckets - 1);   // a pair costs ~1.5 singles
+            cost[u] = (uint16_t)c;
+            atomicAdd(&hist[kBuckets - 1 - c], 1);   // bucket order = descending cost
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // exclusive prefix sum of the buckets: lane l owns buckets [32 l, 32 l + 32)
+            int32_t sum = 0;
+            for (int b = 32 * lane; b < 32 * lane + 32; ++b) sum += hist[b];
+            int32_t inc = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            int32_t run = inc - sum;
+            for (int b = 32 * lane; b < 32 * lane + 32; ++b) {
+                const int32_t t = hist[b];
+                hist[b] = run;
+                run += t;
+            }
+            __syncwarp();
+            // ranks in unit order, 32 units at a time; rank -> CTA by the back-and-forth deal
+            for (int base = 0; base < U; base += 32) {
+                const int u = base + lane;
+                const int b = u < U ? kBuckets - 1 - cost[u] : -1 - lane;
+                const unsigned same = __match_any_sync(0xffffffffu, b);
+                const int before = __popc(same & ((1u << lane) - 1u));
+                const int start = u < U ? hist[b] : 0;
+                __syncwarp();
+                if (u < U && before == 0) hist[b] = start + __popc(same);
+                __syncwarp();
+                if (u < U) {
+                    const int rank = start + before;
+                    const int k = rank / (int)grid, c = rank - k * (int)grid;
+                    if (((k & 1) ? (int)grid - 1 - c : c) == (int)blockIdx.x) mine[k] = u;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    // this CTA's units, in the order it runs them: one per full round of the deal, and one in the
+    // last, partial round if the deal reaches it there
+    int n_mine;
+    if (lpt) {
+        const int full = (int)(U / grid), rem = (int)(U - full * grid);
+        const int c = (int)blockIdx.x;
+        n_mine = full + ((full & 1) ? ((int)grid - 1 - c < rem) : (c < rem));
+    } else {
+        n_mine = U > blockIdx.x ? (int)((U - 1 - blockIdx.x) / grid + 1) : 0;
+    }
+    auto unit_id = [&](int i) -> int64_t { return lpt ? mine[i] : blockIdx.x + i * grid; };
+
     if (warp == 0 || warp == kWarpV) {
         // ================= TMA producers (warp 0: Q and K, last warp: V) =================
         const bool is_v = warp == kWarpV;
         int64_t j = 0;   // key-tile sequence number in this CTA
         int uq = 0;      // units with key tiles
-        for (int64_t u = blockIdx.x; u < U && !*abort_flag; u += gridDim.x) {
+        for (int i = 0; i < n_mine && !*abort_flag; ++i) {
+            const int64_t u = unit_id(i);
             const Unit x = unit_at(a, pre, u, T);
             if (x.nk == 0) continue;
             if (!is_v) {
@@ -362,7 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     const uint64_t bdesc = sdesc(v_base + kk * 2048, kHalfBytes, 1024);
-                    mma_bf16_ts(tmem + col_o(xb), tmem + col_s(xb) + 8u * kk, bdesc, kIdescO,
+                    // keys 16 kk .. 16 kk + 15: P of keys 0..63 is packed over S columns 0..31
+                    // and that of keys 64..127 over columns 64..95 (each key half's own columns)
+                    const uint32_t pcol = (kk < 4 ? 0u : 64u) + 8u * (uint32_t)(kk & 3);
+                    mma_bf16_ts(tmem + col_o(xb), tmem + col_s(xb) + pcol, bdesc, kIdescO,
                                 (first && kk == 0) ? 0u : 1u);
                 }
                 return true;
@@ -378,7 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(bar_sfull(xb));
             };
-            for (int64_t u = blockIdx.x; ok && u < U; u += gridDim.x) {
+            for (int i = 0; ok && i < n_mine; ++i) {
+                const int64_t u = unit_id(i);
                 const Unit x = unit_at(a, pre, u, T);
                 if (x.nk == 0) continue;
                 const bool has_b = x.ntok[1] > 0;
@@ -422,8 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp < kWarpV) {
-        // ================= softmax (warps 2..5: tile A, 6..9: tile B; one query row per thread) =================
-        const int xb = (warp - 2) >> 2;                  // query tile of this warpgroup
+        // ====== softmax (warps 2..9: tile A, 10..17: tile B; per tile one warpgroup per half of the
+        // ====== keys, one query row per thread) ======
+        const int xb = (warp - 2) >> 3;                  // query tile of this warpgroup
+        const int kh = ((warp - 2) >> 2) & 1;            // its half of each key tile: keys [64 kh, 64 kh + 64)
         const int qw = warp & 3;                         // TMEM lane quarter this warp may access
         const int row = 32 * qw + lane;                  // query row of the tile: token row / G, head row % G
         const uint32_t lane_base = (uint32_t)(32 * qw) << 16;
@@ -435,7 +531,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ns = 0;          // S tiles of this query tile seen so far
         int no = 0;          // units of this query tile finished so far
         bool ok = true;
-        for (int64_t u = blockIdx.x; ok && u < U; u += gridDim.x) {
+        // Bounded exchange point of this warp and the warp that holds the other key half of the
+        // same rows (an mbarrier, so that a timed-out wait elsewhere never leaves a warp stuck)
+        uint32_t pphase = 0;
+        auto pair_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_pair(xb, qw));
+            const bool r = mbar_wait_warp(bar_pair(xb, qw), pphase, abort_flag);
+            pphase ^= 1u;
+            return r;
+        };
+        float *xmax = reinterpret_cast<float *>(smem + kOffXmax) + xb * (2 * 2 * kTile);   // [half][parity][row]
+        float *xsum = reinterpret_cast<float *>(smem + kOffXsum) + xb * (2 * kTile);       // [half][row]
+        for (int i = 0; ok && i < n_mine; ++i) {
+            const int64_t u = unit_id(i);
             const Unit x = unit_at(a, pre, u, T);
             const int ntok = x.ntok[xb];
             if (ntok <= 0) {      // no tile B in this unit
@@ -449,9 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool warp_valid = __any_sync(0xffffffffu, valid);
             __nv_bfloat16 *out =
                 static_cast<__nv_bfloat16 *>(a.out) + ((x.t0 + tok) * a.H_q + (int64_t)x.g * G + hh) * kD;
-            if (x.nk == 0) {
+            if (x.nk == 0) {   // nothing visible: this half's 64 output values are 0
                 if (valid)
-                    for (int d = 0; d < kD; d += 8) *reinterpret_cast<uint4 *>(out + d) = make_uint4(0, 0, 0, 0);
+                    for (int d = 64 * kh; d < 64 * kh + 64; d += 8)
+                        *reinterpret_cast<uint4 *>(out + d) = make_uint4(0, 0, 0, 0);
                 continue;
             }
             float m = -INFINITY, l = 0.f;
@@ -492,16 +602,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     return v;
                 };
-                // Every key of the tile visible to every row of this warp (the common
+                // Every key of this half visible to every row of this warp (the common
                 // case inside a long prefix): no per-key tests.
-                const bool full = __all_sync(0xffffffffu, lim == kTile) && segs;
+                const bool full = __all_sync(0xffffffffu, lim >= 64 * kh + 64) && segs;
                 // A warp with no valid row does no softmax work: its P rows feed O rows
                 // that are never stored, and the MMA keeps rows apart.
                 // V rows loaded past the cache end (the last segment's tail) must be zero
                 // for P V; softmax A clears them (every warp its 32 rows of the tile)
                 // once the V tile has landed; P V of tile B is issued after that of A.
                 auto zero_v_rows = [&]() -> bool {
-                    if (xb != 0) return true;
+                    if (xb != 0 || kh != 0) return true;
                     const bool zero_row = ((mword >> (row >> seg_shift)) & 1u) && k0 + row >= x.L;
                     if (!__any_sync(0xffffffffu, zero_row)) return true;
                     if (!mbar_wait_warp(bar_vfull(s), (uint32_t)((j / kStages) & 1), abort_flag)) return false;
@@ -527,10 +637,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(bar_pfull(xb));
                     continue;
                 }
-                // pass 1: the tile max of the raw scores (the scale is positive), as a tree
+                // pass 1: this half's max of the raw scores (the scale is positive), as a tree,
+                // then the tile max of the row from the two halves
                 float mraw = -INFINITY;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 2 * kh; c < 2 * kh + 2; ++c) {
                     float sv[32];
                     tmem_ld32(s_col + 32u * c, sv);
                     if (!full) {
@@ -540,17 +651,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mraw = fmaxf(mraw, tree_max32(sv));
                 }
+                float *xm = xmax + (int)(j & 1) * kTile;     // this tile's exchange slots, parity j
+                xm[kh * 2 * kTile + row] = mraw;
+                if (!pair_sync()) {
+                    ok = false;
+                    break;
+                }
+                mraw = fmaxf(mraw, xm[(1 - kh) * 2 * kTile + row]);
                 const float mt = mraw * a.scale_log2;
                 // Lazy rescale: the reference max m moves (and O, l are rescaled) only
                 // when the tile max passes it by more than kSlack, so weights stay
-                // below 2^kSlack and most tiles leave O alone.
+                // below 2^kSlack and most tiles leave O alone.  Both halves take the same
+                // decision from the same maximum.
                 const bool bump = mt > m + kSlack;
                 const float mn = bump ? mt : m;
                 const float corr = bump ? fast_exp2(m - mn) : 1.f;
-                // O_X(kt - 1) completed before S_X(kt) did: rescale it in place
+                // O_X(kt - 1) completed before S_X(kt) did: rescale this half's 64 columns of it
                 if (kt > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 2 * kh; c < 2 * kh + 2; ++c) {
                         float ov[32];
                         tmem_ld32(o_col + 32u * c, ov);
 #pragma unroll
@@ -558,15 +677,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(o_col + 32u * c, ov);
                     }
                 }
-                // pass 2: weights 2^(s * scale - mn) (0 where masked), their sum, and P
-                // (bf16) over the first 64 columns of S: chunk c's 8 packed columns
-                // [8c, 8c + 8) lie at or below the 16 columns [16c, 16c + 16) just read
+                // pass 2: weights 2^(s * scale - mn) (0 where masked), their sum, and P (bf16)
+                // packed over the first 32 of this half's 64 S columns: chunk c's 8 packed
+                // columns lie at or below the 16 columns of the chunk just read
                 float psum = 0.f;
                 {
                     const float nb = -mn;
                     uint32_t vm = 0;
 #pragma unroll 1
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 4 * kh; c < 4 * kh + 4; ++c) {
                         float sv[16];
                         tmem_ld16(s_col + 16u * c, sv);
                         if (full) {
@@ -589,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pk[k >> 1] = *reinterpret_cast<const uint32_t *>(&pb);
                             psum += sv[k] + sv[k + 1];
                         }
-                        tmem_st8(s_col + 8u * c, pk);
+                        tmem_st8(s_col + 64u * kh + 8u * (c & 3), pk);
                     }
                     tmem_st_wait();
                 }
@@ -611,9 +730,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++no;
             tc_fence_after();
+            // the row's weight sum from the two halves (both warps of a pair have the same rows,
+            // so they take this exchange together or skip it together)
+            if (warp_valid) {
+                xsum[kh * kTile + row] = l;
+                if (!pair_sync()) {
+                    ok = false;
+                    break;
+                }
+                l += xsum[(1 - kh) * kTile + row];
+            }
             const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 2 * kh; c < 2 * kh + 2; ++c) {
                 float ov[32];
                 tmem_ld32(o_col + 32u * c, ov);
                 if (valid) {
