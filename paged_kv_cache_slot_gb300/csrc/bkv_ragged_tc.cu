@@ -95,8 +95,8 @@ constexpr int kMaxMine = 64;
 constexpr int kOffCost = kOffXsum + 2 * 2 * kTile * 4;
 constexpr int kOffHist = kOffCost + kSchedUnits * 2;
 constexpr int kOffMine = kOffHist + kBuckets * 4;
-constexpr int kOffNMine = kOffMine + kMaxMine * 4;
-constexpr int kSmemUsed = kOffNMine + 16;
+constexpr int kOffUnits = kOffMine + kMaxMine * 4;      // this CTA's units, decoded once
+constexpr int kSmemUsed = kOffUnits + kMaxMine * 48;
 constexpr int kSmemBytes = kSmemUsed + 1024;             // slack for 1024 alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
 
@@ -113,6 +113,8 @@ struct Unit {
     int32_t kend;        // keys [0, kend) may be visible to some row of the unit
     int32_t nk;          // key tiles
 };
+
+static_assert(sizeof(Unit) <= 48 && alignof(Unit) <= 16, "the shared-memory unit list holds 48 bytes per unit");
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
 
@@ -302,7 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         for (int u = threadIdx.x; u < U; u += kThreads) {
             const Unit x = unit_at(a, pre, u, T);
-            const int c = min(x.nk * (x.ntok[1] > 0 ? 3 : 2), kBuckets - 1);   // a pair costs ~1.5 singles
+            // a unit's time follows its key tiles: with two query tiles the second softmax runs
+            // beside the first, and measured pairs take about as long per key tile as singles
+            const int c = min(x.nk, kBuckets - 1);
             cost[u] = (uint16_t)c;
             atomicAdd(&hist[kBuckets - 1 - c], 1);   // bucket order = descending cost
         }
@@ -354,6 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_mine = U > blockIdx.x ? (int)((U - 1 - blockIdx.x) / grid + 1) : 0;
     }
     auto unit_id = [&](int i) -> int64_t { return lpt ? mine[i] : blockIdx.x + i * grid; };
+    // every role walks the same units: decode them once into shared memory
+    Unit *units_s = reinterpret_cast<Unit *>(smem + kOffUnits);
+    const bool cached = n_mine <= kMaxMine;
+    if (cached) {
+        for (int i = threadIdx.x; i < n_mine; i += kThreads) units_s[i] = unit_at(a, pre, unit_id(i), T);
+        __syncthreads();
+    }
+    auto unit_i = [&](int i) -> Unit { return cached ? units_s[i] : unit_at(a, pre, unit_id(i), T); };
 
     if (warp == 0 || warp == kWarpV) {
         // ================= TMA producers (warp 0: Q and K, last warp: V) =================
@@ -361,8 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t j = 0;   // key-tile sequence number in this CTA
         int uq = 0;      // units with key tiles
         for (int i = 0; i < n_mine && !*abort_flag; ++i) {
-            const int64_t u = unit_id(i);
-            const Unit x = unit_at(a, pre, u, T);
+            const Unit x = unit_i(i);
             if (x.nk == 0) continue;
             if (!is_v) {
                 if (!mbar_wait_warp(bar_qempty, (uint32_t)(uq & 1) ^ 1u, abort_flag)) break;
@@ -472,8 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(bar_sfull(xb));
             };
             for (int i = 0; ok && i < n_mine; ++i) {
-                const int64_t u = unit_id(i);
-                const Unit x = unit_at(a, pre, u, T);
+                const Unit x = unit_i(i);
                 if (x.nk == 0) continue;
                 const bool has_b = x.ntok[1] > 0;
                 ++nu[0];
@@ -544,8 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *xmax = reinterpret_cast<float *>(smem + kOffXmax) + xb * (2 * 2 * kTile);   // [half][parity][row]
         float *xsum = reinterpret_cast<float *>(smem + kOffXsum) + xb * (2 * kTile);       // [half][row]
         for (int i = 0; ok && i < n_mine; ++i) {
-            const int64_t u = unit_id(i);
-            const Unit x = unit_at(a, pre, u, T);
+            const Unit x = unit_i(i);
             const int ntok = x.ntok[xb];
             if (ntok <= 0) {      // no tile B in this unit
                 j += x.nk;
