@@ -213,9 +213,11 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
 // Merge: out = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over a stream's
 // partial slots, M = max_c m_c; 0 when no slot saw a visible key.  One CTA
 // per stream (request, KV head); each warp takes query rows warp, warp + 4,
-// ...: the lanes read the slots' (m, l) pairs in one round, turn them into
-// weights in the warp's own shared-memory strip, and then each lane sums
-// four head_dim elements over the slots with 16-byte loads.
+// ...: the lanes read the slots' (m, l) pairs in one round and keep the
+// weights (up to 32 slots: lane k slot k; beyond, in the warp's own shared-
+// memory strip), and then each lane sums four head_dim elements over the
+// slots with 16-byte loads, eight slots (up to 8 slots and head_dim 128:
+// all of them) per round of loads.
 // The stream's slots follow from the context lengths alone (the stream-K
 // split of the tensor-core kernel), which the partition kernel does not
 // write: they are read and the slot range computed before the grid-
@@ -284,38 +286,56 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
             if (a.lse && lane == 0)
                 a.lse[orow] = (M == -INFINITY || !(lsum > 0.f)) ? -INFINITY : (M + log2f(lsum)) * kLn2;
         };
-        if (nch <= 8 && a.D == 128) {
-            // few slots: every load of the row (each lane's slot (m, l) and its four
-            // head_dim elements of every slot) is issued in one round
+        if (nch <= 32 && (a.D & 3) == 0) {
+            // up to 32 slots: lane k reads slot k's (m, l) and keeps its weight; the partials
+            // are read eight slots at a time, the first eight issued together with the
+            // (m, l) loads (they do not depend on the weights), so up to 8 slots and head_dim
+            // 128 take one round of loads
+            // every lane runs every round (the shuffles need the whole warp); lanes past head_dim / 4
+            // load and store nothing
             const float2 ml = lane < nch
                                   ? *reinterpret_cast<const float2 *>(a.ws_ml + ((unit0 + lane) * a.nq + row) * 2)
                                   : make_float2(-INFINITY, 0.f);
-            float4 v[8];
+            float wl = 0.f, iv = 0.f;
+            for (int base = 0; base < a.D / 4; base += 32) {
+                const int d4 = base + lane;
+                const bool act = d4 < a.D / 4;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c = 0; c < nch; c += 8) {
+                    float4 v[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k < nch) v[k] = *reinterpret_cast<const float4 *>(a.ws_o + ((unit0 + k) * a.nq + row) * a.D + 4 * lane);
-            float M = ml.x;
+                    for (int k = 0; k < 8; ++k)
+                        if (act && c + k < nch)
+                            v[k] = *reinterpret_cast<const float4 *>(a.ws_o + ((unit0 + c + k) * a.nq + row) * a.D +
+                                                                     4 * d4);
+                    if (base == 0 && c == 0) {
+                        float M = ml.x;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            const float wl = (M == -INFINITY || lane >= nch) ? 0.f : exp2f(ml.x - M);
-            const float lsum = warp_sum(wl * ml.y);
-            const float iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : a.v_scale / lsum;
-            put_lse(M, lsum);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                        wl = (M == -INFINITY || lane >= nch) ? 0.f : exp2f(ml.x - M);
+                        const float lsum = warp_sum(wl * ml.y);
+                        iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : a.v_scale / lsum;
+                        put_lse(M, lsum);
+                    }
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (k < nch) {
-                    const float wgt = __shfl_sync(0xffffffffu, wl, k);
-                    acc.x = fmaf(wgt, v[k].x, acc.x);
-                    acc.y = fmaf(wgt, v[k].y, acc.y);
-                    acc.z = fmaf(wgt, v[k].z, acc.z);
-                    acc.w = fmaf(wgt, v[k].w, acc.w);
+                    for (int k = 0; k < 8; ++k) {
+                        const float wgt = __shfl_sync(0xffffffffu, wl, (c + k) & 31);
+                        if (act && c + k < nch) {
+                            acc.x = fmaf(wgt, v[k].x, acc.x);
+                            acc.y = fmaf(wgt, v[k].y, acc.y);
+                            acc.z = fmaf(wgt, v[k].z, acc.z);
+                            acc.w = fmaf(wgt, v[k].w, acc.w);
+                        }
+                    }
+                }
+                if (act) {
+                    store_out(out + 4 * d4 + 0, acc.x * iv);
+                    store_out(out + 4 * d4 + 1, acc.y * iv);
+                    store_out(out + 4 * d4 + 2, acc.z * iv);
+                    store_out(out + 4 * d4 + 3, acc.w * iv);
                 }
             }
-            store_out(out + 4 * lane + 0, acc.x * iv);
-            store_out(out + 4 * lane + 1, acc.y * iv);
-            store_out(out + 4 * lane + 2, acc.z * iv);
-            store_out(out + 4 * lane + 3, acc.w * iv);
+            if (nch == 0) put_lse(-INFINITY, 0.f);
             continue;
         }
         float M = -INFINITY;
