@@ -257,17 +257,17 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
         all = red[0][0] + red[0][1] + red[0][2] + red[0][3];
         before = red[1][0] + red[1][1] + red[1][2] + red[1][3];
         const int64_t Ts = sk_tiles(a, __ldg(a.ctx + r));   // tiles of the stream
-        const int64_t TT = (int64_t)a.H_kv * all;
+        const int64_t TP = all;
         if (Ts > 0 && L > 0) {
-            // stream s has Ts tiles starting at global tile S; CTA k of geff =
-            // min(sk_grid, TT) covers [k TT / geff, (k + 1) TT / geff) and writes
-            // slots 2 (k + s) and 2 (k + s) + 1 for its overlap with s
-            const int64_t geff = TT < (int64_t)a.sk_grid ? TT : (int64_t)a.sk_grid;
-            const int64_t S = (int64_t)a.H_kv * before + g * Ts;
-            const int64_t k0 = ((S + 1) * geff - 1) / TT;
-            const int64_t k1 = ((S + Ts) * geff - 1) / TT;
-            nch = (int)(2 * (k1 - k0 + 1));
-            unit0 = 2 * (k0 + rg);
+            // request r's Ts position tiles start at tile `before`; of the P = sk_grid /
+            // H_kv groups, group q of peff = min(P, TP) covers [q TP / peff, (q + 1) TP /
+            // peff), and its CTA for head g writes slots 2 (g (P + R) + q + r) + {0, 1}
+            const int64_t P = a.sk_grid / a.H_kv;
+            const int64_t peff = TP < P ? TP : P;
+            const int64_t q0 = ((before + 1) * peff - 1) / TP;
+            const int64_t q1 = ((before + Ts) * peff - 1) / TP;
+            nch = (int)(2 * (q1 - q0 + 1));
+            unit0 = 2 * ((int64_t)g * (P + a.num_reqs) + q0 + r);
         }
     } else {
         nch = L > 0 ? (int)ceil_div<int32_t>(L, a.chunk) * a.parts : 0;
@@ -439,10 +439,11 @@ bool make_decode_plan(int32_t num_reqs, int32_t q_len, int32_t num_q_heads, int3
     plan->chunk = (int32_t)chunk;
     plan->n_chunks = (int32_t)n_chunks;
     plan->nq = (int32_t)nq;
-    plan->sk_grid = (int32_t)sms;
+    // the tensor-core kernel's grid: whole groups of one CTA per KV head
+    plan->sk_grid = (int32_t)(num_kv_heads <= sms ? (sms / num_kv_heads) * num_kv_heads : num_kv_heads);
     plan->header_bytes = 256;
     const int64_t slots_generic = units * n_chunks;
-    const int64_t slots_sk = 2 * (sms + units);
+    const int64_t slots_sk = 2 * (plan->sk_grid + units);
     const int64_t slots = slots_generic > slots_sk ? slots_generic : slots_sk;
     const int64_t prows = slots * nq;
     const int64_t o_bytes = ceil_div<int64_t>(prows * head_dim * 4, 256) * 256;

@@ -10,17 +10,18 @@
 // partials of each stream.
 //
 // Design (sm_103a):
-// * Stream-K schedule.  The streams' tiles (ceil(len / 128) per request and
-//   KV head, requests in order, heads in order) are laid end to end; the
-//   persistent CTA k (one per SM) takes the global tiles
-//   [k * TT / grid, (k + 1) * TT / grid), so every SM gets the same number
-//   of tiles to within one, whatever the mix of lengths (grid = min(SMs,
-//   TT), so that no participating CTA has an empty range).  Each overlap of a
-//   CTA range with a stream is a unit; the i-th unit along the sequence is
-//   the overlap of CTA k and stream s with k + s increasing by at least one
-//   per step, so unit (k, s) writes partial slots 2 (k + s) and
-//   2 (k + s) + 1 (one per softmax warpgroup), and stream s's slots are the
-//   contiguous range the merge recomputes from the context lengths.
+// * Head-grouped stream-K schedule.  The persistent grid (one CTA per SM)
+//   is P groups of H_kv CTAs.  The requests' position tiles (ceil(len / 128)
+//   per request, requests in order) are laid end to end and group q takes
+//   [q * TP / P, (q + 1) * TP / P) of them, CTA g of the group for KV head
+//   g, so every SM gets the same number of tiles to within one whatever the
+//   mix of lengths, and the H_kv CTAs of a group read the same positions of
+//   all heads at the same time: whole cache rows (a row holds every head of
+//   one position), where a CTA alone would take a 128- or 256-byte piece
+//   of each row.  Each overlap of a CTA range with a stream (request,
+//   head) is a unit; it writes two partial slots (one per softmax
+//   warpgroup), and a stream's slots are the contiguous range the merge
+//   recomputes from the context lengths.
 // * Warp roles: warp 0 gathers K tiles (and Q), the last warp gathers V
 //   tiles, warp 1 issues tcgen05.mma from one thread and owns the TMEM
 //   allocation, and two warpgroups (warps 2..5 and 6..9) run the softmax and
@@ -54,11 +55,12 @@
 //   K . Q^T runs as kind::f8f6f4 on the codes straight from TMA, with q split
 //   beforehand (q_split_e4m3_kernel) into two E4M3 parts whose sum is the
 //   query row divided by a power of two, so the products are exact; the
-//   softmax multiplies each column back.  P V runs on f16: the softmax
-//   warpgroup that owns a tile widens its E4M3 V rows to f16 (exact) into its
-//   own V slot before it reads S, and writes P as f16.  Widening every K and
-//   V element on chip was measured slower (the conversions, not the bytes,
-//   bound the kernel), which is why K is never widened.
+//   softmax multiplies each column back.  O^T = V^T . P^T runs as
+//   kind::f8f6f4 too, with V^T read MN-major straight from the E4M3 TMA
+//   tile (one 128-code span per row) and P^T as two E4M3 parts, P 2^8 =
+//   hi + lo, accumulated in one TMEM tile: the softmax never touches V.
+//   (Widening V to f16 in the softmax warpgroups, the earlier design, made
+//   the per-tile chain longer than the halved load time.)
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -84,20 +86,22 @@ constexpr int kN = 16;                // query rows per MMA (padded)
 #define BKV_V_STAGES 3
 #endif
 static_assert(BKV_K_STAGES >= 2 && BKV_K_STAGES <= 3, "the 8-entry mask ring assumes at most 3 K slots");
-// FP8 caches: slots of the E4M3 K ring (read by the MMAs as loaded) and of
-// the E4M3 V ring (widened to f16 by the softmax warpgroups)
+// FP8 caches: slots of the E4M3 K and V rings (16 KB each, read by the MMAs as loaded)
 #ifndef BKV_F8_K_STAGES
-#define BKV_F8_K_STAGES 4
+#define BKV_F8_K_STAGES 5
 #endif
-#ifndef BKV_F8_STAGES
-#define BKV_F8_STAGES 4
+#ifndef BKV_F8_V_STAGES
+#define BKV_F8_V_STAGES 6
 #endif
 static_assert(BKV_F8_K_STAGES >= 2 && BKV_F8_K_STAGES <= 5, "the 8-entry mask ring assumes at most 5 K slots");
+// FP8 caches: the weights enter the P.V MMA as p 2^kF8PExp (p <= 1, so at most
+// 256 < 448, the largest finite E4M3 value); the partial output takes it back
+constexpr int kF8PExp = 8;
 constexpr int kHalfBytes = kTile * 128;          // 128 rows x 64 bf16 (128 B): one head_dim half
 constexpr int kTileBytes = 2 * kHalfBytes;       // K or V tile: 32 KB
 constexpr int kT8Bytes = kTile * 128;            // an FP8 K or V tile as loaded: 128 rows x 128 codes, 16 KB
-constexpr int kQBytes = 2 * kN * 128;            // 16 rows x 128 B x 2 halves: 4 KB
-constexpr int kPBytes = 2 * kN * 128;            // 16 rows x 128 positions (2 x 64) bf16: 4 KB
+constexpr int kQBytes = 2 * kN * 128;            // 16 rows x 128 B x 2 halves (FP8: 2 parts): 4 KB
+constexpr int kPBytes = 2 * kN * 128;            // 16 rows x 128 positions, 2 x 64 bf16 or 2 E4M3 parts: 4 KB
 constexpr int kWarpV = 10;                       // the V producer's warp
 constexpr int kTmemCols = 64;                    // S x2 (16 cols each) + O x2
 constexpr int kTimeoutErr = 1 << 24;
@@ -105,27 +109,25 @@ constexpr int kMaxReqs = 2048;                   // requests the in-kernel tile 
 constexpr int kWinBlocks = 128;                  // table entries a producer caches per window
 
 // Shared-memory layout and role counts (offsets from a 1024-aligned base).
-// kF8: FP8 caches.  S = K Q^T runs on E4M3 operands (kind::f8f6f4): K tiles
-// straight from TMA, q as two E4M3 parts prepared by q_split_e4m3_kernel.
-// P V runs on f16 operands: each softmax warpgroup widens its tiles' E4M3 V
-// rows to f16 (exactly) into its own V slot and writes P as f16.
+// kF8: FP8 caches.  Both MMAs run on E4M3 operands (kind::f8f6f4): K and V
+// tiles straight from TMA, q as two E4M3 parts prepared by
+// q_split_e4m3_kernel, P as two E4M3 parts written by the softmax.
 template <bool kF8>
 struct Cfg {
     static constexpr int kThreads = 352;                 // K producer, MMA, two softmax warpgroups, V producer
     static constexpr int kKStages = kF8 ? BKV_F8_K_STAGES : BKV_K_STAGES;
-    static constexpr int kVStages = kF8 ? 2 : BKV_V_STAGES;   // FP8: one f16 V slot per softmax warpgroup
-    static constexpr int k8Stages = kF8 ? BKV_F8_STAGES : 0;  // E4M3 V slots
+    static constexpr int kVStages = kF8 ? BKV_F8_V_STAGES : BKV_V_STAGES;
     static constexpr int kKSlot = kF8 ? kT8Bytes : kTileBytes;
+    static constexpr int kVSlot = kKSlot;
     static constexpr int kOffK = 0;                                  // kKStages K slots
     static constexpr int kOffV = kOffK + kKStages * kKSlot;          // kVStages V slots
-    static constexpr int kOffV8 = kOffV + kVStages * kTileBytes;     // k8Stages E4M3 V slots
-    static constexpr int kOffQ = kOffV8 + k8Stages * kT8Bytes;
+    static constexpr int kOffQ = kOffV + kVStages * kVSlot;
     static constexpr int kOffP = kOffQ + 2 * kQBytes;
     static constexpr int kOffMask = kOffP + 2 * kPBytes;             // 8 words: loaded segments per tile (ring)
     static constexpr int kOffRedMax = kOffMask + 64;                 // [warpgroup][2][16 rows][4 warps] floats
     static constexpr int kOffRedSum = kOffRedMax + 4 * kN * 4 * 4;   // [warpgroup][16 rows][4 warps] floats
     static constexpr int kOffBar = kOffRedSum + 2 * kN * 4 * 4;      // barriers (8 B each)
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 8 + 2 * k8Stages;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 8;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffPre = kOffAbort + 4;                    // [kMaxReqs + 1] tile prefix per request
@@ -138,9 +140,8 @@ struct Cfg {
     static constexpr int kLensPerThread = (kMaxReqs + kThreads - 1) / kThreads;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
     static_assert(kOffEnt % 16 == 0, "entry buffers must stay aligned");
-    static_assert(kOffV % 1024 == 0 && kOffV8 % 1024 == 0 && kOffQ % 1024 == 0, "swizzled tiles need 1 KB alignment");
+    static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1 KB alignment");
     static_assert(kWarpV == kThreads / 32 - 1, "warp roles");
-    static_assert(!kF8 || kVStages == 2, "FP8: each softmax warpgroup widens its tiles' V into its own slot");
 };
 
 // The first NQ accumulator columns of this thread's TMEM lane.
@@ -189,7 +190,7 @@ __device__ void schedule_loads(const DecodeArgs &a, int32_t *pre, uint8_t *lrem,
     }
     const uint4 z = make_uint4(0, 0, 0, 0);
     uint4 *v = reinterpret_cast<uint4 *>(smem + C::kOffV);
-    for (int i = threadIdx.x; i < C::kVStages * kTileBytes / 16; i += kThreads) v[i] = z;
+    for (int i = threadIdx.x; i < C::kVStages * C::kVSlot / 16; i += kThreads) v[i] = z;
 #pragma unroll
     for (int i = 0; i < kLensPerThread; ++i) {
         const int r = threadIdx.x + i * kThreads;
@@ -253,56 +254,69 @@ __device__ void scan_prefix(const DecodeArgs &a, int32_t *pre, int32_t *tot) {
 // One unit: tiles [lo, hi) of stream s = r * H_kv + g, counted from the
 // stream's first tile f (0, or the tile holding the sliding window's first
 // visible key): positions [start, cend) with start = (f + lo) * 128, cend =
-// min((f + hi) * 128, L).
+// min((f + hi) * 128, L).  Its partials go to slots slot2 and slot2 + 1.
 struct Unit {
     int r, g;
-    int64_t s;
+    int64_t s, slot2;
     int32_t L, start, cend, ntiles;
 };
 
-// Walks this CTA's units in order.
+// Walks this CTA's units in order.  The grid is P groups of H_kv CTAs; the
+// requests' position tiles (pre[r] .. pre[r + 1] for request r) are laid end
+// to end and group q takes [q TP / Peff, (q + 1) TP / Peff) of them (TP
+// tiles in all, Peff = min(P, TP)), CTA g of the group for KV head g.  The
+// H_kv CTAs of a group thus read the same positions of all heads at the
+// same time, i.e. whole cache rows (one row holds every head of a
+// position).  Unit (group q, request r, head g) writes slots
+// 2 (g (P + R) + q + r) + {0, 1}: q + r grows by at least one from one unit
+// of a head to the next, so the slots are distinct, and a stream's slots
+// are the contiguous range the merge recomputes from the context lengths.
 struct StreamK {
     const int32_t *pre;
     const uint8_t *lrem;
-    int n, H;
-    int64_t t, t1;   // next global tile, end of this CTA's range
+    int n, H, q, g;
+    int64_t t, t1;   // next position tile, end of this CTA's range
+    int64_t hbase;   // g (P + R): this head's slot block
     int r;
     __device__ void init(const DecodeArgs &a, const int32_t *pre_, const uint8_t *lrem_) {
         pre = pre_;
         lrem = lrem_;
         n = a.num_reqs;
         H = a.H_kv;
-        // split over min(grid, TT) CTAs so every participating CTA has at
+        const int P = (int)gridDim.x / H;
+        q = (int)blockIdx.x / H;
+        g = (int)blockIdx.x - q * H;
+        hbase = (int64_t)g * (P + n);
+        // split over min(P, TP) groups so every participating CTA has at
         // least one tile (the merge recomputes the slots with the same rule)
-        const int64_t TT = (int64_t)H * pre[n];
-        const int64_t geff = TT < (int64_t)gridDim.x ? TT : (int64_t)gridDim.x;
-        if ((int64_t)blockIdx.x < geff) {
-            t = TT * blockIdx.x / geff;
-            t1 = TT * (blockIdx.x + 1) / geff;
+        const int64_t TP = pre[n];
+        const int64_t peff = TP < (int64_t)P ? TP : (int64_t)P;
+        if ((int64_t)q < peff) {
+            t = TP * q / peff;
+            t1 = TP * (q + 1) / peff;
         } else {
-            t = t1 = TT;
+            t = t1 = TP;
         }
         // first request whose tiles end after t
         int lo = 0, hi = n;   // invariant: answer in [lo, hi]
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
-            if ((int64_t)H * pre[mid + 1] > t) hi = mid;
+            if ((int64_t)pre[mid + 1] > t) hi = mid;
             else lo = mid + 1;
         }
         r = lo;
     }
     __device__ bool next(const DecodeArgs &a, Unit &x) {
         if (t >= t1) return false;
-        while (r < n && (int64_t)H * pre[r + 1] <= t) ++r;
-        const int64_t Tr = pre[r + 1] - pre[r];
-        const int64_t S0 = (int64_t)H * pre[r];
-        const int g = (int)((t - S0) / Tr);
-        const int64_t S = S0 + g * Tr;
+        while (r < n && (int64_t)pre[r + 1] <= t) ++r;
+        const int64_t S = pre[r];
+        const int64_t Tr = pre[r + 1] - S;
         const int64_t lo = t - S;
         const int64_t hi = (t1 - S) < Tr ? (t1 - S) : Tr;
         x.r = r;
         x.g = g;
         x.s = (int64_t)r * H + g;
+        x.slot2 = 2 * (hbase + q + r);
         int64_t f = 0;
         if (a.window > 0) {
             // the tile count no longer gives the length: read it (clamped) again
@@ -370,78 +384,6 @@ __device__ __forceinline__ bool reduced_writer(int lane) {
     return (lane & ((1 << (5 - k)) - 1)) == 0;
 }
 
-// E4M3 codes to f16 for the MMAs.  Two ways, both exact:
-// * BKV_F8_HWCVT: the hardware conversion (one instruction per two codes),
-//   giving the codes' values;
-// * otherwise byte-parallel integer operations on four codes at a time,
-//   giving the values times 2^-8: with a code's exponent field e (4 bits) and
-//   mantissa m (3 bits), the f16 with sign bit 15, exponent field e and
-//   mantissa m << 7 is 2^(e-15) (1 + m/8) for e > 0 and the subnormal
-//   m 2^-17 for e = 0, i.e. the E4M3 value 2^(e-7) (1 + m/8), resp. m 2^-9,
-//   times 2^-8.  Its high byte is sign | (e m) >> 1 and its low byte
-//   (m & 1) << 7; the NaN codes (magnitude 0x7F) also set high-byte bit 6,
-//   which makes an f16 NaN.
-// kF8Unscale is the factor the scores and the output take back (exactly).
-#ifndef BKV_F8_HWCVT
-#define BKV_F8_HWCVT 1
-#endif
-constexpr float kF8Unscale = BKV_F8_HWCVT ? 1.f : 256.f;
-
-
-// Four codes (byte k = code k) -> four f16 in two words (codes 0, 1 in a; 2, 3 in b).
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &a, uint32_t &b) {
-#if BKV_F8_HWCVT
-    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
-    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-    a = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-    b = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-#else
-    const uint32_t mag = w & 0x7F7F7F7Fu;
-    const uint32_t nan7 = (mag + 0x01010101u) & 0x80808080u;          // 0x80 in the bytes with mag 0x7F
-    const uint32_t hb = (((mag | nan7) >> 1) & 0x7F7F7F7Fu) | (w & 0x80808080u);
-    const uint32_t lb = (w << 7) & 0x80808080u;
-    a = __byte_perm(lb, hb, 0x5140);   // [lb0 hb0 lb1 hb1]
-    b = __byte_perm(lb, hb, 0x7362);   // [lb2 hb2 lb3 hb3]
-#endif
-}
-
-// Row r of an E4M3 tile as TMA leaves it (128-byte rows, 16-byte chunk c of
-// row r at chunk c ^ (r & 7)) into row r of an f16 tile in the MMA layout
-// (two head_dim halves of 128-byte rows, the same chunk swizzle): code chunk
-// c (head_dim 16c .. 16c + 15) becomes f16 chunks 2(c & 3), 2(c & 3) + 1 of
-// half c / 4.  Conflict-free when consecutive lanes take consecutive rows.
-__device__ __forceinline__ void widen_row_e4m3(const uint8_t *__restrict__ src_tile, uint8_t *__restrict__ dst_tile,
-                                               int r) {
-    const uint8_t *src = src_tile + r * 128;
-    const int sw = r & 7;
-    // all eight loads first: the stores could otherwise not pass the next load
-    uint4 w[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) w[c] = *reinterpret_cast<const uint4 *>(src + ((c ^ sw) << 4));
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint4 lo, hi;
-        e4m3x4_to_f16x4(w[c].x, lo.x, lo.y);
-        e4m3x4_to_f16x4(w[c].y, lo.z, lo.w);
-        e4m3x4_to_f16x4(w[c].z, hi.x, hi.y);
-        e4m3x4_to_f16x4(w[c].w, hi.z, hi.w);
-        uint8_t *dst = dst_tile + (c >> 2) * kHalfBytes + r * 128;
-        const int c2 = 2 * (c & 3);
-        *reinterpret_cast<uint4 *>(dst + ((c2 ^ sw) << 4)) = lo;
-        *reinterpret_cast<uint4 *>(dst + (((c2 + 1) ^ sw) << 4)) = hi;
-    }
-}
-
-// Row r of a widened tile as zeros (a row no load wrote: P is 0 there, and
-// 0 times stale bits must not be NaN).
-__device__ __forceinline__ void zero_row_f16(uint8_t *dst_tile, int r) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        *reinterpret_cast<uint4 *>(dst_tile + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(dst_tile + kHalfBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-    }
-}
-
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -453,7 +395,6 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
     constexpr int kThreads = C::kThreads;
     constexpr int kKStages = C::kKStages;
     constexpr int kVStages = C::kVStages;
-    constexpr int k8Stages = C::k8Stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -482,9 +423,6 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
     auto bar_group = [&](int k) { return bar0 + 8u * (kB + 10 + k); };   // four warps of warpgroup k
     // "loaded segments" word of tile j: mask_words[j & 7], published with bar_mask(j & 7)
     auto bar_mask = [&](int m) { return bar0 + 8u * (kB + 12 + m); };
-    // E4M3 V ring (kF8): V producer -> the softmax warpgroup that widens the tile
-    auto bar_v8full = [&](int s) { return bar0 + 8u * (kB + 20 + s); };
-    auto bar_v8empty = [&](int s) { return bar0 + 8u * (kB + 20 + k8Stages + s); };
     const uint32_t sm_k = sbase + C::kOffK;
     const uint32_t sm_v = sbase + C::kOffV;
     const uint32_t sm_q = sbase + C::kOffQ;
@@ -496,14 +434,9 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
             mbar_init(bar_kfull(s), 1);
             mbar_init(bar_kempty(s), 1);
         }
-        // with FP8 caches the f16 V slots are filled by the four warps of a softmax warpgroup
         for (int s = 0; s < kVStages; ++s) {
-            mbar_init(bar_vfull(s), kF8 ? 4u : 1u);
+            mbar_init(bar_vfull(s), 1);
             mbar_init(bar_vempty(s), 1);
-        }
-        for (int s = 0; s < k8Stages; ++s) {
-            mbar_init(bar_v8full(s), 1);
-            mbar_init(bar_v8empty(s), 4);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_qfull(b), 1);
@@ -647,12 +580,10 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 }
             }
             for (int jt = cur.t0; jt < cur.t1; ++jt, ++j) {
-                // FP8 caches: V tiles go to the E4M3 V ring, which the softmax
-                // warpgroups drain; K tiles go to the K ring the MMAs read
-                const int nst = (kF8 && is_v) ? k8Stages : (is_v ? kVStages : kKStages);
+                const int nst = is_v ? kVStages : kKStages;
                 const int s = (int)(j % nst);
-                const uint32_t bar_e = (kF8 && is_v) ? bar_v8empty(s) : (is_v ? bar_vempty(s) : bar_kempty(s));
-                const uint32_t bar_f = (kF8 && is_v) ? bar_v8full(s) : (is_v ? bar_vfull(s) : bar_kfull(s));
+                const uint32_t bar_e = is_v ? bar_vempty(s) : bar_kempty(s);
+                const uint32_t bar_f = is_v ? bar_vfull(s) : bar_kfull(s);
                 if (!mbar_wait_warp(bar_e, (uint32_t)((j / nst) & 1) ^ 1u, abort_flag)) break;
                 const int32_t ts = x.start + jt * kTile;
                 // lane i handles block segment i of the tile
@@ -694,8 +625,7 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     const int z = (int)row0;
                     if constexpr (kF8) {
                         // one box of seg_rows rows x 128 codes (the whole head_dim)
-                        const uint32_t dst = sbase + (is_v ? C::kOffV8 : C::kOffK) + s * kT8Bytes +
-                                             lane * seg_rows * 128;
+                        const uint32_t dst = (is_v ? sm_v : sm_k) + s * kT8Bytes + lane * seg_rows * 128;
                         tma_load_3d(dst, map, bar_f, 0, x.g, z);
                     } else {
                         const uint32_t dst = (is_v ? sm_v : sm_k) + s * kTileBytes + lane * seg_rows * 128;
@@ -720,8 +650,8 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
     } else if (warp == 1) {
         // ================= MMA issuer (one thread) =================
         if (lane == 0) {
-            // K (K-major) x Q (K-major); V^T (MN-major) x P (K-major).  FP8 caches: S on E4M3
-            // operands (the descriptor's E4M3 type codes are 0, as f16's), P V on f16 operands
+            // K (K-major) x Q (K-major); V^T (MN-major) x P (K-major).  FP8 caches: both on
+            // E4M3 operands (the descriptor's E4M3 type codes are 0, as f16's)
             constexpr uint32_t kIdescS = kF8 ? idesc_f16(128, kN, 0, 0) : idesc_bf16(128, kN, 0, 0);
             constexpr uint32_t kIdescO = kF8 ? idesc_f16(128, kN, 1, 0) : idesc_bf16(128, kN, 1, 0);
             int64_t j = 0;
@@ -735,14 +665,29 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     !mbar_wait(bar_pfull(b), (uint32_t)((jp >> 1) & 1), abort_flag))
                     return false;
                 tc_fence_after();
-                const uint32_t v_base = sm_v + stage * kTileBytes;
                 const uint32_t p_base = sm_p + b * kPBytes;
                 const uint32_t d_tmem = tmem + 32u + 16u * b;
+                if constexpr (kF8) {
+                    // O^T = V^T (E4M3 codes, MN-major: a row's 128 codes are one 128-byte
+                    // span, 8-row groups 1024 bytes apart) . (P_hi + P_lo)^T, 32 positions
+                    // per step
+                    const uint32_t v_base = sm_v + stage * kT8Bytes;
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint64_t adesc = sdesc(v_base + kk * 2048, kHalfBytes, 1024);
-                    const uint64_t bdesc = sdesc(p_base + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
-                    mma_bf16(d_tmem, adesc, bdesc, kIdescO, kk > 0);
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 32; ++kk) {
+                            const uint64_t adesc = sdesc(v_base + kk * 4096, 16, 1024);
+                            const uint64_t bdesc = sdesc(p_base + part * (kN * 128) + kk * 32, 16, 1024);
+                            mma_f8(d_tmem, adesc, bdesc, kIdescO, (part | kk) > 0);
+                        }
+                } else {
+                    const uint32_t v_base = sm_v + stage * kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint64_t adesc = sdesc(v_base + kk * 2048, kHalfBytes, 1024);
+                        const uint64_t bdesc = sdesc(p_base + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+                        mma_bf16(d_tmem, adesc, bdesc, kIdescO, kk > 0);
+                    }
                 }
                 mma_commit(bar_ofull(b));
                 mma_commit(bar_vempty(stage));
@@ -810,9 +755,10 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         // 2 (CTA + stream) + k of every unit.
         const int wg = (warp - 2) >> 2;
         // FP8 caches: query row i entered the S MMA divided by qexp[i] (a power of two),
-        // taken back per column below; the values may enter the P.V MMA as 2^-8 times
-        // theirs (kF8Unscale), taken back at the partial output
+        // taken back per column below; the weights enter the P.V MMA and the row sums
+        // as p 2^kF8PExp, taken back at the partial output
         const float s_scale = a.scale_log2;
+        constexpr float kOutScale = kF8 ? 1.f / (float)(1 << kF8PExp) : 1.f;
         const int row = 32 * (warp & 3) + lane;          // TMEM lane: position in tile / head_dim row
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const int wq = warp & 3;
@@ -831,9 +777,11 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         };
         // This thread's byte offset in the P^T operand (K-major, 128-byte
         // swizzle): position `row`, query row n adds n * 128 and swizzles the
-        // 16-byte chunk index with n & 7.
-        const int p_row_off = (row >> 6) * (kN * 128) + (row & 7) * 2;
-        const int p_chunk = (row & 63) >> 3;
+        // 16-byte chunk index with n & 7.  bf16: positions 64 h .. 64 h + 63
+        // form block h of 16 rows x 128 bytes; E4M3: one block of 128
+        // positions per part (hi, then lo).
+        const int p_row_off = kF8 ? (row & 15) : (row >> 6) * (kN * 128) + (row & 7) * 2;
+        const int p_chunk = kF8 ? (row >> 4) : (row & 63) >> 3;
         const int red_row = reduced_row<NQ>(lane);
         const bool red_writer = reduced_writer<NQ>(lane);
         float *my_red_sum = red_sum + wg * (kN * 4);
@@ -867,33 +815,6 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 const int sv_slot = (int)(j % kVStages);
                 const int b = wg;
                 const uint32_t par = (uint32_t)((j >> 1) & 1);
-                // FP8: widen this tile's E4M3 V rows into this warpgroup's V slot (j % 2 == wg;
-                // its previous P.V, two tiles back, completed before that tile's O update),
-                // zeros where nothing was loaded or past the end.  Done before the wait for S
-                // (measured faster than after writing P).
-                auto widen_v = [&]() -> bool {
-                    const int s8 = (int)(j % k8Stages);
-                    if (!mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag) ||
-                        !mbar_wait_warp(bar_v8full(s8), (uint32_t)((j / k8Stages) & 1), abort_flag))
-                        return false;
-                    const int32_t vpos = x.start + jt * kTile + row;
-                    uint8_t *vdst = smem + C::kOffV + sv_slot * kTileBytes;
-                    if (((mask_words[j & 7] >> (row >> seg_shift)) & 1u) && vpos < x.cend)
-                        widen_row_e4m3(smem + C::kOffV8 + s8 * kT8Bytes, vdst, row);
-                    else
-                        zero_row_f16(vdst, row);
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(bar_vfull(sv_slot));
-                        mbar_arrive(bar_v8empty(s8));
-                    }
-                    return true;
-                };
-                if (kF8 && !widen_v()) {
-                    ok = false;
-                    break;
-                }
                 if (!mbar_wait_warp(bar_sfull(b), par, abort_flag) ||
                     !mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag)) {
                     ok = false;
@@ -919,42 +840,62 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 }
                 float corr[NQ];
                 uint8_t *pgen = smem + C::kOffP + b * kPBytes + p_row_off;
-#pragma unroll
-                for (int n = 0; n < NQ; ++n) {
+                // new running max, rescale factor and weight of each query row, then
+                // P as the MMA's operand type; the row sums take the rounded weights
+                auto weight = [&](int n) -> float {
                     const float4 t4 = *reinterpret_cast<const float4 *>(rm + n * 4);
                     const float mt = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
                     const float mn = fmaxf(mrun[n], mt);
                     corr[n] = (mn == -INFINITY) ? 1.f : fast_exp2(mrun[n] - mn);
                     mrun[n] = mn;
-                    const float p = (sv[n] == -INFINITY) ? 0.f : fast_exp2(sv[n] - mn);
-                    // P as the MMA's operand type; the sum takes the rounded weights
-                    if constexpr (kF8) {
-                        const __half pv = __float2half_rn(p);
-                        lsum[n] = fmaf(lsum[n], corr[n], __half2float(pv));
-                        *reinterpret_cast<__half *>(pgen + n * 128 + ((p_chunk ^ (n & 7)) << 4)) = pv;
-                    } else {
-                        const __nv_bfloat16 pbv = __float2bfloat16_rn(p);
+                    return (sv[n] == -INFINITY) ? 0.f : fast_exp2(sv[n] - mn);
+                };
+                if constexpr (kF8) {
+                    // p 2^8 = hi + lo, two E4M3 codes per weight, two query rows per
+                    // conversion: hi is p 2^8 to 4 significant bits, lo the remainder to
+                    // 4 more (absolute error at most 2^-10 in p 2^8)
+#pragma unroll
+                    for (int n = 0; n < NQ; n += 2) {
+                        const float p0 = weight(n), p1 = weight(n + 1);
+                        const float2 x2 = make_float2(p0 * (float)(1 << kF8PExp), p1 * (float)(1 << kF8PExp));
+                        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(x2, __NV_SATFINITE, __NV_E4M3);
+                        const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+                        const __nv_fp8x2_storage_t lo =
+                            __nv_cvt_float2_to_fp8x2(make_float2(x2.x - hf.x, x2.y - hf.y), __NV_SATFINITE, __NV_E4M3);
+                        const float2 lf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)));
+                        lsum[n] = fmaf(lsum[n], corr[n], hf.x + lf.x);
+                        lsum[n + 1] = fmaf(lsum[n + 1], corr[n + 1], hf.y + lf.y);
+                        uint8_t *d0 = pgen + n * 128 + ((p_chunk ^ (n & 7)) << 4);
+                        uint8_t *d1 = pgen + (n + 1) * 128 + ((p_chunk ^ ((n + 1) & 7)) << 4);
+                        d0[0] = (uint8_t)(hi & 0xFF);
+                        d1[0] = (uint8_t)(hi >> 8);
+                        d0[kN * 128] = (uint8_t)(lo & 0xFF);
+                        d1[kN * 128] = (uint8_t)(lo >> 8);
+                    }
+                } else {
+#pragma unroll
+                    for (int n = 0; n < NQ; ++n) {
+                        const __nv_bfloat16 pbv = __float2bfloat16_rn(weight(n));
                         lsum[n] = fmaf(lsum[n], corr[n], __bfloat162float(pbv));
                         *reinterpret_cast<__nv_bfloat16 *>(pgen + n * 128 + ((p_chunk ^ (n & 7)) << 4)) = pbv;
                     }
                 }
                 // V rows that were loaded but lie past the end must be zero for P.V
-                // (after the V tile has landed; with FP8 caches the converter writes
-                // zeros for every row it does not convert)
-                const bool zero_row = !kF8 && loaded && pos >= x.cend;
+                // (after the V tile has landed)
+                const bool zero_row = loaded && pos >= x.cend;
                 if (__any_sync(0xffffffffu, zero_row) &&
                     !mbar_wait_warp(bar_vfull(sv_slot), (uint32_t)((j / kVStages) & 1), abort_flag)) {
                     ok = false;
                     break;
                 }
                 if (zero_row) {
-                    uint4 *vrow0 = reinterpret_cast<uint4 *>(smem + C::kOffV + sv_slot * kTileBytes + row * 128);
-                    uint4 *vrow1 =
-                        reinterpret_cast<uint4 *>(smem + C::kOffV + sv_slot * kTileBytes + kHalfBytes + row * 128);
+                    uint4 *vrow = reinterpret_cast<uint4 *>(smem + C::kOffV + sv_slot * C::kVSlot + row * 128);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        vrow0[c] = make_uint4(0, 0, 0, 0);
-                        vrow1[c] = make_uint4(0, 0, 0, 0);
+                    for (int c = 0; c < 8; ++c) vrow[c] = make_uint4(0, 0, 0, 0);
+                    if constexpr (!kF8) {
+                        vrow = reinterpret_cast<uint4 *>(smem + C::kOffV + sv_slot * kTileBytes + kHalfBytes + row * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) vrow[c] = make_uint4(0, 0, 0, 0);
                     }
                 }
                 fence_proxy_async();
@@ -981,10 +922,10 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     ok = false;
                     break;
                 }
-                const int64_t prow0 = (2 * ((int64_t)blockIdx.x + x.s) + wg) * nq;
+                const int64_t prow0 = (x.slot2 + wg) * nq;
 #pragma unroll
                 for (int n = 0; n < NQ; ++n)
-                    if (n < nq) a.ws_o[(prow0 + n) * kD + row] = kF8 ? o[n] * kF8Unscale : o[n];
+                    if (n < nq) a.ws_o[(prow0 + n) * kD + row] = o[n] * kOutScale;
                 if (row < nq) {
                     const float4 t4 = *reinterpret_cast<const float4 *>(my_red_sum + row * 4);
                     float m_row = -INFINITY;
@@ -992,7 +933,7 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     for (int n = 0; n < NQ; ++n)
                         if (n == row) m_row = mrun[n];
                     a.ws_ml[(prow0 + row) * 2 + 0] = m_row;
-                    a.ws_ml[(prow0 + row) * 2 + 1] = (t4.x + t4.y) + (t4.z + t4.w);
+                    a.ws_ml[(prow0 + row) * 2 + 1] = ((t4.x + t4.y) + (t4.z + t4.w)) * kOutScale;
                 }
                 if (!group_sync()) {   // the row-sum buffer is reused by the next unit
                     ok = false;
