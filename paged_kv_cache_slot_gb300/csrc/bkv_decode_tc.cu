@@ -22,12 +22,14 @@
 //   head) is a unit; it writes two partial slots (one per softmax
 //   warpgroup), and a stream's slots are the contiguous range the merge
 //   recomputes from the context lengths.
-// * Warp roles: warp 0 gathers K tiles (and Q), the last warp gathers V
-//   tiles, warp 1 issues tcgen05.mma from one thread and owns the TMEM
-//   allocation, and two warpgroups (warps 2..5 and 6..9) run the softmax and
-//   the output update on alternate tiles.  K and V have separate 3-slot
-//   rings of 32 KB: a K slot is released as soon as the S MMA that reads it
-//   completes.
+// * Warp roles: warp 0 gathers K tiles (and Q), warp 10 gathers V tiles,
+//   warp 1 issues the S MMAs from one thread and owns the TMEM allocation,
+//   warp 11 issues the P.V MMAs from one thread, and two warpgroups (warps
+//   2..5 and 6..9) run the softmax and the output update on alternate
+//   tiles.  K and V have separate rings (bf16: 3 slots of 32 KB each): a K
+//   slot is released as soon as the S MMA that reads it completes, an S
+//   tile as soon as its softmax warpgroup has read it, so the next S MMA
+//   into that tile need not wait for the P.V MMA.
 // * A tile's K (or V) rows of KV head g are gathered through the block
 //   table with 3-D TMA loads (cp.async.bulk.tensor; map over (head_dim,
 //   H_kv, total_blocks * block_size), box = 64 x 1 x min(block_size, 128)
@@ -103,7 +105,10 @@ constexpr int kT8Bytes = kTile * 128;            // an FP8 K or V tile as loaded
 constexpr int kQBytes = 2 * kN * 128;            // 16 rows x 128 B x 2 halves (FP8: 2 parts): 4 KB
 constexpr int kPBytes = 2 * kN * 128;            // 16 rows x 128 positions, 2 x 64 bf16 or 2 E4M3 parts: 4 KB
 constexpr int kWarpV = 10;                       // the V producer's warp
-constexpr int kTmemCols = 64;                    // S x2 (16 cols each) + O x2
+constexpr int kWarpPV = 11;                      // the P.V MMA issuer's warp
+// TMEM: S tile b at columns 32 b, O tile b at 64 + 32 b (FP8: the hi and lo
+// parts' products side by side, 16 columns each; bf16: the first 16)
+constexpr int kTmemCols = 128;
 constexpr int kTimeoutErr = 1 << 24;
 constexpr int kMaxReqs = 2048;                   // requests the in-kernel tile prefix handles
 constexpr int kWinBlocks = 128;                  // table entries a producer caches per window
@@ -114,7 +119,8 @@ constexpr int kWinBlocks = 128;                  // table entries a producer cac
 // q_split_e4m3_kernel, P as two E4M3 parts written by the softmax.
 template <bool kF8>
 struct Cfg {
-    static constexpr int kThreads = 352;                 // K producer, MMA, two softmax warpgroups, V producer
+    // K producer, S MMA issuer, two softmax warpgroups, V producer, P.V MMA issuer
+    static constexpr int kThreads = 384;
     static constexpr int kKStages = kF8 ? BKV_F8_K_STAGES : BKV_K_STAGES;
     static constexpr int kVStages = kF8 ? BKV_F8_V_STAGES : BKV_V_STAGES;
     static constexpr int kKSlot = kF8 ? kT8Bytes : kTileBytes;
@@ -127,7 +133,7 @@ struct Cfg {
     static constexpr int kOffRedMax = kOffMask + 64;                 // [warpgroup][2][16 rows][4 warps] floats
     static constexpr int kOffRedSum = kOffRedMax + 4 * kN * 4 * 4;   // [warpgroup][16 rows][4 warps] floats
     static constexpr int kOffBar = kOffRedSum + 2 * kN * 4 * 4;      // barriers (8 B each)
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 8;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 8 + 2;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffPre = kOffAbort + 4;                    // [kMaxReqs + 1] tile prefix per request
@@ -141,7 +147,7 @@ struct Cfg {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA exceeds the sm_103a limit");
     static_assert(kOffEnt % 16 == 0, "entry buffers must stay aligned");
     static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1 KB alignment");
-    static_assert(kWarpV == kThreads / 32 - 1, "warp roles");
+    static_assert(kWarpPV == kThreads / 32 - 1 && kWarpV == kWarpPV - 1, "warp roles");
 };
 
 // The first NQ accumulator columns of this thread's TMEM lane.
@@ -151,6 +157,39 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NQ]) {
     else if constexpr (NQ == 8) tmem_ld8(taddr, v);
     else tmem_ld4(taddr, v);
 }
+
+// FP8 caches: an S or O tile holds the products with the hi part in columns
+// [0, 16) and with the lo part in [16, 32); the sum of the first NQ of each.
+template <int NQ>
+__device__ __forceinline__ void tmem_ld_sum2(uint32_t taddr, float (&v)[NQ]) {
+    uint32_t h[NQ], l[NQ];
+    if constexpr (NQ == 16) {
+        tmem_ld16_nw(taddr, h);
+        tmem_ld16_nw(taddr + 16u, l);
+    } else if constexpr (NQ == 8) {
+        tmem_ld8_nw(taddr, h);
+        tmem_ld8_nw(taddr + 16u, l);
+    } else {
+        tmem_ld4_nw(taddr, h);
+        tmem_ld4_nw(taddr + 16u, l);
+    }
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) v[i] = __uint_as_float(h[i]) + __uint_as_float(l[i]);
+}
+
+// A ring slot and its phase parity, advanced one tile at a time (no division
+// by the ring size on the per-tile path).
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void advance(int n) {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
 
 // ---------------------------------------------------------------------------
 // Stream-K schedule
@@ -423,6 +462,8 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
     auto bar_group = [&](int k) { return bar0 + 8u * (kB + 10 + k); };   // four warps of warpgroup k
     // "loaded segments" word of tile j: mask_words[j & 7], published with bar_mask(j & 7)
     auto bar_mask = [&](int m) { return bar0 + 8u * (kB + 12 + m); };
+    // S tile b read into registers (four softmax warps): the S issuer may overwrite it
+    auto bar_sfree = [&](int b) { return bar0 + 8u * (kB + 20 + b); };
     const uint32_t sm_k = sbase + C::kOffK;
     const uint32_t sm_v = sbase + C::kOffV;
     const uint32_t sm_q = sbase + C::kOffQ;
@@ -447,6 +488,8 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         }
         mbar_init(bar_group(0), 4);
         mbar_init(bar_group(1), 4);
+        mbar_init(bar_sfree(0), 4);
+        mbar_init(bar_sfree(1), 4);
         for (int m = 0; m < 8; ++m) mbar_init(bar_mask(m), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -548,6 +591,8 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         int64_t j = 0;   // tile sequence number in this CTA
         int us = 0;      // unit sequence number in this CTA
         int ws = 0;      // window sequence number
+        const int nst = is_v ? kVStages : kKStages;
+        Ring ring;       // slot of tile j in this producer's ring
         Win cur, nxt;
         bool have = next_win(cur);
         if (have) {
@@ -579,12 +624,11 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     }
                 }
             }
-            for (int jt = cur.t0; jt < cur.t1; ++jt, ++j) {
-                const int nst = is_v ? kVStages : kKStages;
-                const int s = (int)(j % nst);
+            for (int jt = cur.t0; jt < cur.t1; ++jt, ++j, ring.advance(nst)) {
+                const int s = ring.slot;
                 const uint32_t bar_e = is_v ? bar_vempty(s) : bar_kempty(s);
                 const uint32_t bar_f = is_v ? bar_vfull(s) : bar_kfull(s);
-                if (!mbar_wait_warp(bar_e, (uint32_t)((j / nst) & 1) ^ 1u, abort_flag)) break;
+                if (!mbar_wait_warp(bar_e, ring.phase ^ 1u, abort_flag)) break;
                 const int32_t ts = x.start + jt * kTile;
                 // lane i handles block segment i of the tile
                 bool load = false;
@@ -608,10 +652,11 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 const uint32_t ballot = __ballot_sync(0xffffffffu, load);
                 if (lane == 0) {
                     // bit i: segment i was loaded.  A ring of 8 words by tile number with
-                    // its own barriers: the K producer writes tile j's word only after
-                    // the S MMA of tile j - kKStages completed, which is issued only after
-                    // the softmax released tile j - kKStages - 2, so it is never more than
-                    // kKStages + 2 <= 5 tiles ahead of the reader and phases cannot alias.
+                    // its own barriers: the K producer writes tile j's word only after the
+                    // S MMA of tile j - kKStages completed, which is issued only after the
+                    // softmax read S (and, before that, the word) of tile j - kKStages - 2,
+                    // so the writer is at most kKStages + 2 <= 7 tiles ahead of the reader
+                    // and neither words nor barrier phases alias.
                     if (!is_v) {
                         mask_words[j & 7] = ballot;
                         mbar_arrive(bar_mask((int)(j & 7)));
@@ -647,54 +692,22 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
             while (global_ns() - t0 < 200000ull) {
             }
         }
-    } else if (warp == 1) {
-        // ================= MMA issuer (one thread) =================
-        if (lane == 0) {
-            // K (K-major) x Q (K-major); V^T (MN-major) x P (K-major).  FP8 caches: both on
-            // E4M3 operands (the descriptor's E4M3 type codes are 0, as f16's)
-            constexpr uint32_t kIdescS = kF8 ? idesc_f16(128, kN, 0, 0) : idesc_bf16(128, kN, 0, 0);
-            constexpr uint32_t kIdescO = kF8 ? idesc_f16(128, kN, 1, 0) : idesc_bf16(128, kN, 1, 0);
+    } else if (warp == 1 || warp == kWarpPV) {
+        // ================= MMA issuers (one thread each) =================
+        // Warp 1 issues the S MMAs, warp kWarpPV the P.V MMAs, so neither waits on
+        // the other's operands.  K (K-major) x Q (K-major); V^T (MN-major) x P
+        // (K-major).  FP8 caches: both on E4M3 operands (the descriptor's E4M3
+        // type codes are 0, as f16's), with the hi and lo parts of Q (resp. P)
+        // stacked as 32 B rows, so one MMA of N = 32 multiplies both.
+        constexpr int kNM = kF8 ? 2 * kN : kN;
+        bool ok = true;
+        StreamK sk;
+        sk.init(a, pre, lrem);
+        if (lane == 0 && warp == 1) {
+            constexpr uint32_t kIdescS = kF8 ? idesc_f16(128, kNM, 0, 0) : idesc_bf16(128, kNM, 0, 0);
             int64_t j = 0;
             int us = 0;
-            int64_t pending = -1;        // tile whose P.V MMA is still to be issued
-            int pending_stage = 0;
-            bool ok = true;
-            auto issue_pv = [&](int64_t jp, int stage) -> bool {
-                const int b = (int)(jp & 1);
-                if (!mbar_wait(bar_vfull(stage), (uint32_t)((jp / kVStages) & 1), abort_flag) ||
-                    !mbar_wait(bar_pfull(b), (uint32_t)((jp >> 1) & 1), abort_flag))
-                    return false;
-                tc_fence_after();
-                const uint32_t p_base = sm_p + b * kPBytes;
-                const uint32_t d_tmem = tmem + 32u + 16u * b;
-                if constexpr (kF8) {
-                    // O^T = V^T (E4M3 codes, MN-major: a row's 128 codes are one 128-byte
-                    // span, 8-row groups 1024 bytes apart) . (P_hi + P_lo)^T, 32 positions
-                    // per step
-                    const uint32_t v_base = sm_v + stage * kT8Bytes;
-#pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < kTile / 32; ++kk) {
-                            const uint64_t adesc = sdesc(v_base + kk * 4096, 16, 1024);
-                            const uint64_t bdesc = sdesc(p_base + part * (kN * 128) + kk * 32, 16, 1024);
-                            mma_f8(d_tmem, adesc, bdesc, kIdescO, (part | kk) > 0);
-                        }
-                } else {
-                    const uint32_t v_base = sm_v + stage * kTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
-                        const uint64_t adesc = sdesc(v_base + kk * 2048, kHalfBytes, 1024);
-                        const uint64_t bdesc = sdesc(p_base + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
-                        mma_bf16(d_tmem, adesc, bdesc, kIdescO, kk > 0);
-                    }
-                }
-                mma_commit(bar_ofull(b));
-                mma_commit(bar_vempty(stage));
-                return true;
-            };
-            StreamK sk;
-            sk.init(a, pre, lrem);
+            Ring kr;
             Unit x;
             while (ok && sk.next(a, x)) {
                 const int qb = us & 1;
@@ -702,29 +715,29 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     ok = false;
                     break;
                 }
-                for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
-                    const int s = (int)(j % kKStages);
-                    if (!mbar_wait(bar_kfull(s), (uint32_t)((j / kKStages) & 1), abort_flag)) {
+                const uint32_t q_base = sm_q + qb * kQBytes;
+                for (int jt = 0; jt < x.ntiles; ++jt, ++j, kr.advance(kKStages)) {
+                    const int b = (int)(j & 1);
+                    // K landed, and the softmax has read S tile b of tile j - 2
+                    if (!mbar_wait(bar_kfull(kr.slot), kr.phase, abort_flag) ||
+                        (j >= 2 && !mbar_wait(bar_sfree(b), (uint32_t)((j >> 1) & 1) ^ 1u, abort_flag))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t q_base = sm_q + qb * kQBytes;
-                    const uint32_t d_tmem = tmem + 16u * (uint32_t)(j & 1);
+                    const uint32_t d_tmem = tmem + 32u * (uint32_t)b;
                     if constexpr (kF8) {
-                        // S^T = K (E4M3, 128-code rows) . (Q_1 + Q_2)^T: two parts of four
-                        // 32-code steps, accumulated in one TMEM tile
-                        const uint32_t k_base = sm_k + s * kT8Bytes;
+                        // S^T[:, 0:16] = K . Q_hi^T, S^T[:, 16:32] = K . Q_lo^T (E4M3, 128-code
+                        // rows): four 32-code steps
+                        const uint32_t k_base = sm_k + kr.slot * kT8Bytes;
 #pragma unroll
-                        for (int part = 0; part < 2; ++part)
-#pragma unroll
-                            for (int kk = 0; kk < kD / 32; ++kk) {
-                                const uint64_t adesc = sdesc(k_base + kk * 32, 16, 1024);
-                                const uint64_t bdesc = sdesc(q_base + part * (kN * 128) + kk * 32, 16, 1024);
-                                mma_f8(d_tmem, adesc, bdesc, kIdescS, (part | kk) > 0);
-                            }
+                        for (int kk = 0; kk < kD / 32; ++kk) {
+                            const uint64_t adesc = sdesc(k_base + kk * 32, 16, 1024);
+                            const uint64_t bdesc = sdesc(q_base + kk * 32, 16, 1024);
+                            mma_f8(d_tmem, adesc, bdesc, kIdescS, kk > 0);
+                        }
                     } else {
-                        const uint32_t k_base = sm_k + s * kTileBytes;
+                        const uint32_t k_base = sm_k + kr.slot * kTileBytes;
 #pragma unroll
                         for (int kk = 0; kk < kD / 16; ++kk) {
                             const uint32_t half = (uint32_t)(kk >> 2) * kHalfBytes;
@@ -733,19 +746,48 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                             mma_bf16(d_tmem, adesc, bdesc, kIdescS, kk > 0);
                         }
                     }
-                    mma_commit(bar_sfull((int)(j & 1)));
-                    mma_commit(bar_kempty(s));
+                    mma_commit(bar_sfull(b));
+                    mma_commit(bar_kempty(kr.slot));
                     if (jt == x.ntiles - 1) mma_commit(bar_qempty(qb));
-                    if (pending >= 0 && !issue_pv(pending, pending_stage)) {
-                        ok = false;
-                        break;
-                    }
-                    pending = j;
-                    pending_stage = (int)(j % kVStages);
                 }
                 ++us;
             }
-            if (ok && pending >= 0) issue_pv(pending, pending_stage);
+        } else if (lane == 0) {
+            constexpr uint32_t kIdescO = kF8 ? idesc_f16(128, kNM, 1, 0) : idesc_bf16(128, kNM, 1, 0);
+            // the P.V MMAs do not depend on unit boundaries: this CTA's tiles in order
+            const int64_t ntot = sk.t1 - sk.t;
+            Ring vr;
+            for (int64_t j = 0; j < ntot; ++j, vr.advance(kVStages)) {
+                const int b = (int)(j & 1);
+                if (!mbar_wait(bar_vfull(vr.slot), vr.phase, abort_flag) ||
+                    !mbar_wait(bar_pfull(b), (uint32_t)((j >> 1) & 1), abort_flag))
+                    break;
+                tc_fence_after();
+                const uint32_t p_base = sm_p + b * kPBytes;
+                const uint32_t d_tmem = tmem + 64u + 32u * (uint32_t)b;
+                if constexpr (kF8) {
+                    // O^T[:, 0:16] = V^T . P_hi^T, O^T[:, 16:32] = V^T . P_lo^T; V^T as E4M3
+                    // codes MN-major (a row's 128 codes are one 128-byte span, 8-row groups
+                    // 1024 bytes apart), 32 positions per step
+                    const uint32_t v_base = sm_v + vr.slot * kT8Bytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 32; ++kk) {
+                        const uint64_t adesc = sdesc(v_base + kk * 4096, 16, 1024);
+                        const uint64_t bdesc = sdesc(p_base + kk * 32, 16, 1024);
+                        mma_f8(d_tmem, adesc, bdesc, kIdescO, kk > 0);
+                    }
+                } else {
+                    const uint32_t v_base = sm_v + vr.slot * kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint64_t adesc = sdesc(v_base + kk * 2048, kHalfBytes, 1024);
+                        const uint64_t bdesc = sdesc(p_base + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+                        mma_bf16(d_tmem, adesc, bdesc, kIdescO, kk > 0);
+                    }
+                }
+                mma_commit(bar_ofull(b));
+                mma_commit(bar_vempty(vr.slot));
+            }
         }
         __syncwarp();
     } else if (warp < kWarpV) {
@@ -764,6 +806,7 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         const int wq = warp & 3;
         float o[NQ], lsum[NQ], mrun[NQ];
         int64_t j = 0;
+        Ring vring;      // V slot of tile j (rows past the end are zeroed there)
         bool ok = true;
         uint32_t gphase = 0;
         // Bounded barrier of the warpgroup's four warps (an mbarrier, so that a
@@ -810,9 +853,9 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 lastv[n] = (n < nq) ? (a.mask_mode == 0 ? Lg - a.q_len + t : Lg - 1) : -1;
                 firstv[n] = a.window > 0 ? Lg - a.q_len + t - a.window + 1 : INT32_MIN;
             }
-            for (int jt = 0; jt < x.ntiles; ++jt, ++j) {
+            for (int jt = 0; jt < x.ntiles; ++jt, ++j, vring.advance(kVStages)) {
                 if ((int)(j & 1) != wg) continue;
-                const int sv_slot = (int)(j % kVStages);
+                const int sv_slot = vring.slot;
                 const int b = wg;
                 const uint32_t par = (uint32_t)((j >> 1) & 1);
                 if (!mbar_wait_warp(bar_sfull(b), par, abort_flag) ||
@@ -820,11 +863,19 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     ok = false;
                     break;
                 }
+                // the loaded-segment word is read before S tile b is released: the K
+                // producer can rewrite word j & 7 (for tile j + 8) only after the S MMA
+                // of tile j + 2 completed, which waits for that release
+                const bool loaded = (mask_words[j & 7] >> (row >> seg_shift)) & 1u;
                 tc_fence_after();
                 float sv[NQ];
-                tmem_ld_cols<NQ>(tmem + lane_base + 16u * b, sv);
+                if constexpr (kF8) tmem_ld_sum2<NQ>(tmem + lane_base + 32u * b, sv);
+                else tmem_ld_cols<NQ>(tmem + lane_base + 32u * b, sv);
+                // S tile b may now be overwritten (by the S MMA of tile j + 2)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_sfree(b));
                 const int32_t pos = x.start + jt * kTile + row;
-                const bool loaded = (mask_words[j & 7] >> (row >> seg_shift)) & 1u;
                 const bool inrange = loaded && pos < x.cend;
                 const int32_t gpos = kCP ? cp_global32(a, pos) : pos;
 #pragma unroll
@@ -883,8 +934,7 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 // V rows that were loaded but lie past the end must be zero for P.V
                 // (after the V tile has landed)
                 const bool zero_row = loaded && pos >= x.cend;
-                if (__any_sync(0xffffffffu, zero_row) &&
-                    !mbar_wait_warp(bar_vfull(sv_slot), (uint32_t)((j / kVStages) & 1), abort_flag)) {
+                if (__any_sync(0xffffffffu, zero_row) && !mbar_wait_warp(bar_vfull(sv_slot), vring.phase, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -909,7 +959,8 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 }
                 tc_fence_after();
                 float ot[NQ];
-                tmem_ld_cols<NQ>(tmem + lane_base + 32u + 16u * b, ot);
+                if constexpr (kF8) tmem_ld_sum2<NQ>(tmem + lane_base + 64u + 32u * b, ot);
+                else tmem_ld_cols<NQ>(tmem + lane_base + 64u + 32u * b, ot);
 #pragma unroll
                 for (int n = 0; n < NQ; ++n) o[n] = fmaf(o[n], corr[n], ot[n]);
             }
