@@ -87,15 +87,17 @@ constexpr int kN = 16;                // query rows per MMA (padded)
 #ifndef BKV_V_STAGES
 #define BKV_V_STAGES 3
 #endif
-static_assert(BKV_K_STAGES >= 2 && BKV_K_STAGES <= 3, "the 8-entry mask ring assumes at most 3 K slots");
+// tiles whose loaded-segment words are kept (a ring indexed by tile number)
+constexpr int kMaskRing = 16;
+static_assert(BKV_K_STAGES >= 2 && BKV_K_STAGES <= 3, "K slots of the bf16 ring");
 // FP8 caches: slots of the E4M3 K and V rings (16 KB each, read by the MMAs as loaded)
 #ifndef BKV_F8_K_STAGES
-#define BKV_F8_K_STAGES 5
+#define BKV_F8_K_STAGES 4
 #endif
 #ifndef BKV_F8_V_STAGES
-#define BKV_F8_V_STAGES 6
+#define BKV_F8_V_STAGES 4
 #endif
-static_assert(BKV_F8_K_STAGES >= 2 && BKV_F8_K_STAGES <= 5, "the 8-entry mask ring assumes at most 5 K slots");
+static_assert(BKV_F8_K_STAGES >= 2 && BKV_F8_K_STAGES + 2 < kMaskRing, "the mask ring needs more than K slots + 2 words");
 // FP8 caches: the weights enter the P.V MMA as p 2^kF8PExp (p <= 1, so at most
 // 256 < 448, the largest finite E4M3 value); the partial output takes it back
 constexpr int kF8PExp = 8;
@@ -129,11 +131,11 @@ struct Cfg {
     static constexpr int kOffV = kOffK + kKStages * kKSlot;          // kVStages V slots
     static constexpr int kOffQ = kOffV + kVStages * kVSlot;
     static constexpr int kOffP = kOffQ + 2 * kQBytes;
-    static constexpr int kOffMask = kOffP + 2 * kPBytes;             // 8 words: loaded segments per tile (ring)
-    static constexpr int kOffRedMax = kOffMask + 64;                 // [warpgroup][2][16 rows][4 warps] floats
+    static constexpr int kOffMask = kOffP + 2 * kPBytes;             // kMaskRing words: loaded segments per tile
+    static constexpr int kOffRedMax = kOffMask + 4 * kMaskRing;      // [warpgroup][2][16 rows][4 warps] floats
     static constexpr int kOffRedSum = kOffRedMax + 4 * kN * 4 * 4;   // [warpgroup][16 rows][4 warps] floats
     static constexpr int kOffBar = kOffRedSum + 2 * kN * 4 * 4;      // barriers (8 B each)
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 8 + 2;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + kMaskRing + 2;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffPre = kOffAbort + 4;                    // [kMaxReqs + 1] tile prefix per request
@@ -327,12 +329,15 @@ struct StreamK {
         g = (int)blockIdx.x - q * H;
         hbase = (int64_t)g * (P + n);
         // split over min(P, TP) groups so every participating CTA has at
-        // least one tile (the merge recomputes the slots with the same rule)
-        const int64_t TP = pre[n];
-        const int64_t peff = TP < (int64_t)P ? TP : (int64_t)P;
-        if ((int64_t)q < peff) {
-            t = TP * q / peff;
-            t1 = TP * (q + 1) / peff;
+        // least one tile (the merge recomputes the slots with the same rule);
+        // floor(TP q / peff) in 32-bit operations: TP = A peff + B gives
+        // A q + floor(B q / peff), and B q < peff^2 is small
+        const int32_t TP = pre[n];
+        const int32_t peff = TP < P ? TP : P;
+        if (q < peff) {
+            const int32_t A = TP / peff, B = TP - A * peff;
+            t = (int64_t)A * q + (B * q) / peff;
+            t1 = (int64_t)A * (q + 1) + (B * (q + 1)) / peff;
         } else {
             t = t1 = TP;
         }
@@ -460,10 +465,10 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
     auto bar_pfull = [&](int b) { return bar0 + 8u * (kB + 6 + b); };
     auto bar_ofull = [&](int b) { return bar0 + 8u * (kB + 8 + b); };
     auto bar_group = [&](int k) { return bar0 + 8u * (kB + 10 + k); };   // four warps of warpgroup k
-    // "loaded segments" word of tile j: mask_words[j & 7], published with bar_mask(j & 7)
+    // "loaded segments" word of tile j: mask_words[j % kMaskRing], published with bar_mask(j % kMaskRing)
     auto bar_mask = [&](int m) { return bar0 + 8u * (kB + 12 + m); };
     // S tile b read into registers (four softmax warps): the S issuer may overwrite it
-    auto bar_sfree = [&](int b) { return bar0 + 8u * (kB + 20 + b); };
+    auto bar_sfree = [&](int b) { return bar0 + 8u * (kB + 12 + kMaskRing + b); };
     const uint32_t sm_k = sbase + C::kOffK;
     const uint32_t sm_v = sbase + C::kOffV;
     const uint32_t sm_q = sbase + C::kOffQ;
@@ -490,7 +495,7 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         mbar_init(bar_group(1), 4);
         mbar_init(bar_sfree(0), 4);
         mbar_init(bar_sfree(1), 4);
-        for (int m = 0; m < 8; ++m) mbar_init(bar_mask(m), 1);
+        for (int m = 0; m < kMaskRing; ++m) mbar_init(bar_mask(m), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -651,15 +656,15 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 }
                 const uint32_t ballot = __ballot_sync(0xffffffffu, load);
                 if (lane == 0) {
-                    // bit i: segment i was loaded.  A ring of 8 words by tile number with
-                    // its own barriers: the K producer writes tile j's word only after the
-                    // S MMA of tile j - kKStages completed, which is issued only after the
-                    // softmax read S (and, before that, the word) of tile j - kKStages - 2,
-                    // so the writer is at most kKStages + 2 <= 7 tiles ahead of the reader
-                    // and neither words nor barrier phases alias.
+                    // bit i: segment i was loaded.  A ring of kMaskRing words by tile number
+                    // with its own barriers: the K producer writes tile j's word only after
+                    // the S MMA of tile j - kKStages completed, which is issued only after
+                    // the softmax read S (and, before that, the word) of tile
+                    // j - kKStages - 2, so the writer is at most kKStages + 2 < kMaskRing
+                    // tiles ahead of the reader and neither words nor barrier phases alias.
                     if (!is_v) {
-                        mask_words[j & 7] = ballot;
-                        mbar_arrive(bar_mask((int)(j & 7)));
+                        mask_words[j & (kMaskRing - 1)] = ballot;
+                        mbar_arrive(bar_mask((int)(j & (kMaskRing - 1))));
                     }
                     const uint32_t bytes = (uint32_t)__popc(ballot) * (uint32_t)seg_rows * 128u * (kF8 ? 1u : 2u);
                     mbar_arrive_expect_tx(bar_f, bytes);
@@ -859,14 +864,14 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                 const int b = wg;
                 const uint32_t par = (uint32_t)((j >> 1) & 1);
                 if (!mbar_wait_warp(bar_sfull(b), par, abort_flag) ||
-                    !mbar_wait_warp(bar_mask((int)(j & 7)), (uint32_t)((j >> 3) & 1), abort_flag)) {
+                    !mbar_wait_warp(bar_mask((int)(j & (kMaskRing - 1))), (uint32_t)((j / kMaskRing) & 1), abort_flag)) {
                     ok = false;
                     break;
                 }
                 // the loaded-segment word is read before S tile b is released: the K
-                // producer can rewrite word j & 7 (for tile j + 8) only after the S MMA
-                // of tile j + 2 completed, which waits for that release
-                const bool loaded = (mask_words[j & 7] >> (row >> seg_shift)) & 1u;
+                // producer can rewrite this word (for tile j + kMaskRing) only after the
+                // S MMA of tile j + 2 completed, which waits for that release
+                const bool loaded = (mask_words[j & (kMaskRing - 1)] >> (row >> seg_shift)) & 1u;
                 tc_fence_after();
                 float sv[NQ];
                 if constexpr (kF8) tmem_ld_sum2<NQ>(tmem + lane_base + 32u * b, sv);
