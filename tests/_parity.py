@@ -23,11 +23,25 @@ Guards, so that no bar can silently stop biting:
 * ``min_magnitude`` (the loud variants): the median row magnitude must reach
   it, so that the absolute bar bites as well.
 """
+import os
+
 import numpy as np
 
 ABS = {"bf16": 1e-2, "f32": 1e-5}
 REL = {"bf16": 1e-2, "f32": 1e-5}
 FLOOR = {"bf16": 1e-6, "f32": 1e-9}
+
+# worst errors seen per test (node id -> [dtype, rows checked, worst |got - want|, worst of that over the
+# row's magnitude]); tests/conftest.py prints them at the end of the session
+WORST = {}
+
+
+def _record(dtype, rows, err_abs, err_rel):
+    key = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    e = WORST.setdefault(key, [dtype, 0, 0.0, 0.0])
+    e[1] += rows
+    e[2] = max(e[2], err_abs)
+    e[3] = max(e[3], err_rel)
 
 
 def check_attention(got, want, dtype, label="", min_magnitude=None):
@@ -65,4 +79,6 @@ def check_attention(got, want, dtype, label="", min_magnitude=None):
     if min_magnitude is not None:
         med = float(np.median(mag[nz]))
         assert med >= min_magnitude, f"{label}: median row magnitude {med:.3e} < {min_magnitude} (not loud)"
-    return float(err[nz].max()), float((err[nz] / mag[nz]).max())
+    worst = (float(err[nz].max()), float((err[nz] / mag[nz]).max()))
+    _record(dtype, int(nz.sum()), *worst)
+    return worst
