@@ -520,7 +520,15 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    pdl_wait();                // global memory is read from here on
+    // Global memory is read from here on.  bf16: the preceding kernel may be
+    // the caller's and may have written anything read below, so wait for it.
+    // E4M3: the preceding kernel is this call's query split
+    // (q_split_e4m3_kernel), which waited for its own predecessors before
+    // letting this grid start, so only its outputs (the split queries and
+    // their scales) wait: the K producer before the first Q load, the softmax
+    // before the first scale read; the schedule, the table and the first K and
+    // V loads overlap the split.
+    if constexpr (!kF8) pdl_wait();
     pdl_trigger();
     uint8_t *lrem = smem + C::kOffLrem;
     schedule_loads<kF8>(a, pre, lrem, smem);
@@ -611,10 +619,12 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
             const int32_t lb_first = win_first_block(cur);
             const Unit &x = cur.u;
             const int32_t wlo = window_lo(a, x.L);   // segments ending at or before it are not needed
-            if (cur.t0 == 0 && !is_v) {
+            // the unit's Q (K producer), once its buffer is free; the first unit's E4M3
+            // queries go after its first K tile, behind the wait for the query split
+            auto issue_q = [&]() {
                 const int qb = us & 1;
-                if (!mbar_wait_warp(bar_qempty(qb), ((us >> 1) & 1) ^ 1, abort_flag)) break;
                 if (lane == 0) {
+                    if (kF8 && us == 0) pdl_wait();   // the split queries are the query split's output
                     mbar_arrive_expect_tx(bar_qfull(qb), 2u * 128u * (uint32_t)nq);
                     const uint32_t dq = sm_q + qb * kQBytes;
                     if constexpr (kF8) {
@@ -628,6 +638,13 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                         tma_load_3d(dq + kN * 128, &tmQ, bar_qfull(qb), 64, x.g * G, x.r * a.q_len);
                     }
                 }
+                __syncwarp();
+            };
+            bool q_after_first = false;
+            if (cur.t0 == 0 && !is_v) {
+                if (!mbar_wait_warp(bar_qempty(us & 1), ((us >> 1) & 1) ^ 1, abort_flag)) break;
+                if (kF8 && us == 0) q_after_first = true;
+                else issue_q();
             }
             for (int jt = cur.t0; jt < cur.t1; ++jt, ++j, ring.advance(nst)) {
                 const int s = ring.slot;
@@ -684,7 +701,12 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
                     }
                 }
                 __syncwarp();
+                if (q_after_first) {
+                    issue_q();
+                    q_after_first = false;
+                }
             }
+            if (q_after_first) issue_q();   // (a window without tiles: never, kept for safety)
             if (have_n) park_entries(nxt, (ws + 1) & 1);
             if (cur.t1 == x.ntiles) ++us;
             ++ws;
@@ -835,6 +857,7 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         float *my_red_sum = red_sum + wg * (kN * 4);
         StreamK sk;
         sk.init(a, pre, lrem);
+        if constexpr (kF8) pdl_wait();   // the query scales are the query split's output
         Unit x;
         while (ok && sk.next(a, x)) {
             // masks are in global positions: with context parallelism x.L counts
