@@ -119,6 +119,29 @@ def test_small_shapes(case, mask_mode):
     assert (got[w.num_rows - 1] == 0).all()
 
 
+# KV-head counts off the persistent grid: the tensor-core kernel runs P = floor(SMs / H_kv) groups of
+# H_kv CTAs (152 SMs: 3 -> 150 CTAs, 7 -> 147), and one group of H_kv CTAs when H_kv exceeds the SM count
+# (160: two waves); the merge recomputes each stream's slots from the same rule
+OFF_GRID = [
+    # q_len, H_q, H_kv, D, bs, prior
+    (1, 6, 3, 128, 16, (900, 40, 2100, 5)),
+    (2, 35, 7, 128, 32, (1500, 300, 4100)),
+    (1, 160, 160, 128, 16, (200, 50, 700)),
+]
+
+
+@pytest.mark.parametrize("case", OFF_GRID, ids=lambda c: f"q{c[0]}_h{c[1]}x{c[2]}")
+@pytest.mark.parametrize("mask_mode", [0, 1])
+def test_kv_head_counts_off_the_sm_grid(case, mask_mode):
+    q_len, H_q, H_kv, D, bs, prior = case
+    w = _custom(q_len, H_q, H_kv, D, bs, list(prior) + [0], "bf16", null_rows=(len(prior),), seed=515)
+    dw = DeviceWorkload(w)
+    dw.write_step()
+    got, _ = _check(dw, range(w.num_rows), mask_mode, f"off-grid {case}")   # (workspace NaN-filled first)
+    assert (got[w.num_rows - 1] == 0).all()
+    assert int(dw.err_count.item()) == 0
+
+
 VARIANTS = {"literal": {}, "sharp": {"sharp": True}, "loud": {"loud": True}}
 
 

@@ -203,6 +203,7 @@ SMALL = [
     (3, 16, 2, 64, 16, (90, 1100, 5, 400), "bf16"),
     (4, 8, 2, 32, 4, (50, 3, 260), "f32"),
     (1, 32, 8, 128, 16, (900, 4), "f32"),
+    (1, 15, 5, 128, 64, (1200, 77, 3000), "bf16"),      # 5 KV heads: a grid of 150 CTAs on 152 SMs
 ]
 
 
