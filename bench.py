@@ -38,6 +38,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -93,7 +94,7 @@ def _describe(w, window, cp=(1, 0, 1), fp8=None):
     """The workload's name and sizes, as the JSON line's config.workload."""
     if fp8 is not None:
         return (_describe(w, window, cp) + f", E4M3 KV cache (k_scale {fp8[0]:g}, v_scale {fp8[1]:g}; 1 byte per "
-                "element, K used as loaded by E4M3 tensor cores, V widened to f16 on chip)")
+                "element, K and V used as loaded by E4M3 tensor cores)")
     if cp[0] > 1:
         return (_describe(w, window) + f", decode-context-parallel rank {cp[1]} of {cp[0]} (interleave {cp[2]}): "
                 f"its own share of every request's keys")
@@ -110,12 +111,23 @@ def _describe(w, window, cp=(1, 0, 1), fp8=None):
     return d + (f", sliding window {window}" if window else "")
 
 
+def _code_only(text):
+    """C/CUDA source without comments or blank lines, runs of blanks as one space (string literals in
+    these sources hold neither comment markers nor blank runs), so that a comment edit does not count
+    as a new kernel."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
+
+
 def _decode_source_sha():
+    """Hash of the decode kernels' code (comments ignored): the committed ncu summary's traffic line
+    is reported only while it matches."""
     h = hashlib.sha256()
     for f in DECODE_SOURCES:
         p = os.path.join(ROOT, "paged_kv_cache_slot_gb300", "csrc", f)
         if os.path.exists(p):
-            h.update(open(p, "rb").read())
+            h.update(_code_only(open(p).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -344,7 +344,8 @@ int bkv_slot_mapping_cache_write_fp8(const int32_t *block_table, int32_t num_req
  *   most 16 query rows per KV head runs the tensor-core kernel: q . k on
  *   E4M3 tensor cores with each query row split into two E4M3 parts (exact
  *   for elements down to 2^-10 of the row's largest, within 2^-17 of it
- *   below), P . v on f16 with the value codes widened exactly; anything else
+ *   below), P . v on E4M3 tensor cores with the value codes as stored and
+ *   the weights as two E4M3 parts (within 2^-10 of p 2^8); anything else
  *   runs the CUDA-core kernel on the exact code values.  The workspace
  *   (bkv_paged_decode_workspace_size) includes the split queries.
  *   Errors: as bkv_paged_decode_swa, plus INVALID_ARG for a scale that is

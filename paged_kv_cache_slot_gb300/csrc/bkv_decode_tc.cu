@@ -821,7 +821,7 @@ __global__ void __launch_bounds__(Cfg<kF8>::kThreads, 1)
         // ================= softmax + output (two warpgroups of 128 threads) =================
         // Warpgroup k takes the tiles with (tile sequence number & 1) == k,
         // i.e. the S / P / O buffers of parity k, and writes partial slot
-        // 2 (CTA + stream) + k of every unit.
+        // slot2 + k of every unit.
         const int wg = (warp - 2) >> 2;
         // FP8 caches: query row i entered the S MMA divided by qexp[i] (a power of two),
         // taken back per column below; the weights enter the P.V MMA and the row sums

@@ -37,6 +37,15 @@ def test_clock_summary_without_samples(tmp_path):
     assert s.summary() is None
 
 
+def test_decode_source_hash_ignores_comments_only():
+    # a comment edit leaves the kernel (and the profiled traffic) valid; a code edit does not
+    a = "int f(int x) {  // twice\n    /* doubled\n       here */ return 2 * x;\n}\n"
+    b = "int f(int x) {\n\n    return 2 * x;   \n}\n"
+    c = "int f(int x) {\n    return 3 * x;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+
+
 def test_profiled_traffic_follows_the_decode_sources(tmp_path, monkeypatch):
     # the traffic is reported only while the summary carries the hash of the current decode sources
     fake = tmp_path / "profile.txt"
