@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(const DecodeArgs a)
 // dependency wait, so that only the partials' loads follow it.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int max_slots) {
+// (six CTAs per SM: on batches of thousands of streams the merge runs in waves)
+__global__ void __launch_bounds__(128, 6) decode_merge_kernel(const DecodeArgs a, int max_slots) {
     extern __shared__ float sw[];   // [4 warps][max_slots] weights
     __shared__ int64_t red[2][4];
     const int lane = threadIdx.x & 31;
@@ -275,6 +276,63 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
     }
     pdl_wait();
     pdl_trigger();
+    if (nch <= 4 && (a.D & 3) == 0 && a.D <= 128) {
+        // at most 4 slots and head_dim <= 128 (streams no CTA split, or split once): a warp's rows
+        // (warp, warp + 4, ...) two at a time, every (m, l) and partial load of the two issued
+        // before either is used, so two rows cost one round of loads (two, not more: the
+        // registers stay low enough for six CTAs per SM); lane k keeps slot k's weight, lanes past
+        // head_dim / 4 load and store no partials
+        const bool act = lane < a.D / 4;
+        for (int row0 = warp; row0 < a.nq; row0 += 8) {
+            float2 ml[2];
+            float4 v[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int row = row0 + 4 * i;
+                const bool rv = row < a.nq;
+                ml[i] = (rv && lane < nch) ? *reinterpret_cast<const float2 *>(a.ws_ml + ((unit0 + lane) * a.nq + row) * 2)
+                                           : make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    v[i][k] = (rv && act && k < nch)
+                                  ? *reinterpret_cast<const float4 *>(a.ws_o + ((unit0 + k) * a.nq + row) * a.D + 4 * lane)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int row = row0 + 4 * i;
+                if (row >= a.nq) break;   // the same for the whole warp
+                const int t = row / a.G;
+                const int h = g * a.G + (row - t * a.G);
+                const int64_t orow = ((int64_t)r * a.q_len + t) * a.H_q + h;
+                T *out = static_cast<T *>(a.out) + orow * a.D;
+                float M = ml[i].x;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                const float wl = (M == -INFINITY || lane >= nch) ? 0.f : exp2f(ml[i].x - M);
+                const float lsum = warp_sum(wl * ml[i].y);
+                const float iv = (M == -INFINITY || !(lsum > 0.f)) ? 0.f : a.v_scale / lsum;
+                if (a.lse && lane == 0)
+                    a.lse[orow] = (M == -INFINITY || !(lsum > 0.f)) ? -INFINITY : (M + log2f(lsum)) * kLn2;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float wgt = __shfl_sync(0xffffffffu, wl, k);
+                    acc.x = fmaf(wgt, v[i][k].x, acc.x);
+                    acc.y = fmaf(wgt, v[i][k].y, acc.y);
+                    acc.z = fmaf(wgt, v[i][k].z, acc.z);
+                    acc.w = fmaf(wgt, v[i][k].w, acc.w);
+                }
+                if (act) {
+                    store_out(out + 4 * lane + 0, acc.x * iv);
+                    store_out(out + 4 * lane + 1, acc.y * iv);
+                    store_out(out + 4 * lane + 2, acc.z * iv);
+                    store_out(out + 4 * lane + 3, acc.w * iv);
+                }
+            }
+        }
+        return;
+    }
     float *wts = sw + (size_t)warp * max_slots;
     for (int row = warp; row < a.nq; row += 4) {
         const int t = row / a.G;
